@@ -1,0 +1,675 @@
+// Host side of the C ABI: argument checks, the workspace arena, and the order
+// of kernel launches of one EAGLE-3 round (prefill, draft passes, tree build,
+// verification).  Everything runs on the caller's stream with no host
+// synchronisation; the only allocation is the arena made at create time.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/eagle3.h"
+#include "common.cuh"
+#include "gemm_tc.h"
+#include "kernels.h"
+
+using namespace e3;
+
+namespace {
+constexpr int kPrefillChunk = 2048;   // prefill rows per pass through the layer
+constexpr int kTargetBlocks = 2 * 148;
+
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+}  // namespace
+
+struct eagle3_ctx {
+  eagle3_config cfg;
+  eagle3_weights w;
+  bool bf;
+  int esz;
+  int M, M1, k, D, pool_n, n_slots, slot_words, tree_words, mask_words;
+  int rows_cap, rows_pf, rope_rows;
+  // arena
+  char* arena = nullptr;
+  size_t arena_bytes = 0;
+  // activations
+  float *g, *part, *q, *r, *S, *o_part, *ml_part;
+  void *x, *o, *z, *a, *h, *h_root, *h_ver;
+  void *tk, *tv, *vk, *vv;
+  size_t part_elems, attn_elems;
+  float2* rope;
+  // plans
+  RowPlan rp;
+  int *n_prefix, *root_tok, *root_pos;
+  // draft head
+  HeadParts hp;
+  int* top_tok;
+  float *top_logq, *top_lse;
+  // pool
+  PoolDev pool;
+  int* frontier;
+  uint32_t* slot_mask;
+  // verify
+  int *child_tok, *child_node, *n_child, *z_arg, *g_arg;
+  float *child_z, *vpart, *z_max, *lse, *g_max;
+  int n_vparts;
+  int* flags;
+  // tcgen05 GEMM plans
+  TcGemm* tc = nullptr;
+  // bookkeeping
+  cudaStream_t last = nullptr;
+  std::string err;
+  int launches = 0;
+  bool have_round = false;
+  int last_B = 0;
+};
+
+namespace {
+
+eagle3_status fail(eagle3_ctx* c, eagle3_status s, const std::string& msg) {
+  if (c) c->err = msg;
+  return s;
+}
+
+eagle3_status cuda_status(eagle3_ctx* c, const char* where) {
+  cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(c, EAGLE3_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+  }
+  return EAGLE3_OK;
+}
+
+int splits_for(int R, int N, int K) {
+  int tiles = cdiv(N, 64) * cdiv(R, 64);
+  int s = std::max(1, kTargetBlocks / std::max(1, tiles));
+  s = std::min(s, std::max(1, K / 256));
+  return std::min(s, 32);
+}
+
+// ---------------------------------------------------------------------------- dtype dispatch
+#define DISPATCH(c, FN, ...) \
+  do {                        \
+    if ((c)->bf)              \
+      FN<bf16>(__VA_ARGS__);  \
+    else                      \
+      FN<float>(__VA_ARGS__); \
+  } while (0)
+
+// Y[s][r][col0 + n] = X W^T over K, split S ways.
+void gemm(eagle3_ctx* c, int wid, const void* X, int ldx, const void* W, int N, int K, float* Y,
+          int ldy, int col0, int R, int S, size_t split_stride, cudaStream_t st) {
+  if (c->tc && tc_gemm(c->tc, wid, X, ldx, W, N, K, Y, ldy, col0, R, S, split_stride, st)) {
+    c->launches++;
+    return;
+  }
+  DISPATCH(c, launch_gemm_simt, X, ldx, W, K, Y, ldy, col0, R, N, K, S, split_stride, st);
+  c->launches++;
+}
+
+struct KvTarget {  // where a pass writes K/V
+  void *k, *v;
+  int slots;  // tree slots per request (0: prefix cache)
+};
+
+// fusion + input build + QKV (or KV only) + RoPE + KV write, for rp.kv_* rows.
+// hid_base rows for the input come from `g` when fuse_from != NULL.
+void kv_rows(eagle3_ctx* c, int R, const void* feats, bool has_q, const float* hid_base,
+             const eagle3_kv* kv, KvTarget tgt, cudaStream_t st) {
+  const eagle3_config& f = c->cfg;
+  const int d = f.d;
+  if (feats) {
+    int S = splits_for(R, d, 3 * d);
+    gemm(c, TCW_FC, feats, 3 * d, c->w.w_fc, d, 3 * d, c->part, d, 0, R, S, (size_t)R * d, st);
+    launch_reduce_parts(R, d, S, c->part, c->g, st);
+    c->launches++;
+    hid_base = c->g;
+  }
+  DISPATCH(c, launch_build_input, R, d, f.vocab, f.rms_eps, c->rp.kv_tok, hid_base, c->rp.kv_hid,
+           c->w.embed, c->w.g_emb, c->w.g_hid, c->x, c->flags, st);
+  c->launches++;
+  const int qd = f.n_q_heads * f.head_dim, kvd = f.n_kv_heads * f.head_dim;
+  const int ld = (has_q ? qd : 0) + 2 * kvd;
+  int S = splits_for(R, ld, 2 * d);
+  size_t ss = (size_t)R * ld;
+  int col = 0;
+  if (has_q) {
+    gemm(c, TCW_Q, c->x, 2 * d, c->w.w_q, qd, 2 * d, c->part, ld, 0, R, S, ss, st);
+    col = qd;
+  }
+  gemm(c, TCW_K, c->x, 2 * d, c->w.w_k, kvd, 2 * d, c->part, ld, col, R, S, ss, st);
+  gemm(c, TCW_V, c->x, 2 * d, c->w.w_v, kvd, 2 * d, c->part, ld, col + kvd, R, S, ss, st);
+  QkvEpi p{};
+  p.R = R;
+  p.S = S;
+  p.Hq = f.n_q_heads;
+  p.Hkv = f.n_kv_heads;
+  p.dh = f.head_dim;
+  p.has_q = has_q;
+  p.part = c->part;
+  p.rope = c->rope;
+  p.rope_rows = c->rope_rows;
+  p.row_b = c->rp.kv_b;
+  p.row_pos = c->rp.kv_pos;
+  p.row_dst = c->rp.kv_dst;
+  p.q_out = c->q;
+  p.cache_k = kv->k;
+  p.cache_v = kv->v;
+  p.page_table = f.page_size ? kv->page_table : nullptr;
+  p.page_size = f.page_size;
+  p.max_pages = kv->max_pages;
+  p.n_pages = kv->n_pages;
+  p.max_prefix = f.max_prefix;
+  p.tree_k = tgt.k;
+  p.tree_v = tgt.v;
+  p.tree_slots = tgt.slots;
+  p.flags = c->flags;
+  DISPATCH(c, launch_qkv_epilogue, p, st);
+  c->launches++;
+}
+
+void attn_splits(const eagle3_ctx* c, int B, int rows_per_req, int& kps, int& nps) {
+  const eagle3_config& f = c->cfg;
+  int blocks = B * f.n_kv_heads * attention_qgroups(rows_per_req, f.n_q_heads, f.n_kv_heads);
+  int maxp = f.max_prefix;
+  nps = std::max(1, std::min(cdiv(kTargetBlocks, blocks), cdiv(maxp, 64)));
+  kps = cdiv(cdiv(maxp, nps), 64) * 64;
+  nps = cdiv(maxp, kps);
+}
+
+// attention + O + FFN + final norm for rp.t_* rows (rows_per_req per request).
+void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, const eagle3_kv* kv,
+               KvTarget tree, void* h_base, cudaStream_t st) {
+  const eagle3_config& f = c->cfg;
+  const int d = f.d, R = B * rows_per_req;
+  const int qd = f.n_q_heads * f.head_dim;
+  AttnArgs a{};
+  a.B = B;
+  a.rows_per_req = rows_per_req;
+  a.Hq = f.n_q_heads;
+  a.Hkv = f.n_kv_heads;
+  a.dh = f.head_dim;
+  a.q = c->q;
+  a.q_row = c->rp.t_q;
+  a.n_prefix = c->n_prefix;
+  a.cache_k = kv->k;
+  a.cache_v = kv->v;
+  a.page_table = f.page_size ? kv->page_table : nullptr;
+  a.page_size = f.page_size;
+  a.max_pages = kv->max_pages;
+  a.n_pages = kv->n_pages;
+  a.max_prefix = f.max_prefix;
+  a.tree_k = tree.k;
+  a.tree_v = tree.v;
+  a.tree_slots = tree.slots;
+  a.mask = c->rp.t_mask;
+  a.mask_words = c->mask_words;
+  attn_splits(c, B, rows_per_req, a.keys_per_split, a.n_prefix_splits);
+  a.n_tree_splits = cdiv(tree.slots, 64);
+  a.o_part = c->o_part;
+  a.ml_part = c->ml_part;
+  a.out = c->o;
+  a.flags = c->flags;
+  DISPATCH(c, launch_tree_attention, a, st);
+  c->launches += 2;
+  // r = hid + W_o o ; z = rms(r)
+  int S = splits_for(R, d, qd);
+  gemm(c, TCW_O, c->o, qd, c->w.w_o, d, qd, c->part, d, 0, R, S, (size_t)R * d, st);
+  DISPATCH(c, launch_o_epilogue, R, d, S, f.rms_eps, c->part, hid_base, c->rp.t_hid, c->w.g_post,
+           c->r, c->z, st);
+  c->launches++;
+  // a = silu(W_g z) * W_u z
+  int Sf = splits_for(R, f.ffn, d);
+  float* gp = c->part;
+  float* up = c->part + (size_t)Sf * R * f.ffn;
+  gemm(c, TCW_GATE, c->z, d, c->w.w_gate, f.ffn, d, gp, f.ffn, 0, R, Sf, (size_t)R * f.ffn, st);
+  gemm(c, TCW_UP, c->z, d, c->w.w_up, f.ffn, d, up, f.ffn, 0, R, Sf, (size_t)R * f.ffn, st);
+  DISPATCH(c, launch_swiglu, R, f.ffn, Sf, gp, up, c->a, st);
+  c->launches++;
+  // s = r + W_down a ; h = rms(s)
+  int Sd = splits_for(R, d, f.ffn);
+  gemm(c, TCW_DOWN, c->a, f.ffn, c->w.w_down, d, f.ffn, c->part, d, 0, R, Sd, (size_t)R * d, st);
+  DISPATCH(c, launch_down_epilogue, R, d, Sd, f.rms_eps, c->part, c->r, c->w.g_final, c->rp.t_sdst,
+           c->S, c->rp.t_out, h_base, st);
+  c->launches++;
+}
+
+void draft_head(eagle3_ctx* c, const void* H, int R, int* tok, float* logq, float* lse,
+                cudaStream_t st) {
+  HeadParts hp = c->hp;
+  hp.R = R;
+  if (c->tc && tc_lm_head(c->tc, H, R, hp, st)) {
+    c->launches++;
+  } else {
+    DISPATCH(c, launch_lm_head_simt, H, c->w.w_lm, R, c->cfg.vocab, c->cfg.d, hp, st);
+    c->launches++;
+  }
+  launch_topk_merge(hp, tok, logq, lse, 0, st);
+  c->launches++;
+}
+
+bool kv_ok(const eagle3_ctx* c, const eagle3_kv* kv) {
+  if (!kv || !kv->k || !kv->v || !kv->seq_lens) return false;
+  if (c->cfg.page_size) {
+    if (!kv->page_table || kv->max_pages <= 0 || kv->n_pages <= 0) return false;
+  }
+  return true;
+}
+
+bool tree_ok(const eagle3_tree* t) {
+  return t && t->tokens && t->parent && t->depth && t->pos && t->pool_index && t->score && t->mask;
+}
+
+void* carve(char*& p, size_t bytes) {
+  void* r = p;
+  p += align_up(bytes, 256);
+  return r;
+}
+
+}  // namespace
+
+// ============================================================================ C ABI
+extern "C" {
+
+eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, eagle3_ctx** out) {
+  if (!cfg || !w || !out) return EAGLE3_ERR_INVALID_ARG;
+  *out = nullptr;
+  const eagle3_config& f = *cfg;
+  if (f.d <= 0 || f.d % 8 || f.n_q_heads <= 0 || f.n_kv_heads <= 0 || f.n_q_heads % f.n_kv_heads ||
+      f.head_dim <= 0 || f.head_dim % 16 || f.head_dim > 128 || f.ffn <= 0 || f.ffn % 8 ||
+      f.vocab <= 0 || f.dtype < 0 || f.dtype > 1 || f.max_batch <= 0 || f.max_prefix <= 0 ||
+      f.max_new <= 0 || f.page_size < 0 || !(f.rms_eps >= 0.f) || !(f.rope_theta > 0.f))
+    return EAGLE3_ERR_INVALID_ARG;
+  if (f.depth < 1 || f.depth > 16 || f.topk < 1 || f.topk > 16 || f.n_verify < 1 || f.n_verify > 128)
+    return EAGLE3_ERR_UNSUPPORTED;
+  const int pool_n = f.topk + (f.depth - 1) * f.topk * f.topk;
+  if (f.n_verify > pool_n) return EAGLE3_ERR_SHAPE;
+  if (f.lr_rank < 0 || (f.lr_rank > 0 && (f.lr_cand < f.topk || f.lr_cand > 128 || !w->lr_u || !w->lr_v)))
+    return EAGLE3_ERR_INVALID_ARG;
+  if (f.lr_rank > 0) return EAGLE3_ERR_UNSUPPORTED;  // two-stage head: not built yet
+  if (!w->w_fc || !w->embed || !w->w_q || !w->w_k || !w->w_v || !w->w_o || !w->w_gate || !w->w_up ||
+      !w->w_down || !w->g_emb || !w->g_hid || !w->g_post || !w->g_final || !w->w_lm)
+    return EAGLE3_ERR_INVALID_ARG;
+
+  eagle3_ctx* c = new eagle3_ctx();
+  c->cfg = f;
+  c->w = *w;
+  c->bf = f.dtype == EAGLE3_BF16;
+  c->esz = c->bf ? 2 : 4;
+  c->k = f.topk;
+  c->D = f.depth;
+  c->M = f.n_verify;
+  c->M1 = f.n_verify + 1;
+  c->pool_n = pool_n;
+  c->n_slots = (f.depth - 1) * f.topk;
+  c->slot_words = std::max(1, cdiv(c->n_slots, 32));
+  c->tree_words = cdiv(c->M1, 32);
+  c->mask_words = std::max(c->slot_words, c->tree_words);
+  const int B = f.max_batch, d = f.d, k = f.topk;
+  const int qd = f.n_q_heads * f.head_dim, kvd = f.n_kv_heads * f.head_dim;
+  c->rows_pf = std::min(kPrefillChunk, std::max(1, B * f.max_prefix));
+  c->rows_cap = std::max({c->rows_pf, B * f.max_new, B * k, B * c->M1});
+  c->rope_rows = f.max_prefix + f.depth + 1;
+
+  // partial buffer: largest S * R * N over the GEMMs this context runs
+  size_t part = 0;
+  auto need = [&](int R, int N, int K, int mult) {
+    part = std::max(part, (size_t)mult * splits_for(R, N, K) * R * N);
+  };
+  for (int R : {c->rows_pf, B * f.max_new}) {
+    need(R, d, 3 * d, 1);
+    need(R, qd + 2 * kvd, 2 * d, 1);
+  }
+  for (int R : {B, B * k, B * c->M}) {
+    need(R, qd + 2 * kvd, 2 * d, 1);
+    need(R, d, qd, 1);
+    need(R, f.ffn, d, 2);
+    need(R, d, f.ffn, 1);
+  }
+  c->part_elems = part;
+  size_t attn = 0;
+  {
+    struct P { int B, rpr, slots; };
+    for (P p : {P{B, 1, 0}, P{B, k, c->n_slots}, P{B, c->M, c->M1}}) {
+      int kps, nps;
+      attn_splits(c, p.B, p.rpr, kps, nps);
+      attn = std::max(attn, (size_t)(nps + cdiv(p.slots, 64)) * p.B * p.rpr * qd);
+    }
+  }
+  c->attn_elems = attn;
+  const int lm_parts = lm_head_simt_parts(f.vocab);
+  c->n_vparts = verify_head_simt_parts(f.vocab);
+  const int Rlm = B * k, Rv = B * c->M1;
+  const int n_state = B * (1 + c->n_slots);
+
+  // sizes
+  std::vector<std::pair<void**, size_t>> plan;
+  auto add = [&](void** p, size_t bytes) { plan.emplace_back(p, bytes); };
+  add((void**)&c->g, (size_t)std::max(c->rows_pf, B * f.max_new) * d * 4);
+  add(&c->x, (size_t)c->rows_cap * 2 * d * c->esz);
+  add((void**)&c->part, c->part_elems * 4);
+  add((void**)&c->q, (size_t)c->rows_cap * qd * 4);
+  add(&c->tk, (size_t)B * std::max(1, c->n_slots) * kvd * c->esz);
+  add(&c->tv, (size_t)B * std::max(1, c->n_slots) * kvd * c->esz);
+  add(&c->vk, (size_t)B * c->M1 * kvd * c->esz);
+  add(&c->vv, (size_t)B * c->M1 * kvd * c->esz);
+  add((void**)&c->o_part, c->attn_elems * 4);
+  add((void**)&c->ml_part, c->attn_elems / f.head_dim * 2 * 4);
+  add(&c->o, (size_t)c->rows_cap * qd * c->esz);
+  add((void**)&c->r, (size_t)c->rows_cap * d * 4);
+  add(&c->z, (size_t)c->rows_cap * d * c->esz);
+  add(&c->a, (size_t)c->rows_cap * f.ffn * c->esz);
+  add((void**)&c->S, (size_t)n_state * d * 4);
+  add(&c->h, (size_t)Rlm * d * c->esz);
+  add(&c->h_root, (size_t)B * d * c->esz);
+  add(&c->h_ver, (size_t)Rv * d * c->esz);
+  add((void**)&c->rope, (size_t)c->rope_rows * (f.head_dim / 2) * sizeof(float2));
+  int* rp_int[10] = {};
+  for (int i = 0; i < 10; ++i) add((void**)&rp_int[i], (size_t)c->rows_cap * 4);
+  add((void**)&c->rp.t_mask, (size_t)c->rows_cap * c->mask_words * 4);
+  add((void**)&c->n_prefix, (size_t)B * 4);
+  add((void**)&c->root_tok, (size_t)B * 4);
+  add((void**)&c->root_pos, (size_t)B * 4);
+  add((void**)&c->hp.ms, (size_t)lm_parts * Rlm * 2 * 4);
+  add((void**)&c->hp.val, (size_t)lm_parts * Rlm * k * 4);
+  add((void**)&c->hp.idx, (size_t)lm_parts * Rlm * k * 4);
+  add((void**)&c->top_tok, (size_t)Rlm * k * 4);
+  add((void**)&c->top_logq, (size_t)Rlm * k * 4);
+  add((void**)&c->top_lse, (size_t)Rlm * 4);
+  add((void**)&c->pool.tok, (size_t)B * pool_n * 4);
+  add((void**)&c->pool.parent, (size_t)B * pool_n * 4);
+  add((void**)&c->pool.depth, (size_t)B * pool_n * 4);
+  add((void**)&c->pool.fwd, (size_t)B * pool_n * 4);
+  add((void**)&c->pool.score, (size_t)B * pool_n * 4);
+  add((void**)&c->pool.logq, (size_t)B * pool_n * 4);
+  add((void**)&c->frontier, (size_t)B * k * 4);
+  add((void**)&c->slot_mask, (size_t)B * std::max(1, c->n_slots) * c->slot_words * 4);
+  add((void**)&c->child_tok, (size_t)Rv * k * 4);
+  add((void**)&c->child_node, (size_t)Rv * k * 4);
+  add((void**)&c->n_child, (size_t)Rv * 4);
+  add((void**)&c->child_z, (size_t)Rv * k * 4);
+  add((void**)&c->vpart, (size_t)c->n_vparts * Rv * 6 * 4);
+  add((void**)&c->z_max, (size_t)Rv * 4);
+  add((void**)&c->z_arg, (size_t)Rv * 4);
+  add((void**)&c->lse, (size_t)Rv * 4);
+  add((void**)&c->g_arg, (size_t)Rv * 4);
+  add((void**)&c->g_max, (size_t)Rv * 4);
+  add((void**)&c->flags, 64);
+  size_t total = 0;
+  for (auto& p : plan) total += align_up(p.second, 256);
+  if (cudaMalloc(&c->arena, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return EAGLE3_ERR_OOM;
+  }
+  c->arena_bytes = total;
+  char* p = c->arena;
+  for (auto& e : plan) *e.first = carve(p, e.second);
+  c->rp.kv_b = rp_int[0];
+  c->rp.kv_tok = rp_int[1];
+  c->rp.kv_hid = rp_int[2];
+  c->rp.kv_pos = rp_int[3];
+  c->rp.kv_dst = rp_int[4];
+  c->rp.t_q = rp_int[5];
+  c->rp.t_b = rp_int[6];
+  c->rp.t_hid = rp_int[7];
+  c->rp.t_sdst = rp_int[8];
+  c->rp.t_out = rp_int[9];
+  c->rp.mask_words = c->mask_words;
+  c->hp.n_parts = lm_parts;
+  c->hp.k = k;
+  c->pool.n = pool_n;
+
+  // RoPE table, rotate-half pairs: angle = pos * theta^(-2j/dh) in double
+  {
+    const int half = f.head_dim / 2;
+    std::vector<float2> tab((size_t)c->rope_rows * half);
+    for (int pos = 0; pos < c->rope_rows; ++pos)
+      for (int j = 0; j < half; ++j) {
+        double inv = std::pow((double)f.rope_theta, -2.0 * j / f.head_dim);
+        double ang = pos * inv;
+        tab[(size_t)pos * half + j] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    if (cudaMemset(c->arena, 0, total) != cudaSuccess ||
+        cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(c->arena);
+      delete c;
+      return EAGLE3_ERR_CUDA;
+    }
+  }
+  if (c->bf) c->tc = tc_create(c->cfg, c->w, c);
+  *out = c;
+  return EAGLE3_OK;
+}
+
+void eagle3_destroy(eagle3_ctx* c) {
+  if (!c) return;
+  if (c->tc) tc_destroy(c->tc);
+  if (c->arena) cudaFree(c->arena);
+  delete c;
+}
+
+eagle3_status eagle3_prefill(eagle3_ctx* c, int B, int total_rows, const int* cu_rows,
+                             const void* feats, const int* tokens, const eagle3_kv* kv,
+                             eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  if (B < 1 || B > c->cfg.max_batch) return fail(c, EAGLE3_ERR_SHAPE, "B out of range");
+  if (total_rows < 0) return fail(c, EAGLE3_ERR_SHAPE, "total_rows < 0");
+  if (total_rows > 0 && (!cu_rows || !feats || !tokens))
+    return fail(c, EAGLE3_ERR_INVALID_ARG, "null input");
+  if (!kv_ok(c, kv)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad kv descriptor");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last = st;
+  const int d = c->cfg.d;
+  for (int r0 = 0; r0 < total_rows; r0 += c->rows_pf) {
+    int R = std::min(c->rows_pf, total_rows - r0);
+    launch_plan_prefill(R, r0, B, cu_rows, tokens, kv->seq_lens, c->rp, st);
+    c->launches++;
+    const char* f = (const char*)feats + (size_t)r0 * 3 * d * c->esz;
+    kv_rows(c, R, f, false, nullptr, kv, KvTarget{nullptr, nullptr, 0}, st);
+  }
+  return cuda_status(c, "prefill");
+}
+
+eagle3_status eagle3_draft_round(eagle3_ctx* c, int B, int n_new, const void* feats_new,
+                                 const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
+                                 eagle3_pool* pool_out, eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  if (B < 1 || B > c->cfg.max_batch) return fail(c, EAGLE3_ERR_SHAPE, "B out of range");
+  if (n_new < 1 || n_new > c->cfg.max_new) return fail(c, EAGLE3_ERR_SHAPE, "n_new out of range");
+  if (!feats_new || !tokens_new) return fail(c, EAGLE3_ERR_INVALID_ARG, "null input");
+  if (!kv_ok(c, kv)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad kv descriptor");
+  if (!tree_ok(out)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad tree output");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last = st;
+  const int k = c->k, D = c->D;
+  // pass 0: the new rows' K/V, then the root row through the whole layer
+  launch_plan_root(B, n_new, tokens_new, kv->seq_lens, c->n_slots, c->rp, c->root_tok, c->root_pos,
+                   c->n_prefix, st);
+  c->launches++;
+  kv_rows(c, B * n_new, feats_new, true, nullptr, kv, KvTarget{nullptr, nullptr, 0}, st);
+  tail_rows(c, B, 1, c->g, kv, KvTarget{nullptr, nullptr, 0}, c->h_root, st);
+  draft_head(c, c->h_root, B, c->top_tok, c->top_logq, c->top_lse, st);
+  launch_expand(B, 0, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
+                c->slot_words, c->root_pos, c->n_slots, c->rp, st);
+  c->launches++;
+  // passes 1..D-1: the frontier of each depth with the parent's state as hid
+  KvTarget tree{c->tk, c->tv, c->n_slots};
+  for (int t = 1; t < D; ++t) {
+    kv_rows(c, B * k, nullptr, true, c->S, kv, tree, st);
+    tail_rows(c, B, k, c->S, kv, tree, c->h, st);
+    draft_head(c, c->h, B * k, c->top_tok, c->top_logq, c->top_lse, st);
+    launch_expand(B, t, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
+                  c->slot_words, c->root_pos, c->n_slots, c->rp, st);
+    c->launches++;
+  }
+  launch_build_tree(B, c->pool_n, c->M, c->pool.tok, c->pool.parent, c->pool.score, c->pool.depth,
+                    c->root_tok, c->root_pos, out->tokens, out->parent, out->depth, out->pos,
+                    out->pool_index, out->score, out->mask, c->flags, st);
+  c->launches++;
+  if (pool_out) {
+    launch_copy_pool(B, c->pool, pool_out->tok, pool_out->parent, pool_out->depth, pool_out->fwd,
+                     pool_out->score, pool_out->logq, st);
+    c->launches++;
+  }
+  eagle3_status s = cuda_status(c, "draft_round");
+  if (s == EAGLE3_OK) {
+    c->have_round = true;
+    c->last_B = B;
+  }
+  return s;
+}
+
+eagle3_status eagle3_build_tree(eagle3_ctx* c, int B, int pool_n, const int* pool_tok,
+                                const int* pool_parent, const float* pool_score,
+                                const int* pool_depth, const int* root_tok, const int* root_pos,
+                                eagle3_tree* out, eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  if (B < 1 || B > c->cfg.max_batch) return fail(c, EAGLE3_ERR_SHAPE, "B out of range");
+  if (pool_n < c->M || pool_n > 4096) return fail(c, EAGLE3_ERR_SHAPE, "pool_n must be in [M, 4096]");
+  if (!pool_tok || !pool_parent || !pool_score || !pool_depth || !root_tok || !root_pos)
+    return fail(c, EAGLE3_ERR_INVALID_ARG, "null input");
+  if (!tree_ok(out)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad tree output");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last = st;
+  launch_build_tree(B, pool_n, c->M, pool_tok, pool_parent, pool_score, pool_depth, root_tok,
+                    root_pos, out->tokens, out->parent, out->depth, out->pos, out->pool_index,
+                    out->score, out->mask, c->flags, st);
+  c->launches++;
+  return cuda_status(c, "build_tree");
+}
+
+eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const eagle3_kv* kv,
+                            int mode, float temperature, unsigned long long seed,
+                            unsigned long long round_id, int* accept_len, int* path,
+                            int* out_tokens, eagle3_verify_stats* stats, eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  if (!c->have_round) return fail(c, EAGLE3_ERR_STATE, "verify needs a draft round on this context");
+  if (B != c->last_B) return fail(c, EAGLE3_ERR_SHAPE, "B differs from the last draft round");
+  if (mode != 0 && mode != 1) return fail(c, EAGLE3_ERR_INVALID_ARG, "mode must be 0 or 1");
+  if (mode == 1 && !(temperature > 0.f)) return fail(c, EAGLE3_ERR_INVALID_ARG, "temperature must be > 0");
+  if (!c->w.w_target) return fail(c, EAGLE3_ERR_INVALID_ARG, "no target head in the weights");
+  if (!tree_ok((eagle3_tree*)tree) || !accept_len || !path || !out_tokens)
+    return fail(c, EAGLE3_ERR_INVALID_ARG, "null output");
+  if (!kv_ok(c, kv)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad kv descriptor");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last = st;
+  const eagle3_config& f = c->cfg;
+  const int M = c->M, M1 = c->M1, k = c->k, d = f.d;
+  launch_plan_verify(B, M, k, tree->tokens, tree->parent, tree->pos, tree->pool_index, tree->mask,
+                     c->pool.fwd, c->pool_n, c->n_slots, c->rp, c->n_prefix, c->child_tok,
+                     c->child_node, c->n_child, c->flags, st);
+  c->launches++;
+  launch_copy_rows(B, d, c->esz, c->h_root, 1, c->h_ver, M1, st);
+  c->launches++;
+  KvTarget vt{c->vk, c->vv, M1};
+  kv_rows(c, B * M, nullptr, true, c->S, kv, vt, st);
+  tail_rows(c, B, M, c->S, kv, vt, c->h_ver, st);
+  VerifyHeadArgs va{};
+  va.R = B * M1;
+  va.V = f.vocab;
+  va.d = d;
+  va.M1 = M1;
+  va.kmax = k;
+  va.sampling = mode == 1;
+  va.inv_t = mode == 1 ? 1.f / temperature : 1.f;
+  va.seed = seed;
+  va.round_id = round_id;
+  va.child_tok = c->child_tok;
+  va.child_z = c->child_z;
+  va.n_parts = c->n_vparts;
+  va.part = c->vpart;
+  if (c->tc && tc_verify_head(c->tc, c->h_ver, va, st)) {
+    c->launches++;
+  } else {
+    DISPATCH(c, launch_verify_head_simt, c->h_ver, c->w.w_target, va, st);
+    c->launches++;
+  }
+  launch_verify_merge(va, c->z_max, c->z_arg, c->lse, c->g_arg, c->g_max, st);
+  c->launches++;
+  WalkArgs wa{};
+  wa.B = B;
+  wa.M1 = M1;
+  wa.kmax = k;
+  wa.D = c->D;
+  wa.sampling = mode == 1;
+  wa.inv_t = va.inv_t;
+  wa.seed = seed;
+  wa.round_id = round_id;
+  wa.t_tok = tree->tokens;
+  wa.child_node = c->child_node;
+  wa.n_child = c->n_child;
+  wa.child_z = c->child_z;
+  wa.lse = c->lse;
+  wa.z_arg = c->z_arg;
+  wa.g_arg = c->g_arg;
+  wa.accept_len = accept_len;
+  wa.path = path;
+  wa.out_tokens = out_tokens;
+  launch_walk(wa, st);
+  c->launches++;
+  if (stats) {
+    size_t n = (size_t)B * M1;
+    if (stats->z_max) cudaMemcpyAsync(stats->z_max, c->z_max, n * 4, cudaMemcpyDeviceToDevice, st);
+    if (stats->lse) cudaMemcpyAsync(stats->lse, c->lse, n * 4, cudaMemcpyDeviceToDevice, st);
+    if (stats->z_argmax) cudaMemcpyAsync(stats->z_argmax, c->z_arg, n * 4, cudaMemcpyDeviceToDevice, st);
+    if (stats->g_argmax) cudaMemcpyAsync(stats->g_argmax, c->g_arg, n * 4, cudaMemcpyDeviceToDevice, st);
+  }
+  return cuda_status(c, "verify");
+}
+
+eagle3_status eagle3_lm_head_topk(eagle3_ctx* c, int R, const void* h, int* tok, float* logq,
+                                  float* lse, eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  if (R < 1 || R > c->cfg.max_batch * c->k) return fail(c, EAGLE3_ERR_SHAPE, "R out of range");
+  if (!h || !tok || !logq) return fail(c, EAGLE3_ERR_INVALID_ARG, "null pointer");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last = st;
+  draft_head(c, h, R, tok, logq, lse, st);
+  return cuda_status(c, "lm_head_topk");
+}
+
+eagle3_status eagle3_check(eagle3_ctx* c) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(c->last);
+  if (e != cudaSuccess) return fail(c, EAGLE3_ERR_CUDA, std::string("sync: ") + cudaGetErrorString(e));
+  int flags = 0;
+  e = cudaMemcpy(&flags, c->flags, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(c, EAGLE3_ERR_CUDA, std::string("flag read: ") + cudaGetErrorString(e));
+  if (!flags) return EAGLE3_OK;
+  cudaMemset(c->flags, 0, sizeof(int));
+  std::string m = "device check failed:";
+  if (flags & FLAG_TREE_NOT_CLOSED) m += " kept set not ancestor-closed;";
+  if (flags & FLAG_PAGE_RANGE) m += " page index out of range;";
+  if (flags & FLAG_TOKEN_RANGE) m += " token id out of range;";
+  if (flags & FLAG_POS_RANGE) m += " position beyond cache capacity;";
+  if (flags & FLAG_TIMEOUT) {
+    m += " bounded wait timed out;";
+    return fail(c, EAGLE3_ERR_TIMEOUT, m);
+  }
+  return fail(c, EAGLE3_ERR_DEVICE_ASSERT, m);
+}
+
+const char* eagle3_last_error(const eagle3_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+size_t eagle3_workspace_bytes(const eagle3_ctx* c) { return c ? c->arena_bytes : 0; }
+
+int eagle3_last_launch_count(const eagle3_ctx* c) { return c ? c->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Shared device helpers of the CUDA path: element loads/stores for the two
+// storage types, warp reductions, the device error flag.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace e3 {
+
+typedef __nv_bfloat16 bf16;
+
+// device error flag bits (or-ed into ctx->d_flags[0])
+enum : int {
+  FLAG_TREE_NOT_CLOSED = 1,   // kept set of a supplied pool is not ancestor-closed
+  FLAG_PAGE_RANGE = 2,        // page table entry outside [0, n_pages)
+  FLAG_TOKEN_RANGE = 4,       // token id outside [0, V)
+  FLAG_POS_RANGE = 8,         // row position beyond the cache capacity
+  FLAG_TIMEOUT = 16,          // a bounded wait gave up
+};
+
+template <typename T> __device__ __forceinline__ float ldf(const T* p);
+template <> __device__ __forceinline__ float ldf<float>(const float* p) { return *p; }
+template <> __device__ __forceinline__ float ldf<bf16>(const bf16* p) { return __bfloat162float(*p); }
+
+template <typename T> __device__ __forceinline__ void stf(T* p, float v);
+template <> __device__ __forceinline__ void stf<float>(float* p, float v) { *p = v; }
+template <> __device__ __forceinline__ void stf<bf16>(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// (value desc, index asc) total order used by every top-k and argmax.
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Warp-wide best (value, index) under `better`; result in every lane.
+__device__ __forceinline__ void warp_best(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+}
+
+// Block-wide sum of a float for blockDim.x <= 1024; `red` holds >= 32 floats.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float t = (threadIdx.x < nw) ? red[threadIdx.x] : 0.f;
+  if (wid == 0) t = warp_sum(t);
+  if (threadIdx.x == 0) red[0] = t;
+  __syncthreads();
+  float r = red[0];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ void raise_flag(int* flags, int bit) { atomicOr(flags, bit); }
+
+}  // namespace e3

@@ -1,0 +1,264 @@
+// Decoder-layer kernels around the GEMMs of the one-layer EAGLE-3 drafter.
+//
+// "EAGLE-3 精读" §1 (paragraph 2): the decoder combines the fused target
+// feature g (or, along draft paths, its own state: §2 Training-Time Test) with
+// the token embedding.  This build reads that as x = [rms(E[y]); rms(hid)],
+// followed by one pre-norm Llama-style layer:
+//   q, k, v = W_q x, W_k x, W_v x   (rotate-half RoPE on q, k)
+//   r = hid + W_o attn(q, K, V);  z = rms(r)
+//   s = r + W_down(silu(W_gate z) * W_up z);  h = rms(s)
+// Every GEMM writes fp32 split-K partials [S][R][N]; the kernels here sum the
+// partials and apply the element-wise parts.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace e3 {
+
+// ----------------------------------------------------------------------------- x = [rms(E[y]); rms(hid)]
+template <typename T>
+__global__ void build_input_kernel(int R, int d, int V, float eps, const int* __restrict__ tok,
+                                   const float* __restrict__ hid_base, const int* __restrict__ hid_row,
+                                   const T* __restrict__ E, const T* __restrict__ g_emb,
+                                   const T* __restrict__ g_hid, T* __restrict__ x, int* flags) {
+  __shared__ float red[32];
+  int r = blockIdx.x;
+  int t = tok[r];
+  if (t < 0 || t >= V) {
+    if (threadIdx.x == 0) raise_flag(flags, FLAG_TOKEN_RANGE);
+    t = t < 0 ? 0 : V - 1;
+  }
+  const T* e = E + (size_t)t * d;
+  const float* h = hid_base + (size_t)hid_row[r] * d;
+  float se = 0.f, sh = 0.f;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    float a = ldf(e + j), b = h[j];
+    se += a * a;
+    sh += b * b;
+  }
+  se = block_sum(se, red);
+  sh = block_sum(sh, red);
+  float ie = rsqrtf(se / d + eps), ih = rsqrtf(sh / d + eps);
+  T* xr = x + (size_t)r * 2 * d;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    stf(xr + j, ldf(e + j) * ie * ldf(g_emb + j));
+    stf(xr + d + j, h[j] * ih * ldf(g_hid + j));
+  }
+}
+
+// ----------------------------------------------------------------------------- split-K sum
+__device__ __forceinline__ float sum_parts(const float* p, size_t stride, int S) {
+  float v = p[0];
+  for (int s = 1; s < S; ++s) v += p[(size_t)s * stride];
+  return v;
+}
+
+// g = sum of fusion partials (fp32 [R, d])
+__global__ void reduce_parts_kernel(int R, int N, int S, const float* __restrict__ part,
+                                    float* __restrict__ out) {
+  size_t n = (size_t)R * N;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    out[i] = sum_parts(part + i, n, S);
+}
+
+// ----------------------------------------------------------------------------- RoPE + KV write
+// One thread per rotate-half pair (j, j + dh/2) of one head.  Heads are laid
+// out [q heads | k heads | v heads] in the partials when has_q, else [k | v].
+template <typename T>
+__global__ void qkv_epilogue_kernel(QkvEpi p) {
+  int r = blockIdx.y;
+  int half = p.dh / 2;
+  int nh = (p.has_q ? p.Hq : 0) + 2 * p.Hkv;
+  int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= nh * half) return;
+  int hh = idx / half, j = idx % half;
+  int ld = nh * p.dh;
+  size_t stride = (size_t)p.R * ld;
+  const float* base = p.part + (size_t)r * ld + (size_t)hh * p.dh;
+  float x1 = sum_parts(base + j, stride, p.S);
+  float x2 = sum_parts(base + j + half, stride, p.S);
+  int pos = p.row_pos[r];
+  if (pos < 0 || pos >= p.rope_rows) {
+    if (idx == 0) raise_flag(p.flags, FLAG_POS_RANGE);
+    return;
+  }
+  int qh = p.has_q ? p.Hq : 0;
+  if (hh < qh + p.Hkv) {  // q or k head: rotate
+    float2 cs = p.rope[(size_t)pos * half + j];
+    float y1 = x1 * cs.x - x2 * cs.y;
+    float y2 = x2 * cs.x + x1 * cs.y;
+    x1 = y1;
+    x2 = y2;
+  }
+  if (hh < qh) {
+    float* q = p.q_out + (size_t)r * p.Hq * p.dh + (size_t)hh * p.dh;
+    q[j] = x1;
+    q[j + half] = x2;
+    return;
+  }
+  bool is_v = hh >= qh + p.Hkv;
+  int kvh = is_v ? hh - qh - p.Hkv : hh - qh;
+  int b = p.row_b[r];
+  int dst = p.row_dst[r];
+  T* out;
+  if (dst >= 0) {  // tree scratch slot of this request
+    size_t off = (((size_t)b * p.tree_slots + dst) * p.Hkv + kvh) * p.dh;
+    out = (T*)(is_v ? p.tree_v : p.tree_k) + off;
+  } else {  // prefix cache at `pos`
+    size_t row;
+    if (p.page_table) {
+      int lp = pos / p.page_size;
+      if (lp >= p.max_pages) {
+        if (j == 0) raise_flag(p.flags, FLAG_POS_RANGE);
+        return;
+      }
+      int pg = p.page_table[(size_t)b * p.max_pages + lp];
+      if (pg < 0 || pg >= p.n_pages) {
+        if (j == 0) raise_flag(p.flags, FLAG_PAGE_RANGE);
+        return;
+      }
+      row = (size_t)pg * p.page_size + pos % p.page_size;
+    } else {
+      if (pos >= p.max_prefix) {
+        if (j == 0) raise_flag(p.flags, FLAG_POS_RANGE);
+        return;
+      }
+      row = (size_t)b * p.max_prefix + pos;
+    }
+    out = (T*)(is_v ? p.cache_v : p.cache_k) + (row * p.Hkv + kvh) * p.dh;
+  }
+  stf(out + j, x1);
+  stf(out + j + half, x2);
+}
+
+// ----------------------------------------------------------------------------- r = hid + W_o o;  z = rms(r)
+template <typename T>
+__global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* __restrict__ part,
+                                  const float* __restrict__ hid_base, const int* __restrict__ hid_row,
+                                  const T* __restrict__ g_post, float* __restrict__ r_out,
+                                  T* __restrict__ z_out) {
+  __shared__ float red[32];
+  int r = blockIdx.x;
+  const float* h = hid_base + (size_t)hid_row[r] * d;
+  size_t stride = (size_t)R * d;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    float v = h[j] + sum_parts(part + (size_t)r * d + j, stride, S);
+    r_out[(size_t)r * d + j] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  float inv = rsqrtf(ss / d + eps);
+  for (int j = threadIdx.x; j < d; j += blockDim.x)
+    stf(z_out + (size_t)r * d + j, r_out[(size_t)r * d + j] * inv * ldf(g_post + j));
+}
+
+// ----------------------------------------------------------------------------- a = silu(W_g z) * (W_u z)
+template <typename T>
+__global__ void swiglu_kernel(int R, int F, int S, const float* __restrict__ gate_part,
+                              const float* __restrict__ up_part, T* __restrict__ a) {
+  size_t n = (size_t)R * F;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    float g = sum_parts(gate_part + i, n, S);
+    float u = sum_parts(up_part + i, n, S);
+    stf(a + i, g / (1.f + expf(-g)) * u);
+  }
+}
+
+// ----------------------------------------------------------------------------- s = r + W_down a;  h = rms(s)
+template <typename T>
+__global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float* __restrict__ part,
+                                     const float* __restrict__ r_in, const T* __restrict__ g_final,
+                                     const int* __restrict__ s_dst, float* __restrict__ s_base,
+                                     const int* __restrict__ h_dst, T* __restrict__ h_base) {
+  __shared__ float red[32];
+  extern __shared__ float srow[];
+  int r = blockIdx.x;
+  size_t stride = (size_t)R * d;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    float v = r_in[(size_t)r * d + j] + sum_parts(part + (size_t)r * d + j, stride, S);
+    srow[j] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  float inv = rsqrtf(ss / d + eps);
+  int sd = s_dst ? s_dst[r] : -1;
+  int hd = h_dst ? h_dst[r] : r;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    if (sd >= 0) s_base[(size_t)sd * d + j] = srow[j];
+    stf(h_base + (size_t)hd * d + j, srow[j] * inv * ldf(g_final + j));
+  }
+}
+
+// ----------------------------------------------------------------------------- host launchers
+template <typename T>
+void launch_build_input(int R, int d, int V, float eps, const int* tok, const float* hid_base,
+                        const int* hid_row, const void* E, const void* g_emb, const void* g_hid,
+                        void* x, int* flags, cudaStream_t st) {
+  if (R <= 0) return;
+  build_input_kernel<T><<<R, 256, 0, st>>>(R, d, V, eps, tok, hid_base, hid_row, (const T*)E,
+                                           (const T*)g_emb, (const T*)g_hid, (T*)x, flags);
+}
+
+void launch_reduce_parts(int R, int N, int S, const float* part, float* out, cudaStream_t st) {
+  size_t n = (size_t)R * N;
+  if (!n) return;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 148 * 8) blocks = 148 * 8;
+  reduce_parts_kernel<<<blocks, 256, 0, st>>>(R, N, S, part, out);
+}
+
+template <typename T>
+void launch_qkv_epilogue(const QkvEpi& p, cudaStream_t st) {
+  if (p.R <= 0) return;
+  int nh = (p.has_q ? p.Hq : 0) + 2 * p.Hkv;
+  int pairs = nh * p.dh / 2;
+  dim3 grid((pairs + 255) / 256, p.R);
+  qkv_epilogue_kernel<T><<<grid, 256, 0, st>>>(p);
+}
+
+template <typename T>
+void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const float* hid_base,
+                       const int* hid_row, const void* g_post, float* r_out, void* z_out,
+                       cudaStream_t st) {
+  if (R <= 0) return;
+  o_epilogue_kernel<T><<<R, 256, 0, st>>>(R, d, S, eps, part, hid_base, hid_row, (const T*)g_post,
+                                          r_out, (T*)z_out);
+}
+
+template <typename T>
+void launch_swiglu(int R, int F, int S, const float* gate_part, const float* up_part, void* a,
+                   cudaStream_t st) {
+  size_t n = (size_t)R * F;
+  if (!n) return;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 148 * 16) blocks = 148 * 16;
+  swiglu_kernel<T><<<blocks, 256, 0, st>>>(R, F, S, gate_part, up_part, (T*)a);
+}
+
+template <typename T>
+void launch_down_epilogue(int R, int d, int S, float eps, const float* part, const float* r_in,
+                          const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
+                          void* h_base, cudaStream_t st) {
+  if (R <= 0) return;
+  down_epilogue_kernel<T><<<R, 256, d * sizeof(float), st>>>(R, d, S, eps, part, r_in,
+                                                            (const T*)g_final, s_dst, s_base, h_dst,
+                                                            (T*)h_base);
+}
+
+#define E3_INST(T)                                                                                   \
+  template void launch_build_input<T>(int, int, int, float, const int*, const float*, const int*,   \
+                                      const void*, const void*, const void*, void*, int*,           \
+                                      cudaStream_t);                                                 \
+  template void launch_qkv_epilogue<T>(const QkvEpi&, cudaStream_t);                                 \
+  template void launch_o_epilogue<T>(int, int, int, float, const float*, const float*, const int*,  \
+                                     const void*, float*, void*, cudaStream_t);                      \
+  template void launch_swiglu<T>(int, int, int, const float*, const float*, void*, cudaStream_t);    \
+  template void launch_down_epilogue<T>(int, int, int, float, const float*, const float*,           \
+                                        const void*, const int*, float*, const int*, void*,         \
+                                        cudaStream_t);
+E3_INST(float)
+E3_INST(bf16)
+#undef E3_INST
+
+}  // namespace e3

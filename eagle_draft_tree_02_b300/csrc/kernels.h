@@ -1,0 +1,152 @@
+// Internal launch interface of the CUDA path (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace e3 {
+
+// ----------------------------------------------------------------------------- decoder.cu
+struct QkvEpi {
+  int R, S, Hq, Hkv, dh, has_q;
+  const float* part;        // [S][R][(has_q*Hq + 2Hkv) dh]
+  const float2* rope;       // [rope_rows][dh/2] (cos, sin)
+  int rope_rows;
+  const int *row_b, *row_pos, *row_dst;
+  float* q_out;             // [R][Hq dh]
+  void *cache_k, *cache_v;  // prefix cache
+  const int* page_table;    // NULL = contiguous
+  int page_size, max_pages, n_pages, max_prefix;
+  void *tree_k, *tree_v;    // tree scratch [B][tree_slots][Hkv][dh]
+  int tree_slots;
+  int* flags;
+};
+
+template <typename T>
+void launch_build_input(int R, int d, int V, float eps, const int* tok, const float* hid_base,
+                        const int* hid_row, const void* E, const void* g_emb, const void* g_hid,
+                        void* x, int* flags, cudaStream_t st);
+void launch_reduce_parts(int R, int N, int S, const float* part, float* out, cudaStream_t st);
+template <typename T> void launch_qkv_epilogue(const QkvEpi& p, cudaStream_t st);
+template <typename T>
+void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const float* hid_base,
+                       const int* hid_row, const void* g_post, float* r_out, void* z_out,
+                       cudaStream_t st);
+template <typename T>
+void launch_swiglu(int R, int F, int S, const float* gate_part, const float* up_part, void* a,
+                   cudaStream_t st);
+template <typename T>
+void launch_down_epilogue(int R, int d, int S, float eps, const float* part, const float* r_in,
+                          const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
+                          void* h_base, cudaStream_t st);
+
+// ----------------------------------------------------------------------------- gemm_simt.cu
+// Y[s][r][col0 + n] = sum_{k in split s} X[r][k] W[n][k]  (fp32 accumulate)
+template <typename T>
+void launch_gemm_simt(const void* X, int ldx, const void* W, int ldw, float* Y, int ldy, int col0,
+                      int R, int N, int K, int S, size_t split_stride, cudaStream_t st);
+
+// ----------------------------------------------------------------------------- attention.cu
+struct AttnArgs {
+  int B, rows_per_req, Hq, Hkv, dh;
+  const float* q;          // [*, Hq dh] fp32, row via q_row
+  const int* q_row;        // [R] row of q for tail row r
+  const int* n_prefix;     // [B] prefix keys 0..n_prefix-1
+  const void *cache_k, *cache_v;
+  const int* page_table;
+  int page_size, max_pages, n_pages, max_prefix;
+  const void *tree_k, *tree_v;  // [B][tree_slots][Hkv][dh]
+  int tree_slots;
+  const uint32_t* mask;    // [R][mask_words] bits over tree slots
+  int mask_words;
+  int keys_per_split, n_prefix_splits, n_tree_splits;
+  float* o_part;           // [n_splits][R][Hq][dh]
+  float* ml_part;          // [n_splits][R][Hq][2]
+  void* out;               // [R][Hq dh] storage type
+  int* flags;
+};
+template <typename T> void launch_tree_attention(const AttnArgs& a, cudaStream_t st);
+int attention_qgroups(int rows_per_req, int Hq, int Hkv);
+
+// ----------------------------------------------------------------------------- lmhead.cu
+struct HeadParts {
+  int n_parts, R, k;
+  float* ms;     // [n_parts][R][2]    running max, sum exp
+  float* val;    // [n_parts][R][k]
+  int* idx;      // [n_parts][R][k]
+};
+template <typename T>
+void launch_lm_head_simt(const void* H, const void* W, int R, int V, int d, const HeadParts& hp,
+                         cudaStream_t st);
+int lm_head_simt_parts(int V);
+void launch_topk_merge(const HeadParts& hp, int* tok, float* logq, float* lse, int row_stride_tok,
+                       cudaStream_t st);
+
+struct VerifyHeadArgs {
+  int R, V, d, M1, kmax;     // rows = B*(M+1); M1 = M+1
+  float inv_t;               // 1/T (1 when greedy)
+  int sampling;
+  unsigned long long seed, round_id;
+  const int* child_tok;      // [R][kmax] (-1 padded)
+  float* child_z;            // [R][kmax]  target logit at each child token
+  int n_parts;
+  float* part;               // [n_parts][R][6]
+};
+template <typename T>
+void launch_verify_head_simt(const void* H, const void* W, const VerifyHeadArgs& a, cudaStream_t st);
+int verify_head_simt_parts(int V);
+void launch_verify_merge(const VerifyHeadArgs& a, float* z_max, int* z_arg, float* lse, int* g_arg,
+                         float* g_max, cudaStream_t st);
+
+// ----------------------------------------------------------------------------- tree.cu
+struct RowPlan {
+  // rows whose K/V are produced (input build + QKV)
+  int *kv_b, *kv_tok, *kv_hid, *kv_pos, *kv_dst;
+  // rows that run attention and the rest of the layer
+  int *t_q, *t_b, *t_hid, *t_sdst, *t_out;
+  uint32_t* t_mask;
+  int mask_words;
+};
+struct PoolDev {
+  int *tok, *parent, *depth, *fwd;
+  float *score, *logq;
+  int n;  // pool_n
+};
+void launch_plan_root(int B, int n_new, const int* tokens_new, const int* seq_lens, int n_slots,
+                      const RowPlan& rp, int* root_tok, int* root_pos, int* n_prefix, cudaStream_t st);
+void launch_plan_prefill(int rows, int r0, int B, const int* cu_rows, const int* tokens,
+                         const int* seq_lens, const RowPlan& rp, cudaStream_t st);
+void launch_expand(int B, int t, int k, int D, const int* top_tok, const float* top_logq,
+                   const PoolDev& pool, int* frontier, uint32_t* slot_mask, int slot_words,
+                   const int* root_pos, int n_slots, const RowPlan& rp, cudaStream_t st);
+void launch_build_tree(int B, int pool_n, int M, const int* tok, const int* parent,
+                       const float* score, const int* depth, const int* root_tok,
+                       const int* root_pos, int* t_tok, int* t_parent, int* t_depth, int* t_pos,
+                       int* t_pidx, float* t_score, uint32_t* t_mask, int* flags, cudaStream_t st);
+void launch_plan_verify(int B, int M, int kmax, const int* t_tok, const int* t_parent,
+                        const int* t_pos, const int* t_pidx, const uint32_t* t_mask,
+                        const int* pool_fwd, int pool_n, int n_slots, const RowPlan& rp,
+                        int* n_prefix, int* child_tok, int* child_node, int* n_child, int* flags,
+                        cudaStream_t st);
+void launch_copy_rows(int B, int d, int elem_bytes, const void* src, int src_stride_rows,
+                      void* dst, int dst_stride_rows, cudaStream_t st);
+void launch_copy_pool(int B, const PoolDev& pool, int* tok, int* parent, int* depth, int* fwd,
+                      float* score, float* logq, cudaStream_t st);
+
+// ----------------------------------------------------------------------------- verify.cu
+struct WalkArgs {
+  int B, M1, kmax, D, sampling;
+  float inv_t;
+  unsigned long long seed, round_id;
+  const int* t_tok;       // [B][M1]
+  const int* child_node;  // [B][M1][kmax] tree indices (-1 padded)
+  const int* n_child;     // [B][M1]
+  const float* child_z;   // [B*M1][kmax]
+  const float* lse;       // [B*M1]
+  const int* z_arg;       // [B*M1]
+  const int* g_arg;       // [B*M1]
+  int *accept_len, *path, *out_tokens;
+};
+void launch_walk(const WalkArgs& a, cudaStream_t st);
+
+}  // namespace e3

@@ -1,0 +1,184 @@
+"""Python driver for the C ABI: puts a round's inputs in device memory (torch is
+used only to allocate and copy), creates a context, runs prefill, draft rounds
+and verification through ``eagle3`` and returns the outputs as torch tensors.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import eagle3 as E
+from .configs import RoundConfig
+from .synth import RoundInputs
+
+
+def to_device(a: np.ndarray, device) -> torch.Tensor:
+    """numpy array (bf16 kept as uint16 bits) -> torch tensor on `device`."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def make_config(cfg: RoundConfig, max_prefix: int, max_new: int = 1, max_batch: int | None = None):
+    c = E.eagle3_config()
+    c.d, c.n_q_heads, c.n_kv_heads, c.head_dim = cfg.d, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    c.ffn, c.vocab, c.lr_rank, c.lr_cand = cfg.ffn, cfg.vocab, cfg.lr_rank, cfg.lr_cand
+    c.rope_theta, c.rms_eps = cfg.rope_theta, cfg.rms_eps
+    c.dtype = E.BF16 if cfg.dtype == "bf16" else E.FP32
+    c.depth, c.topk, c.n_verify, c.page_size = cfg.depth, cfg.topk, cfg.n_verify, cfg.page_size
+    c.max_batch = max_batch or cfg.batch
+    c.max_prefix, c.max_new = max_prefix, max_new
+    return c
+
+
+@dataclass
+class TreeOut:
+    tokens: torch.Tensor
+    parent: torch.Tensor
+    depth: torch.Tensor
+    pos: torch.Tensor
+    pool_index: torch.Tensor
+    score: torch.Tensor
+    mask: torch.Tensor
+
+    def struct(self) -> E.eagle3_tree:
+        t = E.eagle3_tree()
+        for n in ("tokens", "parent", "depth", "pos", "pool_index", "score", "mask"):
+            setattr(t, n, getattr(self, n).data_ptr())
+        return t
+
+
+@dataclass
+class PoolOut:
+    tok: torch.Tensor
+    parent: torch.Tensor
+    depth: torch.Tensor
+    fwd: torch.Tensor
+    score: torch.Tensor
+    logq: torch.Tensor
+
+    def struct(self) -> E.eagle3_pool:
+        p = E.eagle3_pool()
+        for n in ("tok", "parent", "depth", "fwd", "score", "logq"):
+            setattr(p, n, getattr(self, n).data_ptr())
+        return p
+
+
+class Engine:
+    """One context plus the device copies of one round's inputs and its KV cache."""
+
+    def __init__(self, inputs: RoundInputs, device="cuda", max_new: int = 1, with_target=True):
+        self.inp = inputs
+        cfg = self.cfg = inputs.cfg
+        self.device = torch.device(device)
+        dev = self.device
+        self.B = cfg.batch
+        self.w = {k: to_device(v, dev) for k, v in inputs.w.items()
+                  if with_target or k != "w_target"}
+        self.max_prefix = int(inputs.prefix_lens.max())
+        if cfg.page_size:
+            self.max_prefix = inputs.page_table.shape[1] * cfg.page_size
+        ws = E.eagle3_weights()
+        for n in E.WEIGHT_NAMES:
+            setattr(ws, n, self.w[n].data_ptr() if n in self.w else None)
+        self.cstruct = make_config(cfg, self.max_prefix, max_new)
+        s, self.ctx = E.eagle3_create(self.cstruct, ws)
+        if s != E.OK:
+            raise E.Eagle3Error(s, "eagle3_create")
+        self._ws = ws
+        # KV cache
+        dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+        kvd = (cfg.n_kv_heads, cfg.head_dim)
+        self.kv = E.eagle3_kv()
+        if cfg.page_size:
+            n_pages = inputs.n_pages
+            self.k_cache = torch.zeros((n_pages, cfg.page_size) + kvd, dtype=dt, device=dev)
+            self.v_cache = torch.zeros_like(self.k_cache)
+            self.page_table = to_device(inputs.page_table.astype(np.int32), dev)
+            self.kv.page_table = self.page_table.data_ptr()
+            self.kv.max_pages = inputs.page_table.shape[1]
+            self.kv.n_pages = n_pages
+        else:
+            self.k_cache = torch.zeros((self.B, self.max_prefix) + kvd, dtype=dt, device=dev)
+            self.v_cache = torch.zeros_like(self.k_cache)
+        self.kv.k, self.kv.v = self.k_cache.data_ptr(), self.v_cache.data_ptr()
+        self.seq_lens = torch.zeros(self.B, dtype=torch.int32, device=dev)
+        self.kv.seq_lens = self.seq_lens.data_ptr()
+        # the round's new row per request: the last prefix row (the root)
+        cu = inputs.cu_rows
+        last = cu[1:] - 1
+        self.feats_all = to_device(inputs.feats, dev)
+        self.tokens_all = to_device(inputs.tokens, dev)
+        self.cu_rows = to_device(cu.astype(np.int32), dev)
+        self.feats_new = self.feats_all[torch.from_numpy(last).to(dev)].unsqueeze(1).contiguous()
+        self.tokens_new = self.tokens_all[torch.from_numpy(last).to(dev)].unsqueeze(1).contiguous()
+        M1 = cfg.n_verify + 1
+        W = (M1 + 31) // 32
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.tree = TreeOut(*(torch.empty((self.B, M1), **i32) for _ in range(5)),
+                            torch.empty((self.B, M1), dtype=torch.float32, device=dev),
+                            torch.empty((self.B, M1, W), **i32))
+        pn = cfg.pool_size
+        self.pool = PoolOut(*(torch.empty((self.B, pn), **i32) for _ in range(4)),
+                            torch.empty((self.B, pn), dtype=torch.float32, device=dev),
+                            torch.empty((self.B, pn), dtype=torch.float32, device=dev))
+        D = cfg.depth
+        self.accept_len = torch.empty(self.B, **i32)
+        self.path = torch.empty((self.B, D), **i32)
+        self.out_tokens = torch.empty((self.B, D + 1), **i32)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.stats_t = dict(z_max=torch.empty((self.B, M1), **f32), lse=torch.empty((self.B, M1), **f32),
+                            z_argmax=torch.empty((self.B, M1), **i32),
+                            g_argmax=torch.empty((self.B, M1), **i32))
+        self.stats = E.eagle3_verify_stats(*(self.stats_t[n].data_ptr()
+                                             for n in ("z_max", "lse", "z_argmax", "g_argmax")))
+        self._tree_s = self.tree.struct()
+        self._pool_s = self.pool.struct()
+
+    def stream(self) -> int:
+        return torch.cuda.current_stream(self.device).cuda_stream
+
+    def close(self):
+        if self.ctx:
+            E.eagle3_destroy(self.ctx)
+            self.ctx = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self):
+        """K/V of every prefix row (the root row included; the round rewrites it)."""
+        self.seq_lens.zero_()
+        rows = int(self.inp.cu_rows[-1])
+        s = E.eagle3_prefill(self.ctx, self.B, rows, self.cu_rows.data_ptr(), self.feats_all.data_ptr(),
+                             self.tokens_all.data_ptr(), self.kv, self.stream())
+        E.check(self.ctx, s)
+        self.seq_lens.copy_(torch.from_numpy(self.inp.prefix_lens - 1).to(self.device))
+
+    def draft_round(self, with_pool=True, feats_new=None, tokens_new=None):
+        f = self.feats_new if feats_new is None else feats_new
+        t = self.tokens_new if tokens_new is None else tokens_new
+        s = E.eagle3_draft_round(self.ctx, self.B, 1, f.data_ptr(), t.data_ptr(), self.kv,
+                                 self._tree_s, self._pool_s if with_pool else None, self.stream())
+        E.check(self.ctx, s)
+        return self.tree
+
+    def verify(self, temperature=0.0, seed=0, round_id=0, with_stats=True):
+        mode = 0 if temperature == 0 else 1
+        s = E.eagle3_verify(self.ctx, self.B, self._tree_s, self.kv, mode, float(temperature or 1.0),
+                            seed, round_id, self.accept_len.data_ptr(), self.path.data_ptr(),
+                            self.out_tokens.data_ptr(), self.stats if with_stats else None,
+                            self.stream())
+        E.check(self.ctx, s)
+        return self.accept_len, self.path, self.out_tokens
+
+    def check(self):
+        E.check(self.ctx, E.eagle3_check(self.ctx))
+
+    def launches(self) -> int:
+        return E.eagle3_last_launch_count(self.ctx)

@@ -135,24 +135,33 @@ def make_inputs(cfg: RoundConfig, seed: int | None = None, threads: int | None =
         v32 = bf16_bits_to_f32(w["lr_v"]) if dt == "bf16" else w["lr_v"]
         lm = np.empty((V, d), dtype=np.uint16 if dt == "bf16" else np.float32)
         step = 8192
-        for i in range(0, V, step):
+
+        def lm_block(i):
             j = min(V, i + step)
             noise = _draw(seed, T_LRN * 1000 + i // step, (j - i) * d, 1.0, "fp32", 1)
             blk = (u32[i:j] @ v32).astype(np.float64) + 0.5 * 0.02 * noise.reshape(j - i, d)
             lm[i:j] = bf16_bits_from_f64(blk).reshape(j - i, d) if dt == "bf16" else blk
+
+        with ThreadPoolExecutor(max(1, threads)) as ex:
+            list(ex.map(lm_block, range(0, V, step)))
         w["w_lm"] = lm
     else:
         w["w_lm"] = W(T_WLM, V, d, cfg.lm_std)
 
     if with_target:
-        lm = bf16_bits_to_f32(w["w_lm"]) if dt == "bf16" else w["w_lm"]
-        wt = np.empty((V, d), dtype=w["w_lm"].dtype)
+        lm_bits = w["w_lm"]
+        wt = np.empty((V, d), dtype=lm_bits.dtype)
         step = 8192
-        for i in range(0, V, step):
+
+        def target_block(i):
             j = min(V, i + step)
             g = _draw(seed, T_G * 1000 + i // step, (j - i) * d, 0.02, "fp32", 1)
-            blk = lm[i:j].astype(np.float64) + cfg.eps_target * g.reshape(j - i, d).astype(np.float64)
+            lm = bf16_bits_to_f32(lm_bits[i:j]) if dt == "bf16" else lm_bits[i:j]
+            blk = lm.astype(np.float64) + cfg.eps_target * g.reshape(j - i, d).astype(np.float64)
             wt[i:j] = bf16_bits_from_f64(blk).reshape(j - i, d) if dt == "bf16" else blk
+
+        with ThreadPoolExecutor(max(1, threads)) as ex:
+            list(ex.map(target_block, range(0, V, step)))
         w["w_target"] = wt
 
     B = cfg.batch

@@ -1,0 +1,217 @@
+/*
+ * eagle3.h -- C ABI of one EAGLE-3 draft-and-verify round on a single B300.
+ *
+ * The operations follow the pages' statement of the problem:
+ *   - multi-layer feature fusion and the one-layer draft decoder
+ *     ("EAGLE-3 精读" §1 为什么推翻 feature regression, paragraph 2; abstract
+ *     of "EAGLE-3: Scaling up Inference Acceleration of Large Language Models
+ *     via Training-Time Test");
+ *   - the draft's own states fed back along draft paths with a tree attention
+ *     mask ("EAGLE-3 精读" §2 Training-Time Test);
+ *   - the EAGLE-2 confidence-value dynamic tree ("EAGLE-3 精读" 核心变化, and
+ *     §2 last paragraph), confidence = product of draft probabilities (EAGLE-4
+ *     blog, 几条技术路线正在收敛, second trend);
+ *   - strict verification, greedy and sampling with residual correction
+ *     ("EAGLE-3 精读" §5 正确性、复现与风险);
+ *   - the two-stage "Efficient LM Head" (EAGLE-4 blog, sections on the
+ *     Efficient LM Head): low-rank recall, exact rerank.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must be device memory of the current
+ *     CUDA device; the caller owns them and keeps them alive until the work on
+ *     `stream` has finished.  The library never frees caller memory.
+ *   - Weights are borrowed, never copied: row-major [out, in] matrices in the
+ *     storage type of the config (fp32 or bf16).  They must stay valid and
+ *     unchanged for the life of the context.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  Outputs
+ *     are valid once the stream has reached the call's end.  Nothing inside a
+ *     call synchronises with the host.
+ *   - Arguments are checked on the host before any launch; a bad argument
+ *     returns a status and launches nothing.  EAGLE3_ERR_CUDA wraps a launch
+ *     error.  Device-side checks (page index in range, ancestor closure of a
+ *     supplied pool, ...) raise a flag read by eagle3_check().
+ *   - A context is not thread-safe; use one context per host thread.
+ */
+#ifndef EAGLE3_H
+#define EAGLE3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct eagle3_ctx eagle3_ctx;
+typedef struct CUstream_st* eagle3_stream; /* same handle as cudaStream_t */
+
+typedef enum {
+  EAGLE3_OK = 0,
+  EAGLE3_ERR_INVALID_ARG = 1,   /* null pointer, value out of range */
+  EAGLE3_ERR_SHAPE = 2,         /* sizes inconsistent with the config or capacity */
+  EAGLE3_ERR_UNSUPPORTED = 3,   /* valid request this build does not implement */
+  EAGLE3_ERR_OOM = 4,           /* workspace allocation failed at create time */
+  EAGLE3_ERR_CUDA = 5,          /* a CUDA call or kernel launch failed */
+  EAGLE3_ERR_TIMEOUT = 6,       /* a bounded device wait gave up */
+  EAGLE3_ERR_DEVICE_ASSERT = 7, /* a device-side check failed (see eagle3_last_error) */
+  EAGLE3_ERR_STATE = 8          /* call order violated (e.g. verify before any draft round) */
+} eagle3_status;
+
+enum { EAGLE3_FP32 = 0, EAGLE3_BF16 = 1 };
+
+/* Shapes of the draft model and of the round.  All sizes in elements. */
+typedef struct {
+  int d;           /* model width */
+  int n_q_heads;   /* query heads Hq */
+  int n_kv_heads;  /* key/value heads Hkv (Hq % Hkv == 0) */
+  int head_dim;    /* dh, even, <= 128 */
+  int ffn;         /* SwiGLU inner width F */
+  int vocab;       /* V */
+  int lr_rank;     /* two-stage head: rank r of U [V, r] V_lr [r, d]; 0 = single-stage head */
+  int lr_cand;     /* two-stage head: candidates rescored by the exact head (<= 128) */
+  float rope_theta;
+  float rms_eps;
+  int dtype;       /* EAGLE3_FP32 or EAGLE3_BF16: weights, features, KV cache */
+  int depth;       /* D: sequential decoder passes per round, 1..16 */
+  int topk;        /* k: children per expanded node and frontier width, 1..16 */
+  int n_verify;    /* M: nodes kept for verification, 1..128 and <= pool size */
+  int page_size;   /* 0 = contiguous cache, else rows per KV page */
+  int max_batch;   /* largest B of any call */
+  int max_prefix;  /* rows one request may hold in the cache (contiguous layout stride) */
+  int max_new;     /* largest n_new of a draft round */
+} eagle3_config;
+
+/* Device pointers of the draft weights (row-major [out, in], config dtype).
+ *   w_fc [d, 3d]; embed [V, d]; w_q [Hq*dh, 2d]; w_k, w_v [Hkv*dh, 2d];
+ *   w_o [d, Hq*dh]; w_gate, w_up [F, d]; w_down [d, F];
+ *   g_emb, g_hid, g_post, g_final [d] RMSNorm gains;
+ *   w_lm [V, d] draft LM head; w_target [V, d] synthetic target head used by
+ *   eagle3_verify; lr_u [V, r], lr_v [r, d] the two-stage head (else NULL). */
+typedef struct {
+  const void *w_fc, *embed, *w_q, *w_k, *w_v, *w_o, *w_gate, *w_up, *w_down;
+  const void *g_emb, *g_hid, *g_post, *g_final;
+  const void *w_lm, *w_target, *lr_u, *lr_v;
+} eagle3_weights;
+
+/* Draft KV cache, caller-owned, config dtype, K after RoPE.
+ *   contiguous (page_size == 0): k, v are [max_batch, max_prefix, Hkv, dh];
+ *   paged: k, v are [n_pages, page_size, Hkv, dh] and page_table [B, max_pages]
+ *   (int32, device) maps request b's logical page j to a physical page.
+ * seq_lens [B] (int32, device): rows already committed per request.  No entry
+ * point changes seq_lens: the caller advances it after committing rows. */
+typedef struct {
+  void *k, *v;
+  const int* page_table;
+  const int* seq_lens;
+  int max_pages;
+  int n_pages;
+} eagle3_kv;
+
+/* The kept tree, device arrays.  Node 0 of request b is the root (the newest
+ * row), nodes 1..M the kept draft nodes in canonical order (depth ascending,
+ * then selection rank).  Shapes [B, M+1]; mask [B, M+1, W] with
+ * W = (M + 32) / 32 words: bit j of row i is set iff node j is an ancestor of
+ * node i or i itself.  parent of the root is -1; pool_index is the node's index
+ * in the round's pool (-1 for the root). */
+typedef struct {
+  int *tokens, *parent, *depth, *pos, *pool_index;
+  float* score;
+  uint32_t* mask;
+} eagle3_tree;
+
+/* Every node the round created, device arrays [B, pool_n] with
+ * pool_n = k + (D-1) k^2, in creation order (depth, parent's frontier rank,
+ * child rank).  parent is a pool index (-1 = root); fwd is the node's frontier
+ * slot if it was expanded, else -1; score = cumulative log q. */
+typedef struct {
+  int *tok, *parent, *depth, *fwd;
+  float *score, *logq;
+} eagle3_pool;
+
+/* Optional per-node verification details, device arrays [B, M+1]:
+ * z_max / z_argmax: largest target logit and its token (ties: lowest token);
+ * lse: log-sum-exp of z / T (of z when greedy); g_argmax: Gumbel-argmax of
+ * z / T over the tokens that are not children of the node (sampling only). */
+typedef struct {
+  float *z_max, *lse;
+  int *z_argmax, *g_argmax;
+} eagle3_verify_stats;
+
+/* Create a context: checks the config, borrows the weights, allocates the
+ * workspace for max_batch requests once (nothing is allocated later) and
+ * prepares the kernels' tensor maps.  Returns EAGLE3_ERR_OOM if the workspace
+ * does not fit, EAGLE3_ERR_UNSUPPORTED for shapes outside the limits above. */
+eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, eagle3_ctx** out);
+
+/* Free the workspace.  The caller must have finished all work on the context. */
+void eagle3_destroy(eagle3_ctx* ctx);
+
+/* Prefix rows into the draft KV cache ("EAGLE-3 精读" §1: g from the target's
+ * low/mid/high features, then the decoder input [rms(E[y]); rms(g)]).
+ * cu_rows [B+1] (int32, device) splits the packed rows by request; row r of
+ * request b gets position seq_lens[b] + (r - cu_rows[b]).  feats [total_rows, 3d]
+ * (low, mid, high concatenated), tokens [total_rows] (the token emitted after
+ * each row's position).  Only K and V are produced: in a one-layer drafter a
+ * prefix row's layer output feeds nothing. */
+eagle3_status eagle3_prefill(eagle3_ctx* ctx, int B, int total_rows, const int* cu_rows,
+                             const void* feats, const int* tokens, const eagle3_kv* kv,
+                             eagle3_stream stream);
+
+/* One draft round: appends n_new rows per request at positions
+ * seq_lens[b] .. seq_lens[b] + n_new - 1 (the last is the tree's root), runs D
+ * decoder passes (root, then one per tree depth), builds the pool of
+ * k + (D-1) k^2 nodes and keeps the global top-M as `out`.
+ * feats_new [B, n_new, 3d], tokens_new [B, n_new] (device).  pool_out may be
+ * NULL.  The round keeps its node states in the context for eagle3_verify. */
+eagle3_status eagle3_draft_round(eagle3_ctx* ctx, int B, int n_new, const void* feats_new,
+                                 const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
+                                 eagle3_pool* pool_out, eagle3_stream stream);
+
+/* Tree builder alone (for tests and outside drafters): keeps the top-M of a
+ * pool by (score desc, depth asc, pool index asc) and writes the canonical
+ * tree.  pool arrays [B, pool_n] (device; parent = pool index or -1), root_tok
+ * and root_pos [B] (device).  pool_n <= 4096.  The kept set must be
+ * ancestor-closed (child score <= parent score); otherwise the device flag
+ * EAGLE3_ERR_DEVICE_ASSERT is raised and the tree is left partial. */
+eagle3_status eagle3_build_tree(eagle3_ctx* ctx, int B, int pool_n, const int* pool_tok,
+                                const int* pool_parent, const float* pool_score,
+                                const int* pool_depth, const int* root_tok, const int* root_pos,
+                                eagle3_tree* out, eagle3_stream stream);
+
+/* Strict verification of the tree of the last eagle3_draft_round on this
+ * context ("EAGLE-3 精读" §5).  The synthetic target reruns the decoder over
+ * the M kept nodes with the tree mask and applies w_target.  mode 0: greedy
+ * (walk while the target argmax is a child's token); mode 1: sampling at
+ * `temperature` > 0 with sequential point-mass acceptance and a Gumbel draw
+ * from the residual, using Philox4x64-10 with key (seed, 0) and counter
+ * (round_id, b * 2^32 + node, idx, stream).  Outputs (device): accept_len [B],
+ * path [B, D] (tree indices, -1 padded), out_tokens [B, D+1] (accepted tokens
+ * then the bonus token, -1 padded).  stats may be NULL. */
+eagle3_status eagle3_verify(eagle3_ctx* ctx, int B, const eagle3_tree* tree, const eagle3_kv* kv,
+                            int mode, float temperature, unsigned long long seed,
+                            unsigned long long round_id, int* accept_len, int* path,
+                            int* out_tokens, eagle3_verify_stats* stats, eagle3_stream stream);
+
+/* The draft LM head alone on R given rows h [R, d] (config dtype, device):
+ * per row the top-k (token, log q) and the log-sum-exp of the logits (for the
+ * two-stage head: normalised over the candidate set).  tok [R, k] int32,
+ * logq [R, k] fp32, lse [R] fp32 (may be NULL).  R <= max_batch * topk. */
+eagle3_status eagle3_lm_head_topk(eagle3_ctx* ctx, int R, const void* h, int* tok, float* logq,
+                                  float* lse, eagle3_stream stream);
+
+/* Wait for the context's last stream, then report and clear the device flag. */
+eagle3_status eagle3_check(eagle3_ctx* ctx);
+
+/* Text of the last error on this context ("" if none).  Valid until the next call. */
+const char* eagle3_last_error(const eagle3_ctx* ctx);
+
+/* Bytes of device workspace the context holds. */
+size_t eagle3_workspace_bytes(const eagle3_ctx* ctx);
+
+/* Kernel launches issued by the last call on this context. */
+int eagle3_last_launch_count(const eagle3_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE3_H */

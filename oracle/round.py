@@ -166,18 +166,21 @@ def draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec: Decisions, b
     pool = Pool()
     states, hs, node_logq, frontiers, tree_kv = {}, {}, {}, [], {}
 
-    def expand(depth, rank, h_row, parent, parent_score):
-        cand, logq, lowrank = L.draft_logq(w, cfg, h_row[None])
-        cand, logq = cand[0], logq[0]
-        if lowrank is not None:  # candidate choice of the low-rank stage may be conditioned
-            order = dec.candidates(b, depth, rank, lowrank[0], cfg.lr_cand)
-            ell = np.array([L.f64(w["w_lm"][c]) @ L.f64(h_row) for c in order])
-            cand, logq = order, ell - L.logsumexp(ell)
-        node_logq[(depth, rank)] = (np.asarray(cand), logq)
-        for j in dec.children(b, depth, rank, cand, logq, k_):
-            pool.add(cand[j], parent, parent_score + logq[j], depth + 1, logq[j])
+    def expand(depth, nodes, h_rows):
+        """LM head on a pass's rows (one call), then each node's k children."""
+        cands, logqs, lowrank = L.draft_logq(w, cfg, h_rows)
+        for rank, parent in enumerate(nodes):
+            cand, logq = cands[rank], logqs[rank]
+            if lowrank is not None:  # candidate choice of the low-rank stage may be conditioned
+                order = dec.candidates(b, depth, rank, lowrank[rank], cfg.lr_cand)
+                ell = np.array([L.f64(w["w_lm"][c]) @ L.f64(h_rows[rank]) for c in order])
+                cand, logq = order, ell - L.logsumexp(ell)
+            node_logq[(depth, rank)] = (np.asarray(cand), logq)
+            base = 0.0 if parent < 0 else pool.score[parent]
+            for j in dec.children(b, depth, rank, cand, logq, k_):
+                pool.add(cand[j], parent, base + logq[j], depth + 1, logq[j])
 
-    expand(0, 0, h_root, -1, 0.0)
+    expand(0, [-1], h_root[None])
     frontier = list(range(k_)) if D >= 2 else []
     for t in range(1, D):
         for r, i in enumerate(frontier):
@@ -187,7 +190,7 @@ def draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec: Decisions, b
         base = len(pool.tok)
         for r, i in enumerate(frontier):
             states[i], hs[i] = s[r], h[r]
-            expand(t, r, h[r], i, pool.score[i])
+        expand(t, frontier, h)
         if t + 1 < D:
             sc = np.array(pool.score[base:])
             frontier = [base + int(j) for j in dec.frontier(b, t + 1, sc, k_)]

@@ -1,0 +1,68 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point that include/eagle3.h declares, and rejects bad arguments
+before touching the device."""
+import ctypes as C
+
+import pytest
+
+
+@pytest.fixture(scope="module")
+def E(lib_built):
+    from eagle_draft_tree_02_b300 import eagle3
+    return eagle3
+
+
+def test_library_exports_every_declared_symbol(E):
+    names = E.declared_functions()
+    assert "eagle3_draft_round" in names and "eagle3_build_tree" in names and "eagle3_verify" in names
+    for n in names:
+        assert hasattr(E.lib, n), n
+
+
+def _cfg(E, **kw):
+    from eagle_draft_tree_02_b300.configs import CONFIGS
+    from eagle_draft_tree_02_b300.runner import make_config
+    c = make_config(CONFIGS[0], max_prefix=64)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _weights(E, missing=()):
+    w = E.eagle3_weights()
+    for i, n in enumerate(E.WEIGHT_NAMES):
+        if n not in missing and n not in ("lr_u", "lr_v"):
+            setattr(w, n, 0x1000 * (i + 1))
+    return w
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("d", 0, 1), ("d", 100, 1), ("head_dim", 200, 1), ("n_kv_heads", 3, 1), ("dtype", 5, 1),
+    ("depth", 0, 3), ("depth", 17, 3), ("topk", 17, 3), ("n_verify", 129, 3),
+    ("n_verify", 1000, 3), ("max_batch", 0, 1), ("max_new", 0, 1),
+])
+def test_create_rejects_bad_config(E, field, value, status):
+    s, ctx = E.eagle3_create(_cfg(E, **{field: value}), _weights(E))
+    assert s == status and ctx == 0
+
+
+def test_create_rejects_pool_smaller_than_m(E):
+    s, ctx = E.eagle3_create(_cfg(E, depth=1, topk=4, n_verify=5), _weights(E))
+    assert s == E.ERR_SHAPE and ctx == 0
+
+
+def test_create_rejects_missing_weight(E):
+    s, ctx = E.eagle3_create(_cfg(E), _weights(E, missing=("w_lm",)))
+    assert s == E.ERR_INVALID_ARG and ctx == 0
+
+
+def test_null_context_calls_fail_cleanly(E):
+    kv, tree = E.eagle3_kv(), E.eagle3_tree()
+    assert E.eagle3_draft_round(0, 1, 1, 1, 1, kv, tree) == E.ERR_INVALID_ARG
+    assert E.eagle3_verify(0, 1, tree, kv, 0, 1.0, 0, 0, 1, 1, 1) == E.ERR_INVALID_ARG
+    assert E.eagle3_build_tree(0, 1, 4, 1, 1, 1, 1, 1, 1, tree) == E.ERR_INVALID_ARG
+    assert E.eagle3_prefill(0, 1, 1, 1, 1, 1, kv) == E.ERR_INVALID_ARG
+    assert E.eagle3_lm_head_topk(0, 1, 1, 1, 1) == E.ERR_INVALID_ARG
+    assert E.eagle3_check(0) == E.ERR_INVALID_ARG
+    assert E.eagle3_last_error(0) == "null context"
+    assert E.eagle3_workspace_bytes(0) == 0
