@@ -1,0 +1,327 @@
+#!/usr/bin/env python
+"""Throughput of one EAGLE-3 draft-and-verify round on B300, as one JSON line.
+
+A step is the whole hot path on one batch: the draft round (fusion, D decoder
+passes with tree attention, fused LM-head top-k, frontier expansion, global
+top-M tree) followed by verification (the tree-masked verify pass, the target
+head and the accept/sample walk).  Inputs are seeded synthetic tensors with the
+shapes of the named workload, resident in HBM before timing; the prefix is
+prefilled once, outside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU as an
+independent replica (disjoint requests, no collective on the data path); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "llama31_8b_b1_tree"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU works."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = [ln.split(",") for ln in open(self.f.name).read().splitlines() if ln.strip()]
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows if len(r) >= 9 for n, v in zip(names, r[5:9])
+                          if v.strip() == "Active"})
+        busy = [s for s in sm if s > 0]
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def step_temperature(cfg):
+    hot = [t for t in cfg.temperatures if t > 0]
+    return hot[0] if hot else 0.0
+
+
+def cpu_oracle_round(cfg, inp, seconds_hint=True):
+    """One oracle round (draft + verify) of request 0 on the host cores; returns seconds."""
+    import numpy as np
+    from oracle import round as R
+    w = R.weights_f32(inp)
+    f = inp.feats_f32()
+    lo, hi = int(inp.cu_rows[0]), int(inp.cu_rows[1])
+    K, V = R.prefix_kv(w, cfg, f[lo:hi], inp.tokens[lo:hi])
+    T = step_temperature(cfg)
+    t0 = time.perf_counter()
+    R.round_request(w, cfg, K, V, f[hi - 1], inp.tokens[hi - 1], hi - lo - 1, temperatures=(T,))
+    return time.perf_counter() - t0
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+def run_reference(args, cfg):
+    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from eagle_draft_tree_02_b300.synth import make_inputs
+    inp = make_inputs(cfg)
+    budget = 150.0
+    warm = min(args.warmup, 1)
+    for _ in range(warm):
+        cpu_oracle_round(cfg, inp)
+    times = []
+    for _ in range(args.steps):
+        times.append(cpu_oracle_round(cfg, inp))
+        if sum(times) > budget:
+            break
+    # B requests per round on the GPU; the oracle sample is request 0, so scale to the batch
+    per_round = sum(times) / len(times) * cfg.batch
+    value = 1.0 / per_round
+    cores = blas_threads()
+    sample = (f"{len(times)} oracle round(s) of request 0 (draft D={cfg.depth} passes + verify), "
+              f"scaled by B={cfg.batch}; {warm} warm-up")
+    print(json.dumps({
+        "impl": "reference", "metric": "draft-tree rounds/s", "value": value, "unit": "rounds/s",
+        "n_gpus": args.gpus, "steps": len(times), "warmup": warm, "ms_per_step": per_round * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": cfg.name},
+        "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    from eagle_draft_tree_02_b300.configs import by_name
+    cfg = by_name(args.config)
+    if args.impl == "reference":
+        run_reference(args, cfg)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    from eagle_draft_tree_02_b300 import eagle3 as E
+    from eagle_draft_tree_02_b300.roofline import head_bytes, round_bytes
+    from eagle_draft_tree_02_b300.runner import Engine
+    from eagle_draft_tree_02_b300.synth import make_inputs
+
+    inp = make_inputs(cfg, seed=None)
+    eng = Engine(inp, device=dev)
+    eng.prefill()
+    torch.cuda.synchronize()
+    eng.check()
+    T = step_temperature(cfg)
+    launches = {"n": 0}
+
+    def step(i, count=False):
+        eng.draft_round(with_pool=False)
+        n = eng.launches()
+        eng.verify(T, seed=0, round_id=i, with_stats=False)
+        if count:
+            launches["n"] += n + eng.launches()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    eng.check()
+    barrier()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for i in range(args.steps):
+        step(args.warmup + i, count=True)
+    s1.record()
+    s1.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    eng.check()
+    ms = s0.elapsed_time(s1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * args.steps / (ms / 1e3)
+
+    # draft round alone (same inputs), for the draft-only rate
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nd = max(10, args.steps // 2)
+    d0.record()
+    for _ in range(nd):
+        eng.draft_round(with_pool=False)
+    d1.record()
+    d1.synchronize()
+    draft_ms = d0.elapsed_time(d1) / nd
+
+    # dominant kernel: the draft LM head with its fused softmax/top-k, on B*k rows
+    hbm, tflops, src = peaks()
+    Rh = cfg.batch * cfg.topk
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    h = torch.randn(Rh, cfg.d, device=dev).to(dt)
+    tok = torch.empty((Rh, cfg.topk), dtype=torch.int32, device=dev)
+    lq = torch.empty((Rh, cfg.topk), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    for _ in range(5):
+        E.check(eng.ctx, E.eagle3_lm_head_topk(eng.ctx, Rh, h.data_ptr(), tok.data_ptr(), lq.data_ptr(),
+                                               None, stream))
+    nh = 50
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0.record()
+    for _ in range(nh):
+        E.eagle3_lm_head_topk(eng.ctx, Rh, h.data_ptr(), tok.data_ptr(), lq.data_ptr(), None, stream)
+    h1.record()
+    h1.synchronize()
+    head_s = h0.elapsed_time(h1) / nh / 1e3
+    hb = head_bytes(cfg, Rh)
+    achieved = hb / head_s / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        try:
+            import hashlib
+            j = json.load(open(tp))
+            src_hash = hashlib.sha256(open(os.path.join(ROOT, "eagle_draft_tree_02_b300", "csrc",
+                                                        "gemm_tc.cu"), "rb").read()).hexdigest()[:16]
+            e = j.get("lm_head", {})
+            if e.get("source_sha256_16") == src_hash and e.get("config") == cfg.name:
+                traffic = e.get("dram_bytes_per_launch")
+        except Exception:
+            traffic = None
+    roof = {"bound": "hbm", "kernel": "tc_gemm_kernel<1> (draft LM head + fused softmax/top-k, incl. merge)",
+            "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
+            "algorithmic_bytes_per_launch": hb, "launch_us": round(head_s * 1e6, 2)}
+
+    # end to end through the ABI with host buffers: H2D of the step's inputs, D2H of its result
+    fh = eng.feats_new.cpu().pin_memory()
+    th = eng.tokens_new.cpu().pin_memory()
+    out_h = torch.empty((cfg.batch, cfg.depth + 2), dtype=torch.int32).pin_memory()
+    fd, td = torch.empty_like(eng.feats_new), torch.empty_like(eng.tokens_new)
+    ne = max(10, args.steps // 2)
+    for i in range(3 + ne):
+        if i == 3:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        fd.copy_(fh, non_blocking=True)
+        td.copy_(th, non_blocking=True)
+        eng.draft_round(with_pool=False, feats_new=fd, tokens_new=td)
+        a, p, o = eng.verify(T, seed=0, round_id=10 ** 6 + i, with_stats=False)
+        out_h[:, 0].copy_(a, non_blocking=True)
+        out_h[:, 1:].copy_(o, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+    e2e_s = (time.perf_counter() - t0) / ne
+    h2d = fh.numel() * fh.element_size() + th.numel() * th.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+
+    rb = round_bytes(cfg, prefix_mean=float(np.mean(inp.prefix_lens)))
+    line = {
+        "metric": "draft-tree rounds/s", "value": round(value, 3), "unit": "rounds/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.dtype, "data": "synthetic (seeded weights, features, tokens; no trained model)",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "prefix": cfg.prefix, "d": cfg.d,
+                   "vocab": cfg.vocab, "depth": cfg.depth, "topk": cfg.topk, "n_verify": cfg.n_verify,
+                   "verify": f"T={T}" if T else "greedy",
+                   "l2": f"inputs larger than L2: {rb['step'] / 1e9:.2f} GB of weights/KV streamed per step"},
+        "draft_tokens_per_s": round(value * cfg.batch * cfg.n_verify, 1),
+        "draft_rounds_per_s_draft_only": round(world * 1e3 / draft_ms, 2),
+        "step_algorithmic_bytes": rb["step"],
+        "step_hbm_frac": round(rb["step"] / (ms_per_step / 1e3) / 1e9 / hbm, 4),
+        "draft_hbm_frac": round(rb["draft"] / (draft_ms / 1e3) / 1e9 / hbm, 4),
+        "roofline": roof,
+        "e2e": {"value": round(world / e2e_s, 3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches["n"],
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t = cpu_oracle_round(cfg, inp)
+        line["cpu_baseline"] = {"value": round(1.0 / (t * cfg.batch), 6), "unit": "rounds/s",
+                                "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"1 oracle round of request 0 (draft + verify at T={T}), "
+                                          f"scaled by B={cfg.batch}; prefix K/V precomputed"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    eng.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -64,6 +64,7 @@ struct eagle3_ctx {
   // bookkeeping
   cudaStream_t last = nullptr;
   std::string err;
+  std::string host_err;  // a launch the host refused inside the current call
   int launches = 0;
   bool have_round = false;
   int last_B = 0;
@@ -76,7 +77,16 @@ eagle3_status fail(eagle3_ctx* c, eagle3_status s, const std::string& msg) {
   return s;
 }
 
+void tc_error(eagle3_ctx* c, const char* what) {
+  if (c->host_err.empty()) c->host_err = what;
+}
+
 eagle3_status cuda_status(eagle3_ctx* c, const char* where) {
+  if (!c->host_err.empty()) {
+    std::string m = std::string(where) + ": " + c->host_err;
+    c->host_err.clear();
+    return fail(c, EAGLE3_ERR_CUDA, m);
+  }
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -85,7 +95,9 @@ eagle3_status cuda_status(eagle3_ctx* c, const char* where) {
   return EAGLE3_OK;
 }
 
-int splits_for(int R, int N, int K) {
+// K splits of a GEMM with output width N (the sum over its segments) on R rows.
+int splits_for(const eagle3_ctx* c, int R, int N, int K) {
+  if (c->bf) return tc_splits(R, cdiv(N, 128), K);
   int tiles = cdiv(N, 64) * cdiv(R, 64);
   int s = std::max(1, kTargetBlocks / std::max(1, tiles));
   s = std::min(s, std::max(1, K / 256));
@@ -101,15 +113,29 @@ int splits_for(int R, int N, int K) {
       FN<float>(__VA_ARGS__); \
   } while (0)
 
-// Y[s][r][col0 + n] = X W^T over K, split S ways.
-void gemm(eagle3_ctx* c, int wid, const void* X, int ldx, const void* W, int N, int K, float* Y,
-          int ldy, int col0, int R, int S, size_t split_stride, cudaStream_t st) {
-  if (c->tc && tc_gemm(c->tc, wid, X, ldx, W, N, K, Y, ldy, col0, R, S, split_stride, st)) {
+void tc_error(eagle3_ctx* c, const char* what);
+
+// Y[s][r][seg.col0 + n] = X W_seg^T over K, split S ways: tcgen05 for bf16
+// storage, the fp32 CUDA-core kernel for fp32 storage.
+void gemm(eagle3_ctx* c, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
+          int ldy, int R, int S, size_t split_stride, cudaStream_t st) {
+  if (c->bf) {
+    if (!tc_gemm(c->tc, segs, nseg, X, ldx, K, Y, ldy, R, S, split_stride, c->flags, st))
+      tc_error(c, "tcgen05 GEMM rejected its arguments");
     c->launches++;
     return;
   }
-  DISPATCH(c, launch_gemm_simt, X, ldx, W, K, Y, ldy, col0, R, N, K, S, split_stride, st);
-  c->launches++;
+  for (int i = 0; i < nseg; ++i) {
+    launch_gemm_simt<float>(X, ldx, segs[i].W, K, Y, ldy, segs[i].col0, R, segs[i].N, K, S,
+                            split_stride, st);
+    c->launches++;
+  }
+}
+
+void gemm1(eagle3_ctx* c, int wid, const void* X, int ldx, const void* W, int N, int K, float* Y,
+           int ldy, int R, int S, size_t split_stride, cudaStream_t st) {
+  GemmSeg g{wid, W, N, 0};
+  gemm(c, &g, 1, X, ldx, K, Y, ldy, R, S, split_stride, st);
 }
 
 struct KvTarget {  // where a pass writes K/V
@@ -124,8 +150,8 @@ void kv_rows(eagle3_ctx* c, int R, const void* feats, bool has_q, const float* h
   const eagle3_config& f = c->cfg;
   const int d = f.d;
   if (feats) {
-    int S = splits_for(R, d, 3 * d);
-    gemm(c, TCW_FC, feats, 3 * d, c->w.w_fc, d, 3 * d, c->part, d, 0, R, S, (size_t)R * d, st);
+    int S = splits_for(c, R, d, 3 * d);
+    gemm1(c, TCW_FC, feats, 3 * d, c->w.w_fc, d, 3 * d, c->part, d, R, S, (size_t)R * d, st);
     launch_reduce_parts(R, d, S, c->part, c->g, st);
     c->launches++;
     hid_base = c->g;
@@ -135,15 +161,17 @@ void kv_rows(eagle3_ctx* c, int R, const void* feats, bool has_q, const float* h
   c->launches++;
   const int qd = f.n_q_heads * f.head_dim, kvd = f.n_kv_heads * f.head_dim;
   const int ld = (has_q ? qd : 0) + 2 * kvd;
-  int S = splits_for(R, ld, 2 * d);
+  int S = splits_for(c, R, ld, 2 * d);
   size_t ss = (size_t)R * ld;
-  int col = 0;
+  GemmSeg segs[3];
+  int n = 0, col = 0;
   if (has_q) {
-    gemm(c, TCW_Q, c->x, 2 * d, c->w.w_q, qd, 2 * d, c->part, ld, 0, R, S, ss, st);
+    segs[n++] = GemmSeg{TCW_Q, c->w.w_q, qd, 0};
     col = qd;
   }
-  gemm(c, TCW_K, c->x, 2 * d, c->w.w_k, kvd, 2 * d, c->part, ld, col, R, S, ss, st);
-  gemm(c, TCW_V, c->x, 2 * d, c->w.w_v, kvd, 2 * d, c->part, ld, col + kvd, R, S, ss, st);
+  segs[n++] = GemmSeg{TCW_K, c->w.w_k, kvd, col};
+  segs[n++] = GemmSeg{TCW_V, c->w.w_v, kvd, col + kvd};
+  gemm(c, segs, n, c->x, 2 * d, 2 * d, c->part, ld, R, S, ss, st);
   QkvEpi p{};
   p.R = R;
   p.S = S;
@@ -218,22 +246,21 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   DISPATCH(c, launch_tree_attention, a, st);
   c->launches += 2;
   // r = hid + W_o o ; z = rms(r)
-  int S = splits_for(R, d, qd);
-  gemm(c, TCW_O, c->o, qd, c->w.w_o, d, qd, c->part, d, 0, R, S, (size_t)R * d, st);
+  int S = splits_for(c, R, d, qd);
+  gemm1(c, TCW_O, c->o, qd, c->w.w_o, d, qd, c->part, d, R, S, (size_t)R * d, st);
   DISPATCH(c, launch_o_epilogue, R, d, S, f.rms_eps, c->part, hid_base, c->rp.t_hid, c->w.g_post,
            c->r, c->z, st);
   c->launches++;
-  // a = silu(W_g z) * W_u z
-  int Sf = splits_for(R, f.ffn, d);
-  float* gp = c->part;
-  float* up = c->part + (size_t)Sf * R * f.ffn;
-  gemm(c, TCW_GATE, c->z, d, c->w.w_gate, f.ffn, d, gp, f.ffn, 0, R, Sf, (size_t)R * f.ffn, st);
-  gemm(c, TCW_UP, c->z, d, c->w.w_up, f.ffn, d, up, f.ffn, 0, R, Sf, (size_t)R * f.ffn, st);
-  DISPATCH(c, launch_swiglu, R, f.ffn, Sf, gp, up, c->a, st);
+  // a = silu(W_g z) * W_u z  (gate and up in one GEMM: columns [0, F) and [F, 2F))
+  const int F = f.ffn;
+  int Sf = splits_for(c, R, 2 * F, d);
+  GemmSeg gu[2] = {GemmSeg{TCW_GATE, c->w.w_gate, F, 0}, GemmSeg{TCW_UP, c->w.w_up, F, F}};
+  gemm(c, gu, 2, c->z, d, d, c->part, 2 * F, R, Sf, (size_t)R * 2 * F, st);
+  DISPATCH(c, launch_swiglu, R, F, Sf, c->part, c->a, st);
   c->launches++;
   // s = r + W_down a ; h = rms(s)
-  int Sd = splits_for(R, d, f.ffn);
-  gemm(c, TCW_DOWN, c->a, f.ffn, c->w.w_down, d, f.ffn, c->part, d, 0, R, Sd, (size_t)R * d, st);
+  int Sd = splits_for(c, R, d, F);
+  gemm1(c, TCW_DOWN, c->a, F, c->w.w_down, d, F, c->part, d, R, Sd, (size_t)R * d, st);
   DISPATCH(c, launch_down_epilogue, R, d, Sd, f.rms_eps, c->part, c->r, c->w.g_final, c->rp.t_sdst,
            c->S, c->rp.t_out, h_base, st);
   c->launches++;
@@ -243,12 +270,12 @@ void draft_head(eagle3_ctx* c, const void* H, int R, int* tok, float* logq, floa
                 cudaStream_t st) {
   HeadParts hp = c->hp;
   hp.R = R;
-  if (c->tc && tc_lm_head(c->tc, H, R, hp, st)) {
-    c->launches++;
+  if (c->bf) {
+    if (!tc_lm_head(c->tc, H, R, hp, c->flags, st)) tc_error(c, "tcgen05 LM head rejected its arguments");
   } else {
-    DISPATCH(c, launch_lm_head_simt, H, c->w.w_lm, R, c->cfg.vocab, c->cfg.d, hp, st);
-    c->launches++;
+    launch_lm_head_simt<float>(H, c->w.w_lm, R, c->cfg.vocab, c->cfg.d, hp, st);
   }
+  c->launches++;
   launch_topk_merge(hp, tok, logq, lse, 0, st);
   c->launches++;
 }
@@ -296,11 +323,21 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
       !w->w_down || !w->g_emb || !w->g_hid || !w->g_post || !w->g_final || !w->w_lm)
     return EAGLE3_ERR_INVALID_ARG;
 
+  // bf16: the tcgen05 LM head takes at most 256 rows per launch
+  if (f.dtype == EAGLE3_BF16 && f.max_batch * f.topk > 256) return EAGLE3_ERR_UNSUPPORTED;
   eagle3_ctx* c = new eagle3_ctx();
   c->cfg = f;
   c->w = *w;
   c->bf = f.dtype == EAGLE3_BF16;
   c->esz = c->bf ? 2 : 4;
+  if (c->bf) {
+    char msg[256] = {0};
+    c->tc = tc_create(f, *w, msg, sizeof(msg));
+    if (!c->tc) {
+      delete c;
+      return EAGLE3_ERR_UNSUPPORTED;
+    }
+  }
   c->k = f.topk;
   c->D = f.depth;
   c->M = f.n_verify;
@@ -318,32 +355,36 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
 
   // partial buffer: largest S * R * N over the GEMMs this context runs
   size_t part = 0;
-  auto need = [&](int R, int N, int K, int mult) {
-    part = std::max(part, (size_t)mult * splits_for(R, N, K) * R * N);
+  auto need = [&](int R, int N, int K) {
+    part = std::max(part, (size_t)splits_for(c, R, N, K) * R * N);
   };
-  for (int R : {c->rows_pf, B * f.max_new}) {
-    need(R, d, 3 * d, 1);
-    need(R, qd + 2 * kvd, 2 * d, 1);
+  // every row count a call can use: prefill chunks / new rows, and B' <= max_batch requests
+  for (int R = 1; R <= std::max(c->rows_pf, B * f.max_new); ++R) {
+    need(R, d, 3 * d);
+    need(R, qd + 2 * kvd, 2 * d);
+    need(R, 2 * kvd, 2 * d);
   }
-  for (int R : {B, B * k, B * c->M}) {
-    need(R, qd + 2 * kvd, 2 * d, 1);
-    need(R, d, qd, 1);
-    need(R, f.ffn, d, 2);
-    need(R, d, f.ffn, 1);
-  }
+  for (int b = 1; b <= B; ++b)
+    for (int R : {b, b * k, b * c->M}) {
+      need(R, qd + 2 * kvd, 2 * d);
+      need(R, d, qd);
+      need(R, 2 * f.ffn, d);
+      need(R, d, f.ffn);
+    }
   c->part_elems = part;
   size_t attn = 0;
   {
-    struct P { int B, rpr, slots; };
-    for (P p : {P{B, 1, 0}, P{B, k, c->n_slots}, P{B, c->M, c->M1}}) {
-      int kps, nps;
-      attn_splits(c, p.B, p.rpr, kps, nps);
-      attn = std::max(attn, (size_t)(nps + cdiv(p.slots, 64)) * p.B * p.rpr * qd);
-    }
+    struct P { int rpr, slots; };
+    for (int b = 1; b <= B; ++b)
+      for (P p : {P{1, 0}, P{k, c->n_slots}, P{c->M, c->M1}}) {
+        int kps, nps;
+        attn_splits(c, b, p.rpr, kps, nps);
+        attn = std::max(attn, (size_t)(nps + cdiv(p.slots, 64)) * b * p.rpr * qd);
+      }
   }
   c->attn_elems = attn;
-  const int lm_parts = lm_head_simt_parts(f.vocab);
-  c->n_vparts = verify_head_simt_parts(f.vocab);
+  const int lm_parts = c->bf ? tc_head_parts(f.vocab) : lm_head_simt_parts(f.vocab);
+  c->n_vparts = c->bf ? tc_head_parts(f.vocab) : verify_head_simt_parts(f.vocab);
   const int Rlm = B * k, Rv = B * c->M1;
   const int n_state = B * (1 + c->n_slots);
 
@@ -404,6 +445,7 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
   for (auto& p : plan) total += align_up(p.second, 256);
   if (cudaMalloc(&c->arena, total) != cudaSuccess) {
     cudaGetLastError();
+    tc_destroy(c->tc);
     delete c;
     return EAGLE3_ERR_OOM;
   }
@@ -439,11 +481,11 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
         cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
       cudaGetLastError();
       cudaFree(c->arena);
+      tc_destroy(c->tc);
       delete c;
       return EAGLE3_ERR_CUDA;
     }
   }
-  if (c->bf) c->tc = tc_create(c->cfg, c->w, c);
   *out = c;
   return EAGLE3_OK;
 }
@@ -593,12 +635,13 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   va.child_z = c->child_z;
   va.n_parts = c->n_vparts;
   va.part = c->vpart;
-  if (c->tc && tc_verify_head(c->tc, c->h_ver, va, st)) {
-    c->launches++;
+  if (c->bf) {
+    if (!tc_verify_head(c->tc, c->h_ver, va, c->flags, st))
+      tc_error(c, "tcgen05 verify head rejected its arguments");
   } else {
-    DISPATCH(c, launch_verify_head_simt, c->h_ver, c->w.w_target, va, st);
-    c->launches++;
+    launch_verify_head_simt<float>(c->h_ver, c->w.w_target, va, st);
   }
+  c->launches++;
   launch_verify_merge(va, c->z_max, c->z_arg, c->lse, c->g_arg, c->g_max, st);
   c->launches++;
   WalkArgs wa{};
@@ -643,6 +686,30 @@ eagle3_status eagle3_lm_head_topk(eagle3_ctx* c, int R, const void* h, int* tok,
   c->last = st;
   draft_head(c, h, R, tok, logq, lse, st);
   return cuda_status(c, "lm_head_topk");
+}
+
+eagle3_status eagle3_linear(eagle3_ctx* c, int which, int R, const void* X, float* Y,
+                            eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  const eagle3_config& f = c->cfg;
+  const int d = f.d, qd = f.n_q_heads * f.head_dim, kvd = f.n_kv_heads * f.head_dim;
+  struct Wd { int id; const void* p; int N, K; };
+  const Wd defs[] = {{TCW_FC, c->w.w_fc, d, 3 * d},   {TCW_Q, c->w.w_q, qd, 2 * d},
+                     {TCW_K, c->w.w_k, kvd, 2 * d},   {TCW_V, c->w.w_v, kvd, 2 * d},
+                     {TCW_O, c->w.w_o, d, qd},        {TCW_GATE, c->w.w_gate, f.ffn, d},
+                     {TCW_UP, c->w.w_up, f.ffn, d},   {TCW_DOWN, c->w.w_down, d, f.ffn},
+                     {TCW_LM, c->w.w_lm, f.vocab, d}, {TCW_T, c->w.w_target, f.vocab, d}};
+  if (which < 0 || which > 9) return fail(c, EAGLE3_ERR_INVALID_ARG, "which must be in 0..9");
+  const Wd& e = defs[which];
+  if (!e.p) return fail(c, EAGLE3_ERR_INVALID_ARG, "that weight is not set");
+  if (R < 1 || R > c->rows_cap) return fail(c, EAGLE3_ERR_SHAPE, "R out of range");
+  if (!X || !Y) return fail(c, EAGLE3_ERR_INVALID_ARG, "null pointer");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last = st;
+  gemm1(c, e.id, X, e.K, e.p, e.N, e.K, Y, e.N, R, 1, (size_t)R * e.N, st);
+  return cuda_status(c, "linear");
 }
 
 eagle3_status eagle3_check(eagle3_ctx* c) {

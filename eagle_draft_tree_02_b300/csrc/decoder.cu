@@ -153,13 +153,16 @@ __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* _
 }
 
 // ----------------------------------------------------------------------------- a = silu(W_g z) * (W_u z)
+// part: [S][R][2F], gate in columns [0, F), up in [F, 2F)
 template <typename T>
-__global__ void swiglu_kernel(int R, int F, int S, const float* __restrict__ gate_part,
-                              const float* __restrict__ up_part, T* __restrict__ a) {
+__global__ void swiglu_kernel(int R, int F, int S, const float* __restrict__ part, T* __restrict__ a) {
   size_t n = (size_t)R * F;
+  size_t stride = (size_t)R * 2 * F;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    float g = sum_parts(gate_part + i, n, S);
-    float u = sum_parts(up_part + i, n, S);
+    size_t r = i / F, c = i % F;
+    const float* p = part + r * 2 * F + c;
+    float g = sum_parts(p, stride, S);
+    float u = sum_parts(p + F, stride, S);
     stf(a + i, g / (1.f + expf(-g)) * u);
   }
 }
@@ -227,13 +230,12 @@ void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const 
 }
 
 template <typename T>
-void launch_swiglu(int R, int F, int S, const float* gate_part, const float* up_part, void* a,
-                   cudaStream_t st) {
+void launch_swiglu(int R, int F, int S, const float* part, void* a, cudaStream_t st) {
   size_t n = (size_t)R * F;
   if (!n) return;
   int blocks = (int)((n + 255) / 256);
   if (blocks > 148 * 16) blocks = 148 * 16;
-  swiglu_kernel<T><<<blocks, 256, 0, st>>>(R, F, S, gate_part, up_part, (T*)a);
+  swiglu_kernel<T><<<blocks, 256, 0, st>>>(R, F, S, part, (T*)a);
 }
 
 template <typename T>
@@ -253,7 +255,7 @@ void launch_down_epilogue(int R, int d, int S, float eps, const float* part, con
   template void launch_qkv_epilogue<T>(const QkvEpi&, cudaStream_t);                                 \
   template void launch_o_epilogue<T>(int, int, int, float, const float*, const float*, const int*,  \
                                      const void*, float*, void*, cudaStream_t);                      \
-  template void launch_swiglu<T>(int, int, int, const float*, const float*, void*, cudaStream_t);    \
+  template void launch_swiglu<T>(int, int, int, const float*, void*, cudaStream_t);                  \
   template void launch_down_epilogue<T>(int, int, int, float, const float*, const float*,           \
                                         const void*, const int*, float*, const int*, void*,         \
                                         cudaStream_t);

@@ -77,7 +77,5 @@ void launch_gemm_simt(const void* X, int ldx, const void* W, int ldw, float* Y, 
 
 template void launch_gemm_simt<float>(const void*, int, const void*, int, float*, int, int, int,
                                       int, int, int, size_t, cudaStream_t);
-template void launch_gemm_simt<bf16>(const void*, int, const void*, int, float*, int, int, int,
-                                     int, int, int, size_t, cudaStream_t);
 
 }  // namespace e3

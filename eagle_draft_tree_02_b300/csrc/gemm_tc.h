@@ -1,5 +1,13 @@
-// tcgen05 (5th-generation tensor core) GEMMs for bf16 storage: weights stream
-// through TMA into shared memory, accumulators live in tensor memory.
+// tcgen05 (5th-generation tensor core) GEMMs for bf16 storage.
+//
+// Y = X W^T with W [N, K] (weights, row-major) and X [R, K] (activation rows).
+// The weights take the MMA's M side (128 output features per tile) and the
+// activation rows its N side (16..256), so a round's few rows never pad the
+// 128-wide M dimension ("swap AB").  Both operands stream through TMA into
+// 128-byte-swizzled shared memory; the fp32 accumulator lives in tensor memory
+// and is read back with tcgen05.ld for the epilogue.  Epilogues: split-K
+// partial store, the draft LM head's online softmax + top-k, and the verify
+// head's argmax / log-sum-exp / Gumbel-argmax.
 #pragma once
 #include <cuda_runtime.h>
 
@@ -10,12 +18,24 @@ namespace e3 {
 
 enum TcWeight { TCW_FC, TCW_Q, TCW_K, TCW_V, TCW_O, TCW_GATE, TCW_UP, TCW_DOWN, TCW_LM, TCW_T, TCW_N };
 
+struct GemmSeg {  // one weight matrix whose output columns start at col0
+  int wid;
+  const void* W;
+  int N;
+  int col0;
+};
+
 struct TcGemm;
-TcGemm* tc_create(const eagle3_config& cfg, const eagle3_weights& w, eagle3_ctx* owner);
+// Returns nullptr and fills `err` when the driver entry point for tensor maps is missing.
+TcGemm* tc_create(const eagle3_config& cfg, const eagle3_weights& w, char* err, int errlen);
 void tc_destroy(TcGemm* t);
-bool tc_gemm(TcGemm* t, int wid, const void* X, int ldx, const void* W, int N, int K, float* Y,
-             int ldy, int col0, int R, int S, size_t split_stride, cudaStream_t st);
-bool tc_lm_head(TcGemm* t, const void* H, int R, const HeadParts& hp, cudaStream_t st);
-bool tc_verify_head(TcGemm* t, const void* H, const VerifyHeadArgs& a, cudaStream_t st);
+int tc_splits(int R, int n_mtiles, int K);
+int tc_head_parts(int V);
+// Y[s][r][col0 + n] for each segment; all segments share X and K.  Returns
+// false (and nothing is launched) on an unusable argument.
+bool tc_gemm(TcGemm* t, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
+             int ldy, int R, int S, size_t split_stride, int* flags, cudaStream_t st);
+bool tc_lm_head(TcGemm* t, const void* H, int R, const HeadParts& hp, int* flags, cudaStream_t st);
+bool tc_verify_head(TcGemm* t, const void* H, const VerifyHeadArgs& a, int* flags, cudaStream_t st);
 
 }  // namespace e3

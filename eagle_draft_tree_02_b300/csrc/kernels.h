@@ -32,9 +32,9 @@ template <typename T>
 void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const float* hid_base,
                        const int* hid_row, const void* g_post, float* r_out, void* z_out,
                        cudaStream_t st);
+// part: [S][R][2F] with the gate in columns [0, F) and up in [F, 2F)
 template <typename T>
-void launch_swiglu(int R, int F, int S, const float* gate_part, const float* up_part, void* a,
-                   cudaStream_t st);
+void launch_swiglu(int R, int F, int S, const float* part, void* a, cudaStream_t st);
 template <typename T>
 void launch_down_epilogue(int R, int d, int S, float eps, const float* part, const float* r_in,
                           const void* g_final, const int* s_dst, float* s_base, const int* h_dst,

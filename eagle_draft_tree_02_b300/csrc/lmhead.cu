@@ -283,11 +283,7 @@ void launch_verify_merge(const VerifyHeadArgs& a, float* z_max, int* z_arg, floa
 
 template void launch_lm_head_simt<float>(const void*, const void*, int, int, int, const HeadParts&,
                                          cudaStream_t);
-template void launch_lm_head_simt<bf16>(const void*, const void*, int, int, int, const HeadParts&,
-                                        cudaStream_t);
 template void launch_verify_head_simt<float>(const void*, const void*, const VerifyHeadArgs&,
                                              cudaStream_t);
-template void launch_verify_head_simt<bf16>(const void*, const void*, const VerifyHeadArgs&,
-                                            cudaStream_t);
 
 }  // namespace e3

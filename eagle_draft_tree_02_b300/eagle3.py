@@ -71,6 +71,7 @@ _sig = {
                                 C.c_float, C.c_ulonglong, C.c_ulonglong, _P, _P, _P,
                                 C.POINTER(eagle3_verify_stats), _P]),
     "eagle3_lm_head_topk": (C.c_int, [_P, C.c_int, _P, _P, _P, _P, _P]),
+    "eagle3_linear": (C.c_int, [_P, C.c_int, C.c_int, _P, _P, _P]),
     "eagle3_check": (C.c_int, [_P]),
     "eagle3_last_error": (C.c_char_p, [_P]),
     "eagle3_workspace_bytes": (C.c_size_t, [_P]),
@@ -135,6 +136,10 @@ def eagle3_verify(ctx, B, tree: eagle3_tree, kv: eagle3_kv, mode, temperature, s
 
 def eagle3_lm_head_topk(ctx, R, h, tok, logq, lse=None, stream=0) -> int:
     return lib.eagle3_lm_head_topk(ctx, R, h, tok, logq, lse, stream)
+
+
+def eagle3_linear(ctx, which, R, X, Y, stream=0) -> int:
+    return lib.eagle3_linear(ctx, which, R, X, Y, stream)
 
 
 def eagle3_check(ctx) -> int:

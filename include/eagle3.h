@@ -199,6 +199,14 @@ eagle3_status eagle3_verify(eagle3_ctx* ctx, int B, const eagle3_tree* tree, con
 eagle3_status eagle3_lm_head_topk(eagle3_ctx* ctx, int R, const void* h, int* tok, float* logq,
                                   float* lse, eagle3_stream stream);
 
+/* One of the context's weight matrices applied to R given rows, for kernel
+ * tests: Y [R, N] (fp32, device) = X [R, K] (config dtype, device) W^T, with
+ * which = 0 w_fc, 1 w_q, 2 w_k, 3 w_v, 4 w_o, 5 w_gate, 6 w_up, 7 w_down,
+ * 8 w_lm, 9 w_target.  Runs the same GEMM kernel as the round (tcgen05 for
+ * bf16 storage).  R <= the context's row capacity. */
+eagle3_status eagle3_linear(eagle3_ctx* ctx, int which, int R, const void* X, float* Y,
+                            eagle3_stream stream);
+
 /* Wait for the context's last stream, then report and clear the device flag. */
 eagle3_status eagle3_check(eagle3_ctx* ctx);
 

@@ -120,10 +120,12 @@ def test_build_tree_entry_point_random_pools(cuda, lib_built):
                     n += 1
             front = sorted(range(base, n), key=lambda i: (-sc[b, i], i))[:k]
     dev = torch.device("cuda")
-    T = lambda a: torch.from_numpy(a).to(dev)
-    rt = T(np.arange(B, dtype=np.int32) + 100); rpos = T(np.full(B, 50, np.int32))
-    s = E.eagle3_build_tree(eng.ctx, B, pool_n, T(tok).data_ptr(), T(par).data_ptr(), T(sc).data_ptr(),
-                            T(dep).data_ptr(), rt.data_ptr(), rpos.data_ptr(), eng._tree_s, eng.stream())
+    # keep every device tensor alive until the kernel has run
+    d_tok, d_par, d_sc, d_dep = (torch.from_numpy(a).to(dev) for a in (tok, par, sc, dep))
+    rt = torch.from_numpy(np.arange(B, dtype=np.int32) + 100).to(dev)
+    rpos = torch.from_numpy(np.full(B, 50, np.int32)).to(dev)
+    s = E.eagle3_build_tree(eng.ctx, B, pool_n, d_tok.data_ptr(), d_par.data_ptr(), d_sc.data_ptr(),
+                            d_dep.data_ptr(), rt.data_ptr(), rpos.data_ptr(), eng._tree_s, eng.stream())
     assert s == E.OK
     torch.cuda.synchronize()
     eng.check()
