@@ -48,6 +48,7 @@ __global__ void build_input_kernel(int R, int d, int V, float eps, const int* __
 // ----------------------------------------------------------------------------- split-K sum
 __device__ __forceinline__ float sum_parts(const float* p, size_t stride, int S) {
   float v = p[0];
+#pragma unroll 4
   for (int s = 1; s < S; ++s) v += p[(size_t)s * stride];
   return v;
 }
@@ -194,12 +195,16 @@ __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float
 }
 
 // ----------------------------------------------------------------------------- host launchers
+// Row kernels run one block per row; a full block keeps enough loads of the
+// split-K partials in flight for the few rows of a draft pass.
+constexpr int kRowThreads = 1024;
+
 template <typename T>
 void launch_build_input(int R, int d, int V, float eps, const int* tok, const float* hid_base,
                         const int* hid_row, const void* E, const void* g_emb, const void* g_hid,
                         void* x, int* flags, cudaStream_t st) {
   if (R <= 0) return;
-  build_input_kernel<T><<<R, 256, 0, st>>>(R, d, V, eps, tok, hid_base, hid_row, (const T*)E,
+  build_input_kernel<T><<<R, kRowThreads, 0, st>>>(R, d, V, eps, tok, hid_base, hid_row, (const T*)E,
                                            (const T*)g_emb, (const T*)g_hid, (T*)x, flags);
 }
 
@@ -225,7 +230,7 @@ void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const 
                        const int* hid_row, const void* g_post, float* r_out, void* z_out,
                        cudaStream_t st) {
   if (R <= 0) return;
-  o_epilogue_kernel<T><<<R, 256, 0, st>>>(R, d, S, eps, part, hid_base, hid_row, (const T*)g_post,
+  o_epilogue_kernel<T><<<R, kRowThreads, 0, st>>>(R, d, S, eps, part, hid_base, hid_row, (const T*)g_post,
                                           r_out, (T*)z_out);
 }
 
@@ -243,7 +248,7 @@ void launch_down_epilogue(int R, int d, int S, float eps, const float* part, con
                           const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
                           void* h_base, cudaStream_t st) {
   if (R <= 0) return;
-  down_epilogue_kernel<T><<<R, 256, d * sizeof(float), st>>>(R, d, S, eps, part, r_in,
+  down_epilogue_kernel<T><<<R, kRowThreads, d * sizeof(float), st>>>(R, d, S, eps, part, r_in,
                                                             (const T*)g_final, s_dst, s_base, h_dst,
                                                             (T*)h_base);
 }

@@ -111,65 +111,134 @@ void launch_lm_head_simt(const void* H, const void* W, int R, int V, int d, cons
 }
 
 // ----------------------------------------------------------------------------- merge: LSE + top-k
-__global__ void topk_merge_kernel(HeadParts hp, int* tok, float* logq, float* lse_out) {
-  __shared__ float red_v[32];
+// One block per row.  Each thread folds a strided subset of the partials into
+// an online (max, sum-exp) and a sorted register list of its best k (value,
+// token); partial lists are sorted best-first, so a list is abandoned at its
+// first entry that does not beat the thread's current k-th.  Then k block-wide
+// rounds each take the best list head, and its owner pops it.  Token ids are
+// unique across partials, so (value desc, token asc) is a strict order.
+namespace {
+constexpr int kMergeThreads = 512;
+
+// (m, s) <- (m, s) (+) (m2, s2) for s = sum exp(x - m)
+__device__ __forceinline__ void lse_fold(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;  // exp(-inf) = 0 covers the empty state
+    m = m2;
+  } else {
+    s += s2 * expf(m2 - m);
+  }
+}
+
+__device__ __forceinline__ void warp_lse(float& m, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_fold(m, s, m2, s2);
+  }
+}
+}  // namespace
+
+template <int K>
+__global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(HeadParts hp, int* tok, float* logq,
+                                                                   float* lse_out) {
+  __shared__ float red_m[32], red_s[32];
   __shared__ int red_i[32];
-  __shared__ float sh_lse;
-  int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
-  // log-sum-exp over parts
-  float m = -INFINITY;
-  for (int p = tid; p < hp.n_parts; p += blockDim.x) m = fmaxf(m, hp.ms[((size_t)p * hp.R + r) * 2]);
-  m = warp_max(m);
-  if (lane == 0) red_v[wid] = m;
+  __shared__ float win_v;
+  __shared__ int win_i;
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int nw = blockDim.x >> 5, k = K;
+  float m = -INFINITY, s = 0.f;
+  float lv[K];
+  int li[K];
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    lv[j] = -INFINITY;
+    li[j] = 0x7fffffff;
+  }
+  float tv = -INFINITY;  // current k-th kept (value, token)
+  int ti = 0x7fffffff;
+  for (int p = tid; p < hp.n_parts; p += blockDim.x) {
+    const size_t pr = (size_t)p * hp.R + r;
+    lse_fold(m, s, hp.ms[pr * 2], hp.ms[pr * 2 + 1]);
+    const float* pv = hp.val + pr * k;
+    const int* pi = hp.idx + pr * k;
+    for (int q = 0; q < k; ++q) {
+      const int i = pi[q];
+      const float v = pv[q];
+      if (i < 0 || !better(v, i, tv, ti)) break;
+      float cv = v;
+      int ci = i;
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        if (better(cv, ci, lv[j], li[j])) {
+          const float t = lv[j];
+          const int u = li[j];
+          lv[j] = cv;
+          li[j] = ci;
+          cv = t;
+          ci = u;
+        }
+      }
+      tv = lv[K - 1];
+      ti = li[K - 1];
+    }
+  }
+  // block log-sum-exp
+  warp_lse(m, s);
+  if (lane == 0) {
+    red_m[wid] = m;
+    red_s[wid] = s;
+  }
   __syncthreads();
   if (wid == 0) {
-    float t = lane < nw ? red_v[lane] : -INFINITY;
-    t = warp_max(t);
-    if (lane == 0) red_v[0] = t;
-  }
-  __syncthreads();
-  m = red_v[0];
-  __syncthreads();
-  float s = 0.f;
-  for (int p = tid; p < hp.n_parts; p += blockDim.x) {
-    const float* ms = hp.ms + ((size_t)p * hp.R + r) * 2;
-    if (ms[0] != -INFINITY) s += ms[1] * expf(ms[0] - m);
-  }
-  s = block_sum(s, red_v);
-  if (tid == 0) sh_lse = m + logf(s);
-  __syncthreads();
-  float lse = sh_lse;
-  if (tid == 0 && lse_out) lse_out[r] = lse;
-  // k rounds: best candidate strictly after the previous winner in (value desc, token asc)
-  float pv = INFINITY;
-  int pi = -1;
-  for (int j = 0; j < hp.k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int c = tid; c < hp.n_parts * hp.k; c += blockDim.x) {
-      int p = c / hp.k, q = c % hp.k;
-      size_t o = ((size_t)p * hp.R + r) * hp.k + q;
-      int i = hp.idx[o];
-      if (i < 0) continue;
-      float v = hp.val[o];
-      if (better(pv, pi, v, i) && better(v, i, bv, bi)) { bv = v; bi = i; }
+    float m2 = lane < nw ? red_m[lane] : -INFINITY;
+    float s2 = lane < nw ? red_s[lane] : 0.f;
+    warp_lse(m2, s2);
+    if (lane == 0) {
+      red_m[0] = m2;
+      red_s[0] = s2;
     }
+  }
+  __syncthreads();
+  const float lse = red_m[0] + logf(red_s[0]);
+  if (tid == 0 && lse_out) lse_out[r] = lse;
+  // k rounds of block argmax over the list heads
+  for (int j = 0; j < k; ++j) {
+    __syncthreads();  // red_* and win_* free again
+    float bv = lv[0];
+    int bi = li[0];
     warp_best(bv, bi);
-    if (lane == 0) { red_v[wid] = bv; red_i[wid] = bi; }
+    if (lane == 0) {
+      red_m[wid] = bv;
+      red_i[wid] = bi;
+    }
     __syncthreads();
     if (wid == 0) {
-      float tv = lane < nw ? red_v[lane] : -INFINITY;
-      int ti = lane < nw ? red_i[lane] : 0x7fffffff;
-      warp_best(tv, ti);
-      if (lane == 0) { red_v[0] = tv; red_i[0] = ti; }
+      float v2 = lane < nw ? red_m[lane] : -INFINITY;
+      int i2 = lane < nw ? red_i[lane] : 0x7fffffff;
+      warp_best(v2, i2);
+      if (lane == 0) {
+        win_v = v2;
+        win_i = i2;
+      }
     }
     __syncthreads();
-    pv = red_v[0];
-    pi = red_i[0];
-    __syncthreads();
+    const int wi = win_i;
+    if (wi != 0x7fffffff && li[0] == wi) {  // the owner pops its head
+#pragma unroll
+      for (int q = 0; q < K - 1; ++q) {
+        lv[q] = lv[q + 1];
+        li[q] = li[q + 1];
+      }
+      lv[K - 1] = -INFINITY;
+      li[K - 1] = 0x7fffffff;
+    }
     if (tid == 0) {
-      tok[(size_t)r * hp.k + j] = pi == 0x7fffffff ? -1 : pi;
-      logq[(size_t)r * hp.k + j] = pv - lse;
+      tok[(size_t)r * k + j] = wi == 0x7fffffff ? -1 : wi;
+      logq[(size_t)r * k + j] = win_v - lse;
     }
   }
 }
@@ -177,7 +246,19 @@ __global__ void topk_merge_kernel(HeadParts hp, int* tok, float* logq, float* ls
 void launch_topk_merge(const HeadParts& hp, int* tok, float* logq, float* lse, int /*unused*/,
                        cudaStream_t st) {
   if (hp.R <= 0) return;
-  topk_merge_kernel<<<hp.R, 256, 0, st>>>(hp, tok, logq, lse);
+  switch (hp.k) {
+#define E3_MERGE_CASE(K) \
+  case K:                \
+    topk_merge_kernel<K><<<hp.R, kMergeThreads, 0, st>>>(hp, tok, logq, lse); \
+    break;
+    E3_MERGE_CASE(1) E3_MERGE_CASE(2) E3_MERGE_CASE(3) E3_MERGE_CASE(4) E3_MERGE_CASE(5)
+    E3_MERGE_CASE(6) E3_MERGE_CASE(7) E3_MERGE_CASE(8) E3_MERGE_CASE(9) E3_MERGE_CASE(10)
+    E3_MERGE_CASE(11) E3_MERGE_CASE(12) E3_MERGE_CASE(13) E3_MERGE_CASE(14) E3_MERGE_CASE(15)
+    E3_MERGE_CASE(16)
+#undef E3_MERGE_CASE
+    default:
+      break;  // k is checked to lie in 1..16 before any launch
+  }
 }
 
 // ----------------------------------------------------------------------------- verify head
@@ -249,36 +330,55 @@ void launch_verify_head_simt(const void* H, const void* W, const VerifyHeadArgs&
   verify_head_simt_kernel<T><<<grid, 256, 0, st>>>((const T*)H, (const T*)W, a);
 }
 
-__global__ void verify_merge_kernel(VerifyHeadArgs a, float* z_max, int* z_arg, float* lse,
-                                    int* g_arg, float* g_max) {
-  int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= a.R) return;
-  float zb = -INFINITY, gb = -INFINITY, m = -INFINITY;
+// One block per tree node: best target logit (ties: lowest token), log-sum-exp
+// of z/T and the Gumbel-argmax over the partials of every vocabulary tile.
+__global__ void __launch_bounds__(256) verify_merge_kernel(VerifyHeadArgs a, float* z_max, int* z_arg,
+                                                           float* lse, int* g_arg, float* g_max) {
+  __shared__ float sh_zb[32], sh_m[32], sh_s[32], sh_gb[32];
+  __shared__ int sh_zi[32], sh_gi[32];
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int nw = blockDim.x >> 5;
+  float zb = -INFINITY, gb = -INFINITY, m = -INFINITY, s = 0.f;
   int zi = 0x7fffffff, gi = 0x7fffffff;
-  for (int p = 0; p < a.n_parts; ++p) {
+  for (int p = tid; p < a.n_parts; p += blockDim.x) {
     const float* o = a.part + ((size_t)p * a.R + r) * 6;
-    int i = __float_as_int(o[1]);
-    if (better(o[0], i, zb, zi)) { zb = o[0]; zi = i; }
-    int j = __float_as_int(o[5]);
-    if (better(o[4], j, gb, gi)) { gb = o[4]; gi = j; }
-    m = fmaxf(m, o[2]);
+    const float v0 = o[0], v2 = o[2], v3 = o[3], v4 = o[4];
+    const int i1 = __float_as_int(o[1]), i5 = __float_as_int(o[5]);
+    if (better(v0, i1, zb, zi)) { zb = v0; zi = i1; }
+    if (better(v4, i5, gb, gi)) { gb = v4; gi = i5; }
+    lse_fold(m, s, v2, v3);
   }
-  float s = 0.f;
-  for (int p = 0; p < a.n_parts; ++p) {
-    const float* o = a.part + ((size_t)p * a.R + r) * 6;
-    if (o[2] != -INFINITY) s += o[3] * expf(o[2] - m);
+  warp_best(zb, zi);
+  warp_best(gb, gi);
+  warp_lse(m, s);
+  if (lane == 0) {
+    sh_zb[wid] = zb; sh_zi[wid] = zi; sh_gb[wid] = gb; sh_gi[wid] = gi; sh_m[wid] = m; sh_s[wid] = s;
   }
-  z_max[r] = zb;
-  z_arg[r] = zi == 0x7fffffff ? -1 : zi;
-  lse[r] = m + logf(s);
-  g_arg[r] = gi == 0x7fffffff ? -1 : gi;
-  if (g_max) g_max[r] = gb;
+  __syncthreads();
+  if (wid == 0) {
+    zb = lane < nw ? sh_zb[lane] : -INFINITY;
+    zi = lane < nw ? sh_zi[lane] : 0x7fffffff;
+    gb = lane < nw ? sh_gb[lane] : -INFINITY;
+    gi = lane < nw ? sh_gi[lane] : 0x7fffffff;
+    m = lane < nw ? sh_m[lane] : -INFINITY;
+    s = lane < nw ? sh_s[lane] : 0.f;
+    warp_best(zb, zi);
+    warp_best(gb, gi);
+    warp_lse(m, s);
+    if (lane == 0) {
+      z_max[r] = zb;
+      z_arg[r] = zi == 0x7fffffff ? -1 : zi;
+      lse[r] = m + logf(s);
+      g_arg[r] = gi == 0x7fffffff ? -1 : gi;
+      if (g_max) g_max[r] = gb;
+    }
+  }
 }
 
 void launch_verify_merge(const VerifyHeadArgs& a, float* z_max, int* z_arg, float* lse, int* g_arg,
                          float* g_max, cudaStream_t st) {
   if (a.R <= 0) return;
-  verify_merge_kernel<<<(a.R + 127) / 128, 128, 0, st>>>(a, z_max, z_arg, lse, g_arg, g_max);
+  verify_merge_kernel<<<a.R, 256, 0, st>>>(a, z_max, z_arg, lse, g_arg, g_max);
 }
 
 template void launch_lm_head_simt<float>(const void*, const void*, int, int, int, const HeadParts&,
