@@ -22,6 +22,9 @@ using namespace e3;
 namespace {
 constexpr int kPrefillChunk = 2048;   // prefill rows per pass through the layer
 constexpr int kTargetBlocks = 2 * 148;
+// bf16 GEMM inputs of at most this many rows are stored split (hi, lo): the
+// MMA then runs 2R columns, which is free while the weights bound the time.
+constexpr int kSplitMaxRows = 128;
 
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -33,7 +36,7 @@ struct eagle3_ctx {
   bool bf;
   int esz;
   int M, M1, k, D, pool_n, n_slots, slot_words, tree_words, mask_words;
-  int rows_cap, rows_pf, rope_rows;
+  int rows_cap, rows_pf, rope_rows, act_rows;
   // arena
   char* arena = nullptr;
   size_t arena_bytes = 0;
@@ -71,6 +74,8 @@ struct eagle3_ctx {
 };
 
 namespace {
+
+bool use_split(const eagle3_ctx* c, int R) { return c->bf && R <= kSplitMaxRows; }
 
 eagle3_status fail(eagle3_ctx* c, eagle3_status s, const std::string& msg) {
   if (c) c->err = msg;
@@ -118,9 +123,9 @@ void tc_error(eagle3_ctx* c, const char* what);
 // Y[s][r][seg.col0 + n] = X W_seg^T over K, split S ways: tcgen05 for bf16
 // storage, the fp32 CUDA-core kernel for fp32 storage.
 void gemm(eagle3_ctx* c, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
-          int ldy, int R, int S, size_t split_stride, cudaStream_t st) {
+          int ldy, int R, bool split, int S, size_t split_stride, cudaStream_t st) {
   if (c->bf) {
-    if (!tc_gemm(c->tc, segs, nseg, X, ldx, K, Y, ldy, R, S, split_stride, c->flags, st))
+    if (!tc_gemm(c->tc, segs, nseg, X, ldx, K, Y, ldy, R, split, S, split_stride, c->flags, st))
       tc_error(c, "tcgen05 GEMM rejected its arguments");
     c->launches++;
     return;
@@ -133,9 +138,9 @@ void gemm(eagle3_ctx* c, const GemmSeg* segs, int nseg, const void* X, int ldx, 
 }
 
 void gemm1(eagle3_ctx* c, int wid, const void* X, int ldx, const void* W, int N, int K, float* Y,
-           int ldy, int R, int S, size_t split_stride, cudaStream_t st) {
+           int ldy, int R, bool split, int S, size_t split_stride, cudaStream_t st) {
   GemmSeg g{wid, W, N, 0};
-  gemm(c, &g, 1, X, ldx, K, Y, ldy, R, S, split_stride, st);
+  gemm(c, &g, 1, X, ldx, K, Y, ldy, R, split, S, split_stride, st);
 }
 
 struct KvTarget {  // where a pass writes K/V
@@ -146,18 +151,18 @@ struct KvTarget {  // where a pass writes K/V
 // fusion + input build + QKV (or KV only) + RoPE + KV write, for rp.kv_* rows.
 // hid_base rows for the input come from `g` when fuse_from != NULL.
 void kv_rows(eagle3_ctx* c, int R, const void* feats, bool has_q, const float* hid_base,
-             const eagle3_kv* kv, KvTarget tgt, cudaStream_t st) {
+             const eagle3_kv* kv, KvTarget tgt, bool split, cudaStream_t st) {
   const eagle3_config& f = c->cfg;
   const int d = f.d;
-  if (feats) {
+  if (feats) {  // the caller's features are exact storage values: never split
     int S = splits_for(c, R, d, 3 * d);
-    gemm1(c, TCW_FC, feats, 3 * d, c->w.w_fc, d, 3 * d, c->part, d, R, S, (size_t)R * d, st);
+    gemm1(c, TCW_FC, feats, 3 * d, c->w.w_fc, d, 3 * d, c->part, d, R, false, S, (size_t)R * d, st);
     launch_reduce_parts(R, d, S, c->part, c->g, st);
     c->launches++;
     hid_base = c->g;
   }
   DISPATCH(c, launch_build_input, R, d, f.vocab, f.rms_eps, c->rp.kv_tok, hid_base, c->rp.kv_hid,
-           c->w.embed, c->w.g_emb, c->w.g_hid, c->x, c->flags, st);
+           c->w.embed, c->w.g_emb, c->w.g_hid, c->x, split, c->flags, st);
   c->launches++;
   const int qd = f.n_q_heads * f.head_dim, kvd = f.n_kv_heads * f.head_dim;
   const int ld = (has_q ? qd : 0) + 2 * kvd;
@@ -171,7 +176,7 @@ void kv_rows(eagle3_ctx* c, int R, const void* feats, bool has_q, const float* h
   }
   segs[n++] = GemmSeg{TCW_K, c->w.w_k, kvd, col};
   segs[n++] = GemmSeg{TCW_V, c->w.w_v, kvd, col + kvd};
-  gemm(c, segs, n, c->x, 2 * d, 2 * d, c->part, ld, R, S, ss, st);
+  gemm(c, segs, n, c->x, 2 * d, 2 * d, c->part, ld, R, split, S, ss, st);
   QkvEpi p{};
   p.R = R;
   p.S = S;
@@ -212,7 +217,7 @@ void attn_splits(const eagle3_ctx* c, int B, int rows_per_req, int& kps, int& np
 
 // attention + O + FFN + final norm for rp.t_* rows (rows_per_req per request).
 void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, const eagle3_kv* kv,
-               KvTarget tree, void* h_base, cudaStream_t st) {
+               KvTarget tree, void* h_base, bool split, cudaStream_t st) {
   const eagle3_config& f = c->cfg;
   const int d = f.d, R = B * rows_per_req;
   const int qd = f.n_q_heads * f.head_dim;
@@ -242,36 +247,38 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   a.o_part = c->o_part;
   a.ml_part = c->ml_part;
   a.out = c->o;
+  a.split = split;
   a.flags = c->flags;
   DISPATCH(c, launch_tree_attention, a, st);
   c->launches += 2;
   // r = hid + W_o o ; z = rms(r)
   int S = splits_for(c, R, d, qd);
-  gemm1(c, TCW_O, c->o, qd, c->w.w_o, d, qd, c->part, d, R, S, (size_t)R * d, st);
+  gemm1(c, TCW_O, c->o, qd, c->w.w_o, d, qd, c->part, d, R, split, S, (size_t)R * d, st);
   DISPATCH(c, launch_o_epilogue, R, d, S, f.rms_eps, c->part, hid_base, c->rp.t_hid, c->w.g_post,
-           c->r, c->z, st);
+           c->r, c->z, split, st);
   c->launches++;
   // a = silu(W_g z) * W_u z  (gate and up in one GEMM: columns [0, F) and [F, 2F))
   const int F = f.ffn;
   int Sf = splits_for(c, R, 2 * F, d);
   GemmSeg gu[2] = {GemmSeg{TCW_GATE, c->w.w_gate, F, 0}, GemmSeg{TCW_UP, c->w.w_up, F, F}};
-  gemm(c, gu, 2, c->z, d, d, c->part, 2 * F, R, Sf, (size_t)R * 2 * F, st);
-  DISPATCH(c, launch_swiglu, R, F, Sf, c->part, c->a, st);
+  gemm(c, gu, 2, c->z, d, d, c->part, 2 * F, R, split, Sf, (size_t)R * 2 * F, st);
+  DISPATCH(c, launch_swiglu, R, F, Sf, c->part, c->a, split, st);
   c->launches++;
   // s = r + W_down a ; h = rms(s)
   int Sd = splits_for(c, R, d, F);
-  gemm1(c, TCW_DOWN, c->a, F, c->w.w_down, d, F, c->part, d, R, Sd, (size_t)R * d, st);
+  gemm1(c, TCW_DOWN, c->a, F, c->w.w_down, d, F, c->part, d, R, split, Sd, (size_t)R * d, st);
   DISPATCH(c, launch_down_epilogue, R, d, Sd, f.rms_eps, c->part, c->r, c->w.g_final, c->rp.t_sdst,
-           c->S, c->rp.t_out, h_base, st);
+           c->S, c->rp.t_out, h_base, split, st);
   c->launches++;
 }
 
-void draft_head(eagle3_ctx* c, const void* H, int R, int* tok, float* logq, float* lse,
+void draft_head(eagle3_ctx* c, const void* H, int R, bool split, int* tok, float* logq, float* lse,
                 cudaStream_t st) {
   HeadParts hp = c->hp;
   hp.R = R;
   if (c->bf) {
-    if (!tc_lm_head(c->tc, H, R, hp, c->flags, st)) tc_error(c, "tcgen05 LM head rejected its arguments");
+    if (!tc_lm_head(c->tc, H, R, split, hp, c->flags, st))
+      tc_error(c, "tcgen05 LM head rejected its arguments");
   } else {
     launch_lm_head_simt<float>(H, c->w.w_lm, R, c->cfg.vocab, c->cfg.d, hp, st);
   }
@@ -352,6 +359,9 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
   c->rows_pf = std::min(kPrefillChunk, std::max(1, B * f.max_prefix));
   c->rows_cap = std::max({c->rows_pf, B * f.max_new, B * k, B * c->M1});
   c->rope_rows = f.max_prefix + f.depth + 1;
+  // rows of a GEMM-input activation buffer: split rows take two
+  c->act_rows = c->bf ? std::max(c->rows_cap, 2 * std::min(c->rows_cap, kSplitMaxRows)) : c->rows_cap;
+  const int sp = c->bf ? 2 : 1;  // row factor of the head inputs, which may be split
 
   // partial buffer: largest S * R * N over the GEMMs this context runs
   size_t part = 0;
@@ -392,23 +402,23 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
   std::vector<std::pair<void**, size_t>> plan;
   auto add = [&](void** p, size_t bytes) { plan.emplace_back(p, bytes); };
   add((void**)&c->g, (size_t)std::max(c->rows_pf, B * f.max_new) * d * 4);
-  add(&c->x, (size_t)c->rows_cap * 2 * d * c->esz);
+  add(&c->x, (size_t)c->act_rows * 2 * d * c->esz);
   add((void**)&c->part, c->part_elems * 4);
   add((void**)&c->q, (size_t)c->rows_cap * qd * 4);
-  add(&c->tk, (size_t)B * std::max(1, c->n_slots) * kvd * c->esz);
-  add(&c->tv, (size_t)B * std::max(1, c->n_slots) * kvd * c->esz);
-  add(&c->vk, (size_t)B * c->M1 * kvd * c->esz);
-  add(&c->vv, (size_t)B * c->M1 * kvd * c->esz);
+  add(&c->tk, (size_t)B * std::max(1, c->n_slots) * kvd * 4);  // tree K/V scratch: fp32
+  add(&c->tv, (size_t)B * std::max(1, c->n_slots) * kvd * 4);
+  add(&c->vk, (size_t)B * c->M1 * kvd * 4);
+  add(&c->vv, (size_t)B * c->M1 * kvd * 4);
   add((void**)&c->o_part, c->attn_elems * 4);
   add((void**)&c->ml_part, c->attn_elems / f.head_dim * 2 * 4);
-  add(&c->o, (size_t)c->rows_cap * qd * c->esz);
+  add(&c->o, (size_t)c->act_rows * qd * c->esz);
   add((void**)&c->r, (size_t)c->rows_cap * d * 4);
-  add(&c->z, (size_t)c->rows_cap * d * c->esz);
-  add(&c->a, (size_t)c->rows_cap * f.ffn * c->esz);
+  add(&c->z, (size_t)c->act_rows * d * c->esz);
+  add(&c->a, (size_t)c->act_rows * f.ffn * c->esz);
   add((void**)&c->S, (size_t)n_state * d * 4);
-  add(&c->h, (size_t)Rlm * d * c->esz);
-  add(&c->h_root, (size_t)B * d * c->esz);
-  add(&c->h_ver, (size_t)Rv * d * c->esz);
+  add(&c->h, (size_t)sp * Rlm * d * c->esz);
+  add(&c->h_root, (size_t)sp * B * d * c->esz);
+  add(&c->h_ver, (size_t)sp * Rv * d * c->esz);
   add((void**)&c->rope, (size_t)c->rope_rows * (f.head_dim / 2) * sizeof(float2));
   int* rp_int[10] = {};
   for (int i = 0; i < 10; ++i) add((void**)&rp_int[i], (size_t)c->rows_cap * 4);
@@ -516,7 +526,7 @@ eagle3_status eagle3_prefill(eagle3_ctx* c, int B, int total_rows, const int* cu
     launch_plan_prefill(R, r0, B, cu_rows, tokens, kv->seq_lens, c->rp, st);
     c->launches++;
     const char* f = (const char*)feats + (size_t)r0 * 3 * d * c->esz;
-    kv_rows(c, R, f, false, nullptr, kv, KvTarget{nullptr, nullptr, 0}, st);
+    kv_rows(c, R, f, false, nullptr, kv, KvTarget{nullptr, nullptr, 0}, use_split(c, R), st);
   }
   return cuda_status(c, "prefill");
 }
@@ -539,18 +549,20 @@ eagle3_status eagle3_draft_round(eagle3_ctx* c, int B, int n_new, const void* fe
   launch_plan_root(B, n_new, tokens_new, kv->seq_lens, c->n_slots, c->rp, c->root_tok, c->root_pos,
                    c->n_prefix, st);
   c->launches++;
-  kv_rows(c, B * n_new, feats_new, true, nullptr, kv, KvTarget{nullptr, nullptr, 0}, st);
-  tail_rows(c, B, 1, c->g, kv, KvTarget{nullptr, nullptr, 0}, c->h_root, st);
-  draft_head(c, c->h_root, B, c->top_tok, c->top_logq, c->top_lse, st);
+  const bool sp0 = use_split(c, B), spk = use_split(c, B * k);
+  kv_rows(c, B * n_new, feats_new, true, nullptr, kv, KvTarget{nullptr, nullptr, 0},
+          use_split(c, B * n_new), st);
+  tail_rows(c, B, 1, c->g, kv, KvTarget{nullptr, nullptr, 0}, c->h_root, sp0, st);
+  draft_head(c, c->h_root, B, sp0, c->top_tok, c->top_logq, c->top_lse, st);
   launch_expand(B, 0, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
                 c->slot_words, c->root_pos, c->n_slots, c->rp, st);
   c->launches++;
   // passes 1..D-1: the frontier of each depth with the parent's state as hid
   KvTarget tree{c->tk, c->tv, c->n_slots};
   for (int t = 1; t < D; ++t) {
-    kv_rows(c, B * k, nullptr, true, c->S, kv, tree, st);
-    tail_rows(c, B, k, c->S, kv, tree, c->h, st);
-    draft_head(c, c->h, B * k, c->top_tok, c->top_logq, c->top_lse, st);
+    kv_rows(c, B * k, nullptr, true, c->S, kv, tree, spk, st);
+    tail_rows(c, B, k, c->S, kv, tree, c->h, spk, st);
+    draft_head(c, c->h, B * k, spk, c->top_tok, c->top_logq, c->top_lse, st);
     launch_expand(B, t, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
                   c->slot_words, c->root_pos, c->n_slots, c->rp, st);
     c->launches++;
@@ -616,11 +628,13 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
                      c->pool.fwd, c->pool_n, c->n_slots, c->rp, c->n_prefix, c->child_tok,
                      c->child_node, c->n_child, c->flags, st);
   c->launches++;
-  launch_copy_rows(B, d, c->esz, c->h_root, 1, c->h_ver, M1, st);
+  // one layout for the whole verify pass, chosen by the head's row count
+  const bool spv = use_split(c, B * M1);
+  launch_copy_rows(B, d, c->esz, c->h_root, 1, use_split(c, B), c->h_ver, M1, spv, st);
   c->launches++;
   KvTarget vt{c->vk, c->vv, M1};
-  kv_rows(c, B * M, nullptr, true, c->S, kv, vt, st);
-  tail_rows(c, B, M, c->S, kv, vt, c->h_ver, st);
+  kv_rows(c, B * M, nullptr, true, c->S, kv, vt, spv, st);
+  tail_rows(c, B, M, c->S, kv, vt, c->h_ver, spv, st);
   VerifyHeadArgs va{};
   va.R = B * M1;
   va.V = f.vocab;
@@ -636,7 +650,7 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   va.n_parts = c->n_vparts;
   va.part = c->vpart;
   if (c->bf) {
-    if (!tc_verify_head(c->tc, c->h_ver, va, c->flags, st))
+    if (!tc_verify_head(c->tc, c->h_ver, spv, va, c->flags, st))
       tc_error(c, "tcgen05 verify head rejected its arguments");
   } else {
     launch_verify_head_simt<float>(c->h_ver, c->w.w_target, va, st);
@@ -684,7 +698,7 @@ eagle3_status eagle3_lm_head_topk(eagle3_ctx* c, int R, const void* h, int* tok,
   if (!h || !tok || !logq) return fail(c, EAGLE3_ERR_INVALID_ARG, "null pointer");
   cudaStream_t st = (cudaStream_t)stream;
   c->last = st;
-  draft_head(c, h, R, tok, logq, lse, st);
+  draft_head(c, h, R, false, tok, logq, lse, st);
   return cuda_status(c, "lm_head_topk");
 }
 
@@ -708,7 +722,7 @@ eagle3_status eagle3_linear(eagle3_ctx* c, int which, int R, const void* X, floa
   if (!X || !Y) return fail(c, EAGLE3_ERR_INVALID_ARG, "null pointer");
   cudaStream_t st = (cudaStream_t)stream;
   c->last = st;
-  gemm1(c, e.id, X, e.K, e.p, e.N, e.K, Y, e.N, R, 1, (size_t)R * e.N, st);
+  gemm1(c, e.id, X, e.K, e.p, e.N, e.K, Y, e.N, R, false, 1, (size_t)R * e.N, st);
   return cuda_status(c, "linear");
 }
 

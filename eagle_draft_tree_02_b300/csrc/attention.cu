@@ -115,20 +115,19 @@ __global__ void __launch_bounds__(NT) tree_attention_kernel(AttnArgs a) {
       int kk = i / dh, dd = i % dh;
       float kv = 0.f, vv = 0.f;
       if (kk < nk) {
-        const T *kp, *vp;
         if (!tree) {
-          kp = kv_row_ptr<T>(a, a.cache_k, b, c0 + kk, kvh);
-          vp = kv_row_ptr<T>(a, a.cache_v, b, c0 + kk, kvh);
-        } else {
+          const T* kp = kv_row_ptr<T>(a, a.cache_k, b, c0 + kk, kvh);
+          const T* vp = kv_row_ptr<T>(a, a.cache_v, b, c0 + kk, kvh);
+          if (kp && vp) {
+            kv = ldf(kp + dd);
+            vv = ldf(vp + dd);
+          } else if (dd == 0) {
+            raise_flag(a.flags, FLAG_PAGE_RANGE);
+          }
+        } else {  // tree scratch is fp32
           size_t off = (((size_t)b * a.tree_slots + c0 + kk) * a.Hkv + kvh) * dh;
-          kp = (const T*)a.tree_k + off;
-          vp = (const T*)a.tree_v + off;
-        }
-        if (kp && vp) {
-          kv = ldf(kp + dd);
-          vv = ldf(vp + dd);
-        } else if (dd == 0) {
-          raise_flag(a.flags, FLAG_PAGE_RANGE);
+          kv = ((const float*)a.tree_k)[off + dd];
+          vv = ((const float*)a.tree_v)[off + dd];
         }
       }
       Ks[kk * (dh + 1) + dd] = kv;
@@ -235,7 +234,8 @@ __global__ void attention_combine_kernel(AttnArgs a) {
       float ms = a.ml_part[base * 2];
       if (ms != -INFINITY) o += a.o_part[base * a.dh + dd] * expf(ms - m);
     }
-    stf((T*)a.out + (size_t)row * a.Hq * a.dh + (size_t)head * a.dh + dd, o * inv);
+    st_act((T*)a.out + act_row(row, a.Hq * a.dh, a.split), a.Hq * a.dh, head * a.dh + dd, o * inv,
+           a.split);
   }
 }
 

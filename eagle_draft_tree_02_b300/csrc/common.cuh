@@ -27,6 +27,25 @@ template <typename T> __device__ __forceinline__ void stf(T* p, float v);
 template <> __device__ __forceinline__ void stf<float>(float* p, float v) { *p = v; }
 template <> __device__ __forceinline__ void stf<bf16>(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
 
+// Activation rows that feed a tcgen05 GEMM.  A "split" bf16 buffer stores row
+// r as two rows of K: hi = bf16(v) at row 2r and lo = bf16(v - hi) at row
+// 2r + 1, so the GEMM sees 2R rows and adds the two accumulator columns of a
+// row: the activation then carries about 16 significant bits instead of 8,
+// and the weights (the streamed operand) are still read once.  fp32 buffers
+// are never split.
+__device__ __forceinline__ size_t act_row(int r, int K, bool split) {
+  return (size_t)r * K * (split ? 2 : 1);
+}
+template <typename T> __device__ __forceinline__ void st_act(T* row, int K, int j, float v, bool split);
+template <> __device__ __forceinline__ void st_act<float>(float* row, int, int j, float v, bool) {
+  row[j] = v;
+}
+template <> __device__ __forceinline__ void st_act<bf16>(bf16* row, int K, int j, float v, bool split) {
+  const bf16 hi = __float2bfloat16_rn(v);
+  row[j] = hi;
+  if (split) row[K + j] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -19,7 +19,8 @@ template <typename T>
 __global__ void build_input_kernel(int R, int d, int V, float eps, const int* __restrict__ tok,
                                    const float* __restrict__ hid_base, const int* __restrict__ hid_row,
                                    const T* __restrict__ E, const T* __restrict__ g_emb,
-                                   const T* __restrict__ g_hid, T* __restrict__ x, int* flags) {
+                                   const T* __restrict__ g_hid, T* __restrict__ x, bool split,
+                                   int* flags) {
   __shared__ float red[32];
   int r = blockIdx.x;
   int t = tok[r];
@@ -38,10 +39,10 @@ __global__ void build_input_kernel(int R, int d, int V, float eps, const int* __
   se = block_sum(se, red);
   sh = block_sum(sh, red);
   float ie = rsqrtf(se / d + eps), ih = rsqrtf(sh / d + eps);
-  T* xr = x + (size_t)r * 2 * d;
+  T* xr = x + act_row(r, 2 * d, split);
   for (int j = threadIdx.x; j < d; j += blockDim.x) {
-    stf(xr + j, ldf(e + j) * ie * ldf(g_emb + j));
-    stf(xr + d + j, h[j] * ih * ldf(g_hid + j));
+    st_act(xr, 2 * d, j, ldf(e + j) * ie * ldf(g_emb + j), split);
+    st_act(xr, 2 * d, d + j, h[j] * ih * ldf(g_hid + j), split);
   }
 }
 
@@ -100,11 +101,15 @@ __global__ void qkv_epilogue_kernel(QkvEpi p) {
   int kvh = is_v ? hh - qh - p.Hkv : hh - qh;
   int b = p.row_b[r];
   int dst = p.row_dst[r];
-  T* out;
-  if (dst >= 0) {  // tree scratch slot of this request
+  if (dst >= 0) {  // tree scratch slot of this request: fp32, the library's own format
     size_t off = (((size_t)b * p.tree_slots + dst) * p.Hkv + kvh) * p.dh;
-    out = (T*)(is_v ? p.tree_v : p.tree_k) + off;
-  } else {  // prefix cache at `pos`
+    float* tout = (float*)(is_v ? p.tree_v : p.tree_k) + off;
+    tout[j] = x1;
+    tout[j + half] = x2;
+    return;
+  }
+  T* out;
+  {  // prefix cache at `pos`, in the cache's storage type
     size_t row;
     if (p.page_table) {
       int lp = pos / p.page_size;
@@ -136,7 +141,7 @@ template <typename T>
 __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* __restrict__ part,
                                   const float* __restrict__ hid_base, const int* __restrict__ hid_row,
                                   const T* __restrict__ g_post, float* __restrict__ r_out,
-                                  T* __restrict__ z_out) {
+                                  T* __restrict__ z_out, bool split) {
   __shared__ float red[32];
   int r = blockIdx.x;
   const float* h = hid_base + (size_t)hid_row[r] * d;
@@ -149,14 +154,16 @@ __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* _
   }
   ss = block_sum(ss, red);
   float inv = rsqrtf(ss / d + eps);
+  T* zr = z_out + act_row(r, d, split);
   for (int j = threadIdx.x; j < d; j += blockDim.x)
-    stf(z_out + (size_t)r * d + j, r_out[(size_t)r * d + j] * inv * ldf(g_post + j));
+    st_act(zr, d, j, r_out[(size_t)r * d + j] * inv * ldf(g_post + j), split);
 }
 
 // ----------------------------------------------------------------------------- a = silu(W_g z) * (W_u z)
 // part: [S][R][2F], gate in columns [0, F), up in [F, 2F)
 template <typename T>
-__global__ void swiglu_kernel(int R, int F, int S, const float* __restrict__ part, T* __restrict__ a) {
+__global__ void swiglu_kernel(int R, int F, int S, const float* __restrict__ part, T* __restrict__ a,
+                              bool split) {
   size_t n = (size_t)R * F;
   size_t stride = (size_t)R * 2 * F;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
@@ -164,7 +171,7 @@ __global__ void swiglu_kernel(int R, int F, int S, const float* __restrict__ par
     const float* p = part + r * 2 * F + c;
     float g = sum_parts(p, stride, S);
     float u = sum_parts(p + F, stride, S);
-    stf(a + i, g / (1.f + expf(-g)) * u);
+    st_act(a + act_row((int)r, F, split), F, (int)c, g / (1.f + expf(-g)) * u, split);
   }
 }
 
@@ -173,7 +180,8 @@ template <typename T>
 __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float* __restrict__ part,
                                      const float* __restrict__ r_in, const T* __restrict__ g_final,
                                      const int* __restrict__ s_dst, float* __restrict__ s_base,
-                                     const int* __restrict__ h_dst, T* __restrict__ h_base) {
+                                     const int* __restrict__ h_dst, T* __restrict__ h_base,
+                                     bool split) {
   __shared__ float red[32];
   extern __shared__ float srow[];
   int r = blockIdx.x;
@@ -188,9 +196,10 @@ __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float
   float inv = rsqrtf(ss / d + eps);
   int sd = s_dst ? s_dst[r] : -1;
   int hd = h_dst ? h_dst[r] : r;
+  T* hr = h_base + act_row(hd, d, split);
   for (int j = threadIdx.x; j < d; j += blockDim.x) {
     if (sd >= 0) s_base[(size_t)sd * d + j] = srow[j];
-    stf(h_base + (size_t)hd * d + j, srow[j] * inv * ldf(g_final + j));
+    st_act(hr, d, j, srow[j] * inv * ldf(g_final + j), split);
   }
 }
 
@@ -202,10 +211,10 @@ constexpr int kRowThreads = 1024;
 template <typename T>
 void launch_build_input(int R, int d, int V, float eps, const int* tok, const float* hid_base,
                         const int* hid_row, const void* E, const void* g_emb, const void* g_hid,
-                        void* x, int* flags, cudaStream_t st) {
+                        void* x, bool split, int* flags, cudaStream_t st) {
   if (R <= 0) return;
   build_input_kernel<T><<<R, kRowThreads, 0, st>>>(R, d, V, eps, tok, hid_base, hid_row, (const T*)E,
-                                           (const T*)g_emb, (const T*)g_hid, (T*)x, flags);
+                                           (const T*)g_emb, (const T*)g_hid, (T*)x, split, flags);
 }
 
 void launch_reduce_parts(int R, int N, int S, const float* part, float* out, cudaStream_t st) {
@@ -228,41 +237,41 @@ void launch_qkv_epilogue(const QkvEpi& p, cudaStream_t st) {
 template <typename T>
 void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const float* hid_base,
                        const int* hid_row, const void* g_post, float* r_out, void* z_out,
-                       cudaStream_t st) {
+                       bool split, cudaStream_t st) {
   if (R <= 0) return;
   o_epilogue_kernel<T><<<R, kRowThreads, 0, st>>>(R, d, S, eps, part, hid_base, hid_row, (const T*)g_post,
-                                          r_out, (T*)z_out);
+                                          r_out, (T*)z_out, split);
 }
 
 template <typename T>
-void launch_swiglu(int R, int F, int S, const float* part, void* a, cudaStream_t st) {
+void launch_swiglu(int R, int F, int S, const float* part, void* a, bool split, cudaStream_t st) {
   size_t n = (size_t)R * F;
   if (!n) return;
   int blocks = (int)((n + 255) / 256);
   if (blocks > 148 * 16) blocks = 148 * 16;
-  swiglu_kernel<T><<<blocks, 256, 0, st>>>(R, F, S, part, (T*)a);
+  swiglu_kernel<T><<<blocks, 256, 0, st>>>(R, F, S, part, (T*)a, split);
 }
 
 template <typename T>
 void launch_down_epilogue(int R, int d, int S, float eps, const float* part, const float* r_in,
                           const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
-                          void* h_base, cudaStream_t st) {
+                          void* h_base, bool split, cudaStream_t st) {
   if (R <= 0) return;
   down_epilogue_kernel<T><<<R, kRowThreads, d * sizeof(float), st>>>(R, d, S, eps, part, r_in,
                                                             (const T*)g_final, s_dst, s_base, h_dst,
-                                                            (T*)h_base);
+                                                            (T*)h_base, split);
 }
 
 #define E3_INST(T)                                                                                   \
   template void launch_build_input<T>(int, int, int, float, const int*, const float*, const int*,   \
-                                      const void*, const void*, const void*, void*, int*,           \
+                                      const void*, const void*, const void*, void*, bool, int*,     \
                                       cudaStream_t);                                                 \
   template void launch_qkv_epilogue<T>(const QkvEpi&, cudaStream_t);                                 \
   template void launch_o_epilogue<T>(int, int, int, float, const float*, const float*, const int*,  \
-                                     const void*, float*, void*, cudaStream_t);                      \
-  template void launch_swiglu<T>(int, int, int, const float*, void*, cudaStream_t);                  \
+                                     const void*, float*, void*, bool, cudaStream_t);                \
+  template void launch_swiglu<T>(int, int, int, const float*, void*, bool, cudaStream_t);            \
   template void launch_down_epilogue<T>(int, int, int, float, const float*, const float*,           \
-                                        const void*, const int*, float*, const int*, void*,         \
+                                        const void*, const int*, float*, const int*, void*, bool,   \
                                         cudaStream_t);
 E3_INST(float)
 E3_INST(bf16)

@@ -35,7 +35,10 @@ constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int kSmemBudget = 100 * 1024;   // per CTA: two CTAs share an SM
 
 struct TcArgs {
-  int R, n_kb, kb_per_split, ntile, stages;
+  int R;       // activation rows
+  int ncols;   // MMA columns = rows of the B operand: R, or 2R for split rows (hi, lo)
+  int split;
+  int n_kb, kb_per_split, ntile, stages;
   uint32_t tmem_cols, idesc;
   int nseg;
   int seg_end[3];   // cumulative m-tile count per segment
@@ -246,12 +249,12 @@ __global__ void __launch_bounds__(128, 1)
   volatile int* abort_f = reinterpret_cast<volatile int*>(gen + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x, split = blockIdx.z;
+  const int mt = blockIdx.x, ks = blockIdx.z;  // m-tile, K split
   int seg = 0;
   while (seg < a.nseg - 1 && mt >= a.seg_end[seg]) ++seg;
   const int m0 = (mt - (seg ? a.seg_end[seg - 1] : 0)) * BM;
   const int n0 = blockIdx.y * a.ntile;
-  const int kb0 = split * a.kb_per_split;
+  const int kb0 = ks * a.kb_per_split;
   const int nkb = max(0, min(a.n_kb, kb0 + a.kb_per_split) - kb0);
 
   if (threadIdx.x == 0) {
@@ -306,32 +309,46 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
 
   const int row_feat = m0 + warp * 32 + lane;  // weight row (output feature / token) of this thread
+  // one accumulator value of activation row r
+  auto emit = [&](int r, float val) {
+    if (MODE == 0) {
+      if (row_feat < a.seg_N[seg])
+        a.Y[(size_t)ks * a.split_stride + (size_t)r * a.ldy + a.seg_col0[seg] + row_feat] = val;
+    } else if (MODE == 1) {
+      const bool ok = row_feat < a.seg_N[0];
+      head_row(a.hp, mt * 4 + warp, r, ok ? val : -INFINITY, ok ? row_feat : 0x7fffffff, lane);
+    } else {
+      verify_row(a.va, mt * 4 + warp, r, val, row_feat, row_feat < a.seg_N[0], lane);
+    }
+  };
   if (run) {
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     for (int c0 = 0; c0 < a.ntile; c0 += 16) {
-      if (n0 + c0 >= a.R) break;
+      if (n0 + c0 >= a.ncols) break;
       uint32_t v[16];
       tmem_ld16(trow + (uint32_t)c0, v);
+      if (a.split) {  // columns 2r, 2r+1 hold row r's hi and lo halves
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int r = n0 + c0 + j;
-        if (r >= a.R) break;
-        const float val = __uint_as_float(v[j]);
-        if (MODE == 0) {
-          if (row_feat < a.seg_N[seg])
-            a.Y[(size_t)split * a.split_stride + (size_t)r * a.ldy + a.seg_col0[seg] + row_feat] = val;
-        } else if (MODE == 1) {
-          const bool ok = row_feat < a.seg_N[0];
-          head_row(a.hp, mt * 4 + warp, r, ok ? val : -INFINITY, ok ? row_feat : 0x7fffffff, lane);
-        } else {
-          verify_row(a.va, mt * 4 + warp, r, val, row_feat, row_feat < a.seg_N[0], lane);
+        for (int j = 0; j < 16; j += 2) {
+          const int col = n0 + c0 + j;
+          if (col >= a.ncols) break;
+          emit(col >> 1, __uint_as_float(v[j]) + __uint_as_float(v[j + 1]));
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = n0 + c0 + j;
+          if (col >= a.ncols) break;
+          emit(col, __uint_as_float(v[j]));
         }
       }
     }
   } else if (MODE == 0 && nkb == 0 && row_feat < a.seg_N[seg]) {
     // an empty K split still contributes its (zero) partial
-    for (int r = n0; r < min(a.R, n0 + a.ntile); ++r)
-      a.Y[(size_t)split * a.split_stride + (size_t)r * a.ldy + a.seg_col0[seg] + row_feat] = 0.f;
+    const int r0 = a.split ? n0 / 2 : n0;
+    const int r1 = min(a.R, a.split ? (n0 + a.ntile) / 2 : n0 + a.ntile);
+    for (int r = r0; r < r1; ++r)
+      a.Y[(size_t)ks * a.split_stride + (size_t)r * a.ldy + a.seg_col0[seg] + row_feat] = 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -446,11 +463,15 @@ uint32_t make_idesc(int n) {
 
 template <int MODE>
 bool launch(TcGemm* t, const CUtensorMap* a0, const CUtensorMap* a1, const CUtensorMap* a2,
-            const void* X, int ldx, int K, int R, int S, TcArgs& args, int grid_x, cudaStream_t st) {
-  Launch L = plan_launch(R);
+            const void* X, int ldx, int K, int R, bool split, int S, TcArgs& args, int grid_x,
+            cudaStream_t st) {
+  const int ncols = split ? 2 * R : R;
+  Launch L = plan_launch(ncols);
   CUtensorMap mb;
-  if (!encode_map(t->encode, &mb, X, R, K, (size_t)ldx * 2, L.ntile)) return false;
+  if (!encode_map(t->encode, &mb, X, ncols, K, (size_t)ldx * 2, L.ntile)) return false;
   args.R = R;
+  args.ncols = ncols;
+  args.split = split ? 1 : 0;
   args.n_kb = cdiv(K, BK);
   args.kb_per_split = cdiv(args.n_kb, S);
   args.ntile = L.ntile;
@@ -470,7 +491,7 @@ bool launch(TcGemm* t, const CUtensorMap* a0, const CUtensorMap* a1, const CUten
 }  // namespace
 
 bool tc_gemm(TcGemm* t, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
-             int ldy, int R, int S, size_t split_stride, int* flags, cudaStream_t st) {
+             int ldy, int R, bool split, int S, size_t split_stride, int* flags, cudaStream_t st) {
   if (!t || nseg < 1 || nseg > 3 || R <= 0) return false;
   TcArgs args{};
   const CUtensorMap* maps[3];
@@ -492,10 +513,11 @@ bool tc_gemm(TcGemm* t, const GemmSeg* segs, int nseg, const void* X, int ldx, i
   args.ldy = ldy;
   args.split_stride = split_stride;
   args.flags = flags;
-  return launch<0>(t, maps[0], maps[1], maps[2], X, ldx, K, R, S, args, tiles, st);
+  return launch<0>(t, maps[0], maps[1], maps[2], X, ldx, K, R, split, S, args, tiles, st);
 }
 
-bool tc_lm_head(TcGemm* t, const void* H, int R, const HeadParts& hp, int* flags, cudaStream_t st) {
+bool tc_lm_head(TcGemm* t, const void* H, int R, bool split, const HeadParts& hp, int* flags,
+                cudaStream_t st) {
   if (!t || !t->wptr[TCW_LM] || R <= 0 || R > 256 || hp.n_parts != tc_head_parts(t->V)) return false;
   TcArgs args{};
   args.nseg = 1;
@@ -504,10 +526,12 @@ bool tc_lm_head(TcGemm* t, const void* H, int R, const HeadParts& hp, int* flags
   args.hp = hp;
   args.flags = flags;
   const CUtensorMap* m = &t->wmap[TCW_LM];
-  return launch<1>(t, m, m, m, H, t->wK[TCW_LM], t->wK[TCW_LM], R, 1, args, args.seg_end[0], st);
+  return launch<1>(t, m, m, m, H, t->wK[TCW_LM], t->wK[TCW_LM], R, split, 1, args, args.seg_end[0],
+                   st);
 }
 
-bool tc_verify_head(TcGemm* t, const void* H, const VerifyHeadArgs& va, int* flags, cudaStream_t st) {
+bool tc_verify_head(TcGemm* t, const void* H, bool split, const VerifyHeadArgs& va, int* flags,
+                    cudaStream_t st) {
   if (!t || !t->wptr[TCW_T] || va.R <= 0 || va.n_parts != tc_head_parts(t->V)) return false;
   TcArgs args{};
   args.nseg = 1;
@@ -516,7 +540,8 @@ bool tc_verify_head(TcGemm* t, const void* H, const VerifyHeadArgs& va, int* fla
   args.va = va;
   args.flags = flags;
   const CUtensorMap* m = &t->wmap[TCW_T];
-  return launch<2>(t, m, m, m, H, t->wK[TCW_T], t->wK[TCW_T], va.R, 1, args, args.seg_end[0], st);
+  return launch<2>(t, m, m, m, H, t->wK[TCW_T], t->wK[TCW_T], va.R, split, 1, args, args.seg_end[0],
+                   st);
 }
 
 }  // namespace e3

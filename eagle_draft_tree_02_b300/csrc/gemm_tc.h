@@ -31,11 +31,14 @@ TcGemm* tc_create(const eagle3_config& cfg, const eagle3_weights& w, char* err, 
 void tc_destroy(TcGemm* t);
 int tc_splits(int R, int n_mtiles, int K);
 int tc_head_parts(int V);
-// Y[s][r][col0 + n] for each segment; all segments share X and K.  Returns
-// false (and nothing is launched) on an unusable argument.
+// Y[s][r][col0 + n] for each segment; all segments share X and K.  With
+// `split`, X holds each row r as a (hi, lo) pair of bf16 rows 2r, 2r+1 (see
+// st_act) and the product is taken on their sum.  Returns false (and nothing
+// is launched) on an unusable argument.
 bool tc_gemm(TcGemm* t, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
-             int ldy, int R, int S, size_t split_stride, int* flags, cudaStream_t st);
-bool tc_lm_head(TcGemm* t, const void* H, int R, const HeadParts& hp, int* flags, cudaStream_t st);
-bool tc_verify_head(TcGemm* t, const void* H, const VerifyHeadArgs& a, int* flags, cudaStream_t st);
-
+             int ldy, int R, bool split, int S, size_t split_stride, int* flags, cudaStream_t st);
+bool tc_lm_head(TcGemm* t, const void* H, int R, bool split, const HeadParts& hp, int* flags,
+                cudaStream_t st);
+bool tc_verify_head(TcGemm* t, const void* H, bool split, const VerifyHeadArgs& a, int* flags,
+                    cudaStream_t st);
 }  // namespace e3

@@ -17,7 +17,7 @@ struct QkvEpi {
   void *cache_k, *cache_v;  // prefix cache
   const int* page_table;    // NULL = contiguous
   int page_size, max_pages, n_pages, max_prefix;
-  void *tree_k, *tree_v;    // tree scratch [B][tree_slots][Hkv][dh]
+  void *tree_k, *tree_v;    // tree scratch [B][tree_slots][Hkv][dh], fp32
   int tree_slots;
   int* flags;
 };
@@ -25,20 +25,20 @@ struct QkvEpi {
 template <typename T>
 void launch_build_input(int R, int d, int V, float eps, const int* tok, const float* hid_base,
                         const int* hid_row, const void* E, const void* g_emb, const void* g_hid,
-                        void* x, int* flags, cudaStream_t st);
+                        void* x, bool split, int* flags, cudaStream_t st);
 void launch_reduce_parts(int R, int N, int S, const float* part, float* out, cudaStream_t st);
 template <typename T> void launch_qkv_epilogue(const QkvEpi& p, cudaStream_t st);
 template <typename T>
 void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const float* hid_base,
                        const int* hid_row, const void* g_post, float* r_out, void* z_out,
-                       cudaStream_t st);
+                       bool split, cudaStream_t st);
 // part: [S][R][2F] with the gate in columns [0, F) and up in [F, 2F)
 template <typename T>
-void launch_swiglu(int R, int F, int S, const float* part, void* a, cudaStream_t st);
+void launch_swiglu(int R, int F, int S, const float* part, void* a, bool split, cudaStream_t st);
 template <typename T>
 void launch_down_epilogue(int R, int d, int S, float eps, const float* part, const float* r_in,
                           const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
-                          void* h_base, cudaStream_t st);
+                          void* h_base, bool split, cudaStream_t st);
 
 // ----------------------------------------------------------------------------- gemm_simt.cu
 // Y[s][r][col0 + n] = sum_{k in split s} X[r][k] W[n][k]  (fp32 accumulate)
@@ -55,14 +55,15 @@ struct AttnArgs {
   const void *cache_k, *cache_v;
   const int* page_table;
   int page_size, max_pages, n_pages, max_prefix;
-  const void *tree_k, *tree_v;  // [B][tree_slots][Hkv][dh]
+  const void *tree_k, *tree_v;  // [B][tree_slots][Hkv][dh], fp32
   int tree_slots;
   const uint32_t* mask;    // [R][mask_words] bits over tree slots
   int mask_words;
   int keys_per_split, n_prefix_splits, n_tree_splits;
   float* o_part;           // [n_splits][R][Hq][dh]
   float* ml_part;          // [n_splits][R][Hq][2]
-  void* out;               // [R][Hq dh] storage type
+  void* out;               // [R][Hq dh] storage type (split rows: see st_act)
+  bool split;
   int* flags;
 };
 template <typename T> void launch_tree_attention(const AttnArgs& a, cudaStream_t st);
@@ -128,8 +129,12 @@ void launch_plan_verify(int B, int M, int kmax, const int* t_tok, const int* t_p
                         const int* pool_fwd, int pool_n, int n_slots, const RowPlan& rp,
                         int* n_prefix, int* child_tok, int* child_node, int* n_child, int* flags,
                         cudaStream_t st);
+// Copy B activation rows of d elements: row b of src (index b * src_stride_rows)
+// to row b * dst_stride_rows of dst, each buffer split or plain (see st_act);
+// a plain source gives a zero lo row in a split destination.
 void launch_copy_rows(int B, int d, int elem_bytes, const void* src, int src_stride_rows,
-                      void* dst, int dst_stride_rows, cudaStream_t st);
+                      bool src_split, void* dst, int dst_stride_rows, bool dst_split,
+                      cudaStream_t st);
 void launch_copy_pool(int B, const PoolDev& pool, int* tok, int* parent, int* depth, int* fwd,
                       float* score, float* logq, cudaStream_t st);
 

@@ -344,17 +344,25 @@ void launch_plan_verify(int B, int M, int kmax, const int* t_tok, const int* t_p
 }
 
 // ----------------------------------------------------------------------------- small copies
-__global__ void copy_rows_kernel(int d_bytes, const char* src, size_t src_stride, char* dst,
-                                 size_t dst_stride) {
-  int b = blockIdx.x;
-  for (int i = threadIdx.x; i < d_bytes; i += blockDim.x) dst[b * dst_stride + i] = src[b * src_stride + i];
+__global__ void copy_rows_kernel(int row_bytes, const char* src, size_t src_step, bool src_split,
+                                 char* dst, size_t dst_step, bool dst_split) {
+  const int b = blockIdx.x;
+  const char* sr = src + b * src_step;
+  char* dr = dst + b * dst_step;
+  for (int i = threadIdx.x; i < row_bytes; i += blockDim.x) {
+    dr[i] = sr[i];
+    if (dst_split) dr[row_bytes + i] = src_split ? sr[row_bytes + i] : 0;
+  }
 }
 
-void launch_copy_rows(int B, int d, int elem_bytes, const void* src, int src_stride_rows, void* dst,
-                      int dst_stride_rows, cudaStream_t st) {
-  size_t row = (size_t)d * elem_bytes;
-  copy_rows_kernel<<<B, 256, 0, st>>>((int)row, (const char*)src, row * src_stride_rows, (char*)dst,
-                                      row * dst_stride_rows);
+void launch_copy_rows(int B, int d, int elem_bytes, const void* src, int src_stride_rows,
+                      bool src_split, void* dst, int dst_stride_rows, bool dst_split,
+                      cudaStream_t st) {
+  const size_t row = (size_t)d * elem_bytes;
+  copy_rows_kernel<<<B, 256, 0, st>>>((int)row, (const char*)src,
+                                      row * src_stride_rows * (src_split ? 2 : 1), src_split,
+                                      (char*)dst, row * dst_stride_rows * (dst_split ? 2 : 1),
+                                      dst_split);
 }
 
 __global__ void copy_pool_kernel(int n, PoolDev p, int* tok, int* parent, int* depth, int* fwd,
