@@ -544,4 +544,28 @@ bool tc_verify_head(TcGemm* t, const void* H, bool split, const VerifyHeadArgs& 
                    st);
 }
 
+bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, const HeadParts& hp,
+                    int* flags, cudaStream_t st) {
+  static const EncodeFn enc = []() -> EncodeFn {  // looked up once, thread-safe
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<EncodeFn>(fn);
+  }();
+  if (!enc) return false;
+  TcGemm t;
+  t.encode = enc;
+  t.V = V;
+  if (!encode_map(enc, &t.wmap[TCW_LM], W, V, d, (size_t)d * 2, BM)) return false;
+  t.wptr[TCW_LM] = W;
+  t.wN[TCW_LM] = V;
+  t.wK[TCW_LM] = d;
+  return tc_lm_head(&t, H, R, false, hp, flags, st);
+}
+
 }  // namespace e3

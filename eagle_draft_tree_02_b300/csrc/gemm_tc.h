@@ -41,4 +41,9 @@ bool tc_lm_head(TcGemm* t, const void* H, int R, bool split, const HeadParts& hp
                 cudaStream_t st);
 bool tc_verify_head(TcGemm* t, const void* H, bool split, const VerifyHeadArgs& a, int* flags,
                     cudaStream_t st);
+// The draft-head launch of tc_lm_head on a bare weight pointer W [V, d] (bf16),
+// with no TcGemm object: the tensor maps are encoded on the host stack and
+// nothing is allocated.  False (nothing launched) on an unusable argument.
+bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, const HeadParts& hp,
+                    int* flags, cudaStream_t st);
 }  // namespace e3

@@ -71,6 +71,8 @@ _sig = {
                                 C.c_float, C.c_ulonglong, C.c_ulonglong, _P, _P, _P,
                                 C.POINTER(eagle3_verify_stats), _P]),
     "eagle3_lm_head_topk": (C.c_int, [_P, C.c_int, _P, _P, _P, _P, _P]),
+    "eagle3_lm_head_topk_noalloc": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, _P, C.c_int, _P,
+                                              _P, _P, _P, _P, _P]),
     "eagle3_linear": (C.c_int, [_P, C.c_int, C.c_int, _P, _P, _P]),
     "eagle3_check": (C.c_int, [_P]),
     "eagle3_last_error": (C.c_char_p, [_P]),
@@ -136,6 +138,12 @@ def eagle3_verify(ctx, B, tree: eagle3_tree, kv: eagle3_kv, mode, temperature, s
 
 def eagle3_lm_head_topk(ctx, R, h, tok, logq, lse=None, stream=0) -> int:
     return lib.eagle3_lm_head_topk(ctx, R, h, tok, logq, lse, stream)
+
+
+def eagle3_lm_head_topk_noalloc(dtype, vocab, d, topk, w_lm, R, h, tok, logq, lse=None,
+                                dev_status=None, stream=0) -> int:
+    return lib.eagle3_lm_head_topk_noalloc(dtype, vocab, d, topk, w_lm, R, h, tok, logq, lse,
+                                           dev_status, stream)
 
 
 def eagle3_linear(ctx, which, R, X, Y, stream=0) -> int:

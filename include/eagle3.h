@@ -199,6 +199,32 @@ eagle3_status eagle3_verify(eagle3_ctx* ctx, int B, const eagle3_tree* tree, con
 eagle3_status eagle3_lm_head_topk(eagle3_ctx* ctx, int R, const void* h, int* tok, float* logq,
                                   float* lse, eagle3_stream stream);
 
+/* The draft LM head and top-k of eagle3_lm_head_topk without a context, for
+ * callers that cannot allocate device memory: a server runtime that has
+ * reserved all of HBM for its own pools, a plugin restricted to its host
+ * framework's allocator, or a latency-critical path that cannot afford
+ * cudaMalloc's implicit synchronisation.  (The pages have no counterpart: this
+ * is a deployment variant of the same computation.)
+ *   w_lm [vocab, d] and h [R, d] in `dtype` (EAGLE3_FP32 or EAGLE3_BF16),
+ *   device, caller-owned; tok [R, topk] int32, logq [R, topk] fp32 and lse [R]
+ *   fp32 (may be NULL) are written as by eagle3_lm_head_topk.  dev_status
+ *   (device int, may be NULL) receives the device error flags of this call
+ *   (0 = none) in stream order.
+ * Scratch: the per-tile partials live in one 16 MiB array in the library's
+ * device global memory (held on every GPU that loads the library until exit).
+ * Calls needing more -- 256 + P*R*(2 + 2*topk)*4 bytes, 256-byte aligned per
+ * part, with P = 4*ceil(vocab/128) (bf16) or ceil(vocab/64) (fp32) -- return
+ * EAGLE3_ERR_SHAPE and launch nothing.  bf16 also needs d % 8 == 0, 16-byte
+ * aligned w_lm and h, and R <= 256 (EAGLE3_ERR_INVALID_ARG / _SHAPE).
+ * Nothing is allocated and no allocating routine is called.  The first call
+ * on a device looks up the array's device address (with that device current)
+ * and caches it; make that first call before capturing any stream.  Every
+ * call shares the array and it keeps the last call's contents: calls whose
+ * work may overlap on the GPU race and must be ordered by the caller. */
+eagle3_status eagle3_lm_head_topk_noalloc(int dtype, int vocab, int d, int topk, const void* w_lm,
+                                          int R, const void* h, int* tok, float* logq, float* lse,
+                                          int* dev_status, eagle3_stream stream);
+
 /* One of the context's weight matrices applied to R given rows, for kernel
  * tests: Y [R, N] (fp32, device) = X [R, K] (config dtype, device) W^T, with
  * which = 0 w_fc, 1 w_q, 2 w_k, 3 w_v, 4 w_o, 5 w_gate, 6 w_up, 7 w_down,

@@ -66,3 +66,22 @@ def test_null_context_calls_fail_cleanly(E):
     assert E.eagle3_check(0) == E.ERR_INVALID_ARG
     assert E.eagle3_last_error(0) == "null context"
     assert E.eagle3_workspace_bytes(0) == 0
+
+
+def test_noalloc_head_rejects_bad_requests_before_launch(E):
+    """Argument checks of the allocation-free head run on the host, before any CUDA call."""
+    ok_args = dict(dtype=E.BF16, vocab=128256, d=4096, topk=10, w_lm=0x10000, R=10, h=0x20000,
+                   tok=0x30000, logq=0x40000)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return E.eagle3_lm_head_topk_noalloc(a["dtype"], a["vocab"], a["d"], a["topk"], a["w_lm"],
+                                             a["R"], a["h"], a["tok"], a["logq"])
+    assert call(dtype=7) == E.ERR_INVALID_ARG
+    assert call(topk=17) == E.ERR_INVALID_ARG
+    assert call(R=0) == E.ERR_INVALID_ARG
+    assert call(w_lm=None) == E.ERR_INVALID_ARG
+    assert call(w_lm=0x10008) == E.ERR_INVALID_ARG      # TMA needs 16-byte aligned bases
+    assert call(d=4100) == E.ERR_INVALID_ARG            # ... and 16-byte rows
+    assert call(R=257) == E.ERR_SHAPE                   # tensor-core head: <= 256 rows
+    assert call(R=200) == E.ERR_SHAPE                   # partials beyond the 16 MiB scratch
