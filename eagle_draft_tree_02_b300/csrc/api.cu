@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "gemm_tc.h"
 #include "kernels.h"
+#include "lowrank.h"
 
 using namespace e3;
 
@@ -57,6 +58,12 @@ struct eagle3_ctx {
   PoolDev pool;
   int* frontier;
   uint32_t* slot_mask;
+  // two-stage head
+  bool lr = false;
+  LowRankArgs la{};  // base pointers and sizes; per call: rows, inputs, outputs
+  void* lr_t = nullptr;
+  int* cand_all = nullptr;  // [B][n_exp][lr_cand] candidates of every expanded node
+  int n_exp = 0;
   // verify
   int *child_tok, *child_node, *n_child, *z_arg, *g_arg;
   float *child_z, *vpart, *z_max, *lse, *g_max;
@@ -272,8 +279,50 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   c->launches++;
 }
 
+// Two-stage head: t = V_lr h, low-rank sample and threshold, threshold append,
+// then per row the sort, exact rescoring, log q over the candidates and top-k.
+// slot0 >= 0 exports the candidates of rows b*rpr + j to node slot slot0 + j.
+void draft_head_lowrank(eagle3_ctx* c, const void* H, int R, bool split, int* tok, float* logq,
+                        float* lse, int slot0, int rpr, cudaStream_t st) {
+  const eagle3_config& f = c->cfg;
+  const int d = f.d, r = f.lr_rank;
+  LowRankArgs la = c->la;
+  la.R = R;
+  la.H = H;
+  la.h_split = split;
+  la.t_split = use_split(c, R);
+  la.tok = tok;
+  la.logq = logq;
+  la.lse = lse;
+  la.cand_out = slot0 >= 0 ? c->cand_all : nullptr;
+  la.cand_slot0 = slot0;
+  la.cand_rpr = rpr;
+  const int S = splits_for(c, R, r, d);
+  gemm1(c, TCW_LRV, H, d, c->w.lr_v, r, d, c->part, r, R, split, S, (size_t)R * r, st);
+  DISPATCH(c, launch_reduce_store, R, r, S, c->part, c->lr_t, la.t_split != 0, st);
+  c->launches++;
+  for (int mode = 0; mode < 2; ++mode) {
+    if (c->bf) {
+      if (!tc_lowrank(c->tc, mode, la, c->flags, st)) tc_error(c, "tcgen05 low-rank head rejected its arguments");
+    } else {
+      launch_lowrank_simt<float>(mode, la, st);
+    }
+    c->launches++;
+    if (mode == 0) {
+      launch_lowrank_threshold(la, st);
+      c->launches++;
+    }
+  }
+  DISPATCH(c, launch_lowrank_select, la, st);
+  c->launches++;
+}
+
 void draft_head(eagle3_ctx* c, const void* H, int R, bool split, int* tok, float* logq, float* lse,
-                cudaStream_t st) {
+                cudaStream_t st, int slot0 = -1, int rpr = 1) {
+  if (c->lr) {
+    draft_head_lowrank(c, H, R, split, tok, logq, lse, slot0, rpr, st);
+    return;
+  }
   HeadParts hp = c->hp;
   hp.R = R;
   if (c->bf) {
@@ -323,9 +372,11 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
     return EAGLE3_ERR_UNSUPPORTED;
   const int pool_n = f.topk + (f.depth - 1) * f.topk * f.topk;
   if (f.n_verify > pool_n) return EAGLE3_ERR_SHAPE;
-  if (f.lr_rank < 0 || (f.lr_rank > 0 && (f.lr_cand < f.topk || f.lr_cand > 128 || !w->lr_u || !w->lr_v)))
+  if (f.lr_rank < 0 || (f.lr_rank > 0 && (f.lr_cand < f.topk || f.lr_cand > 128 || f.lr_cand > f.vocab ||
+                                           f.lr_rank % 8 || f.lr_rank > 4096 || !w->lr_u || !w->lr_v)))
     return EAGLE3_ERR_INVALID_ARG;
-  if (f.lr_rank > 0) return EAGLE3_ERR_UNSUPPORTED;  // two-stage head: not built yet
+  // bf16 streams U [V, r] in 64-column TMA boxes
+  if (f.lr_rank > 0 && f.dtype == EAGLE3_BF16 && f.lr_rank % 64) return EAGLE3_ERR_UNSUPPORTED;
   if (!w->w_fc || !w->embed || !w->w_q || !w->w_k || !w->w_v || !w->w_o || !w->w_gate || !w->w_up ||
       !w->w_down || !w->g_emb || !w->g_hid || !w->g_post || !w->g_final || !w->w_lm)
     return EAGLE3_ERR_INVALID_ARG;
@@ -380,6 +431,7 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
       need(R, d, qd);
       need(R, 2 * f.ffn, d);
       need(R, d, f.ffn);
+      if (f.lr_rank) need(R, f.lr_rank, d);
     }
   c->part_elems = part;
   size_t attn = 0;
@@ -450,6 +502,18 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
   add((void**)&c->lse, (size_t)Rv * 4);
   add((void**)&c->g_arg, (size_t)Rv * 4);
   add((void**)&c->g_max, (size_t)Rv * 4);
+  c->lr = f.lr_rank > 0;
+  c->n_exp = 1 + (f.depth - 1) * k;
+  const int lr_groups = c->lr ? (c->bf ? lowrank_tc_groups(f.vocab) : lowrank_simt_groups(f.vocab)) : 0;
+  if (c->lr) {
+    add(&c->lr_t, (size_t)sp * Rlm * f.lr_rank * c->esz);
+    add((void**)&c->la.gmax, (size_t)lr_groups * Rlm * 4);
+    add((void**)&c->la.thr, (size_t)Rlm * 4);
+    add((void**)&c->la.cnt, (size_t)Rlm * 4);
+    add((void**)&c->la.cval, (size_t)Rlm * kLrCap * 4);
+    add((void**)&c->la.ctok, (size_t)Rlm * kLrCap * 4);
+    add((void**)&c->cand_all, (size_t)B * c->n_exp * f.lr_cand * 4);
+  }
   add((void**)&c->flags, 64);
   size_t total = 0;
   for (auto& p : plan) total += align_up(p.second, 256);
@@ -476,6 +540,19 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
   c->hp.n_parts = lm_parts;
   c->hp.k = k;
   c->pool.n = pool_n;
+  if (c->lr) {
+    c->la.V = f.vocab;
+    c->la.d = d;
+    c->la.r = f.lr_rank;
+    c->la.C = f.lr_cand;
+    c->la.k = k;
+    c->la.n_groups = lr_groups;
+    c->la.t = c->lr_t;
+    c->la.U = w->lr_u;
+    c->la.W = w->w_lm;
+    c->la.cand_n_exp = c->n_exp;
+    c->la.flags = c->flags;
+  }
 
   // RoPE table, rotate-half pairs: angle = pos * theta^(-2j/dh) in double
   {
@@ -553,7 +630,7 @@ eagle3_status eagle3_draft_round(eagle3_ctx* c, int B, int n_new, const void* fe
   kv_rows(c, B * n_new, feats_new, true, nullptr, kv, KvTarget{nullptr, nullptr, 0},
           use_split(c, B * n_new), st);
   tail_rows(c, B, 1, c->g, kv, KvTarget{nullptr, nullptr, 0}, c->h_root, sp0, st);
-  draft_head(c, c->h_root, B, sp0, c->top_tok, c->top_logq, c->top_lse, st);
+  draft_head(c, c->h_root, B, sp0, c->top_tok, c->top_logq, c->top_lse, st, 0, 1);
   launch_expand(B, 0, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
                 c->slot_words, c->root_pos, c->n_slots, c->rp, st);
   c->launches++;
@@ -562,7 +639,7 @@ eagle3_status eagle3_draft_round(eagle3_ctx* c, int B, int n_new, const void* fe
   for (int t = 1; t < D; ++t) {
     kv_rows(c, B * k, nullptr, true, c->S, kv, tree, spk, st);
     tail_rows(c, B, k, c->S, kv, tree, c->h, spk, st);
-    draft_head(c, c->h, B * k, spk, c->top_tok, c->top_logq, c->top_lse, st);
+    draft_head(c, c->h, B * k, spk, c->top_tok, c->top_logq, c->top_lse, st, 1 + (t - 1) * k, k);
     launch_expand(B, t, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
                   c->slot_words, c->root_pos, c->n_slots, c->rp, st);
     c->launches++;
@@ -575,6 +652,9 @@ eagle3_status eagle3_draft_round(eagle3_ctx* c, int B, int n_new, const void* fe
     launch_copy_pool(B, c->pool, pool_out->tok, pool_out->parent, pool_out->depth, pool_out->fwd,
                      pool_out->score, pool_out->logq, st);
     c->launches++;
+    if (c->lr && pool_out->cand)
+      cudaMemcpyAsync(pool_out->cand, c->cand_all, (size_t)B * c->n_exp * c->cfg.lr_cand * 4,
+                      cudaMemcpyDeviceToDevice, st);
   }
   eagle3_status s = cuda_status(c, "draft_round");
   if (s == EAGLE3_OK) {

@@ -49,6 +49,7 @@ struct TcArgs {
   size_t split_stride;
   HeadParts hp;
   VerifyHeadArgs va;
+  LowRankArgs la;
   int* flags;
 };
 
@@ -229,7 +230,8 @@ __device__ __forceinline__ void verify_row(const VerifyHeadArgs& va, int part, i
   }
 }
 
-// MODE 0: split-K partial store; 1: draft head; 2: verify head
+// MODE 0: split-K partial store; 1: draft head; 2: verify head; 3: low-rank
+// group maxima (two-stage head sample); 4: low-rank threshold append
 template <int MODE>
 __global__ void __launch_bounds__(128, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
@@ -317,8 +319,24 @@ __global__ void __launch_bounds__(128, 1)
     } else if (MODE == 1) {
       const bool ok = row_feat < a.seg_N[0];
       head_row(a.hp, mt * 4 + warp, r, ok ? val : -INFINITY, ok ? row_feat : 0x7fffffff, lane);
-    } else {
+    } else if (MODE == 2) {
       verify_row(a.va, mt * 4 + warp, r, val, row_feat, row_feat < a.seg_N[0], lane);
+    } else if (MODE == 3) {
+      const float gm = warp_max(row_feat < a.seg_N[0] ? val : -INFINITY);
+      if (lane == 0) a.la.gmax[(size_t)(mt * 4 + warp) * a.la.R + r] = gm;
+    } else {
+      const bool q = row_feat < a.seg_N[0] && val >= a.la.thr[r];
+      const unsigned bal = __ballot_sync(0xffffffffu, q);
+      if (bal) {
+        int base = 0;
+        if (lane == 0) base = atomicAdd(a.la.cnt + r, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const int pos = base + __popc(bal & ((1u << lane) - 1u));
+        if (q && pos < kLrCap) {
+          a.la.cval[(size_t)r * kLrCap + pos] = val;
+          a.la.ctok[(size_t)r * kLrCap + pos] = row_feat;
+        }
+      }
     }
   };
   if (run) {
@@ -405,7 +423,9 @@ TcGemm* tc_create(const eagle3_config& f, const eagle3_weights& w, char* err, in
                        {TCW_K, w.w_k, kvd, 2 * d},        {TCW_V, w.w_v, kvd, 2 * d},
                        {TCW_O, w.w_o, d, qd},             {TCW_GATE, w.w_gate, f.ffn, d},
                        {TCW_UP, w.w_up, f.ffn, d},        {TCW_DOWN, w.w_down, d, f.ffn},
-                       {TCW_LM, w.w_lm, f.vocab, d},      {TCW_T, w.w_target, f.vocab, d}};
+                       {TCW_LM, w.w_lm, f.vocab, d},      {TCW_T, w.w_target, f.vocab, d},
+                       {TCW_LRU, f.lr_rank ? w.lr_u : nullptr, f.vocab, f.lr_rank},
+                       {TCW_LRV, f.lr_rank ? w.lr_v : nullptr, f.lr_rank, d}};
   for (const Wdef& e : defs) {
     if (!e.p) continue;  // the target head is optional
     if (!encode_map(t->encode, &t->wmap[e.id], e.p, e.N, e.K, (size_t)e.K * 2, BM)) {
@@ -542,6 +562,25 @@ bool tc_verify_head(TcGemm* t, const void* H, bool split, const VerifyHeadArgs& 
   const CUtensorMap* m = &t->wmap[TCW_T];
   return launch<2>(t, m, m, m, H, t->wK[TCW_T], t->wK[TCW_T], va.R, split, 1, args, args.seg_end[0],
                    st);
+}
+
+int lowrank_tc_groups(int V) { return 4 * cdiv(std::min(V, kLrSampleTokens), BM); }
+
+bool tc_lowrank(TcGemm* t, int mode, const LowRankArgs& la, int* flags, cudaStream_t st) {
+  if (!t || !t->wptr[TCW_LRU] || la.R <= 0 || la.R > 256 || (mode != 0 && mode != 1)) return false;
+  TcArgs args{};
+  args.nseg = 1;
+  args.seg_end[0] = cdiv(t->wN[TCW_LRU], BM);
+  args.seg_N[0] = t->wN[TCW_LRU];
+  args.la = la;
+  args.flags = flags;
+  const CUtensorMap* m = &t->wmap[TCW_LRU];
+  const int K = t->wK[TCW_LRU];
+  if (mode == 0) {
+    const int grid = cdiv(std::min(t->wN[TCW_LRU], kLrSampleTokens), BM);
+    return launch<3>(t, m, m, m, la.t, K, K, la.R, la.t_split != 0, 1, args, grid, st);
+  }
+  return launch<4>(t, m, m, m, la.t, K, K, la.R, la.t_split != 0, 1, args, args.seg_end[0], st);
 }
 
 bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, const HeadParts& hp,

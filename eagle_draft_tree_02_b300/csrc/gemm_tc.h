@@ -13,10 +13,13 @@
 
 #include "../../include/eagle3.h"
 #include "kernels.h"
+#include "lowrank.h"
 
 namespace e3 {
 
-enum TcWeight { TCW_FC, TCW_Q, TCW_K, TCW_V, TCW_O, TCW_GATE, TCW_UP, TCW_DOWN, TCW_LM, TCW_T, TCW_N };
+enum TcWeight {
+  TCW_FC, TCW_Q, TCW_K, TCW_V, TCW_O, TCW_GATE, TCW_UP, TCW_DOWN, TCW_LM, TCW_T, TCW_LRU, TCW_LRV, TCW_N
+};
 
 struct GemmSeg {  // one weight matrix whose output columns start at col0
   int wid;
@@ -41,9 +44,14 @@ bool tc_lm_head(TcGemm* t, const void* H, int R, bool split, const HeadParts& hp
                 cudaStream_t st);
 bool tc_verify_head(TcGemm* t, const void* H, bool split, const VerifyHeadArgs& a, int* flags,
                     cudaStream_t st);
+// Low-rank scores U t of the two-stage head: mode 0 writes the 32-token group
+// maxima of the sample tokens, mode 1 appends the tokens that reach the
+// row's threshold (see lowrank.h).
+bool tc_lowrank(TcGemm* t, int mode, const LowRankArgs& la, int* flags, cudaStream_t st);
 // The draft-head launch of tc_lm_head on a bare weight pointer W [V, d] (bf16),
 // with no TcGemm object: the tensor maps are encoded on the host stack and
 // nothing is allocated.  False (nothing launched) on an unusable argument.
 bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, const HeadParts& hp,
                     int* flags, cudaStream_t st);
+
 }  // namespace e3

@@ -51,7 +51,7 @@ class eagle3_tree(C.Structure):
 
 
 class eagle3_pool(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in ("tok", "parent", "depth", "fwd", "score", "logq")]
+    _fields_ = [(n, C.c_void_p) for n in ("tok", "parent", "depth", "fwd", "score", "logq", "cand")]
 
 
 class eagle3_verify_stats(C.Structure):

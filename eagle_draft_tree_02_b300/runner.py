@@ -58,11 +58,13 @@ class PoolOut:
     fwd: torch.Tensor
     score: torch.Tensor
     logq: torch.Tensor
+    cand: torch.Tensor | None = None   # two-stage head: [B, 1 + (D-1)k, lr_cand]
 
     def struct(self) -> E.eagle3_pool:
         p = E.eagle3_pool()
-        for n in ("tok", "parent", "depth", "fwd", "score", "logq"):
-            setattr(p, n, getattr(self, n).data_ptr())
+        for n in ("tok", "parent", "depth", "fwd", "score", "logq", "cand"):
+            t = getattr(self, n)
+            setattr(p, n, t.data_ptr() if t is not None else None)
         return p
 
 
@@ -121,9 +123,11 @@ class Engine:
                             torch.empty((self.B, M1), dtype=torch.float32, device=dev),
                             torch.empty((self.B, M1, W), **i32))
         pn = cfg.pool_size
+        cand = (torch.empty((self.B, 1 + (cfg.depth - 1) * cfg.topk, cfg.lr_cand), **i32)
+                if cfg.lr_rank else None)
         self.pool = PoolOut(*(torch.empty((self.B, pn), **i32) for _ in range(4)),
                             torch.empty((self.B, pn), dtype=torch.float32, device=dev),
-                            torch.empty((self.B, pn), dtype=torch.float32, device=dev))
+                            torch.empty((self.B, pn), dtype=torch.float32, device=dev), cand)
         D = cfg.depth
         self.accept_len = torch.empty(self.B, **i32)
         self.path = torch.empty((self.B, D), **i32)

@@ -67,8 +67,9 @@ typedef struct {
   int head_dim;    /* dh, even, <= 128 */
   int ffn;         /* SwiGLU inner width F */
   int vocab;       /* V */
-  int lr_rank;     /* two-stage head: rank r of U [V, r] V_lr [r, d]; 0 = single-stage head */
-  int lr_cand;     /* two-stage head: candidates rescored by the exact head (<= 128) */
+  int lr_rank;     /* two-stage head: rank r of U [V, r] V_lr [r, d], r % 8 == 0; 0 = single-stage head */
+  int lr_cand;     /* two-stage head: candidates C rescored by the exact head, k <= C <= 128, C <= V;
+                      log q is normalised over C */
   float rope_theta;
   float rms_eps;
   int dtype;       /* EAGLE3_FP32 or EAGLE3_BF16: weights, features, KV cache */
@@ -122,10 +123,14 @@ typedef struct {
 /* Every node the round created, device arrays [B, pool_n] with
  * pool_n = k + (D-1) k^2, in creation order (depth, parent's frontier rank,
  * child rank).  parent is a pool index (-1 = root); fwd is the node's frontier
- * slot if it was expanded, else -1; score = cumulative log q. */
+ * slot if it was expanded, else -1; score = cumulative log q.
+ * cand (two-stage head only, may be NULL): [B, 1 + (D-1) k, lr_cand] int32,
+ * the candidate tokens of every expanded node in low-rank order (score desc,
+ * token asc): the root first, then the frontier slots (depth, rank). */
 typedef struct {
   int *tok, *parent, *depth, *fwd;
   float *score, *logq;
+  int* cand;
 } eagle3_pool;
 
 /* Optional per-node verification details, device arrays [B, M+1]:

@@ -37,6 +37,8 @@ def gpu_round(eng, temps=(0.0,), seed=0, round_id=0) -> GpuRound:
     tree = {k: getattr(eng.tree, k).cpu().numpy() for k in
             ("tokens", "parent", "depth", "pos", "pool_index", "score", "mask")}
     pool = {k: getattr(eng.pool, k).cpu().numpy() for k in ("tok", "parent", "depth", "fwd", "score", "logq")}
+    if eng.pool.cand is not None:
+        pool["cand"] = eng.pool.cand.cpu().numpy()
     out = GpuRound(tree, pool)
     for T in temps:
         a, p, o = eng.verify(T, seed, round_id)
@@ -92,6 +94,13 @@ class Follow(R.Decisions):
             return gpu_choice
         self.rep.failures.append(what)
         return own
+
+    def candidates(self, b, depth, rank, lowrank_row, c):
+        """Two-stage head: the GPU's candidate set of this node, if it is a valid top-c."""
+        own = super().candidates(b, depth, rank, lowrank_row, c)
+        slot = 0 if depth == 0 else 1 + (depth - 1) * self.cfg.topk + rank
+        gpu = self.g.pool["cand"][b, slot]
+        return np.asarray(self._adopt(("candidates", b, depth, rank), own, gpu, lowrank_row, self.tol))
 
     def children(self, b, depth, rank, cand_tokens, logq_row, k):
         own = super().children(b, depth, rank, cand_tokens, logq_row, k)

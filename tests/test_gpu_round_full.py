@@ -7,6 +7,9 @@
 * 70B-shaped tree, batch 4, prefix 8192: sampled K/V rows of the cache are
   checked against the oracle, then the oracle's round for a sampled request
   runs on the GPU's cache (conditioned on the shared prefix K/V).
+* two-stage head tree, batch 16, prefix 4096, vocabulary 151936: as the 70B
+  case, for two sampled requests; the GPU's candidate sets must be valid
+  top-64 sets of the oracle's low-rank scores.
 """
 import numpy as np
 import pytest
@@ -72,3 +75,8 @@ def test_full_8b_batch64_chain_paged(cuda, lib_built):
 @pytest.mark.gpu
 def test_full_70b_batch4_tree(cuda, lib_built):
     _run(CONFIGS[3], requests=[2], conditioned_kv=True, kv_rows_checked=24)
+
+
+@pytest.mark.gpu
+def test_full_two_stage_b16_tree(cuda, lib_built):
+    _run(CONFIGS[4], requests=[0, 11], conditioned_kv=True, kv_rows_checked=24)

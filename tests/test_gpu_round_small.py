@@ -17,6 +17,11 @@ SMALL_BF16 = C0.scaled(name="small_bf16", dtype="bf16", d=256, n_q_heads=4, n_kv
                        head_dim=64, ffn=512, vocab=2048, prefix=100, batch=2, depth=4, topk=4,
                        n_verify=12, lm_std=0.02 * 4, temperatures=(0.0, 1.0))
 
+TWO_STAGE_FP32 = C0.scaled(name="two_stage_fp32", lr_rank=16, lr_cand=32, depth=4, topk=4,
+                           n_verify=12, temperatures=(0.0, 1.0))
+TWO_STAGE_BF16 = SMALL_BF16.scaled(name="two_stage_bf16", vocab=40000, lr_rank=64, lr_cand=64,
+                                   depth=4, topk=5, n_verify=14)
+
 CASES = {
     "tiny_fp32": (C0, 0),
     "tiny_fp32_seed7": (C0, 7),
@@ -27,6 +32,8 @@ CASES = {
     "keep_all": (C0.scaled(depth=3, topk=3, n_verify=3 + 2 * 9), 4),
     "wide_k16": (C0.scaled(depth=2, topk=16, n_verify=40, prefix=70), 5),
     "small_bf16": (SMALL_BF16, 6),
+    "two_stage_fp32": (TWO_STAGE_FP32, 8),
+    "two_stage_bf16_v40k": (TWO_STAGE_BF16, 9),
 }
 
 
@@ -196,3 +203,43 @@ def test_lm_head_topk_planted_ties(cuda, lib_built):
         assert got == order, (r, got, order)
         np.testing.assert_allclose(lq[r].cpu().numpy(), ell[r, order] - L.logsumexp(ell[r]), atol=1e-4)
     assert tok[0].cpu().numpy().tolist()[:3] == [17, 900, 901]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg", [TWO_STAGE_FP32.scaled(vocab=6000), TWO_STAGE_BF16.scaled(vocab=6000)],
+                         ids=["fp32", "bf16"])
+def test_two_stage_head_all_tied_lowrank_scores(cuda, lib_built, cfg):
+    """Identical low-rank rows tie every token's low-rank score: the candidate
+    buffer overflows (6000 tokens > 4096 entries) and the exact radix select
+    must return the lr_cand lowest token ids, as the oracle's order does."""
+    import torch
+    from eagle_draft_tree_02_b300 import eagle3 as E
+    from eagle_draft_tree_02_b300.runner import Engine
+    from oracle import layers as L
+    inp = make_inputs(cfg, seed=12)
+    U = inp.w["lr_u"].copy()
+    U[:] = U[7]
+    inp.w["lr_u"] = U
+    eng = Engine(inp)
+    R, k = 3, cfg.topk
+    rng = np.random.default_rng(3)
+    h = rng.standard_normal((R, cfg.d)).astype(np.float32)
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    hd = torch.from_numpy(h).to(cuda).to(dt)
+    h64 = hd.float().cpu().numpy().astype(np.float64)
+    tok = torch.empty((R, k), dtype=torch.int32, device=cuda)
+    lq = torch.empty((R, k), dtype=torch.float32, device=cuda)
+    lse = torch.empty(R, dtype=torch.float32, device=cuda)
+    s = E.eagle3_lm_head_topk(eng.ctx, R, hd.data_ptr(), tok.data_ptr(), lq.data_ptr(), lse.data_ptr(),
+                              eng.stream())
+    assert s == E.OK, E.eagle3_last_error(eng.ctx)
+    torch.cuda.synchronize()
+    eng.check()
+    w = {n: inp.f32(n) for n in ("lr_u", "lr_v", "w_lm")}
+    cand, logq, _ = L.draft_logq(w, cfg, h64)
+    tol = TOL[cfg.dtype]["logit"]
+    for r in range(R):
+        assert list(cand[r]) == list(range(cfg.lr_cand))     # all tied: lowest ids
+        order = np.lexsort((cand[r], -logq[r]))[:k]
+        assert tok[r].cpu().numpy().tolist() == [int(cand[r][j]) for j in order]
+        np.testing.assert_allclose(lq[r].cpu().numpy(), logq[r][order], atol=tol)
