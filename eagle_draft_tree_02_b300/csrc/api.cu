@@ -213,11 +213,15 @@ void kv_rows(eagle3_ctx* c, int R, const void* feats, bool has_q, const float* h
   c->launches++;
 }
 
+// Prefix key splits of the attention: about 4 blocks per SM in all (the
+// tensor-core kernel holds 2-3 per SM), in multiples of 64 keys.
 void attn_splits(const eagle3_ctx* c, int B, int rows_per_req, int& kps, int& nps) {
   const eagle3_config& f = c->cfg;
-  int blocks = B * f.n_kv_heads * attention_qgroups(rows_per_req, f.n_q_heads, f.n_kv_heads);
+  const bool mma = attention_uses_mma(c->esz, f.head_dim);
+  int blocks = B * f.n_kv_heads * attention_qgroups(rows_per_req, f.n_q_heads, f.n_kv_heads, mma);
   int maxp = f.max_prefix;
-  nps = std::max(1, std::min(cdiv(kTargetBlocks, blocks), cdiv(maxp, 64)));
+  const int target = mma ? 4 * 148 : kTargetBlocks;
+  nps = std::max(1, std::min(cdiv(target, blocks), cdiv(maxp, 64)));
   kps = cdiv(cdiv(maxp, nps), 64) * 64;
   nps = cdiv(maxp, kps);
 }
@@ -257,7 +261,7 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   a.split = split;
   a.flags = c->flags;
   DISPATCH(c, launch_tree_attention, a, st);
-  c->launches += 2;
+  c->launches += attention_uses_mma(c->esz, f.head_dim) && a.n_tree_splits > 0 ? 3 : 2;
   // r = hid + W_o o ; z = rms(r)
   int S = splits_for(c, R, d, qd);
   gemm1(c, TCW_O, c->o, qd, c->w.w_o, d, qd, c->part, d, R, split, S, (size_t)R * d, st);

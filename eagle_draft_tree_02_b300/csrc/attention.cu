@@ -6,13 +6,20 @@
 // rollout nodes cannot see what is not on their path).  Query head h reads KV
 // head h / (Hq / Hkv) (grouped-query attention).
 //
-// Work split: one block per (request, KV head, group of <= 32 query heads,
-// key split).  Key splits 0..n_prefix_splits-1 cover the prefix in ranges of
+// Work split: key splits 0..n_prefix_splits-1 cover the prefix in ranges of
 // keys_per_split rows; the remaining splits cover the tree slots, where each
-// query keeps only the slots whose bit is set in its row of the mask.  Each
-// block streams 64-key chunks of K and V through shared memory (converted to
-// fp32 once), keeps an online softmax per query and writes an unnormalised
-// partial (o, max, sum).  A second kernel merges the splits.
+// query keeps only the slots whose bit is set in its row of the mask.  Every
+// split block keeps an online softmax per query and writes an unnormalised
+// partial (o, max, sum); a second kernel merges the splits.
+//
+// bf16 cache, prefix splits: one block of 4 warps per (request, KV head, group
+// of <= 64 queries, split); 64-key chunks of K and V move by 16-byte cp.async
+// into double-buffered shared memory, and the 16 queries of a warp take
+// Q K^T and P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+// accumulate).  Q and P enter as hi + lo bf16 pairs (two MMAs each), so the
+// products keep about 16 significant bits, and K, V are the cache's exact
+// values.  The tree splits (at most 64 fp32 keys) and the fp32 cache use the
+// CUDA-core kernel: 32 queries per block, K and V staged as fp32.
 #include <math.h>
 
 #include "common.cuh"
@@ -21,15 +28,19 @@
 namespace e3 {
 
 namespace {
-constexpr int QG = 32;   // query heads per block
+constexpr int QG = 32;   // query heads per block (CUDA-core kernel)
+constexpr int QGM = 64;  // queries per block (tensor-core kernel: 4 warps x 16)
 constexpr int KC = 64;   // keys per chunk
-constexpr int NT = 256;  // threads
+constexpr int NT = 256;  // threads (CUDA-core kernel)
 }
 
-int attention_qgroups(int rows_per_req, int Hq, int Hkv) {
+int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma) {
   int per = rows_per_req * (Hq / Hkv);
-  return (per + QG - 1) / QG;
+  const int q = mma ? QGM : QG;
+  return (per + q - 1) / q;
 }
+
+bool attention_uses_mma(int elem_bytes, int dh) { return elem_bytes == 2 && (dh == 64 || dh == 128); }
 
 template <typename T>
 __device__ __forceinline__ const T* kv_row_ptr(const AttnArgs& a, const void* cache, int b, int pos,
@@ -46,7 +57,7 @@ __device__ __forceinline__ const T* kv_row_ptr(const AttnArgs& a, const void* ca
 }
 
 template <typename T>
-__global__ void __launch_bounds__(NT) tree_attention_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(NT) tree_attention_kernel(AttnArgs a, int z_off) {
   extern __shared__ float sm[];
   const int dh = a.dh;
   const int G = a.Hq / a.Hkv;
@@ -59,7 +70,7 @@ __global__ void __launch_bounds__(NT) tree_attention_kernel(AttnArgs a) {
   float* As = Ls + QG;                  // [QG] rescale factor of this chunk
 
   const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv;
-  const int qg = blockIdx.y, split = blockIdx.z;
+  const int qg = blockIdx.y, split = blockIdx.z + z_off;
   const int nq_req = a.rows_per_req * G;
   const int q0 = qg * QG;
   const int nq = min(QG, nq_req - q0);
@@ -212,6 +223,238 @@ __global__ void __launch_bounds__(NT) tree_attention_kernel(AttnArgs a) {
   (void)n_splits;
 }
 
+
+// ----------------------------------------------------------------------------- tensor-core prefix splits
+namespace {
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                              uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 v) {
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// (x0, x1) -> hi = bf16 pair, lo = bf16 pair of the rounding remainders
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  hi = bf2_bits(h);
+  lo = bf2_bits(__floats2bfloat162_rn(x0 - hf.x, x1 - hf.y));
+}
+}  // namespace
+
+template <int DH>
+__global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
+  constexpr int LD = DH + 8;       // shared row stride (bf16): conflict-free fragment loads
+  constexpr int NKT = KC / 8;      // key tiles of 8 per chunk
+  constexpr int NDT = DH / 8;      // output tiles of 8 dims
+  constexpr int NKS = DH / 16;     // k16 steps over dh
+  constexpr int PIECES = DH / 8;   // 16-byte pieces per K or V row
+  extern __shared__ __align__(16) unsigned char att_smem[];
+  bf16* Ks = reinterpret_cast<bf16*>(att_smem);  // [2][KC][LD]
+  bf16* Vs = Ks + 2 * KC * LD;                   // [2][KC][LD]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv, split = blockIdx.z;
+  const int G = a.Hq / a.Hkv, nq = a.rows_per_req * G;
+  const int R = a.B * a.rows_per_req;
+  const int qw = blockIdx.y * QGM + warp * 16;  // first query of this warp
+  int np = a.n_prefix[b];
+  const int cap = a.page_table ? a.max_pages * a.page_size : a.max_prefix;
+  if (np > cap || np < 0) {
+    if (tid == 0 && split == 0 && kvh == 0 && blockIdx.y == 0) raise_flag(a.flags, FLAG_POS_RANGE);
+    np = np < 0 ? 0 : cap;
+  }
+  const int key_lo = split * a.keys_per_split;
+  const int key_hi = min(np, key_lo + a.keys_per_split);
+  const int n_chunks = key_hi > key_lo ? (key_hi - key_lo + KC - 1) / KC : 0;
+
+  // this thread's two query rows (g and g + 8 of the warp's 16), scaled by 1/sqrt(dh)
+  const int qr[2] = {qw + g, qw + g + 8};
+  const float* qp[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    qp[h] = nullptr;
+    if (qr[h] < nq) {
+      const int row = b * a.rows_per_req + qr[h] / G, head = kvh * G + qr[h] % G;
+      qp[h] = a.q + (size_t)a.q_row[row] * a.Hq * DH + (size_t)head * DH;
+    }
+  }
+  const float scale = rsqrtf((float)DH);
+  uint32_t qh[NKS][4], ql[NKS][4];
+#pragma unroll
+  for (int ks = 0; ks < NKS; ++ks) {
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {  // fragment f: row g (+8 if f odd), cols +8 if f >= 2
+      const float* p = qp[f & 1];
+      const int c = ks * 16 + t4 * 2 + (f >> 1) * 8;
+      const float x0 = p ? p[c] * scale : 0.f, x1 = p ? p[c + 1] * scale : 0.f;
+      split_pair(x0, x1, qh[ks][f], ql[ks][f]);
+    }
+  }
+  float o[NDT][4];
+#pragma unroll
+  for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  const bool active = qw < nq;
+
+  auto load_chunk = [&](int c0, int buf) {
+    for (int i = tid; i < KC * PIECES; i += blockDim.x) {
+      const int kk = i / PIECES, piece = i % PIECES, key = c0 + kk;
+      const bf16 *kp = nullptr, *vp = nullptr;
+      if (key < key_hi) {
+        kp = kv_row_ptr<bf16>(a, a.cache_k, b, key, kvh);
+        vp = kv_row_ptr<bf16>(a, a.cache_v, b, key, kvh);
+        if (!kp || !vp) {
+          if (piece == 0) raise_flag(a.flags, FLAG_PAGE_RANGE);
+          kp = vp = nullptr;
+        }
+      }
+      const uint32_t dk = smem_u32(Ks + (size_t)(buf * KC + kk) * LD + piece * 8);
+      const uint32_t dv = smem_u32(Vs + (size_t)(buf * KC + kk) * LD + piece * 8);
+      cp_async16(dk, kp ? (const void*)(kp + piece * 8) : a.cache_k, kp ? 16 : 0);
+      cp_async16(dv, vp ? (const void*)(vp + piece * 8) : a.cache_v, vp ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+
+  if (n_chunks > 0) load_chunk(key_lo, 0);
+  for (int ci = 0; ci < n_chunks; ++ci) {
+    const int c0 = key_lo + ci * KC, buf = ci & 1;
+    if (ci + 1 < n_chunks) {
+      load_chunk(c0 + KC, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    if (active) {
+      const bf16* kb = Ks + (size_t)buf * KC * LD;
+      const bf16* vb = Vs + (size_t)buf * KC * LD;
+      float s[NKT][4];
+#pragma unroll
+      for (int nt = 0; nt < NKT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < NKS; ++ks) {
+#pragma unroll
+        for (int nt = 0; nt < NKT; ++nt) {
+          const bf16* kr = kb + (size_t)(nt * 8 + g) * LD + ks * 16 + t4 * 2;
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + 8);
+          mma_16816(s[nt], qh[ks], b0, b1);
+          mma_16816(s[nt], ql[ks], b0, b1);
+        }
+      }
+      // keys past the split's end
+#pragma unroll
+      for (int nt = 0; nt < NKT; ++nt) {
+        const int key = c0 + nt * 8 + t4 * 2;
+        if (key >= key_hi) s[nt][0] = s[nt][2] = -INFINITY;
+        if (key + 1 >= key_hi) s[nt][1] = s[nt][3] = -INFINITY;
+      }
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < NKT; ++nt) {
+        mx[0] = fmaxf(mx[0], fmaxf(s[nt][0], s[nt][1]));
+        mx[1] = fmaxf(mx[1], fmaxf(s[nt][2], s[nt][3]));
+      }
+      float alpha[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+        const float mn = fmaxf(mrow[h], mx[h]);
+        alpha[h] = (mrow[h] == -INFINITY) ? 0.f : expf(mrow[h] - mn);
+        mrow[h] = mn;
+      }
+      float ps[2] = {0.f, 0.f};
+#pragma unroll
+      for (int nt = 0; nt < NKT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float m = mrow[e >> 1];
+          const float p = (m == -INFINITY || s[nt][e] == -INFINITY) ? 0.f : expf(s[nt][e] - m);
+          s[nt][e] = p;
+          ps[e >> 1] += p;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) lrow[h] = lrow[h] * alpha[h] + ps[h];
+#pragma unroll
+      for (int dt = 0; dt < NDT; ++dt) {
+        o[dt][0] *= alpha[0];
+        o[dt][1] *= alpha[0];
+        o[dt][2] *= alpha[1];
+        o[dt][3] *= alpha[1];
+      }
+      // O += P V over the chunk's keys, 16 at a time
+#pragma unroll
+      for (int kk = 0; kk < KC / 16; ++kk) {
+        uint32_t ph[4], pl[4];
+        split_pair(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+        split_pair(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+        split_pair(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+        split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
+        const int mat = lane >> 3, r8 = lane & 7;
+        const bf16* vrow = vb + (size_t)(kk * 16 + r8 + (mat & 1) * 8) * LD + (mat >> 1) * 8;
+#pragma unroll
+        for (int d2 = 0; d2 < DH / 16; ++d2) {
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_trans(v0, v1, v2, v3, smem_u32(vrow + d2 * 16));
+          mma_16816(o[2 * d2], ph, v0, v1);
+          mma_16816(o[2 * d2], pl, v0, v1);
+          mma_16816(o[2 * d2 + 1], ph, v2, v3);
+          mma_16816(o[2 * d2 + 1], pl, v2, v3);
+        }
+      }
+    }
+    __syncthreads();  // this buffer is refilled two chunks later
+  }
+  // partials: unnormalised o, running max, and the quad's sum of exp
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
+    lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (qr[h] >= nq) continue;
+    const int row = b * a.rows_per_req + qr[h] / G, head = kvh * G + qr[h] % G;
+    const size_t base = ((size_t)split * R + row) * a.Hq + head;
+    float* op = a.o_part + base * DH;
+#pragma unroll
+    for (int dt = 0; dt < NDT; ++dt) {
+      op[dt * 8 + t4 * 2] = o[dt][2 * h];
+      op[dt * 8 + t4 * 2 + 1] = o[dt][2 * h + 1];
+    }
+    if (t4 == 0) {
+      a.ml_part[base * 2] = mrow[h];
+      a.ml_part[base * 2 + 1] = lrow[h];
+    }
+  }
+}
+
 // merge the key splits of one (row, head): o = sum_s o_s e^{m_s - m} / sum_s l_s e^{m_s - m}
 template <typename T>
 __global__ void attention_combine_kernel(AttnArgs a) {
@@ -244,6 +487,7 @@ void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
   int R = a.B * a.rows_per_req;
   if (R <= 0) return;
   int n_splits = a.n_prefix_splits + a.n_tree_splits;
+  const bool mma = attention_uses_mma((int)sizeof(T), a.dh);
   size_t smem = (size_t)(QG * (a.dh + 1) + KC * (a.dh + 1) + KC * a.dh + QG * KC + 3 * QG) *
                 sizeof(float);
   static bool attr_set[2] = {false, false};
@@ -251,10 +495,27 @@ void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
   if (!attr_set[ti]) {
     cudaFuncSetAttribute(tree_attention_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          160 * 1024);
+    cudaFuncSetAttribute(prefix_attention_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         4 * KC * (64 + 8) * 2);
+    cudaFuncSetAttribute(prefix_attention_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         4 * KC * (128 + 8) * 2);
     attr_set[ti] = true;
   }
-  dim3 grid(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv), n_splits);
-  tree_attention_kernel<T><<<grid, NT, smem, st>>>(a);
+  if (mma) {
+    dim3 gp(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, true), a.n_prefix_splits);
+    const size_t sm2 = (size_t)4 * KC * (a.dh + 8) * 2;
+    if (a.dh == 128)
+      prefix_attention_mma_kernel<128><<<gp, 128, sm2, st>>>(a);
+    else
+      prefix_attention_mma_kernel<64><<<gp, 128, sm2, st>>>(a);
+    if (a.n_tree_splits > 0) {
+      dim3 gt(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, false), a.n_tree_splits);
+      tree_attention_kernel<T><<<gt, NT, smem, st>>>(a, a.n_prefix_splits);
+    }
+  } else {
+    dim3 grid(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, false), n_splits);
+    tree_attention_kernel<T><<<grid, NT, smem, st>>>(a, 0);
+  }
   dim3 g2(R, a.Hq);
   attention_combine_kernel<T><<<g2, a.dh, 0, st>>>(a);
 }

@@ -66,8 +66,12 @@ struct AttnArgs {
   bool split;
   int* flags;
 };
+// Launches the prefix splits, the tree splits and the merge (3 launches with a
+// bf16 cache and dh 64/128, else 2).
 template <typename T> void launch_tree_attention(const AttnArgs& a, cudaStream_t st);
-int attention_qgroups(int rows_per_req, int Hq, int Hkv);
+// query groups per (request, KV head) of the prefix-split kernel
+int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma);
+bool attention_uses_mma(int elem_bytes, int dh);
 
 // ----------------------------------------------------------------------------- lmhead.cu
 struct HeadParts {
