@@ -222,6 +222,7 @@ void attn_splits(const eagle3_ctx* c, int B, int rows_per_req, int& kps, int& np
   int maxp = f.max_prefix;
   const int target = mma ? 4 * 148 : kTargetBlocks;
   nps = std::max(1, std::min(cdiv(target, blocks), cdiv(maxp, 64)));
+  nps = std::min(nps, 240);  // the merge keeps one weight per split (with the tree splits) in 256
   kps = cdiv(cdiv(maxp, nps), 64) * 64;
   nps = cdiv(maxp, kps);
 }
@@ -261,7 +262,7 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   a.split = split;
   a.flags = c->flags;
   DISPATCH(c, launch_tree_attention, a, st);
-  c->launches += attention_uses_mma(c->esz, f.head_dim) && a.n_tree_splits > 0 ? 3 : 2;
+  c->launches += 2;
   // r = hid + W_o o ; z = rms(r)
   int S = splits_for(c, R, d, qd);
   gemm1(c, TCW_O, c->o, qd, c->w.w_o, d, qd, c->part, d, R, split, S, (size_t)R * d, st);

@@ -16,10 +16,13 @@
 // of <= 64 queries, split); 64-key chunks of K and V move by 16-byte cp.async
 // into double-buffered shared memory, and the 16 queries of a warp take
 // Q K^T and P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
-// accumulate).  Q and P enter as hi + lo bf16 pairs (two MMAs each), so the
-// products keep about 16 significant bits, and K, V are the cache's exact
-// values.  The tree splits (at most 64 fp32 keys) and the fp32 cache use the
-// CUDA-core kernel: 32 queries per block, K and V staged as fp32.
+// accumulate).  Q enters as a hi + lo bf16 pair (two MMAs), so the scores
+// keep about 16 significant bits; K and V are the cache's exact values.  P
+// enters as bf16 over the prefix (its rounding averages out over many keys,
+// and the sum l is taken from the unrounded weights).  A tree split stages its 64 fp32 slots as bf16 (hi, lo) pairs and
+// adds the lo products (three MMAs per fragment), with the ancestor mask
+// applied per query row.  The fp32 cache uses the CUDA-core kernel: 32
+// queries per block, K and V staged as fp32.
 #include <math.h>
 
 #include "common.cuh"
@@ -280,25 +283,37 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
   const int G = a.Hq / a.Hkv, nq = a.rows_per_req * G;
   const int R = a.B * a.rows_per_req;
   const int qw = blockIdx.y * QGM + warp * 16;  // first query of this warp
-  int np = a.n_prefix[b];
-  const int cap = a.page_table ? a.max_pages * a.page_size : a.max_prefix;
-  if (np > cap || np < 0) {
-    if (tid == 0 && split == 0 && kvh == 0 && blockIdx.y == 0) raise_flag(a.flags, FLAG_POS_RANGE);
-    np = np < 0 ? 0 : cap;
+  // prefix splits: keys [key_lo, key_hi) of the cache; tree splits: 64 tree
+  // slots, fp32 scratch staged as bf16 (hi, lo) pairs in the two buffers
+  const bool tree = split >= a.n_prefix_splits;
+  int key_lo, key_hi;
+  if (!tree) {
+    int np = a.n_prefix[b];
+    const int cap = a.page_table ? a.max_pages * a.page_size : a.max_prefix;
+    if (np > cap || np < 0) {
+      if (tid == 0 && split == 0 && kvh == 0 && blockIdx.y == 0) raise_flag(a.flags, FLAG_POS_RANGE);
+      np = np < 0 ? 0 : cap;
+    }
+    key_lo = split * a.keys_per_split;
+    key_hi = min(np, key_lo + a.keys_per_split);
+  } else {
+    key_lo = (split - a.n_prefix_splits) * KC;
+    key_hi = min(a.tree_slots, key_lo + KC);
   }
-  const int key_lo = split * a.keys_per_split;
-  const int key_hi = min(np, key_lo + a.keys_per_split);
-  const int n_chunks = key_hi > key_lo ? (key_hi - key_lo + KC - 1) / KC : 0;
+  const int n_chunks = key_hi > key_lo ? (tree ? 1 : (key_hi - key_lo + KC - 1) / KC) : 0;
 
   // this thread's two query rows (g and g + 8 of the warp's 16), scaled by 1/sqrt(dh)
   const int qr[2] = {qw + g, qw + g + 8};
   const float* qp[2];
+  const uint32_t* mrow_bits[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     qp[h] = nullptr;
+    mrow_bits[h] = nullptr;
     if (qr[h] < nq) {
       const int row = b * a.rows_per_req + qr[h] / G, head = kvh * G + qr[h] % G;
       qp[h] = a.q + (size_t)a.q_row[row] * a.Hq * DH + (size_t)head * DH;
+      mrow_bits[h] = a.mask + (size_t)row * a.mask_words;
     }
   }
   const float scale = rsqrtf((float)DH);
@@ -338,20 +353,60 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
     }
     cp_async_commit();
   };
+  // tree chunk: buffer 0 holds hi, buffer 1 lo, of K and of V
+  auto load_tree = [&]() {
+    for (int i = tid; i < KC * PIECES; i += blockDim.x) {
+      const int kk = i / PIECES, piece = i % PIECES, slot = key_lo + kk;
+      float kx[8], vx[8];
+      if (slot < key_hi) {
+        const size_t off = (((size_t)b * a.tree_slots + slot) * a.Hkv + kvh) * DH + piece * 8;
+        const float4* kq = reinterpret_cast<const float4*>((const float*)a.tree_k + off);
+        const float4* vq = reinterpret_cast<const float4*>((const float*)a.tree_v + off);
+        const float4 k0 = kq[0], k1 = kq[1], v0 = vq[0], v1 = vq[1];
+        kx[0] = k0.x; kx[1] = k0.y; kx[2] = k0.z; kx[3] = k0.w;
+        kx[4] = k1.x; kx[5] = k1.y; kx[6] = k1.z; kx[7] = k1.w;
+        vx[0] = v0.x; vx[1] = v0.y; vx[2] = v0.z; vx[3] = v0.w;
+        vx[4] = v1.x; vx[5] = v1.y; vx[6] = v1.z; vx[7] = v1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kx[e] = vx[e] = 0.f;
+      }
+      uint32_t khi[4], klo[4], vhi[4], vlo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        split_pair(kx[2 * e], kx[2 * e + 1], khi[e], klo[e]);
+        split_pair(vx[2 * e], vx[2 * e + 1], vhi[e], vlo[e]);
+      }
+      const size_t o0 = (size_t)kk * LD + piece * 8, o1 = (size_t)(KC + kk) * LD + piece * 8;
+      *reinterpret_cast<uint4*>(Ks + o0) = make_uint4(khi[0], khi[1], khi[2], khi[3]);
+      *reinterpret_cast<uint4*>(Ks + o1) = make_uint4(klo[0], klo[1], klo[2], klo[3]);
+      *reinterpret_cast<uint4*>(Vs + o0) = make_uint4(vhi[0], vhi[1], vhi[2], vhi[3]);
+      *reinterpret_cast<uint4*>(Vs + o1) = make_uint4(vlo[0], vlo[1], vlo[2], vlo[3]);
+    }
+  };
 
-  if (n_chunks > 0) load_chunk(key_lo, 0);
+  if (n_chunks > 0) {
+    if (tree)
+      load_tree();
+    else
+      load_chunk(key_lo, 0);
+  }
   for (int ci = 0; ci < n_chunks; ++ci) {
-    const int c0 = key_lo + ci * KC, buf = ci & 1;
-    if (ci + 1 < n_chunks) {
-      load_chunk(c0 + KC, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    const int c0 = key_lo + ci * KC, buf = tree ? 0 : (ci & 1);
+    if (!tree) {
+      if (ci + 1 < n_chunks) {
+        load_chunk(c0 + KC, buf ^ 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
     }
     __syncthreads();
     if (active) {
       const bf16* kb = Ks + (size_t)buf * KC * LD;
       const bf16* vb = Vs + (size_t)buf * KC * LD;
+      const bf16* kbl = Ks + (size_t)KC * LD;  // tree chunk: lo halves
+      const bf16* vbl = Vs + (size_t)KC * LD;
       float s[NKT][4];
 #pragma unroll
       for (int nt = 0; nt < NKT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -359,19 +414,31 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
       for (int ks = 0; ks < NKS; ++ks) {
 #pragma unroll
         for (int nt = 0; nt < NKT; ++nt) {
-          const bf16* kr = kb + (size_t)(nt * 8 + g) * LD + ks * 16 + t4 * 2;
-          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr);
-          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + 8);
+          const size_t ko = (size_t)(nt * 8 + g) * LD + ks * 16 + t4 * 2;
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kb + ko);
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kb + ko + 8);
           mma_16816(s[nt], qh[ks], b0, b1);
           mma_16816(s[nt], ql[ks], b0, b1);
+          if (tree) {
+            const uint32_t c0l = *reinterpret_cast<const uint32_t*>(kbl + ko);
+            const uint32_t c1l = *reinterpret_cast<const uint32_t*>(kbl + ko + 8);
+            mma_16816(s[nt], qh[ks], c0l, c1l);
+          }
         }
       }
-      // keys past the split's end
+      // keys past the split's end; in a tree chunk, slots off the query's path
 #pragma unroll
       for (int nt = 0; nt < NKT; ++nt) {
-        const int key = c0 + nt * 8 + t4 * 2;
-        if (key >= key_hi) s[nt][0] = s[nt][2] = -INFINITY;
-        if (key + 1 >= key_hi) s[nt][1] = s[nt][3] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = c0 + nt * 8 + t4 * 2 + (e & 1);
+          bool ok = key < key_hi;
+          if (ok && tree) {
+            const uint32_t* mb = mrow_bits[e >> 1];
+            ok = mb && ((mb[key >> 5] >> (key & 31)) & 1u);
+          }
+          if (!ok) s[nt][e] = -INFINITY;
+        }
       }
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -417,15 +484,20 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
         split_pair(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
         split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
         const int mat = lane >> 3, r8 = lane & 7;
-        const bf16* vrow = vb + (size_t)(kk * 16 + r8 + (mat & 1) * 8) * LD + (mat >> 1) * 8;
+        const size_t vo = (size_t)(kk * 16 + r8 + (mat & 1) * 8) * LD + (mat >> 1) * 8;
 #pragma unroll
         for (int d2 = 0; d2 < DH / 16; ++d2) {
           uint32_t v0, v1, v2, v3;
-          ldsm_x4_trans(v0, v1, v2, v3, smem_u32(vrow + d2 * 16));
+          ldsm_x4_trans(v0, v1, v2, v3, smem_u32(vb + vo + d2 * 16));
           mma_16816(o[2 * d2], ph, v0, v1);
-          mma_16816(o[2 * d2], pl, v0, v1);
           mma_16816(o[2 * d2 + 1], ph, v2, v3);
-          mma_16816(o[2 * d2 + 1], pl, v2, v3);
+          if (tree) {  // few keys: keep the rounding remainder of P as well
+            mma_16816(o[2 * d2], pl, v0, v1);
+            mma_16816(o[2 * d2 + 1], pl, v2, v3);
+            ldsm_x4_trans(v0, v1, v2, v3, smem_u32(vbl + vo + d2 * 16));
+            mma_16816(o[2 * d2], ph, v0, v1);
+            mma_16816(o[2 * d2 + 1], ph, v2, v3);
+          }
         }
       }
     }
@@ -458,24 +530,44 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
 // merge the key splits of one (row, head): o = sum_s o_s e^{m_s - m} / sum_s l_s e^{m_s - m}
 template <typename T>
 __global__ void attention_combine_kernel(AttnArgs a) {
-  int row = blockIdx.x, head = blockIdx.y;
-  int R = a.B * a.rows_per_req;
-  int n_splits = a.n_prefix_splits + a.n_tree_splits;
+  __shared__ float wts[256];  // per split: its weight e^{m_s - m} / l
+  __shared__ float red[32];
+  const int row = blockIdx.x, head = blockIdx.y, tid = threadIdx.x;
+  const int R = a.B * a.rows_per_req;
+  const int n_splits = a.n_prefix_splits + a.n_tree_splits;
+  // every split's (max, sum) at once, then the global max and sum
   float m = -INFINITY;
-  for (int s = 0; s < n_splits; ++s)
-    m = fmaxf(m, a.ml_part[(((size_t)s * R + row) * a.Hq + head) * 2]);
-  float l = 0.f;
-  for (int s = 0; s < n_splits; ++s) {
-    const float* ml = a.ml_part + (((size_t)s * R + row) * a.Hq + head) * 2;
-    if (ml[0] != -INFINITY) l += ml[1] * expf(ml[0] - m);
+  for (int s = tid; s < n_splits; s += blockDim.x) {
+    const float ms = a.ml_part[(((size_t)s * R + row) * a.Hq + head) * 2];
+    wts[s] = ms;
+    m = fmaxf(m, ms);
   }
-  float inv = l > 0.f ? 1.f / l : 0.f;
-  for (int dd = threadIdx.x; dd < a.dh; dd += blockDim.x) {
+  m = warp_max(m);
+  if ((tid & 31) == 0) red[tid >> 5] = m;
+  __syncthreads();
+  if (tid < 32) {
+    float v = tid < (int)(blockDim.x >> 5) ? red[tid] : -INFINITY;
+    v = warp_max(v);
+    if (tid == 0) red[0] = v;
+  }
+  __syncthreads();
+  m = red[0];
+  __syncthreads();
+  float l = 0.f;
+  for (int s = tid; s < n_splits; s += blockDim.x) {
+    const float ms = wts[s];
+    const float w = ms == -INFINITY ? 0.f : expf(ms - m);
+    l += w * a.ml_part[(((size_t)s * R + row) * a.Hq + head) * 2 + 1];
+    wts[s] = w;
+  }
+  l = block_sum(l, red);
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  for (int dd = tid; dd < a.dh; dd += blockDim.x) {
     float o = 0.f;
+#pragma unroll 4
     for (int s = 0; s < n_splits; ++s) {
-      size_t base = ((size_t)s * R + row) * a.Hq + head;
-      float ms = a.ml_part[base * 2];
-      if (ms != -INFINITY) o += a.o_part[base * a.dh + dd] * expf(ms - m);
+      const float w = wts[s];
+      if (w != 0.f) o += a.o_part[(((size_t)s * R + row) * a.Hq + head) * a.dh + dd] * w;
     }
     st_act((T*)a.out + act_row(row, a.Hq * a.dh, a.split), a.Hq * a.dh, head * a.dh + dd, o * inv,
            a.split);
@@ -501,17 +593,13 @@ void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
                          4 * KC * (128 + 8) * 2);
     attr_set[ti] = true;
   }
-  if (mma) {
-    dim3 gp(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, true), a.n_prefix_splits);
+  if (mma) {  // prefix and tree splits in one launch
+    dim3 gp(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, true), n_splits);
     const size_t sm2 = (size_t)4 * KC * (a.dh + 8) * 2;
     if (a.dh == 128)
       prefix_attention_mma_kernel<128><<<gp, 128, sm2, st>>>(a);
     else
       prefix_attention_mma_kernel<64><<<gp, 128, sm2, st>>>(a);
-    if (a.n_tree_splits > 0) {
-      dim3 gt(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, false), a.n_tree_splits);
-      tree_attention_kernel<T><<<gt, NT, smem, st>>>(a, a.n_prefix_splits);
-    }
   } else {
     dim3 grid(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, false), n_splits);
     tree_attention_kernel<T><<<grid, NT, smem, st>>>(a, 0);

@@ -373,6 +373,298 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) tmem_dealloc(tmem, a.tmem_cols);
 }
 
+
+// ----------------------------------------------------------------------------- persistent heads
+// The vocabulary heads (draft LM head, verify head) as a persistent kernel:
+// one CTA per SM walks the 128-token tiles mt = blockIdx.x, + gridDim.x, ...
+// Warp 0 issues the TMA loads into a ring of stages that runs on across tiles,
+// warp 1 issues the MMAs into one of two TMEM accumulators, and warps 2-5 run
+// the epilogue of tile i while tile i+1 is loaded and multiplied.  Each
+// epilogue warp keeps per-row running state in shared memory across its
+// CTA's tiles -- an online log-sum-exp and a sorted top-k list for the draft
+// head, or (best logit, log-sum-exp of z/T, Gumbel best) for the verify head
+// -- and writes one partial at the end, so the merge reads 4 partials per CTA
+// instead of 4 per tile.
+struct PhArgs {
+  int R, ncols, split, n_kb, ntile, stages, n_mtiles, V, sw;
+  int r_off, R_total;  // this launch's rows are rows r_off .. r_off + R - 1 of R_total
+  uint32_t tmem_cols, acc_cols, idesc;
+  HeadParts hp;
+  VerifyHeadArgs va;
+  int* flags;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// insert (v, i), known to beat the last entry, into a sorted list of k
+__device__ __forceinline__ void list_insert(float* vals, int* idx, int k, float v, int i) {
+  int p = k - 1;
+  while (p > 0 && better(v, i, vals[p - 1], idx[p - 1])) {
+    vals[p] = vals[p - 1];
+    idx[p] = idx[p - 1];
+    --p;
+  }
+  vals[p] = v;
+  idx[p] = i;
+}
+
+__device__ __forceinline__ void lse_fold_dev(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;
+    m = m2;
+  } else {
+    s += s2 * expf(m2 - m);
+  }
+}
+
+// draft head: fold this warp's 32 tokens of one row into the row's state
+// state: [0] max, [1] sum exp, [2, 2+k) values, [2+k, 2+2k) tokens (int bits)
+__device__ __forceinline__ void ph_fold_draft(float* st, int k, float x, int tok, bool valid,
+                                              int lane) {
+  const float mt = warp_max(x);
+  const float stl = warp_sum(x == -INFINITY ? 0.f : expf(x - mt));
+  float* vals = st + 2;
+  int* idx = reinterpret_cast<int*>(st + 2 + k);
+  if (lane == 0) lse_fold_dev(st[0], st[1], mt, stl);
+  __syncwarp();
+  bool q = valid && better(x, tok, vals[k - 1], idx[k - 1]);
+  unsigned bal = __ballot_sync(0xffffffffu, q);
+  while (bal) {
+    float bv = q ? x : -INFINITY;
+    int bi = q ? tok : 0x7fffffff;
+    warp_best(bv, bi);
+    if (lane == 0) list_insert(vals, idx, k, bv, bi);
+    __syncwarp();
+    if (tok == bi) q = false;
+    q = q && better(x, tok, vals[k - 1], idx[k - 1]);
+    bal = __ballot_sync(0xffffffffu, q);
+  }
+}
+
+// verify head: state [0] best z, [1] its token, [2] max z/T, [3] sum exp, [4] best
+// Gumbel score, [5] its token
+__device__ __forceinline__ void ph_fold_verify(float* st, const VerifyHeadArgs& va, int r, float z,
+                                               int x, bool valid, int lane) {
+  const int b = r / va.M1, u = r % va.M1;
+  float zb = valid ? z : -INFINITY;
+  int zi = valid ? x : 0x7fffffff;
+  const float t = valid ? z * va.inv_t : -INFINITY;
+  float gb = -INFINITY;
+  int gi = 0x7fffffff;
+  if (valid) {
+    bool child = false;
+    for (int c = 0; c < va.kmax; ++c) {
+      if (va.child_tok[(size_t)r * va.kmax + c] == x) {
+        child = true;
+        va.child_z[(size_t)r * va.kmax + c] = z;
+      }
+    }
+    if (va.sampling && !child) {
+      gb = t + verify_gumbel(va.seed, va.round_id, b, u, x);
+      gi = x;
+    }
+  }
+  const float m = warp_max(t);
+  const float sl = warp_sum(t == -INFINITY ? 0.f : expf(t - m));
+  warp_best(zb, zi);
+  warp_best(gb, gi);
+  if (lane == 0) {
+    if (better(zb, zi, st[0], __float_as_int(st[1]))) {
+      st[0] = zb;
+      st[1] = __int_as_float(zi);
+    }
+    lse_fold_dev(st[2], st[3], m, sl);
+    if (better(gb, gi, st[4], __float_as_int(st[5]))) {
+      st[4] = gb;
+      st[5] = __int_as_float(gi);
+    }
+  }
+  __syncwarp();
+}
+
+#ifndef E3_HEAD_CTAS_PER_SM
+#define E3_HEAD_CTAS_PER_SM 2
+#endif
+constexpr int kHeadCtasPerSm = E3_HEAD_CTAS_PER_SM;
+
+template <int MODE>
+__global__ void __launch_bounds__(192, 1)
+    tc_head_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
+                   const PhArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = su32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  const uint32_t sA = raw + pad;
+  const int S = a.stages;
+  const uint32_t B_STAGE = (uint32_t)a.ntile * BK * 2;
+  const uint32_t sB = sA + S * A_STAGE;
+  const uint32_t bars = sB + S * B_STAGE;
+  const uint32_t full0 = bars, empty0 = bars + 8 * S, tfull0 = bars + 16 * S, tempty0 = tfull0 + 16;
+  uint8_t* gen = smem_raw + pad + (bars - sA) + 16 * S + 32;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(gen);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(gen + 4);
+  float* state = reinterpret_cast<float*>(gen + 16);  // [4][R][sw]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(tfull0 + 8 * j, 1);
+      mbar_init(tempty0 + 8 * j, 4);
+    }
+    *abort_f = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(su32(tslot), a.tmem_cols);
+  if (warp >= 2) {  // running state of this epilogue warp's rows
+    float* mine = state + (size_t)(warp - 2) * a.R * a.sw;
+    for (int i = lane; i < a.R * a.sw; i += 32) {
+      const int f = i % a.sw;
+      float v;
+      if (MODE == 1) {
+        const int k = a.hp.k;
+        v = (f == 0 || (f >= 2 && f < 2 + k)) ? -INFINITY
+            : (f == 1 ? 0.f : __int_as_float(0x7fffffff));
+      } else {
+        v = (f == 0 || f == 2 || f == 4) ? -INFINITY
+            : (f == 3 ? 0.f : __int_as_float(0x7fffffff));
+      }
+      mine[i] = v;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer: a ring of stages across all of this CTA's tiles
+    const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+    int c = 0;
+    bool ok = true;
+    for (int mt = blockIdx.x; mt < a.n_mtiles && ok; mt += gridDim.x) {
+      for (int kb = 0; kb < a.n_kb; ++kb, ++c) {
+        const int s = c % S;
+        const uint32_t ph = (uint32_t)(c / S) & 1u;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_f, a.flags)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_tx(full0 + 8 * s, A_STAGE + B_STAGE);
+        tma_load_2d(sA + s * A_STAGE, &mA, full0 + 8 * s, kb * BK, mt * BM, pw);
+        tma_load_2d(sB + s * B_STAGE, &mB, full0 + 8 * s, kb * BK, 0, px);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer: tile i accumulates into TMEM buffer i & 1
+    int c = 0, i = 0;
+    bool ok = true;
+    for (int mt = blockIdx.x; mt < a.n_mtiles && ok; mt += gridDim.x, ++i) {
+      const int ab = i & 1;
+      if (!mbar_wait(tempty0 + 8 * ab, ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_f, a.flags)) break;
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)ab * a.acc_cols;
+      for (int kb = 0; kb < a.n_kb; ++kb, ++c) {
+        const int s = c % S;
+        const uint32_t ph = (uint32_t)(c / S) & 1u;
+        if (!mbar_wait(full0 + 8 * s, ph, abort_f, a.flags)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = sw128_desc(sA + s * A_STAGE);
+        const uint64_t bd = sw128_desc(sB + s * B_STAGE);
+#pragma unroll
+        for (int k = 0; k < BK / UK; ++k)
+          mma_bf16(d, ad + (uint64_t)(k * UK * 2 / 16), bd + (uint64_t)(k * UK * 2 / 16), a.idesc,
+                   (kb > 0 || k > 0) ? 1u : 0u);
+        mma_commit(empty0 + 8 * s);
+      }
+      if (ok) mma_commit(tfull0 + 8 * ab);
+    }
+  } else if (warp >= 2) {
+    // ---------------- epilogue: TMEM lanes 32 (warp % 4) .. +31 are this warp's tokens
+    const int e = warp - 2, lg = warp & 3;
+    float* mine = state + (size_t)e * a.R * a.sw;
+    int i = 0;
+    for (int mt = blockIdx.x; mt < a.n_mtiles; mt += gridDim.x, ++i) {
+      const int ab = i & 1;
+      if (!mbar_wait(tfull0 + 8 * ab, (uint32_t)(i >> 1) & 1u, abort_f, a.flags)) break;
+      tc_fence_after();
+      const int tok = mt * BM + lg * 32 + lane;
+      const bool valid = tok < a.V;
+      const uint32_t taddr = tmem + (uint32_t)ab * a.acc_cols + ((uint32_t)(lg * 32) << 16);
+      for (int c0 = 0; c0 < a.ntile; c0 += 16) {
+        if (c0 >= a.ncols) break;
+        uint32_t v[16];
+        tmem_ld16(taddr + (uint32_t)c0, v);
+        const int step = a.split ? 2 : 1;
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          // two columns per iteration: one split row, or two plain rows
+          const int col = c0 + j;
+          if (col >= a.ncols) break;
+          if (step == 2) {
+            const float val = __uint_as_float(v[j]) + __uint_as_float(v[j + 1]);
+            const int r = col >> 1;
+            if (MODE == 1)
+              ph_fold_draft(mine + (size_t)r * a.sw, a.hp.k, valid ? val : -INFINITY, tok, valid, lane);
+            else
+              ph_fold_verify(mine + (size_t)r * a.sw, a.va, a.r_off + r, val, tok, valid, lane);
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int r = col + h;
+              if (r >= a.ncols) break;
+              const float val = __uint_as_float(v[j + h]);
+              if (MODE == 1)
+                ph_fold_draft(mine + (size_t)r * a.sw, a.hp.k, valid ? val : -INFINITY, tok, valid,
+                              lane);
+              else
+                ph_fold_verify(mine + (size_t)r * a.sw, a.va, a.r_off + r, val, tok, valid, lane);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * ab);
+    }
+    // one partial per (CTA, epilogue warp)
+    __syncwarp();
+    if (!*abort_f) {
+      const int part = blockIdx.x * 4 + e;
+      for (int r = 0; r < a.R; ++r) {
+        const float* st = mine + (size_t)r * a.sw;
+        const size_t pr = (size_t)part * a.R_total + a.r_off + r;
+        if (MODE == 1) {
+          const int k = a.hp.k;
+          if (lane < 2) a.hp.ms[pr * 2 + lane] = st[lane];
+          if (lane < k) {
+            const int ix = __float_as_int(st[2 + k + lane]);
+            a.hp.val[pr * k + lane] = st[2 + lane];
+            a.hp.idx[pr * k + lane] = ix == 0x7fffffff ? -1 : ix;
+          }
+        } else {
+          if (lane < 6) a.va.part[pr * 6 + lane] = st[lane];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tmem_dealloc(tmem, a.tmem_cols);
+  }
+}
+
 // ----------------------------------------------------------------------------- host side
 typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
@@ -389,7 +681,18 @@ struct TcGemm {
   const void* wptr[TCW_N] = {};
   int wN[TCW_N] = {}, wK[TCW_N] = {};
   int V = 0;
+  int n_sm = 0;
 };
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 148;
+  }
+  return n;
+}
 
 static bool encode_map(EncodeFn enc, CUtensorMap* m, const void* base, int rows, int cols,
                        size_t row_bytes, int box_rows) {
@@ -417,6 +720,7 @@ TcGemm* tc_create(const eagle3_config& f, const eagle3_weights& w, char* err, in
   TcGemm* t = new TcGemm();
   t->encode = reinterpret_cast<EncodeFn>(fn);
   t->V = f.vocab;
+  t->n_sm = sm_count();
   const int d = f.d, qd = f.n_q_heads * f.head_dim, kvd = f.n_kv_heads * f.head_dim;
   struct Wdef { int id; const void* p; int N, K; };
   const Wdef defs[] = {{TCW_FC, w.w_fc, d, 3 * d},        {TCW_Q, w.w_q, qd, 2 * d},
@@ -508,6 +812,57 @@ bool launch(TcGemm* t, const CUtensorMap* a0, const CUtensorMap* a1, const CUten
   tc_gemm_kernel<MODE><<<grid, 128, L.smem, st>>>(*a0, *a1, *a2, mb, args);
   return true;
 }
+
+// Persistent head launch when it fits: at most 256 MMA columns and the running
+// state plus at least 3 ring stages in shared memory.  Sets n_parts to the
+// partials written (4 per CTA); false when the caller must use tc_gemm_kernel.
+template <int MODE>
+bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X, int R, bool split,
+                 PhArgs& args, int& n_parts, cudaStream_t st, int r_off = 0, int R_total = -1) {
+  const int ncols = split ? 2 * R : R;
+  if (ncols > 256 || ncols <= 0) return false;
+  const int ntile = std::max(16, cdiv(ncols, 16) * 16);
+  uint32_t acc = 32;
+  while (acc < (uint32_t)ntile) acc <<= 1;
+  const int sw = MODE == 1 ? 2 + 2 * args.hp.k : 6;
+  const size_t state = (size_t)4 * R * sw * 4;
+  const size_t stage = A_STAGE + (size_t)ntile * BK * 2;
+  // CTAs per SM: as configured, but their double-buffered accumulators must
+  // share the SM's 512 TMEM columns (an allocation beyond them would wait)
+  const int ctas = std::max(1, std::min(kHeadCtasPerSm, (int)(512 / (2 * acc))));
+  const size_t budget = (size_t)227 * 1024 / ctas - 1024;  // shared memory per CTA
+  const size_t fixed = 1024 + 16 * 16 + 64 + state;
+  if (fixed + 3 * stage > budget) return false;
+  const int stages = (int)std::min<size_t>(12, (budget - fixed) / stage);
+  CUtensorMap mb;
+  if (!encode_map(t->encode, &mb, X, ncols, K, (size_t)K * 2, ntile)) return false;
+  const int n_mtiles = cdiv(V, BM);
+  const int grid = std::min(n_mtiles, ctas * (t->n_sm > 0 ? t->n_sm : 148));
+  args.R = R;
+  args.r_off = r_off;
+  args.R_total = R_total < 0 ? R : R_total;
+  args.ncols = ncols;
+  args.split = split ? 1 : 0;
+  args.n_kb = cdiv(K, BK);
+  args.ntile = ntile;
+  args.stages = stages;
+  args.n_mtiles = n_mtiles;
+  args.V = V;
+  args.sw = sw;
+  args.acc_cols = acc;
+  args.tmem_cols = 2 * acc;
+  args.idesc = make_idesc(ntile);
+  const size_t smem = 1024 + stages * stage + (2 * stages + 4) * 8 + 32 + 16 + state;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(tc_head_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         232448);
+    attr = true;
+  }
+  tc_head_kernel<MODE><<<grid, 192, smem, st>>>(*wmap, mb, args);
+  n_parts = 4 * grid;
+  return true;
+}
 }  // namespace
 
 bool tc_gemm(TcGemm* t, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
@@ -536,32 +891,67 @@ bool tc_gemm(TcGemm* t, const GemmSeg* segs, int nseg, const void* X, int ldx, i
   return launch<0>(t, maps[0], maps[1], maps[2], X, ldx, K, R, split, S, args, tiles, st);
 }
 
-bool tc_lm_head(TcGemm* t, const void* H, int R, bool split, const HeadParts& hp, int* flags,
+bool tc_lm_head(TcGemm* t, const void* H, int R, bool split, HeadParts& hp, int* flags,
                 cudaStream_t st) {
-  if (!t || !t->wptr[TCW_LM] || R <= 0 || R > 256 || hp.n_parts != tc_head_parts(t->V)) return false;
+  if (!t || !t->wptr[TCW_LM] || R <= 0 || R > 256 || hp.n_parts < tc_head_parts(t->V)) return false;
+  const int K = t->wK[TCW_LM];
+  {
+    PhArgs pa{};
+    pa.hp = hp;
+    pa.hp.R = R;
+    pa.flags = flags;
+    int n_parts = 0;
+    if (launch_head<1>(t, &t->wmap[TCW_LM], t->V, K, H, R, split, pa, n_parts, st)) {
+      hp.n_parts = n_parts;
+      return true;
+    }
+  }
   TcArgs args{};
   args.nseg = 1;
   args.seg_end[0] = cdiv(t->V, BM);
   args.seg_N[0] = t->V;
+  hp.n_parts = tc_head_parts(t->V);
   args.hp = hp;
   args.flags = flags;
   const CUtensorMap* m = &t->wmap[TCW_LM];
-  return launch<1>(t, m, m, m, H, t->wK[TCW_LM], t->wK[TCW_LM], R, split, 1, args, args.seg_end[0],
-                   st);
+  return launch<1>(t, m, m, m, H, K, K, R, split, 1, args, args.seg_end[0], st);
 }
 
-bool tc_verify_head(TcGemm* t, const void* H, bool split, const VerifyHeadArgs& va, int* flags,
+bool tc_verify_head(TcGemm* t, const void* H, bool split, VerifyHeadArgs& va, int* flags,
                     cudaStream_t st) {
-  if (!t || !t->wptr[TCW_T] || va.R <= 0 || va.n_parts != tc_head_parts(t->V)) return false;
+  if (!t || !t->wptr[TCW_T] || va.R <= 0 || va.n_parts < tc_head_parts(t->V)) return false;
+  const int K = t->wK[TCW_T];
+  {
+    // rows in equal chunks of at most 256 MMA columns; each chunk streams the
+    // head once and every chunk uses the same grid, so the partials line up
+    const int ncols = split ? 2 * va.R : va.R;
+    const int n_chunks = cdiv(ncols, 256);
+    const int rows = cdiv(va.R, n_chunks);
+    bool ok = true;
+    int n_parts = 0;
+    for (int r0 = 0; r0 < va.R && ok; r0 += rows) {
+      const int Rc = std::min(rows, va.R - r0);
+      PhArgs pa{};
+      pa.va = va;
+      pa.flags = flags;
+      const char* Xc = (const char*)H + (size_t)r0 * (split ? 2 : 1) * K * 2;
+      ok = launch_head<2>(t, &t->wmap[TCW_T], t->V, K, Xc, Rc, split, pa, n_parts, st, r0, va.R);
+      if (!ok && r0 > 0) return false;  // cannot happen: every chunk has the same shape limits
+    }
+    if (ok) {
+      va.n_parts = n_parts;
+      return true;
+    }
+  }
   TcArgs args{};
   args.nseg = 1;
   args.seg_end[0] = cdiv(t->V, BM);
   args.seg_N[0] = t->V;
+  va.n_parts = tc_head_parts(t->V);
   args.va = va;
   args.flags = flags;
   const CUtensorMap* m = &t->wmap[TCW_T];
-  return launch<2>(t, m, m, m, H, t->wK[TCW_T], t->wK[TCW_T], va.R, split, 1, args, args.seg_end[0],
-                   st);
+  return launch<2>(t, m, m, m, H, K, K, va.R, split, 1, args, args.seg_end[0], st);
 }
 
 int lowrank_tc_groups(int V) { return 4 * cdiv(std::min(V, kLrSampleTokens), BM); }
@@ -583,7 +973,7 @@ bool tc_lowrank(TcGemm* t, int mode, const LowRankArgs& la, int* flags, cudaStre
   return launch<4>(t, m, m, m, la.t, K, K, la.R, la.t_split != 0, 1, args, args.seg_end[0], st);
 }
 
-bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, const HeadParts& hp,
+bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, HeadParts& hp,
                     int* flags, cudaStream_t st) {
   static const EncodeFn enc = []() -> EncodeFn {  // looked up once, thread-safe
     void* fn = nullptr;
@@ -600,6 +990,7 @@ bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, const Hea
   TcGemm t;
   t.encode = enc;
   t.V = V;
+  t.n_sm = sm_count();
   if (!encode_map(enc, &t.wmap[TCW_LM], W, V, d, (size_t)d * 2, BM)) return false;
   t.wptr[TCW_LM] = W;
   t.wN[TCW_LM] = V;

@@ -40,9 +40,12 @@ int tc_head_parts(int V);
 // is launched) on an unusable argument.
 bool tc_gemm(TcGemm* t, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
              int ldy, int R, bool split, int S, size_t split_stride, int* flags, cudaStream_t st);
-bool tc_lm_head(TcGemm* t, const void* H, int R, bool split, const HeadParts& hp, int* flags,
+// The vocabulary heads.  hp.n_parts / a.n_parts must hold at least
+// tc_head_parts(V) partials; on return they give the number written, which
+// the merge kernels read.
+bool tc_lm_head(TcGemm* t, const void* H, int R, bool split, HeadParts& hp, int* flags,
                 cudaStream_t st);
-bool tc_verify_head(TcGemm* t, const void* H, bool split, const VerifyHeadArgs& a, int* flags,
+bool tc_verify_head(TcGemm* t, const void* H, bool split, VerifyHeadArgs& a, int* flags,
                     cudaStream_t st);
 // Low-rank scores U t of the two-stage head: mode 0 writes the 32-token group
 // maxima of the sample tokens, mode 1 appends the tokens that reach the
@@ -51,7 +54,7 @@ bool tc_lowrank(TcGemm* t, int mode, const LowRankArgs& la, int* flags, cudaStre
 // The draft-head launch of tc_lm_head on a bare weight pointer W [V, d] (bf16),
 // with no TcGemm object: the tensor maps are encoded on the host stack and
 // nothing is allocated.  False (nothing launched) on an unusable argument.
-bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, const HeadParts& hp,
+bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, HeadParts& hp,
                     int* flags, cudaStream_t st);
 
 }  // namespace e3

@@ -66,8 +66,7 @@ struct AttnArgs {
   bool split;
   int* flags;
 };
-// Launches the prefix splits, the tree splits and the merge (3 launches with a
-// bf16 cache and dh 64/128, else 2).
+// Launches the key splits (prefix and tree) and their merge: 2 launches.
 template <typename T> void launch_tree_attention(const AttnArgs& a, cudaStream_t st);
 // query groups per (request, KV head) of the prefix-split kernel
 int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma);
