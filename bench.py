@@ -184,50 +184,58 @@ def main():
     torch.cuda.synchronize()
     eng.check()
     T = step_temperature(cfg)
-    launches = {"n": 0}
+    # every launch goes to one non-default stream: a CUDA graph is captured on it
+    side = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(side)
 
-    def step(i, count=False):
+    def step_eager(i):
         eng.draft_round(with_pool=False)
         n = eng.launches()
         eng.verify(T, seed=0, round_id=i, with_stats=False)
-        if count:
-            launches["n"] += n + eng.launches()
+        return n + eng.launches()
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            fn(i)
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1)
 
     sampler = ClockSampler(local)
     sampler.start()
     for i in range(args.warmup):
-        step(i)
+        step_eager(i)
+    # the step as one CUDA graph (eagle3_graph_capture / eagle3_graph_launch)
+    eng.capture(temperature=T, seed=0)
+    for i in range(3):
+        eng.replay(round_id=i)
     torch.cuda.synchronize()
     eng.check()
     barrier()
     torch.cuda.synchronize()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record()
-    for i in range(args.steps):
-        step(args.warmup + i, count=True)
-    s1.record()
-    s1.synchronize()
+    launches = {"n": 0}
+
+    def step_graph(i):
+        eng.replay(round_id=args.warmup + i)
+        launches["n"] += eng.launches()
+
+    ms = timed(step_graph, args.steps)
     barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
     eng.check()
-    ms = s0.elapsed_time(s1)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     ms_per_step = ms / args.steps
     value = world * args.steps / (ms / 1e3)
-
-    # draft round alone (same inputs), for the draft-only rate
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the same step as eager calls, and the draft round alone (eager), for reference
+    eager_ms = timed(lambda i: step_eager(10 ** 5 + i), max(10, args.steps // 2)) / max(10, args.steps // 2)
     nd = max(10, args.steps // 2)
-    d0.record()
-    for _ in range(nd):
-        eng.draft_round(with_pool=False)
-    d1.record()
-    d1.synchronize()
-    draft_ms = d0.elapsed_time(d1) / nd
+    draft_ms = timed(lambda i: eng.draft_round(with_pool=False), nd) / nd
 
     # dominant kernel: the draft LM head with its fused softmax/top-k, on B*k rows
     hbm, tflops, src = peaks()
@@ -236,18 +244,13 @@ def main():
     h = torch.randn(Rh, cfg.d, device=dev).to(dt)
     tok = torch.empty((Rh, cfg.topk), dtype=torch.int32, device=dev)
     lq = torch.empty((Rh, cfg.topk), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev).cuda_stream
+    stream = side.cuda_stream
     for _ in range(5):
         E.check(eng.ctx, E.eagle3_lm_head_topk(eng.ctx, Rh, h.data_ptr(), tok.data_ptr(), lq.data_ptr(),
                                                None, stream))
     nh = 50
-    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    h0.record()
-    for _ in range(nh):
-        E.eagle3_lm_head_topk(eng.ctx, Rh, h.data_ptr(), tok.data_ptr(), lq.data_ptr(), None, stream)
-    h1.record()
-    h1.synchronize()
-    head_s = h0.elapsed_time(h1) / nh / 1e3
+    head_s = timed(lambda i: E.eagle3_lm_head_topk(eng.ctx, Rh, h.data_ptr(), tok.data_ptr(),
+                                                   lq.data_ptr(), None, stream), nh) / nh / 1e3
     hb = head_bytes(cfg, Rh)
     achieved = hb / head_s / 1e9
     traffic = None
@@ -263,28 +266,32 @@ def main():
                 traffic = e.get("dram_bytes_per_launch")
         except Exception:
             traffic = None
-    roof = {"bound": "hbm", "kernel": "tc_gemm_kernel<1> (draft LM head + fused softmax/top-k, incl. merge)",
+    head_kernel = ("tc_head_kernel<1> + topk_merge_kernel (draft LM head, fused softmax/top-k)"
+                   if cfg.dtype == "bf16" and not cfg.lr_rank else
+                   "two-stage head (low-rank sample/append + select/rescore)" if cfg.lr_rank else
+                   "lm_head_simt_kernel + topk_merge_kernel")
+    roof = {"bound": "hbm", "kernel": head_kernel,
             "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
             "algorithmic_bytes_per_launch": hb, "launch_us": round(head_s * 1e6, 2)}
 
-    # end to end through the ABI with host buffers: H2D of the step's inputs, D2H of its result
+    # end to end through the ABI with host buffers: each step copies its new rows
+    # from pinned host memory into the captured input buffers, replays the graph
+    # and reads the accepted lengths and tokens back
     fh = eng.feats_new.cpu().pin_memory()
     th = eng.tokens_new.cpu().pin_memory()
     out_h = torch.empty((cfg.batch, cfg.depth + 2), dtype=torch.int32).pin_memory()
-    fd, td = torch.empty_like(eng.feats_new), torch.empty_like(eng.tokens_new)
     ne = max(10, args.steps // 2)
     for i in range(3 + ne):
         if i == 3:
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-        fd.copy_(fh, non_blocking=True)
-        td.copy_(th, non_blocking=True)
-        eng.draft_round(with_pool=False, feats_new=fd, tokens_new=td)
-        a, p, o = eng.verify(T, seed=0, round_id=10 ** 6 + i, with_stats=False)
-        out_h[:, 0].copy_(a, non_blocking=True)
-        out_h[:, 1:].copy_(o, non_blocking=True)
-        torch.cuda.current_stream(dev).synchronize()
+        eng.feats_new.copy_(fh, non_blocking=True)
+        eng.tokens_new.copy_(th, non_blocking=True)
+        eng.replay(round_id=10 ** 6 + i)
+        out_h[:, 0].copy_(eng.accept_len, non_blocking=True)
+        out_h[:, 1:].copy_(eng.out_tokens, non_blocking=True)
+        side.synchronize()
     e2e_s = (time.perf_counter() - t0) / ne
     h2d = fh.numel() * fh.element_size() + th.numel() * th.element_size()
     d2h = out_h.numel() * out_h.element_size()
@@ -300,6 +307,8 @@ def main():
                    "verify": f"T={T}" if T else "greedy",
                    "l2": f"inputs larger than L2: {rb['step'] / 1e9:.2f} GB of weights/KV streamed per step"},
         "draft_tokens_per_s": round(value * cfg.batch * cfg.n_verify, 1),
+        "step": "eagle3_graph_launch: one CUDA graph of eagle3_draft_round + eagle3_verify",
+        "eager_ms_per_step": round(eager_ms, 4),
         "draft_rounds_per_s_draft_only": round(world * 1e3 / draft_ms, 2),
         "step_algorithmic_bytes": rb["step"],
         "step_hbm_frac": round(rb["step"] / (ms_per_step / 1e3) / 1e9 / hbm, 4),

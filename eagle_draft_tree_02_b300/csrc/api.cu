@@ -71,6 +71,11 @@ struct eagle3_ctx {
   int* flags;
   // tcgen05 GEMM plans
   TcGemm* tc = nullptr;
+  // CUDA graph of one step (draft round + verify), replayed by eagle3_graph_launch
+  unsigned long long* d_round = nullptr;        // round id read by the captured verify kernels
+  const unsigned long long* round_ptr = nullptr; // set while capturing
+  cudaGraphExec_t gexec = nullptr;
+  int graph_launches = 0;
   // bookkeeping
   cudaStream_t last = nullptr;
   std::string err;
@@ -214,7 +219,9 @@ void kv_rows(eagle3_ctx* c, int R, const void* feats, bool has_q, const float* h
 }
 
 // Prefix key splits of the attention: about 4 blocks per SM in all (the
-// tensor-core kernel holds 2-3 per SM), in multiples of 64 keys.
+// tensor-core kernel holds 2-3 per SM), in multiples of 64 keys.  (Fewer,
+// longer splits halved the merge but slowed the tensor-core kernel where the
+// queries per KV head make it compute-bound, e.g. 240 verify queries.)
 void attn_splits(const eagle3_ctx* c, int B, int rows_per_req, int& kps, int& nps) {
   const eagle3_config& f = c->cfg;
   const bool mma = attention_uses_mma(c->esz, f.head_dim);
@@ -519,6 +526,7 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
     add((void**)&c->la.ctok, (size_t)Rlm * kLrCap * 4);
     add((void**)&c->cand_all, (size_t)B * c->n_exp * f.lr_cand * 4);
   }
+  add((void**)&c->d_round, 8);
   add((void**)&c->flags, 64);
   size_t total = 0;
   for (auto& p : plan) total += align_up(p.second, 256);
@@ -584,6 +592,7 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
 
 void eagle3_destroy(eagle3_ctx* c) {
   if (!c) return;
+  if (c->gexec) cudaGraphExecDestroy(c->gexec);
   if (c->tc) tc_destroy(c->tc);
   if (c->arena) cudaFree(c->arena);
   delete c;
@@ -730,6 +739,7 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   va.inv_t = mode == 1 ? 1.f / temperature : 1.f;
   va.seed = seed;
   va.round_id = round_id;
+  va.round_ptr = c->round_ptr;
   va.child_tok = c->child_tok;
   va.child_z = c->child_z;
   va.n_parts = c->n_vparts;
@@ -752,6 +762,7 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   wa.inv_t = va.inv_t;
   wa.seed = seed;
   wa.round_id = round_id;
+  wa.round_ptr = c->round_ptr;
   wa.t_tok = tree->tokens;
   wa.child_node = c->child_node;
   wa.n_child = c->n_child;
@@ -772,6 +783,70 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
     if (stats->g_argmax) cudaMemcpyAsync(stats->g_argmax, c->g_arg, n * 4, cudaMemcpyDeviceToDevice, st);
   }
   return cuda_status(c, "verify");
+}
+
+eagle3_status eagle3_graph_capture(eagle3_ctx* c, int B, int n_new, const void* feats_new,
+                                   const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
+                                   int mode, float temperature, unsigned long long seed,
+                                   int* accept_len, int* path, int* out_tokens,
+                                   eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  if (!c->have_round)
+    return fail(c, EAGLE3_ERR_STATE, "run one draft round and verify eagerly before capturing");
+  if (!stream) return fail(c, EAGLE3_ERR_INVALID_ARG, "the legacy default stream cannot be captured");
+  cudaStream_t st = (cudaStream_t)stream;
+  if (c->gexec) {
+    cudaGraphExecDestroy(c->gexec);
+    c->gexec = nullptr;
+  }
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(c, EAGLE3_ERR_CUDA, "cudaStreamBeginCapture failed");
+  }
+  c->round_ptr = c->d_round;
+  eagle3_status s = eagle3_draft_round(c, B, n_new, feats_new, tokens_new, kv, out, nullptr, stream);
+  const int n1 = c->launches;
+  if (s == EAGLE3_OK)
+    s = eagle3_verify(c, B, out, kv, mode, temperature, seed, 0, accept_len, path, out_tokens,
+                      nullptr, stream);
+  const int n2 = c->launches;
+  const std::string why = c->err;
+  c->round_ptr = nullptr;
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamEndCapture(st, &g);
+  if (s != EAGLE3_OK || e != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return fail(c, s != EAGLE3_OK ? s : EAGLE3_ERR_CUDA,
+                s != EAGLE3_OK ? "capture: " + why : "cudaStreamEndCapture failed");
+  }
+  e = cudaGraphInstantiate(&c->gexec, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    c->gexec = nullptr;
+    return fail(c, EAGLE3_ERR_CUDA, std::string("cudaGraphInstantiate: ") + cudaGetErrorString(e));
+  }
+  c->graph_launches = n1 + n2;
+  c->launches = 0;
+  return EAGLE3_OK;
+}
+
+eagle3_status eagle3_graph_launch(eagle3_ctx* c, unsigned long long round_id, eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  if (!c->gexec) return fail(c, EAGLE3_ERR_STATE, "no captured graph on this context");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last = st;
+  launch_set_u64(c->d_round, round_id, st);
+  cudaError_t e = cudaGraphLaunch(c->gexec, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(c, EAGLE3_ERR_CUDA, std::string("cudaGraphLaunch: ") + cudaGetErrorString(e));
+  }
+  c->launches = 1 + c->graph_launches;
+  return cuda_status(c, "graph_launch");
 }
 
 eagle3_status eagle3_lm_head_topk(eagle3_ctx* c, int R, const void* h, int* tok, float* logq,

@@ -211,7 +211,8 @@ __device__ __forceinline__ void verify_row(const VerifyHeadArgs& va, int part, i
       }
     }
     if (va.sampling && !child) {
-      gb = t + verify_gumbel(va.seed, va.round_id, b, u, x);
+      const unsigned long long rid = va.round_ptr ? *va.round_ptr : va.round_id;
+      gb = t + verify_gumbel(va.seed, rid, b, u, x);
       gi = x;
     }
   }
@@ -398,18 +399,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// insert (v, i), known to beat the last entry, into a sorted list of k
-__device__ __forceinline__ void list_insert(float* vals, int* idx, int k, float v, int i) {
-  int p = k - 1;
-  while (p > 0 && better(v, i, vals[p - 1], idx[p - 1])) {
-    vals[p] = vals[p - 1];
-    idx[p] = idx[p - 1];
-    --p;
-  }
-  vals[p] = v;
-  idx[p] = i;
-}
-
 __device__ __forceinline__ void lse_fold_dev(float& m, float& s, float m2, float s2) {
   if (m2 == -INFINITY) return;
   if (m2 > m) {
@@ -420,69 +409,194 @@ __device__ __forceinline__ void lse_fold_dev(float& m, float& s, float m2, float
   }
 }
 
-// draft head: fold this warp's 32 tokens of one row into the row's state
-// state: [0] max, [1] sum exp, [2, 2+k) values, [2+k, 2+2k) tokens (int bits)
+// 64-bit keys ordered like (value desc, token asc): larger key = better
+__device__ __forceinline__ unsigned long long topk_key(float v, int i) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)i);
+}
+__device__ __forceinline__ float key_val(unsigned long long k) {
+  const uint32_t o = (uint32_t)(k >> 32);
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+__device__ __forceinline__ int key_tok(unsigned long long k) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
+}
+
+// Warp-wide bitonic sort of one 64-bit key per lane, descending: lane j ends
+// with the j-th largest key.
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long a, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned long long p = __shfl_xor_sync(0xffffffffu, a, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      a = keep_max ? (a > p ? a : p) : (a < p ? a : p);
+    }
+  }
+  return a;
+}
+
+// Merge a sorted key list A (lane j holds A_j, 0 = empty) into the sorted
+// k-list (vals, idx) in shared memory: element j of either list lands at j
+// plus the number of strictly larger keys in the other list; positions >= k
+// drop out.
+__device__ __forceinline__ void list_merge(float* vals, int* idx, int k, unsigned long long a,
+                                           int lane) {
+  const unsigned long long l = lane < k ? topk_key(vals[lane], idx[lane]) : 0ull;
+  int ra = 0, rl = 0;
+  for (int i = 0; i < k; ++i) {
+    const unsigned long long li = __shfl_sync(0xffffffffu, l, i);
+    const unsigned long long ai = __shfl_sync(0xffffffffu, a, i);
+    ra += li > a;
+    rl += ai > l;
+  }
+  __syncwarp();  // every lane has read the old list
+  if (lane < k) {
+    const int pa = lane + ra, pl = lane + rl;
+    if (pa < k && a != 0ull) {
+      vals[pa] = key_val(a);
+      idx[pa] = key_tok(a);
+    }
+    if (pl < k) {
+      vals[pl] = key_val(l);
+      idx[pl] = key_tok(l);
+    }
+  }
+  __syncwarp();
+}
+
+// draft head: fold this warp's 32 tokens of one row into the row's top-k list
+// (the log-sum-exp part is ph_lse_rows).  state: [0] max, [1] sum exp,
+// [2, 2+k) values, [2+k, 2+2k) tokens (int bits), the list sorted by
+// (value desc, token asc)
 __device__ __forceinline__ void ph_fold_draft(float* st, int k, float x, int tok, bool valid,
                                               int lane) {
-  const float mt = warp_max(x);
-  const float stl = warp_sum(x == -INFINITY ? 0.f : expf(x - mt));
   float* vals = st + 2;
   int* idx = reinterpret_cast<int*>(st + 2 + k);
-  if (lane == 0) lse_fold_dev(st[0], st[1], mt, stl);
-  __syncwarp();
-  bool q = valid && better(x, tok, vals[k - 1], idx[k - 1]);
-  unsigned bal = __ballot_sync(0xffffffffu, q);
-  while (bal) {
-    float bv = q ? x : -INFINITY;
-    int bi = q ? tok : 0x7fffffff;
-    warp_best(bv, bi);
-    if (lane == 0) list_insert(vals, idx, k, bv, bi);
+  const unsigned long long kth = topk_key(vals[k - 1], idx[k - 1]);
+  const unsigned long long mine = valid ? topk_key(x, tok) : 0ull;
+  const bool q = mine > kth;
+  const unsigned bal = __ballot_sync(0xffffffffu, q);
+  if (!bal) return;
+  if (__popc(bal) == 1) {  // one newcomer: shift the list one place from its position
+    const unsigned long long e = __shfl_sync(0xffffffffu, mine, __ffs(bal) - 1);
+    const unsigned long long l = lane < k ? topk_key(vals[lane], idx[lane]) : 0ull;
+    const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && l > e));
+    const unsigned long long up = __shfl_up_sync(0xffffffffu, l, 1);
     __syncwarp();
-    if (tok == bi) q = false;
-    q = q && better(x, tok, vals[k - 1], idx[k - 1]);
-    bal = __ballot_sync(0xffffffffu, q);
+    if (lane < k && lane >= pos) {
+      const unsigned long long nl = lane == pos ? e : up;
+      vals[lane] = key_val(nl);
+      idx[lane] = key_tok(nl);
+    }
+    __syncwarp();
+    return;
   }
+  list_merge(vals, idx, k, warp_sort_desc(q ? mine : 0ull, lane), lane);
 }
 
 // verify head: state [0] best z, [1] its token, [2] max z/T, [3] sum exp, [4] best
-// Gumbel score, [5] its token
-__device__ __forceinline__ void ph_fold_verify(float* st, const VerifyHeadArgs& va, int r, float z,
-                                               int x, bool valid, int lane) {
-  const int b = r / va.M1, u = r % va.M1;
-  float zb = valid ? z : -INFINITY;
-  int zi = valid ? x : 0x7fffffff;
-  const float t = valid ? z * va.inv_t : -INFINITY;
-  float gb = -INFINITY;
-  int gi = 0x7fffffff;
-  if (valid) {
-    bool child = false;
-    for (int c = 0; c < va.kmax; ++c) {
-      if (va.child_tok[(size_t)r * va.kmax + c] == x) {
-        child = true;
-        va.child_z[(size_t)r * va.kmax + c] = z;
+// Gumbel score, [5] its token.  Four rows at once, so that the warp
+// reductions of the rows interleave and their shuffle latencies overlap:
+// row q (< nr) has state st[q], global row r[q], logit z[q] at this lane's
+// token x, and Gumbel noise g[q] (sampling only).
+__device__ __forceinline__ void ph_fold_verify4(float* const (&st)[4], const VerifyHeadArgs& va,
+                                                const int (&r)[4], const float (&z)[4], int nr,
+                                                int x, bool valid, const float (&g)[4], int lane) {
+  float zb[4], t[4], gb[4], m[4], sl[4];
+  int zi[4], gi[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const bool ok = valid && q < nr;
+    zb[q] = ok ? z[q] : -INFINITY;
+    zi[q] = ok ? x : 0x7fffffff;
+    t[q] = ok ? z[q] * va.inv_t : -INFINITY;
+    gb[q] = -INFINITY;
+    gi[q] = 0x7fffffff;
+    if (ok) {
+      bool child = false;
+      const int* ct = va.child_tok + (size_t)r[q] * va.kmax;
+      for (int c = 0; c < va.kmax; ++c) {
+        if (ct[c] == x) {
+          child = true;
+          va.child_z[(size_t)r[q] * va.kmax + c] = z[q];
+        }
+      }
+      if (va.sampling && !child) {
+        gb[q] = t[q] + g[q];
+        gi[q] = x;
       }
     }
-    if (va.sampling && !child) {
-      gb = t + verify_gumbel(va.seed, va.round_id, b, u, x);
-      gi = x;
-    }
+    m[q] = t[q];
   }
-  const float m = warp_max(t);
-  const float sl = warp_sum(t == -INFINITY ? 0.f : expf(t - m));
-  warp_best(zb, zi);
-  warp_best(gb, gi);
-  if (lane == 0) {
-    if (better(zb, zi, st[0], __float_as_int(st[1]))) {
-      st[0] = zb;
-      st[1] = __int_as_float(zi);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], o));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) sl[q] = t[q] == -INFINITY ? 0.f : expf(t[q] - m[q]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      sl[q] += __shfl_xor_sync(0xffffffffu, sl[q], o);
+      const float ozb = __shfl_xor_sync(0xffffffffu, zb[q], o);
+      const int ozi = __shfl_xor_sync(0xffffffffu, zi[q], o);
+      if (better(ozb, ozi, zb[q], zi[q])) {
+        zb[q] = ozb;
+        zi[q] = ozi;
+      }
+      const float ogb = __shfl_xor_sync(0xffffffffu, gb[q], o);
+      const int ogi = __shfl_xor_sync(0xffffffffu, gi[q], o);
+      if (better(ogb, ogi, gb[q], gi[q])) {
+        gb[q] = ogb;
+        gi[q] = ogi;
+      }
     }
-    lse_fold_dev(st[2], st[3], m, sl);
-    if (better(gb, gi, st[4], __float_as_int(st[5]))) {
-      st[4] = gb;
-      st[5] = __int_as_float(gi);
+  if (lane == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (q >= nr) break;
+      float* s = st[q];
+      if (better(zb[q], zi[q], s[0], __float_as_int(s[1]))) {
+        s[0] = zb[q];
+        s[1] = __int_as_float(zi[q]);
+      }
+      lse_fold_dev(s[2], s[3], m[q], sl[q]);
+      if (better(gb[q], gi[q], s[4], __float_as_int(s[5]))) {
+        s[4] = gb[q];
+        s[5] = __int_as_float(gi[q]);
+      }
     }
   }
   __syncwarp();
+}
+
+// draft head, first part for several rows at once: the online log-sum-exp of
+// each row's 32 values, with the rows' reductions interleaved
+template <int N>
+__device__ __forceinline__ void ph_lse_rows(float* const (&st)[N], const float (&x)[N], int nr,
+                                            int lane) {
+  float m[N], sl[N];
+#pragma unroll
+  for (int q = 0; q < N; ++q) m[q] = x[q];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int q = 0; q < N; ++q) m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], o));
+#pragma unroll
+  for (int q = 0; q < N; ++q) sl[q] = x[q] == -INFINITY ? 0.f : expf(x[q] - m[q]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int q = 0; q < N; ++q) sl[q] += __shfl_xor_sync(0xffffffffu, sl[q], o);
+  if (lane == 0) {
+#pragma unroll
+    for (int q = 0; q < N; ++q)
+      if (q < nr) lse_fold_dev(st[q][0], st[q][1], m[q], sl[q]);
+  }
 }
 
 #ifndef E3_HEAD_CTAS_PER_SM
@@ -600,34 +714,93 @@ __global__ void __launch_bounds__(192, 1)
       const int tok = mt * BM + lg * 32 + lane;
       const bool valid = tok < a.V;
       const uint32_t taddr = tmem + (uint32_t)ab * a.acc_cols + ((uint32_t)(lg * 32) << 16);
+      const int tok0 = mt * BM + lg * 32;  // this warp's first token
       for (int c0 = 0; c0 < a.ntile; c0 += 16) {
         if (c0 >= a.ncols) break;
         uint32_t v[16];
         tmem_ld16(taddr + (uint32_t)c0, v);
-        const int step = a.split ? 2 : 1;
+        if (MODE == 1) {
+          // the chunk's rows: 8 split rows (column pairs) or 16 plain rows
+          if (a.split) {
+            float xv[8];
+            float* stp[8];
+            const int r0 = c0 >> 1, nr = min(8, a.R - r0);
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          // two columns per iteration: one split row, or two plain rows
-          const int col = c0 + j;
-          if (col >= a.ncols) break;
-          if (step == 2) {
-            const float val = __uint_as_float(v[j]) + __uint_as_float(v[j + 1]);
-            const int r = col >> 1;
-            if (MODE == 1)
-              ph_fold_draft(mine + (size_t)r * a.sw, a.hp.k, valid ? val : -INFINITY, tok, valid, lane);
-            else
-              ph_fold_verify(mine + (size_t)r * a.sw, a.va, a.r_off + r, val, tok, valid, lane);
+            for (int q = 0; q < 8; ++q) {
+              xv[q] = (valid && q < nr) ? __uint_as_float(v[2 * q]) + __uint_as_float(v[2 * q + 1])
+                                        : -INFINITY;
+              stp[q] = mine + (size_t)(r0 + (q < nr ? q : 0)) * a.sw;
+            }
+            ph_lse_rows<8>(stp, xv, nr, lane);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (q < nr) ph_fold_draft(stp[q], a.hp.k, xv[q], tok, valid, lane);
           } else {
+            float xv[16];
+            float* stp[16];
+            const int r0 = c0, nr = min(16, a.R - r0);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int r = col + h;
-              if (r >= a.ncols) break;
-              const float val = __uint_as_float(v[j + h]);
-              if (MODE == 1)
-                ph_fold_draft(mine + (size_t)r * a.sw, a.hp.k, valid ? val : -INFINITY, tok, valid,
-                              lane);
-              else
-                ph_fold_verify(mine + (size_t)r * a.sw, a.va, a.r_off + r, val, tok, valid, lane);
+            for (int q = 0; q < 16; ++q) {
+              xv[q] = (valid && q < nr) ? __uint_as_float(v[q]) : -INFINITY;
+              stp[q] = mine + (size_t)(r0 + (q < nr ? q : 0)) * a.sw;
+            }
+            ph_lse_rows<16>(stp, xv, nr, lane);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              if (q < nr) ph_fold_draft(stp[q], a.hp.k, xv[q], tok, valid, lane);
+          }
+        } else {
+          // rows in groups of 4: lane l computes the Philox block of row
+          // (l / 8) of the group for tokens tok0 + 4 (l % 8) .. + 3, and each
+          // lane takes its token's word from lane 8 q + lane / 4
+          auto group = [&](int r0, int nr, auto value_of) {
+            uint64_t w[4] = {0ull, 0ull, 0ull, 0ull};
+            if (a.va.sampling) {
+              const int rq = r0 + (lane >> 3);
+              if (rq < a.R) {
+                const int rg = a.r_off + rq;
+                const unsigned long long rid = a.va.round_ptr ? *a.va.round_ptr : a.va.round_id;
+                gumbel_block(a.va.seed, rid, rg / a.va.M1, rg % a.va.M1,
+                             (uint64_t)((tok0 >> 2) + (lane & 7)), w);
+              }
+            }
+            float g[4] = {0.f, 0.f, 0.f, 0.f}, zq[4];
+            int rq[4];
+            float* stp[4];
+            const int nrr = min(nr, a.R - r0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (a.va.sampling) {
+                const int src = q * 8 + (lane >> 2);
+                const uint64_t w0 = __shfl_sync(0xffffffffu, w[0], src);
+                const uint64_t w1 = __shfl_sync(0xffffffffu, w[1], src);
+                const uint64_t w2 = __shfl_sync(0xffffffffu, w[2], src);
+                const uint64_t w3 = __shfl_sync(0xffffffffu, w[3], src);
+                const int sel = lane & 3;
+                g[q] = gumbel_from_word(sel == 0 ? w0 : sel == 1 ? w1 : sel == 2 ? w2 : w3);
+              }
+              const int rr = r0 + (q < nrr ? q : 0);
+              zq[q] = value_of(q);
+              rq[q] = a.r_off + rr;
+              stp[q] = mine + (size_t)rr * a.sw;
+            }
+            ph_fold_verify4(stp, a.va, rq, zq, nrr, tok, valid, g, lane);
+          };
+          if (a.split) {  // 8 rows in this chunk
+#pragma unroll
+            for (int g4 = 0; g4 < 8; g4 += 4) {
+              const int r0 = (c0 >> 1) + g4;
+              if (r0 >= a.R) break;
+              group(r0, 4, [&](int q) {
+                return __uint_as_float(v[2 * (g4 + q)]) + __uint_as_float(v[2 * (g4 + q) + 1]);
+              });
+            }
+          } else {  // 16 rows in this chunk
+#pragma unroll
+            for (int g4 = 0; g4 < 16; g4 += 4) {
+              const int r0 = c0 + g4;
+              if (r0 >= a.R) break;
+              group(r0, 4, [&](int q) { return __uint_as_float(v[g4 + q]); });
             }
           }
         }
@@ -636,12 +809,37 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * ab);
     }
-    // one partial per (CTA, epilogue warp)
-    __syncwarp();
+    // combine the four epilogue warps' states; warp e takes rows r = e (mod 4)
+    // and writes one partial per (CTA, row)
+    asm volatile("bar.sync 1, 128;" ::: "memory");
     if (!*abort_f) {
-      const int part = blockIdx.x * 4 + e;
-      for (int r = 0; r < a.R; ++r) {
-        const float* st = mine + (size_t)r * a.sw;
+      const int part = blockIdx.x;
+      for (int r = e; r < a.R; r += 4) {
+        float* st = state + (size_t)r * a.sw;  // warp 0's state of row r gathers the others
+        for (int o = 1; o < 4; ++o) {
+          const float* so = state + ((size_t)o * a.R + r) * a.sw;
+          if (MODE == 1) {
+            const int k = a.hp.k;
+            if (lane == 0) lse_fold_dev(st[0], st[1], so[0], so[1]);
+            const int* oi = reinterpret_cast<const int*>(so + 2 + k);
+            const unsigned long long ak = lane < k ? topk_key(so[2 + lane], oi[lane]) : 0ull;
+            list_merge(st + 2, reinterpret_cast<int*>(st + 2 + k), k, ak, lane);
+          } else {
+            if (lane == 0) {
+              if (better(so[0], __float_as_int(so[1]), st[0], __float_as_int(st[1]))) {
+                st[0] = so[0];
+                st[1] = so[1];
+              }
+              lse_fold_dev(st[2], st[3], so[2], so[3]);
+              if (better(so[4], __float_as_int(so[5]), st[4], __float_as_int(st[5]))) {
+                st[4] = so[4];
+                st[5] = so[5];
+              }
+            }
+            __syncwarp();
+          }
+        }
+        __syncwarp();
         const size_t pr = (size_t)part * a.R_total + a.r_off + r;
         if (MODE == 1) {
           const int k = a.hp.k;
@@ -815,7 +1013,7 @@ bool launch(TcGemm* t, const CUtensorMap* a0, const CUtensorMap* a1, const CUten
 
 // Persistent head launch when it fits: at most 256 MMA columns and the running
 // state plus at least 3 ring stages in shared memory.  Sets n_parts to the
-// partials written (4 per CTA); false when the caller must use tc_gemm_kernel.
+// partials written (one per CTA); false when the caller must use tc_gemm_kernel.
 template <int MODE>
 bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X, int R, bool split,
                  PhArgs& args, int& n_parts, cudaStream_t st, int r_off = 0, int R_total = -1) {
@@ -860,7 +1058,7 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
     attr = true;
   }
   tc_head_kernel<MODE><<<grid, 192, smem, st>>>(*wmap, mb, args);
-  n_parts = 4 * grid;
+  n_parts = grid;  // one partial per CTA
   return true;
 }
 }  // namespace

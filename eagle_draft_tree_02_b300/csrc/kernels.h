@@ -91,6 +91,7 @@ struct VerifyHeadArgs {
   float inv_t;               // 1/T (1 when greedy)
   int sampling;
   unsigned long long seed, round_id;
+  const unsigned long long* round_ptr;  // if set, the round id is read here (graph replays)
   const int* child_tok;      // [R][kmax] (-1 padded)
   float* child_z;            // [R][kmax]  target logit at each child token
   int n_parts;
@@ -146,6 +147,7 @@ struct WalkArgs {
   int B, M1, kmax, D, sampling;
   float inv_t;
   unsigned long long seed, round_id;
+  const unsigned long long* round_ptr;  // if set, the round id is read here (graph replays)
   const int* t_tok;       // [B][M1]
   const int* child_node;  // [B][M1][kmax] tree indices (-1 padded)
   const int* n_child;     // [B][M1]
@@ -156,5 +158,7 @@ struct WalkArgs {
   int *accept_len, *path, *out_tokens;
 };
 void launch_walk(const WalkArgs& a, cudaStream_t st);
+// *p = v, in stream order (sets the round id a captured graph reads)
+void launch_set_u64(unsigned long long* p, unsigned long long v, cudaStream_t st);
 
 }  // namespace e3

@@ -299,7 +299,8 @@ __global__ void __launch_bounds__(256) verify_head_simt_kernel(const T* __restri
         }
       }
       if (a.sampling && !child) {
-        float g = z * a.inv_t + verify_gumbel(a.seed, a.round_id, b, u, x);
+        const unsigned long long rid = a.round_ptr ? *a.round_ptr : a.round_id;
+        float g = z * a.inv_t + verify_gumbel(a.seed, rid, b, u, x);
         if (better(g, x, gb, gi)) { gb = g; gi = x; }
       }
     }

@@ -24,6 +24,7 @@ namespace e3 {
 __global__ void walk_kernel(WalkArgs a) {
   int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= a.B) return;
+  const unsigned long long rid = a.round_ptr ? *a.round_ptr : a.round_id;
   const size_t tb = (size_t)b * a.M1;
   int u = 0, n = 0;
   int* path = a.path + (size_t)b * a.D;
@@ -44,7 +45,7 @@ __global__ void walk_kernel(WalkArgs a) {
       float lse = a.lse[r], rej = 0.f;
       for (int i = 0; i < nc; ++i) {
         float p = expf(a.child_z[r * a.kmax + i] * a.inv_t - lse);
-        float U = verify_uniform(a.seed, a.round_id, b, u, i);
+        float U = verify_uniform(a.seed, rid, b, u, i);
         if (U * (1.f - rej) < p) { next = a.child_node[r * a.kmax + i]; break; }
         rej += p;
       }
@@ -63,6 +64,12 @@ __global__ void walk_kernel(WalkArgs a) {
 
 void launch_walk(const WalkArgs& a, cudaStream_t st) {
   walk_kernel<<<(a.B + 63) / 64, 64, 0, st>>>(a);
+}
+
+__global__ void set_u64_kernel(unsigned long long* p, unsigned long long v) { *p = v; }
+
+void launch_set_u64(unsigned long long* p, unsigned long long v, cudaStream_t st) {
+  set_u64_kernel<<<1, 1, 0, st>>>(p, v);
 }
 
 }  // namespace e3

@@ -181,6 +181,24 @@ class Engine:
         E.check(self.ctx, s)
         return self.accept_len, self.path, self.out_tokens
 
+    def capture(self, temperature=0.0, seed=0, stream=None):
+        """Capture one step (draft round + verify) into the context's CUDA graph.
+
+        Needs an eager draft round first and a non-default stream; replays read
+        the same input and output buffers (self.feats_new, self.tokens_new,
+        self.tree, self.accept_len, ...)."""
+        mode = 0 if temperature == 0 else 1
+        st = stream if stream is not None else self.stream()
+        s = E.eagle3_graph_capture(self.ctx, self.B, 1, self.feats_new.data_ptr(),
+                                   self.tokens_new.data_ptr(), self.kv, self._tree_s, mode,
+                                   float(temperature or 1.0), seed, self.accept_len.data_ptr(),
+                                   self.path.data_ptr(), self.out_tokens.data_ptr(), st)
+        E.check(self.ctx, s)
+
+    def replay(self, round_id=0, stream=None):
+        st = stream if stream is not None else self.stream()
+        E.check(self.ctx, E.eagle3_graph_launch(self.ctx, round_id, st))
+
     def check(self):
         E.check(self.ctx, E.eagle3_check(self.ctx))
 

@@ -197,6 +197,25 @@ eagle3_status eagle3_verify(eagle3_ctx* ctx, int B, const eagle3_tree* tree, con
                             unsigned long long round_id, int* accept_len, int* path,
                             int* out_tokens, eagle3_verify_stats* stats, eagle3_stream stream);
 
+/* Record one whole step -- eagle3_draft_round followed by eagle3_verify, with
+ * the same arguments as those two calls (no pool or stats outputs) -- into a
+ * CUDA graph kept by the context, replacing any earlier one.  The step's
+ * pointers (new rows, KV descriptor, tree and verification outputs) are fixed
+ * in the graph: refill the same buffers before each replay.  The round id is
+ * not: each eagle3_graph_launch passes its own.  Needs one eager draft round
+ * on the context first (one-time kernel set-up runs there), and a stream
+ * other than the legacy default stream.  Nothing runs during the capture. */
+eagle3_status eagle3_graph_capture(eagle3_ctx* ctx, int B, int n_new, const void* feats_new,
+                                   const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
+                                   int mode, float temperature, unsigned long long seed,
+                                   int* accept_len, int* path, int* out_tokens,
+                                   eagle3_stream stream);
+
+/* Replay the captured step on `stream` with the given round id (the Philox
+ * counter of the sampling draws).  EAGLE3_ERR_STATE if nothing was captured.
+ * The replay's results equal those of the eager calls with that round id. */
+eagle3_status eagle3_graph_launch(eagle3_ctx* ctx, unsigned long long round_id, eagle3_stream stream);
+
 /* The draft LM head alone on R given rows h [R, d] (config dtype, device):
  * per row the top-k (token, log q) and the log-sum-exp of the logits (for the
  * two-stage head: normalised over the candidate set).  tok [R, k] int32,

@@ -12,12 +12,18 @@ generator and the counter layout are this project's reading (stated in the
 design notes).  Use for the round:
 
     key     = (seed, 0)
-    counter = (round_id, b * 2**32 + node, idx, stream)
-    U       = (w0 >> 40) * 2**-24                (stream 0: acceptance tests)
-    U'      = ((w0 >> 40) + 0.5) * 2**-24        (stream 1: Gumbel noise)
-    gumbel  = -log(-log U')
+    acceptance test i at node (b, node), stream 0:
+        counter = (round_id, b * 2**32 + node, i, 0)
+        U  = (w0 >> 40) * 2**-24                   (w0: the first output word)
+    Gumbel noise of token x at node (b, node), stream 1: one block serves
+    four tokens,
+        counter = (round_id, b * 2**32 + node, x // 4, 1)
+        U' = ((w >> 40) + 0.5) * 2**-24            (w: output word x % 4)
+        gumbel = -log(-log U')
 
-where w0 is the first output word.
+The four output words of a Philox block are independent uniform 64-bit
+words (the generator's design), so every token still gets its own
+independent Gumbel variable.
 
 ORACLE / TEST INFRASTRUCTURE ONLY.
 """
@@ -83,9 +89,13 @@ def philox4x64(c0, c1, c2, c3, k0: int, k1: int = 0, rounds: int = ROUNDS):
     return c0, c1, c2, c3
 
 
-def _word0(seed, round_id, b, node, idx, stream):
+def _words(seed, round_id, b, node, idx, stream):
     c1 = (np.asarray(b, dtype=np.uint64) << _S32) + np.asarray(node, dtype=np.uint64)
-    return philox4x64(round_id, c1, idx, stream, int(seed))[0]
+    return philox4x64(round_id, c1, idx, stream, int(seed))
+
+
+def _word0(seed, round_id, b, node, idx, stream):
+    return _words(seed, round_id, b, node, idx, stream)[0]
 
 
 def uniform(seed, round_id, b, node, idx):
@@ -95,7 +105,10 @@ def uniform(seed, round_id, b, node, idx):
 
 
 def gumbel(seed, round_id, b, node, idx):
-    """Gumbel(0, 1) noise from stream 1, using the open-interval uniform U'."""
-    w = _word0(seed, round_id, b, node, idx, 1)
+    """Gumbel(0, 1) noise of token idx from stream 1: word idx % 4 of block idx // 4,
+    through the open-interval uniform U'."""
+    idx = np.asarray(idx, dtype=np.uint64)
+    ws = _words(seed, round_id, b, node, idx >> np.uint64(2), 1)
+    w = np.choose((idx & np.uint64(3)).astype(np.int64), ws)
     u = ((w >> np.uint64(40)).astype(np.float64) + 0.5) * 2.0 ** -24
     return -np.log(-np.log(u))

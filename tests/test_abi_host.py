@@ -85,3 +85,9 @@ def test_noalloc_head_rejects_bad_requests_before_launch(E):
     assert call(d=4100) == E.ERR_INVALID_ARG            # ... and 16-byte rows
     assert call(R=257) == E.ERR_SHAPE                   # tensor-core head: <= 256 rows
     assert call(R=200) == E.ERR_SHAPE                   # partials beyond the 16 MiB scratch
+
+
+def test_graph_calls_need_a_context(E):
+    kv, tree = E.eagle3_kv(), E.eagle3_tree()
+    assert E.eagle3_graph_launch(0, 0, 0) == E.ERR_INVALID_ARG
+    assert E.eagle3_graph_capture(0, 1, 1, 1, 1, kv, tree, 0, 1.0, 0, 1, 1, 1, 0) == E.ERR_INVALID_ARG

@@ -115,6 +115,18 @@ def test_philox_matches_numpy_philox():
         assert tuple(int(v) for v in vec) == philox.philox4x64_scalar(ctr, key)
 
 
+def test_gumbel_stream_layout_against_the_scalar_definition():
+    """Token x reads word x % 4 of the block at counter index x // 4 (stream 1);
+    checked against the word-by-word definition, not the vectorised code."""
+    seed, rid, b, node = 11, 5, 3, 17
+    xs = np.array([0, 1, 2, 3, 4, 7, 8, 1001, 128255], dtype=np.int64)
+    g = philox.gumbel(seed, rid, b, node, xs)
+    for x, gx in zip(xs, g):
+        w = philox.philox4x64_scalar((rid, (b << 32) + node, int(x) // 4, 1), (seed, 0))[int(x) % 4]
+        u = ((w >> 40) + 0.5) * 2.0 ** -24
+        assert gx == -np.log(-np.log(u))
+
+
 def test_philox_uniform_and_gumbel_ranges():
     u = philox.uniform(7, 3, 0, np.arange(1000), 2)
     assert u.min() >= 0 and u.max() < 1
