@@ -622,27 +622,23 @@ eagle3_status eagle3_prefill(eagle3_ctx* c, int B, int total_rows, const int* cu
   return cuda_status(c, "prefill");
 }
 
-eagle3_status eagle3_draft_round(eagle3_ctx* c, int B, int n_new, const void* feats_new,
-                                 const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
-                                 eagle3_pool* pool_out, eagle3_stream stream) {
-  if (!c) return EAGLE3_ERR_INVALID_ARG;
-  c->err.clear();
-  c->launches = 0;
-  if (B < 1 || B > c->cfg.max_batch) return fail(c, EAGLE3_ERR_SHAPE, "B out of range");
-  if (n_new < 1 || n_new > c->cfg.max_new) return fail(c, EAGLE3_ERR_SHAPE, "n_new out of range");
-  if (!feats_new || !tokens_new) return fail(c, EAGLE3_ERR_INVALID_ARG, "null input");
-  if (!kv_ok(c, kv)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad kv descriptor");
-  if (!tree_ok(out)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad tree output");
+}  // extern "C"
+
+namespace {
+// One draft round; the new rows are n_new per request (cu_new NULL) or ragged.
+eagle3_status draft_round_impl(eagle3_ctx* c, int B, int n_new, const int* cu_new, int total_new,
+                               const void* feats_new, const int* tokens_new, const eagle3_kv* kv,
+                               eagle3_tree* out, eagle3_pool* pool_out, eagle3_stream stream) {
   cudaStream_t st = (cudaStream_t)stream;
   c->last = st;
   const int k = c->k, D = c->D;
   // pass 0: the new rows' K/V, then the root row through the whole layer
-  launch_plan_root(B, n_new, tokens_new, kv->seq_lens, c->n_slots, c->rp, c->root_tok, c->root_pos,
-                   c->n_prefix, st);
+  launch_plan_root(B, n_new, cu_new, total_new, c->cfg.max_new, tokens_new, kv->seq_lens,
+                   c->n_slots, c->rp, c->root_tok, c->root_pos, c->n_prefix, c->flags, st);
   c->launches++;
   const bool sp0 = use_split(c, B), spk = use_split(c, B * k);
-  kv_rows(c, B * n_new, feats_new, true, nullptr, kv, KvTarget{nullptr, nullptr, 0},
-          use_split(c, B * n_new), st);
+  kv_rows(c, total_new, feats_new, true, nullptr, kv, KvTarget{nullptr, nullptr, 0},
+          use_split(c, total_new), st);
   tail_rows(c, B, 1, c->g, kv, KvTarget{nullptr, nullptr, 0}, c->h_root, sp0, st);
   draft_head(c, c->h_root, B, sp0, c->top_tok, c->top_logq, c->top_lse, st, 0, 1);
   launch_expand(B, 0, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
@@ -676,6 +672,56 @@ eagle3_status eagle3_draft_round(eagle3_ctx* c, int B, int n_new, const void* fe
     c->last_B = B;
   }
   return s;
+}
+}  // namespace
+
+extern "C" {
+
+eagle3_status eagle3_draft_round(eagle3_ctx* c, int B, int n_new, const void* feats_new,
+                                 const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
+                                 eagle3_pool* pool_out, eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  if (B < 1 || B > c->cfg.max_batch) return fail(c, EAGLE3_ERR_SHAPE, "B out of range");
+  if (n_new < 1 || n_new > c->cfg.max_new) return fail(c, EAGLE3_ERR_SHAPE, "n_new out of range");
+  if (!feats_new || !tokens_new) return fail(c, EAGLE3_ERR_INVALID_ARG, "null input");
+  if (!kv_ok(c, kv)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad kv descriptor");
+  if (!tree_ok(out)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad tree output");
+  return draft_round_impl(c, B, n_new, nullptr, B * n_new, feats_new, tokens_new, kv, out, pool_out,
+                          stream);
+}
+
+eagle3_status eagle3_draft_round_ragged(eagle3_ctx* c, int B, int total_new, const int* cu_new,
+                                        const void* feats_new, const int* tokens_new,
+                                        const eagle3_kv* kv, eagle3_tree* out, eagle3_pool* pool_out,
+                                        eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  if (B < 1 || B > c->cfg.max_batch) return fail(c, EAGLE3_ERR_SHAPE, "B out of range");
+  if (total_new < B || total_new > B * c->cfg.max_new)
+    return fail(c, EAGLE3_ERR_SHAPE, "total_new must be in [B, B * max_new]");
+  if (!cu_new || !feats_new || !tokens_new) return fail(c, EAGLE3_ERR_INVALID_ARG, "null input");
+  if (!kv_ok(c, kv)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad kv descriptor");
+  if (!tree_ok(out)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad tree output");
+  return draft_round_impl(c, B, 0, cu_new, total_new, feats_new, tokens_new, kv, out, pool_out,
+                          stream);
+}
+
+eagle3_status eagle3_next_rows(eagle3_ctx* c, int B, const int* accept_len, const int* out_tokens,
+                               int* cu_new, int* tokens_new, eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  if (B < 1 || B > c->cfg.max_batch || B > 1024) return fail(c, EAGLE3_ERR_SHAPE, "B out of range");
+  if (!accept_len || !out_tokens || !cu_new || !tokens_new)
+    return fail(c, EAGLE3_ERR_INVALID_ARG, "null pointer");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last = st;
+  launch_next_rows(B, c->D, accept_len, out_tokens, cu_new, tokens_new, c->flags, st);
+  c->launches++;
+  return cuda_status(c, "next_rows");
 }
 
 eagle3_status eagle3_build_tree(eagle3_ctx* c, int B, int pool_n, const int* pool_tok,
@@ -787,9 +833,9 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
 
 eagle3_status eagle3_graph_capture(eagle3_ctx* c, int B, int n_new, const void* feats_new,
                                    const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
-                                   int mode, float temperature, unsigned long long seed,
-                                   int* accept_len, int* path, int* out_tokens,
-                                   eagle3_stream stream) {
+                                   int with_verify, int mode, float temperature,
+                                   unsigned long long seed, int* accept_len, int* path,
+                                   int* out_tokens, eagle3_stream stream) {
   if (!c) return EAGLE3_ERR_INVALID_ARG;
   if (!c->have_round)
     return fail(c, EAGLE3_ERR_STATE, "run one draft round and verify eagerly before capturing");
@@ -806,10 +852,12 @@ eagle3_status eagle3_graph_capture(eagle3_ctx* c, int B, int n_new, const void* 
   c->round_ptr = c->d_round;
   eagle3_status s = eagle3_draft_round(c, B, n_new, feats_new, tokens_new, kv, out, nullptr, stream);
   const int n1 = c->launches;
-  if (s == EAGLE3_OK)
+  int n2 = 0;
+  if (s == EAGLE3_OK && with_verify) {
     s = eagle3_verify(c, B, out, kv, mode, temperature, seed, 0, accept_len, path, out_tokens,
                       nullptr, stream);
-  const int n2 = c->launches;
+    n2 = c->launches;
+  }
   const std::string why = c->err;
   c->round_ptr = nullptr;
   cudaGraph_t g = nullptr;
@@ -900,6 +948,7 @@ eagle3_status eagle3_check(eagle3_ctx* c) {
   if (flags & FLAG_PAGE_RANGE) m += " page index out of range;";
   if (flags & FLAG_TOKEN_RANGE) m += " token id out of range;";
   if (flags & FLAG_POS_RANGE) m += " position beyond cache capacity;";
+  if (flags & FLAG_ROWS_RANGE) m += " new-row count or accepted length out of range;";
   if (flags & FLAG_TIMEOUT) {
     m += " bounded wait timed out;";
     return fail(c, EAGLE3_ERR_TIMEOUT, m);

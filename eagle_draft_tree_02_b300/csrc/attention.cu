@@ -37,9 +37,14 @@ constexpr int KC = 64;   // keys per chunk
 constexpr int NT = 256;  // threads (CUDA-core kernel)
 }
 
+// key-sharing warps per query group of the tensor-core kernel
+int attention_kw(int rows_per_req, int Hq, int Hkv) {
+  return rows_per_req * (Hq / Hkv) <= 16 ? 4 : 1;
+}
+
 int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma) {
   int per = rows_per_req * (Hq / Hkv);
-  const int q = mma ? QGM : QG;
+  const int q = mma ? QGM / attention_kw(rows_per_req, Hq, Hkv) : QG;
   return (per + q - 1) / q;
 }
 
@@ -61,6 +66,7 @@ __device__ __forceinline__ const T* kv_row_ptr(const AttnArgs& a, const void* ca
 
 template <typename T>
 __global__ void __launch_bounds__(NT) tree_attention_kernel(AttnArgs a, int z_off) {
+  pdl_begin();
   extern __shared__ float sm[];
   const int dh = a.dh;
   const int G = a.Hq / a.Hkv;
@@ -267,10 +273,14 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 }
 }  // namespace
 
-template <int DH>
+// KW warps share each group of 16 queries, each taking KC / KW keys of every
+// chunk (KW = 4 when a KV head has at most 16 queries, as in a batch of chains),
+// and merge their softmax states at the end; KW = 1: one warp per 16 queries.
+template <int DH, int KW>
 __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
+  pdl_begin();
   constexpr int LD = DH + 8;       // shared row stride (bf16): conflict-free fragment loads
-  constexpr int NKT = KC / 8;      // key tiles of 8 per chunk
+  constexpr int NKT = KC / 8 / KW; // key tiles of 8 per chunk and warp
   constexpr int NDT = DH / 8;      // output tiles of 8 dims
   constexpr int NKS = DH / 16;     // k16 steps over dh
   constexpr int PIECES = DH / 8;   // 16-byte pieces per K or V row
@@ -282,7 +292,8 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
   const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv, split = blockIdx.z;
   const int G = a.Hq / a.Hkv, nq = a.rows_per_req * G;
   const int R = a.B * a.rows_per_req;
-  const int qw = blockIdx.y * QGM + warp * 16;  // first query of this warp
+  const int kslice = warp % KW;                  // this warp's share of each chunk's keys
+  const int qw = blockIdx.y * (QGM / KW) + (warp / KW) * 16;  // first query of this warp
   // prefix splits: keys [key_lo, key_hi) of the cache; tree splits: 64 tree
   // slots, fp32 scratch staged as bf16 (hi, lo) pairs in the two buffers
   const bool tree = split >= a.n_prefix_splits;
@@ -414,7 +425,7 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
       for (int ks = 0; ks < NKS; ++ks) {
 #pragma unroll
         for (int nt = 0; nt < NKT; ++nt) {
-          const size_t ko = (size_t)(nt * 8 + g) * LD + ks * 16 + t4 * 2;
+          const size_t ko = (size_t)((kslice * NKT + nt) * 8 + g) * LD + ks * 16 + t4 * 2;
           const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kb + ko);
           const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kb + ko + 8);
           mma_16816(s[nt], qh[ks], b0, b1);
@@ -431,7 +442,7 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
       for (int nt = 0; nt < NKT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int key = c0 + nt * 8 + t4 * 2 + (e & 1);
+          const int key = c0 + (kslice * NKT + nt) * 8 + t4 * 2 + (e & 1);
           bool ok = key < key_hi;
           if (ok && tree) {
             const uint32_t* mb = mrow_bits[e >> 1];
@@ -477,14 +488,15 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
       }
       // O += P V over the chunk's keys, 16 at a time
 #pragma unroll
-      for (int kk = 0; kk < KC / 16; ++kk) {
+      for (int kk = 0; kk < KC / 16 / KW; ++kk) {
         uint32_t ph[4], pl[4];
         split_pair(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
         split_pair(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
         split_pair(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
         split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
         const int mat = lane >> 3, r8 = lane & 7;
-        const size_t vo = (size_t)(kk * 16 + r8 + (mat & 1) * 8) * LD + (mat >> 1) * 8;
+        const int kg = kslice * (KC / 16 / KW) + kk;  // this 16-key group within the chunk
+        const size_t vo = (size_t)(kg * 16 + r8 + (mat & 1) * 8) * LD + (mat >> 1) * 8;
 #pragma unroll
         for (int d2 = 0; d2 < DH / 16; ++d2) {
           uint32_t v0, v1, v2, v3;
@@ -509,20 +521,67 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
     lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
     lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
   }
+  if (KW == 1) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (qr[h] >= nq) continue;
+      const int row = b * a.rows_per_req + qr[h] / G, head = kvh * G + qr[h] % G;
+      const size_t base = ((size_t)split * R + row) * a.Hq + head;
+      float* op = a.o_part + base * DH;
+#pragma unroll
+      for (int dt = 0; dt < NDT; ++dt) {
+        op[dt * 8 + t4 * 2] = o[dt][2 * h];
+        op[dt * 8 + t4 * 2 + 1] = o[dt][2 * h + 1];
+      }
+      if (t4 == 0) {
+        a.ml_part[base * 2] = mrow[h];
+        a.ml_part[base * 2 + 1] = lrow[h];
+      }
+    }
+    return;
+  }
+  // KW > 1: the warps of a query group merge their states through shared
+  // memory (the K/V buffers are free after the last chunk)
+  float* cm = reinterpret_cast<float*>(att_smem);  // [4 warps][16] max
+  float* cl = cm + 4 * 16;                          // [4][16] sum
+  float* co = cl + 4 * 16;                          // [4][16][DH] unnormalised o
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    if (qr[h] >= nq) continue;
-    const int row = b * a.rows_per_req + qr[h] / G, head = kvh * G + qr[h] % G;
-    const size_t base = ((size_t)split * R + row) * a.Hq + head;
-    float* op = a.o_part + base * DH;
+    const int r16 = g + 8 * h;
+    if (t4 == 0) {
+      cm[warp * 16 + r16] = mrow[h];
+      cl[warp * 16 + r16] = lrow[h];
+    }
 #pragma unroll
     for (int dt = 0; dt < NDT; ++dt) {
-      op[dt * 8 + t4 * 2] = o[dt][2 * h];
-      op[dt * 8 + t4 * 2 + 1] = o[dt][2 * h + 1];
+      co[((size_t)warp * 16 + r16) * DH + dt * 8 + t4 * 2] = o[dt][2 * h];
+      co[((size_t)warp * 16 + r16) * DH + dt * 8 + t4 * 2 + 1] = o[dt][2 * h + 1];
     }
-    if (t4 == 0) {
-      a.ml_part[base * 2] = mrow[h];
-      a.ml_part[base * 2 + 1] = lrow[h];
+  }
+  __syncthreads();
+  constexpr int QWB = 4 / KW;  // query groups in the block
+  for (int idx = tid; idx < QWB * 16 * DH; idx += blockDim.x) {
+    const int grp = idx / (16 * DH), r16 = (idx / DH) % 16, dim = idx % DH;
+    const int q = blockIdx.y * (QGM / KW) + grp * 16 + r16;
+    if (q >= nq) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < KW; ++w) M = fmaxf(M, cm[(grp * KW + w) * 16 + r16]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < KW; ++w) {
+      const int wi = grp * KW + w;
+      const float mw = cm[wi * 16 + r16];
+      const float e = mw == -INFINITY ? 0.f : expf(mw - M);
+      L += cl[wi * 16 + r16] * e;
+      O += co[((size_t)wi * 16 + r16) * DH + dim] * e;
+    }
+    const int row = b * a.rows_per_req + q / G, head = kvh * G + q % G;
+    const size_t base = ((size_t)split * R + row) * a.Hq + head;
+    a.o_part[base * DH + dim] = O;
+    if (dim == 0) {
+      a.ml_part[base * 2] = M;
+      a.ml_part[base * 2 + 1] = L;
     }
   }
 }
@@ -530,6 +589,7 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
 // merge the key splits of one (row, head): o = sum_s o_s e^{m_s - m} / sum_s l_s e^{m_s - m}
 template <typename T>
 __global__ void attention_combine_kernel(AttnArgs a) {
+  pdl_begin();
   __shared__ float wts[256];  // per split: its weight e^{m_s - m} / l
   __shared__ float red[32];
   const int row = blockIdx.x, head = blockIdx.y, tid = threadIdx.x;
@@ -587,25 +647,37 @@ void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
   if (!attr_set[ti]) {
     cudaFuncSetAttribute(tree_attention_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          160 * 1024);
-    cudaFuncSetAttribute(prefix_attention_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         4 * KC * (64 + 8) * 2);
-    cudaFuncSetAttribute(prefix_attention_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         4 * KC * (128 + 8) * 2);
+    cudaFuncSetAttribute(prefix_attention_mma_kernel<64, 1>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * KC * (64 + 8) * 2);
+    cudaFuncSetAttribute(prefix_attention_mma_kernel<128, 1>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * KC * (128 + 8) * 2);
+    cudaFuncSetAttribute(prefix_attention_mma_kernel<64, 4>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * KC * (64 + 8) * 2);
+    cudaFuncSetAttribute(prefix_attention_mma_kernel<128, 4>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * KC * (128 + 8) * 2);
     attr_set[ti] = true;
   }
   if (mma) {  // prefix and tree splits in one launch
     dim3 gp(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, true), n_splits);
     const size_t sm2 = (size_t)4 * KC * (a.dh + 8) * 2;
-    if (a.dh == 128)
-      prefix_attention_mma_kernel<128><<<gp, 128, sm2, st>>>(a);
-    else
-      prefix_attention_mma_kernel<64><<<gp, 128, sm2, st>>>(a);
+    const bool kw4 = attention_kw(a.rows_per_req, a.Hq, a.Hkv) == 4;
+    if (a.dh == 128) {
+      if (kw4)
+        launch_pdl(prefix_attention_mma_kernel<128, 4>, dim3(gp), dim3(128), sm2, st, a);
+      else
+        launch_pdl(prefix_attention_mma_kernel<128, 1>, dim3(gp), dim3(128), sm2, st, a);
+    } else {
+      if (kw4)
+        launch_pdl(prefix_attention_mma_kernel<64, 4>, dim3(gp), dim3(128), sm2, st, a);
+      else
+        launch_pdl(prefix_attention_mma_kernel<64, 1>, dim3(gp), dim3(128), sm2, st, a);
+    }
   } else {
     dim3 grid(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, false), n_splits);
-    tree_attention_kernel<T><<<grid, NT, smem, st>>>(a, 0);
+    launch_pdl(tree_attention_kernel<T>, dim3(grid), dim3(NT), smem, st, a, 0);
   }
   dim3 g2(R, a.Hq);
-  attention_combine_kernel<T><<<g2, a.dh, 0, st>>>(a);
+  launch_pdl(attention_combine_kernel<T>, dim3(g2), dim3(a.dh), 0, st, a);
 }
 
 template void launch_tree_attention<float>(const AttnArgs&, cudaStream_t);

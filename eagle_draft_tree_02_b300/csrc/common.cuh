@@ -17,6 +17,7 @@ enum : int {
   FLAG_TOKEN_RANGE = 4,       // token id outside [0, V)
   FLAG_POS_RANGE = 8,         // row position beyond the cache capacity
   FLAG_TIMEOUT = 16,          // a bounded wait gave up
+  FLAG_ROWS_RANGE = 32,       // a request's new-row count or accepted length out of range
 };
 
 template <typename T> __device__ __forceinline__ float ldf(const T* p);
@@ -89,5 +90,34 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 __device__ __forceinline__ void raise_flag(int* flags, int bit) { atomicOr(flags, bit); }
+
+// Programmatic dependent launch.  Every kernel here is launched with
+// launch_pdl, so it may start while the kernel before it on the stream is
+// still finishing.  pdl_begin() first waits until that kernel has completed
+// and its writes are visible (a no-op for a kernel launched the ordinary way),
+// then lets the next kernel start launching.  It must run before the kernel
+// reads anything a predecessor wrote, and before any thread returns: a kernel
+// completes only after it has waited, which keeps the chain transitive.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` with programmatic stream serialization allowed (see pdl_begin).
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 }  // namespace e3

@@ -21,6 +21,7 @@ __global__ void build_input_kernel(int R, int d, int V, float eps, const int* __
                                    const T* __restrict__ E, const T* __restrict__ g_emb,
                                    const T* __restrict__ g_hid, T* __restrict__ x, bool split,
                                    int* flags) {
+  pdl_begin();
   __shared__ float red[32];
   int r = blockIdx.x;
   int t = tok[r];
@@ -57,6 +58,7 @@ __device__ __forceinline__ float sum_parts(const float* p, size_t stride, int S)
 // g = sum of fusion partials (fp32 [R, d])
 __global__ void reduce_parts_kernel(int R, int N, int S, const float* __restrict__ part,
                                     float* __restrict__ out) {
+  pdl_begin();
   size_t n = (size_t)R * N;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
     out[i] = sum_parts(part + i, n, S);
@@ -67,6 +69,7 @@ __global__ void reduce_parts_kernel(int R, int N, int S, const float* __restrict
 // out [q heads | k heads | v heads] in the partials when has_q, else [k | v].
 template <typename T>
 __global__ void qkv_epilogue_kernel(QkvEpi p) {
+  pdl_begin();
   int r = blockIdx.y;
   int half = p.dh / 2;
   int nh = (p.has_q ? p.Hq : 0) + 2 * p.Hkv;
@@ -142,6 +145,7 @@ __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* _
                                   const float* __restrict__ hid_base, const int* __restrict__ hid_row,
                                   const T* __restrict__ g_post, float* __restrict__ r_out,
                                   T* __restrict__ z_out, bool split) {
+  pdl_begin();
   __shared__ float red[32];
   int r = blockIdx.x;
   const float* h = hid_base + (size_t)hid_row[r] * d;
@@ -164,6 +168,7 @@ __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* _
 template <typename T>
 __global__ void swiglu_kernel(int R, int F, int S, const float* __restrict__ part, T* __restrict__ a,
                               bool split) {
+  pdl_begin();
   size_t n = (size_t)R * F;
   size_t stride = (size_t)R * 2 * F;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
@@ -182,6 +187,7 @@ __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float
                                      const int* __restrict__ s_dst, float* __restrict__ s_base,
                                      const int* __restrict__ h_dst, T* __restrict__ h_base,
                                      bool split) {
+  pdl_begin();
   __shared__ float red[32];
   extern __shared__ float srow[];
   int r = blockIdx.x;
@@ -213,7 +219,7 @@ void launch_build_input(int R, int d, int V, float eps, const int* tok, const fl
                         const int* hid_row, const void* E, const void* g_emb, const void* g_hid,
                         void* x, bool split, int* flags, cudaStream_t st) {
   if (R <= 0) return;
-  build_input_kernel<T><<<R, kRowThreads, 0, st>>>(R, d, V, eps, tok, hid_base, hid_row, (const T*)E,
+  launch_pdl(build_input_kernel<T>, dim3(R), dim3(kRowThreads), 0, st, R, d, V, eps, tok, hid_base, hid_row, (const T*)E,
                                            (const T*)g_emb, (const T*)g_hid, (T*)x, split, flags);
 }
 
@@ -222,7 +228,7 @@ void launch_reduce_parts(int R, int N, int S, const float* part, float* out, cud
   if (!n) return;
   int blocks = (int)((n + 255) / 256);
   if (blocks > 148 * 8) blocks = 148 * 8;
-  reduce_parts_kernel<<<blocks, 256, 0, st>>>(R, N, S, part, out);
+  launch_pdl(reduce_parts_kernel, dim3(blocks), dim3(256), 0, st, R, N, S, part, out);
 }
 
 template <typename T>
@@ -231,7 +237,7 @@ void launch_qkv_epilogue(const QkvEpi& p, cudaStream_t st) {
   int nh = (p.has_q ? p.Hq : 0) + 2 * p.Hkv;
   int pairs = nh * p.dh / 2;
   dim3 grid((pairs + 255) / 256, p.R);
-  qkv_epilogue_kernel<T><<<grid, 256, 0, st>>>(p);
+  launch_pdl(qkv_epilogue_kernel<T>, dim3(grid), dim3(256), 0, st, p);
 }
 
 template <typename T>
@@ -239,7 +245,7 @@ void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const 
                        const int* hid_row, const void* g_post, float* r_out, void* z_out,
                        bool split, cudaStream_t st) {
   if (R <= 0) return;
-  o_epilogue_kernel<T><<<R, kRowThreads, 0, st>>>(R, d, S, eps, part, hid_base, hid_row, (const T*)g_post,
+  launch_pdl(o_epilogue_kernel<T>, dim3(R), dim3(kRowThreads), 0, st, R, d, S, eps, part, hid_base, hid_row, (const T*)g_post,
                                           r_out, (T*)z_out, split);
 }
 
@@ -249,7 +255,7 @@ void launch_swiglu(int R, int F, int S, const float* part, void* a, bool split, 
   if (!n) return;
   int blocks = (int)((n + 255) / 256);
   if (blocks > 148 * 16) blocks = 148 * 16;
-  swiglu_kernel<T><<<blocks, 256, 0, st>>>(R, F, S, part, (T*)a, split);
+  launch_pdl(swiglu_kernel<T>, dim3(blocks), dim3(256), 0, st, R, F, S, part, (T*)a, split);
 }
 
 template <typename T>
@@ -257,7 +263,7 @@ void launch_down_epilogue(int R, int d, int S, float eps, const float* part, con
                           const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
                           void* h_base, bool split, cudaStream_t st) {
   if (R <= 0) return;
-  down_epilogue_kernel<T><<<R, kRowThreads, d * sizeof(float), st>>>(R, d, S, eps, part, r_in,
+  launch_pdl(down_epilogue_kernel<T>, dim3(R), dim3(kRowThreads), d * sizeof(float), st, R, d, S, eps, part, r_in,
                                                             (const T*)g_final, s_dst, s_base, h_dst,
                                                             (T*)h_base, split);
 }

@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ X,
                                                         float* __restrict__ Y, int ldy, int col0,
                                                         int R, int N, int K, int kps,
                                                         size_t split_stride) {
+  pdl_begin();
   __shared__ float Xs[BK][BM + 4];
   __shared__ float Ws[BK][BN + 4];
   int tid = threadIdx.x;
@@ -71,7 +72,7 @@ void launch_gemm_simt(const void* X, int ldx, const void* W, int ldw, float* Y, 
   int kps = (K + S - 1) / S;
   kps = (kps + BK - 1) / BK * BK;
   dim3 grid((N + BN - 1) / BN, (R + BM - 1) / BM, S);
-  gemm_simt_kernel<T><<<grid, 256, 0, st>>>((const T*)X, ldx, (const T*)W, ldw, Y, ldy, col0, R, N,
+  launch_pdl(gemm_simt_kernel<T>, dim3(grid), dim3(256), 0, st, (const T*)X, ldx, (const T*)W, ldw, Y, ldy, col0, R, N,
                                             K, kps, split_stride);
 }
 

@@ -32,7 +32,8 @@ constexpr int BK = 64;                    // K per stage: one 128-byte swizzle r
 constexpr int UK = 16;                    // K per tcgen05.mma (kind::f16)
 constexpr uint32_t A_STAGE = BM * BK * 2;  // 16 KB
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
-constexpr int kSmemBudget = 100 * 1024;   // per CTA: two CTAs share an SM
+constexpr int kSmemBudget = 110 * 1024;   // per CTA when two CTAs share an SM
+constexpr int kSmemBudgetWide = 220 * 1024;  // one CTA per SM: tiles of more than 64 columns
 
 struct TcArgs {
   int R;       // activation rows
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  pdl_begin();  // set-up above overlaps the previous kernel's tail
 
   if (nkb > 0 && warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -500,11 +502,12 @@ __device__ __forceinline__ void ph_fold_draft(float* st, int k, float x, int tok
 // verify head: state [0] best z, [1] its token, [2] max z/T, [3] sum exp, [4] best
 // Gumbel score, [5] its token.  Four rows at once, so that the warp
 // reductions of the rows interleave and their shuffle latencies overlap:
-// row q (< nr) has state st[q], global row r[q], logit z[q] at this lane's
-// token x, and Gumbel noise g[q] (sampling only).
+// row q (< nr) has state st[q], global row r[q], child tokens ct[q] (shared
+// memory), logit z[q] at this lane's token x, and Gumbel noise g[q].
 __device__ __forceinline__ void ph_fold_verify4(float* const (&st)[4], const VerifyHeadArgs& va,
-                                                const int (&r)[4], const float (&z)[4], int nr,
-                                                int x, bool valid, const float (&g)[4], int lane) {
+                                                const int (&r)[4], const int* const (&ct)[4],
+                                                const float (&z)[4], int nr, int x, bool valid,
+                                                const float (&g)[4], int lane) {
   float zb[4], t[4], gb[4], m[4], sl[4];
   int zi[4], gi[4];
 #pragma unroll
@@ -517,9 +520,8 @@ __device__ __forceinline__ void ph_fold_verify4(float* const (&st)[4], const Ver
     gi[q] = 0x7fffffff;
     if (ok) {
       bool child = false;
-      const int* ct = va.child_tok + (size_t)r[q] * va.kmax;
       for (int c = 0; c < va.kmax; ++c) {
-        if (ct[c] == x) {
+        if (ct[q][c] == x) {
           child = true;
           va.child_z[(size_t)r[q] * va.kmax + c] = z[q];
         }
@@ -621,6 +623,7 @@ __global__ void __launch_bounds__(192, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gen);
   volatile int* abort_f = reinterpret_cast<volatile int*>(gen + 4);
   float* state = reinterpret_cast<float*>(gen + 16);  // [4][R][sw]
+  int* child_s = reinterpret_cast<int*>(state + (size_t)4 * a.R * a.sw);  // verify: [R][kmax]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -656,6 +659,12 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  pdl_begin();  // set-up above overlaps the previous kernel's tail
+  if (MODE == 2) {  // this launch's rows' child tokens, read by every tile's epilogue
+    for (int i = threadIdx.x; i < a.R * a.va.kmax; i += blockDim.x)
+      child_s[i] = a.va.child_tok[(size_t)a.r_off * a.va.kmax + i];
+    __syncthreads();
+  }
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer: a ring of stages across all of this CTA's tiles
@@ -767,6 +776,7 @@ __global__ void __launch_bounds__(192, 1)
             float g[4] = {0.f, 0.f, 0.f, 0.f}, zq[4];
             int rq[4];
             float* stp[4];
+            const int* ctp[4];
             const int nrr = min(nr, a.R - r0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -783,8 +793,9 @@ __global__ void __launch_bounds__(192, 1)
               zq[q] = value_of(q);
               rq[q] = a.r_off + rr;
               stp[q] = mine + (size_t)rr * a.sw;
+              ctp[q] = child_s + (size_t)rr * a.va.kmax;
             }
-            ph_fold_verify4(stp, a.va, rq, zq, nrr, tok, valid, g, lane);
+            ph_fold_verify4(stp, a.va, rq, ctp, zq, nrr, tok, valid, g, lane);
           };
           if (a.split) {  // 8 rows in this chunk
 #pragma unroll
@@ -970,7 +981,10 @@ Launch plan_launch(int R) {
   L.tmem_cols = cols;
   const size_t stage = A_STAGE + (size_t)L.ntile * BK * 2;
   const size_t fixed = 1024 + 64;
-  L.stages = (int)std::max<size_t>(2, std::min<size_t>(8, (kSmemBudget - fixed) / stage));
+  // A wide activation tile (a stage of more than 24 KB) would leave two CTAs
+  // with 2-3 stages each; one CTA with the whole shared memory keeps 4+.
+  const size_t budget = stage > 24 * 1024 ? kSmemBudgetWide : kSmemBudget;
+  L.stages = (int)std::max<size_t>(2, std::min<size_t>(8, (budget - fixed) / stage));
   L.smem = fixed + L.stages * stage + 16 * L.stages + 16;
   return L;
 }
@@ -1003,11 +1017,11 @@ bool launch(TcGemm* t, const CUtensorMap* a0, const CUtensorMap* a1, const CUten
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kSmemBudget + 4096);
+                         kSmemBudgetWide + 4096);
     attr = true;
   }
   dim3 grid(grid_x, L.n_tiles, S);
-  tc_gemm_kernel<MODE><<<grid, 128, L.smem, st>>>(*a0, *a1, *a2, mb, args);
+  launch_pdl(tc_gemm_kernel<MODE>, dim3(grid), dim3(128), L.smem, st, *a0, *a1, *a2, mb, args);
   return true;
 }
 
@@ -1023,7 +1037,7 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
   uint32_t acc = 32;
   while (acc < (uint32_t)ntile) acc <<= 1;
   const int sw = MODE == 1 ? 2 + 2 * args.hp.k : 6;
-  const size_t state = (size_t)4 * R * sw * 4;
+  const size_t state = (size_t)4 * R * sw * 4 + (MODE == 2 ? (size_t)R * args.va.kmax * 4 : 0);
   const size_t stage = A_STAGE + (size_t)ntile * BK * 2;
   // CTAs per SM: as configured, but their double-buffered accumulators must
   // share the SM's 512 TMEM columns (an allocation beyond them would wait)
@@ -1057,7 +1071,7 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
                          232448);
     attr = true;
   }
-  tc_head_kernel<MODE><<<grid, 192, smem, st>>>(*wmap, mb, args);
+  launch_pdl(tc_head_kernel<MODE>, dim3(grid), dim3(192), smem, st, *wmap, mb, args);
   n_parts = grid;  // one partial per CTA
   return true;
 }

@@ -70,6 +70,7 @@ struct AttnArgs {
 template <typename T> void launch_tree_attention(const AttnArgs& a, cudaStream_t st);
 // query groups per (request, KV head) of the prefix-split kernel
 int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma);
+int attention_kw(int rows_per_req, int Hq, int Hkv);
 bool attention_uses_mma(int elem_bytes, int dh);
 
 // ----------------------------------------------------------------------------- lmhead.cu
@@ -117,8 +118,13 @@ struct PoolDev {
   float *score, *logq;
   int n;  // pool_n
 };
-void launch_plan_root(int B, int n_new, const int* tokens_new, const int* seq_lens, int n_slots,
-                      const RowPlan& rp, int* root_tok, int* root_pos, int* n_prefix, cudaStream_t st);
+// pass 0 rows: n_new rows per request, or the ragged rows given by cu_new [B+1]
+void launch_plan_root(int B, int n_new, const int* cu_new, int total, int max_new,
+                      const int* tokens_new, const int* seq_lens, int n_slots, const RowPlan& rp,
+                      int* root_tok, int* root_pos, int* n_prefix, int* flags, cudaStream_t st);
+// the next round's new rows from a verification (B <= 1024)
+void launch_next_rows(int B, int D, const int* accept_len, const int* out_tokens, int* cu_new,
+                      int* tokens_new, int* flags, cudaStream_t st);
 void launch_plan_prefill(int rows, int r0, int B, const int* cu_rows, const int* tokens,
                          const int* seq_lens, const RowPlan& rp, cudaStream_t st);
 void launch_expand(int B, int t, int k, int D, const int* top_tok, const float* top_logq,

@@ -66,6 +66,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) lm_head_simt_kernel(const T* __restrict__ H,
                                                            const T* __restrict__ W, int R, int V,
                                                            int d, HeadParts hp) {
+  pdl_begin();
   __shared__ float Lt[TB][TB + 1];
   __shared__ float Hs[TK][TB + 4];
   __shared__ float Ws[TK][TB + 4];
@@ -107,7 +108,7 @@ void launch_lm_head_simt(const void* H, const void* W, int R, int V, int d, cons
                          cudaStream_t st) {
   if (R <= 0) return;
   dim3 grid(lm_head_simt_parts(V), (R + TB - 1) / TB);
-  lm_head_simt_kernel<T><<<grid, 256, 0, st>>>((const T*)H, (const T*)W, R, V, d, hp);
+  launch_pdl(lm_head_simt_kernel<T>, dim3(grid), dim3(256), 0, st, (const T*)H, (const T*)W, R, V, d, hp);
 }
 
 // ----------------------------------------------------------------------------- merge: LSE + top-k
@@ -144,6 +145,7 @@ __device__ __forceinline__ void warp_lse(float& m, float& s) {
 template <int K>
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(HeadParts hp, int* tok, float* logq,
                                                                    float* lse_out) {
+  pdl_begin();
   __shared__ float red_m[32], red_s[32];
   __shared__ int red_i[32];
   __shared__ float win_v;
@@ -249,7 +251,7 @@ void launch_topk_merge(const HeadParts& hp, int* tok, float* logq, float* lse, i
   switch (hp.k) {
 #define E3_MERGE_CASE(K) \
   case K:                \
-    topk_merge_kernel<K><<<hp.R, kMergeThreads, 0, st>>>(hp, tok, logq, lse); \
+    launch_pdl(topk_merge_kernel<K>, dim3(hp.R), dim3(kMergeThreads), 0, st, hp, tok, logq, lse); \
     break;
     E3_MERGE_CASE(1) E3_MERGE_CASE(2) E3_MERGE_CASE(3) E3_MERGE_CASE(4) E3_MERGE_CASE(5)
     E3_MERGE_CASE(6) E3_MERGE_CASE(7) E3_MERGE_CASE(8) E3_MERGE_CASE(9) E3_MERGE_CASE(10)
@@ -266,6 +268,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) verify_head_simt_kernel(const T* __restrict__ H,
                                                                const T* __restrict__ W,
                                                                VerifyHeadArgs a) {
+  pdl_begin();
   __shared__ float Lt[TB][TB + 1];
   __shared__ float Hs[TK][TB + 4];
   __shared__ float Ws[TK][TB + 4];
@@ -328,13 +331,14 @@ template <typename T>
 void launch_verify_head_simt(const void* H, const void* W, const VerifyHeadArgs& a, cudaStream_t st) {
   if (a.R <= 0) return;
   dim3 grid(verify_head_simt_parts(a.V), (a.R + TB - 1) / TB);
-  verify_head_simt_kernel<T><<<grid, 256, 0, st>>>((const T*)H, (const T*)W, a);
+  launch_pdl(verify_head_simt_kernel<T>, dim3(grid), dim3(256), 0, st, (const T*)H, (const T*)W, a);
 }
 
 // One block per tree node: best target logit (ties: lowest token), log-sum-exp
 // of z/T and the Gumbel-argmax over the partials of every vocabulary tile.
 __global__ void __launch_bounds__(256) verify_merge_kernel(VerifyHeadArgs a, float* z_max, int* z_arg,
                                                            float* lse, int* g_arg, float* g_max) {
+  pdl_begin();
   __shared__ float sh_zb[32], sh_m[32], sh_s[32], sh_gb[32];
   __shared__ int sh_zi[32], sh_gi[32];
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(VerifyHeadArgs a, flo
 void launch_verify_merge(const VerifyHeadArgs& a, float* z_max, int* z_arg, float* lse, int* g_arg,
                          float* g_max, cudaStream_t st) {
   if (a.R <= 0) return;
-  verify_merge_kernel<<<a.R, 256, 0, st>>>(a, z_max, z_arg, lse, g_arg, g_max);
+  launch_pdl(verify_merge_kernel, dim3(a.R), dim3(256), 0, st, a, z_max, z_arg, lse, g_arg, g_max);
 }
 
 template void launch_lm_head_simt<float>(const void*, const void*, int, int, int, const HeadParts&,

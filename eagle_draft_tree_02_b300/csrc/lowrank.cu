@@ -49,6 +49,7 @@ __device__ __forceinline__ float act_at(const T* base, int r, int K, int j, bool
 template <typename T>
 __global__ void reduce_store_kernel(int R, int N, int S, const float* __restrict__ part, T* out,
                                     bool split) {
+  pdl_begin();
   const size_t n = (size_t)R * N;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -65,7 +66,7 @@ void launch_reduce_store(int R, int N, int S, const float* part, void* out, bool
   const size_t n = (size_t)R * N;
   if (!n) return;
   int blocks = (int)std::min<size_t>((n + 255) / 256, 148 * 8);
-  reduce_store_kernel<T><<<blocks, 256, 0, st>>>(R, N, S, part, (T*)out, split);
+  launch_pdl(reduce_store_kernel<T>, dim3(blocks), dim3(256), 0, st, R, N, S, part, (T*)out, split);
 }
 
 // ----------------------------------------------------------------------------- fp32 low-rank pass
@@ -75,6 +76,7 @@ int lowrank_simt_groups(int V) { return (std::min(V, kLrSampleTokens) + 31) / 32
 
 template <typename T>
 __global__ void lowrank_simt_kernel(int mode, LowRankArgs a) {
+  pdl_begin();
   const int g = blockIdx.x, r = blockIdx.y, lane = threadIdx.x;
   const int x = g * 32 + lane;
   const bool valid = x < a.V;
@@ -109,11 +111,12 @@ template <typename T>
 void launch_lowrank_simt(int mode, const LowRankArgs& a, cudaStream_t st) {
   const int groups = mode == 0 ? lowrank_simt_groups(a.V) : (a.V + 31) / 32;
   dim3 grid(groups, a.R);
-  lowrank_simt_kernel<T><<<grid, 32, 0, st>>>(mode, a);
+  launch_pdl(lowrank_simt_kernel<T>, dim3(grid), dim3(32), 0, st, mode, a);
 }
 
 // ----------------------------------------------------------------------------- threshold
 __global__ void __launch_bounds__(512) lowrank_threshold_kernel(LowRankArgs a) {
+  pdl_begin();
   __shared__ float sv[1024];
   __shared__ float result;
   const int r = blockIdx.x, tid = threadIdx.x, G = a.n_groups;
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(512) lowrank_threshold_kernel(LowRankArgs a) {
 }
 
 void launch_lowrank_threshold(const LowRankArgs& a, cudaStream_t st) {
-  lowrank_threshold_kernel<<<a.R, 512, 0, st>>>(a);
+  launch_pdl(lowrank_threshold_kernel, dim3(a.R), dim3(512), 0, st, a);
 }
 
 // ----------------------------------------------------------------------------- select + rescore
@@ -218,6 +221,7 @@ __device__ void exact_topc(const LowRankArgs& a, int r, const float* t_s, unsign
 
 template <typename T>
 __global__ void __launch_bounds__(kSelThreads) lowrank_select_kernel(LowRankArgs a) {
+  pdl_begin();
   extern __shared__ unsigned long long sel_smem[];
   unsigned long long* key = sel_smem;                 // [kLrCap]
   float* h_s = reinterpret_cast<float*>(key + kLrCap);  // [d]
@@ -309,7 +313,7 @@ void launch_lowrank_select(const LowRankArgs& a, cudaStream_t st) {
                          200 * 1024);
     attr[ti] = true;
   }
-  lowrank_select_kernel<T><<<a.R, kSelThreads, smem, st>>>(a);
+  launch_pdl(lowrank_select_kernel<T>, dim3(a.R), dim3(kSelThreads), smem, st, a);
 }
 
 template void launch_reduce_store<float>(int, int, int, const float*, void*, bool, cudaStream_t);

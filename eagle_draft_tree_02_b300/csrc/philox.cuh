@@ -72,18 +72,20 @@ __device__ __forceinline__ float verify_uniform(unsigned long long seed, unsigne
 
 // Gumbel noise from one output word.  -log U' is evaluated from an exactly
 // representable operand: U' itself when U' < 1/2, else 1 - U' through log1p,
-// so U' never rounds to 1.
+// so U' never rounds to 1.  The outer log uses the fast intrinsic: its error
+// (about 1e-6 relative) can only move a Gumbel argmax whose two best scores
+// are that close, a near-tie that the parity rule counts.
 __device__ __forceinline__ float gumbel_from_word(uint64_t w) {
   const uint32_t m = (uint32_t)(w >> 40);
   float e;
   if (m < (1u << 23)) {
     float u = ((float)m + 0.5f) * 5.9604644775390625e-08f;
-    e = -logf(u);
+    e = -__logf(u);
   } else {
     float t = ((float)((1u << 24) - m) - 0.5f) * 5.9604644775390625e-08f;  // 1 - U'
     e = -log1pf(-t);
   }
-  return -logf(e);
+  return -__logf(e);
 }
 
 // the Philox block that holds the Gumbel words of tokens 4 blk .. 4 blk + 3

@@ -20,13 +20,26 @@
 namespace e3 {
 
 // ----------------------------------------------------------------------------- pass 0 plan
-__global__ void plan_root_kernel(int B, int n_new, const int* tokens_new, const int* seq_lens,
-                                 int n_slots, RowPlan rp, int* root_tok, int* root_pos,
-                                 int* n_prefix) {
+// Request b's new rows are rows r0 .. r1-1 of the round's packed rows: r0 =
+// cu_new[b], r1 = cu_new[b+1] (or n_new rows each when cu_new is NULL); the
+// last one is the tree's root.  A count outside [1, max_new] or past `total`
+// raises FLAG_ROWS_RANGE and is clamped so that every index stays in range.
+__global__ void plan_root_kernel(int B, int n_new, const int* cu_new, int total, int max_new,
+                                 const int* tokens_new, const int* seq_lens, int n_slots,
+                                 RowPlan rp, int* root_tok, int* root_pos, int* n_prefix,
+                                 int* flags) {
+  pdl_begin();
   int b = blockIdx.x;
   int L = seq_lens[b];
-  for (int j = threadIdx.x; j < n_new; j += blockDim.x) {
-    int r = b * n_new + j;
+  int r0 = cu_new ? cu_new[b] : b * n_new;
+  int r1 = cu_new ? cu_new[b + 1] : r0 + n_new;
+  if (r0 < 0 || r1 > total || r1 - r0 < 1 || r1 - r0 > max_new) {
+    if (threadIdx.x == 0) raise_flag(flags, FLAG_ROWS_RANGE);
+    r0 = min(max(r0, 0), total - 1);
+    r1 = min(max(r1, r0 + 1), min(total, r0 + max_new));
+  }
+  for (int j = threadIdx.x; j < r1 - r0; j += blockDim.x) {
+    int r = r0 + j;
     rp.kv_b[r] = b;
     rp.kv_tok[r] = tokens_new[r];
     rp.kv_hid[r] = r;
@@ -34,29 +47,66 @@ __global__ void plan_root_kernel(int B, int n_new, const int* tokens_new, const 
     rp.kv_dst[r] = -1;
   }
   if (threadIdx.x == 0) {
-    int rr = b * n_new + n_new - 1;
+    int rr = r1 - 1;
     rp.t_q[b] = rr;
     rp.t_b[b] = b;
     rp.t_hid[b] = rr;
     rp.t_sdst[b] = b * (1 + n_slots);
     rp.t_out[b] = b;
     root_tok[b] = tokens_new[rr];
-    root_pos[b] = L + n_new - 1;
-    n_prefix[b] = L + n_new;
+    root_pos[b] = L + (r1 - r0) - 1;
+    n_prefix[b] = L + (r1 - r0);
   }
   for (int w = threadIdx.x; w < rp.mask_words; w += blockDim.x) rp.t_mask[(size_t)b * rp.mask_words + w] = 0u;
 }
 
-void launch_plan_root(int B, int n_new, const int* tokens_new, const int* seq_lens, int n_slots,
-                      const RowPlan& rp, int* root_tok, int* root_pos, int* n_prefix,
-                      cudaStream_t st) {
-  plan_root_kernel<<<B, 64, 0, st>>>(B, n_new, tokens_new, seq_lens, n_slots, rp, root_tok,
-                                     root_pos, n_prefix);
+void launch_plan_root(int B, int n_new, const int* cu_new, int total, int max_new,
+                      const int* tokens_new, const int* seq_lens, int n_slots, const RowPlan& rp,
+                      int* root_tok, int* root_pos, int* n_prefix, int* flags, cudaStream_t st) {
+  launch_pdl(plan_root_kernel, dim3(B), dim3(64), 0, st, B, n_new, cu_new, total, max_new,
+             tokens_new, seq_lens, n_slots, rp, root_tok, root_pos, n_prefix, flags);
+}
+
+// ----------------------------------------------------------------------------- next round's rows
+// From a verification: request b's next rows are its accepted tokens and the
+// bonus token, out_tokens[b][0 .. accept_len[b]], packed by request with
+// offsets cu_new.  One block; the prefix sum over requests is serial.
+__global__ void next_rows_kernel(int B, int D, const int* accept_len, const int* out_tokens,
+                                 int* cu_new, int* tokens_new, int* flags) {
+  pdl_begin();
+  __shared__ int off[1025];
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    off[0] = 0;
+    for (int b = 0; b < B; ++b) {
+      int a = accept_len[b];
+      if (a < 0 || a > D) {
+        raise_flag(flags, FLAG_ROWS_RANGE);
+        a = a < 0 ? 0 : D;
+      }
+      acc += a + 1;
+      off[b + 1] = acc;
+    }
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b <= B; b += blockDim.x) cu_new[b] = off[b];
+  for (int b = 0; b < B; ++b) {
+    const int n = off[b + 1] - off[b];
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+      tokens_new[off[b] + i] = out_tokens[(size_t)b * (D + 1) + i];
+  }
+}
+
+void launch_next_rows(int B, int D, const int* accept_len, const int* out_tokens, int* cu_new,
+                      int* tokens_new, int* flags, cudaStream_t st) {
+  launch_pdl(next_rows_kernel, dim3(1), dim3(256), 0, st, B, D, accept_len, out_tokens, cu_new,
+             tokens_new, flags);
 }
 
 // ----------------------------------------------------------------------------- prefill plan
 __global__ void plan_prefill_kernel(int rows, int r0, int B, const int* cu_rows, const int* tokens,
                                     const int* seq_lens, RowPlan rp) {
+  pdl_begin();
   int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= rows) return;
   int r = r0 + i;
@@ -75,7 +125,7 @@ __global__ void plan_prefill_kernel(int rows, int r0, int B, const int* cu_rows,
 void launch_plan_prefill(int rows, int r0, int B, const int* cu_rows, const int* tokens,
                          const int* seq_lens, const RowPlan& rp, cudaStream_t st) {
   if (rows <= 0) return;
-  plan_prefill_kernel<<<(rows + 255) / 256, 256, 0, st>>>(rows, r0, B, cu_rows, tokens, seq_lens, rp);
+  launch_pdl(plan_prefill_kernel, dim3((rows + 255) / 256), dim3(256), 0, st, rows, r0, B, cu_rows, tokens, seq_lens, rp);
 }
 
 // ----------------------------------------------------------------------------- expansion (per pass)
@@ -87,6 +137,7 @@ __global__ void expand_kernel(int B, int t, int k, int D, const int* __restrict_
                               const float* __restrict__ top_logq, PoolDev pool, int* frontier,
                               uint32_t* slot_mask, int slot_words, const int* root_pos,
                               int n_slots, RowPlan rp) {
+  pdl_begin();
   __shared__ float sc[256];
   __shared__ int nf[16];
   int b = blockIdx.x, tid = threadIdx.x;
@@ -163,7 +214,7 @@ __global__ void expand_kernel(int B, int t, int k, int D, const int* __restrict_
 void launch_expand(int B, int t, int k, int D, const int* top_tok, const float* top_logq,
                    const PoolDev& pool, int* frontier, uint32_t* slot_mask, int slot_words,
                    const int* root_pos, int n_slots, const RowPlan& rp, cudaStream_t st) {
-  expand_kernel<<<B, 256, 0, st>>>(B, t, k, D, top_tok, top_logq, pool, frontier, slot_mask,
+  launch_pdl(expand_kernel, dim3(B), dim3(256), 0, st, B, t, k, D, top_tok, top_logq, pool, frontier, slot_mask,
                                    slot_words, root_pos, n_slots, rp);
 }
 
@@ -177,6 +228,7 @@ __global__ void build_tree_kernel(int pool_n, int M, const int* __restrict__ tok
                                   const int* root_pos, int* t_tok, int* t_parent, int* t_depth,
                                   int* t_pos, int* t_pidx, float* t_score, uint32_t* t_mask,
                                   int* flags) {
+  pdl_begin();
   extern __shared__ int smi[];
   float* ssc = (float*)smi;             // [pool_n]
   int* sdep = smi + pool_n;             // [pool_n]
@@ -268,7 +320,7 @@ void launch_build_tree(int B, int pool_n, int M, const int* tok, const int* pare
     cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
     attr = true;
   }
-  build_tree_kernel<<<B, 512, smem, st>>>(pool_n, M, tok, parent, score, depth, root_tok, root_pos,
+  launch_pdl(build_tree_kernel, dim3(B), dim3(512), smem, st, pool_n, M, tok, parent, score, depth, root_tok, root_pos,
                                           t_tok, t_parent, t_depth, t_pos, t_pidx, t_score, t_mask,
                                           flags);
 }
@@ -283,6 +335,7 @@ __global__ void plan_verify_kernel(int M, int kmax, const int* t_tok, const int*
                                    const int* pool_fwd, int pool_n, int n_slots, RowPlan rp,
                                    int* n_prefix, int* child_tok, int* child_node, int* n_child,
                                    int* flags) {
+  pdl_begin();
   int b = blockIdx.x, tid = threadIdx.x;
   const int M1 = M + 1, W = (M1 + 31) / 32;
   const size_t tb = (size_t)b * M1;
@@ -338,7 +391,7 @@ void launch_plan_verify(int B, int M, int kmax, const int* t_tok, const int* t_p
                         const int* pool_fwd, int pool_n, int n_slots, const RowPlan& rp,
                         int* n_prefix, int* child_tok, int* child_node, int* n_child, int* flags,
                         cudaStream_t st) {
-  plan_verify_kernel<<<B, 128, 0, st>>>(M, kmax, t_tok, t_parent, t_pos, t_pidx, t_mask, pool_fwd,
+  launch_pdl(plan_verify_kernel, dim3(B), dim3(128), 0, st, M, kmax, t_tok, t_parent, t_pos, t_pidx, t_mask, pool_fwd,
                                         pool_n, n_slots, rp, n_prefix, child_tok, child_node,
                                         n_child, flags);
 }
@@ -346,6 +399,7 @@ void launch_plan_verify(int B, int M, int kmax, const int* t_tok, const int* t_p
 // ----------------------------------------------------------------------------- small copies
 __global__ void copy_rows_kernel(int row_bytes, const char* src, size_t src_step, bool src_split,
                                  char* dst, size_t dst_step, bool dst_split) {
+  pdl_begin();
   const int b = blockIdx.x;
   const char* sr = src + b * src_step;
   char* dr = dst + b * dst_step;
@@ -359,7 +413,7 @@ void launch_copy_rows(int B, int d, int elem_bytes, const void* src, int src_str
                       bool src_split, void* dst, int dst_stride_rows, bool dst_split,
                       cudaStream_t st) {
   const size_t row = (size_t)d * elem_bytes;
-  copy_rows_kernel<<<B, 256, 0, st>>>((int)row, (const char*)src,
+  launch_pdl(copy_rows_kernel, dim3(B), dim3(256), 0, st, (int)row, (const char*)src,
                                       row * src_stride_rows * (src_split ? 2 : 1), src_split,
                                       (char*)dst, row * dst_stride_rows * (dst_split ? 2 : 1),
                                       dst_split);
@@ -367,6 +421,7 @@ void launch_copy_rows(int B, int d, int elem_bytes, const void* src, int src_str
 
 __global__ void copy_pool_kernel(int n, PoolDev p, int* tok, int* parent, int* depth, int* fwd,
                                  float* score, float* logq) {
+  pdl_begin();
   int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   if (tok) tok[i] = p.tok[i];
@@ -380,7 +435,7 @@ __global__ void copy_pool_kernel(int n, PoolDev p, int* tok, int* parent, int* d
 void launch_copy_pool(int B, const PoolDev& pool, int* tok, int* parent, int* depth, int* fwd,
                       float* score, float* logq, cudaStream_t st) {
   int n = B * pool.n;
-  copy_pool_kernel<<<(n + 255) / 256, 256, 0, st>>>(n, pool, tok, parent, depth, fwd, score, logq);
+  launch_pdl(copy_pool_kernel, dim3((n + 255) / 256), dim3(256), 0, st, n, pool, tok, parent, depth, fwd, score, logq);
 }
 
 }  // namespace e3

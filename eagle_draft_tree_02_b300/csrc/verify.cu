@@ -22,6 +22,7 @@
 namespace e3 {
 
 __global__ void walk_kernel(WalkArgs a) {
+  pdl_begin();
   int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= a.B) return;
   const unsigned long long rid = a.round_ptr ? *a.round_ptr : a.round_id;
@@ -63,13 +64,13 @@ __global__ void walk_kernel(WalkArgs a) {
 }
 
 void launch_walk(const WalkArgs& a, cudaStream_t st) {
-  walk_kernel<<<(a.B + 63) / 64, 64, 0, st>>>(a);
+  launch_pdl(walk_kernel, dim3((a.B + 63) / 64), dim3(64), 0, st, a);
 }
 
-__global__ void set_u64_kernel(unsigned long long* p, unsigned long long v) { *p = v; }
+__global__ void set_u64_kernel(unsigned long long* p, unsigned long long v) { pdl_begin(); *p = v; }
 
 void launch_set_u64(unsigned long long* p, unsigned long long v, cudaStream_t st) {
-  set_u64_kernel<<<1, 1, 0, st>>>(p, v);
+  launch_pdl(set_u64_kernel, dim3(1), dim3(1), 0, st, p, v);
 }
 
 }  // namespace e3

@@ -65,14 +65,17 @@ _sig = {
     "eagle3_prefill": (C.c_int, [_P, C.c_int, C.c_int, _P, _P, _P, C.POINTER(eagle3_kv), _P]),
     "eagle3_draft_round": (C.c_int, [_P, C.c_int, C.c_int, _P, _P, C.POINTER(eagle3_kv),
                                      C.POINTER(eagle3_tree), C.POINTER(eagle3_pool), _P]),
+    "eagle3_draft_round_ragged": (C.c_int, [_P, C.c_int, C.c_int, _P, _P, _P, C.POINTER(eagle3_kv),
+                                            C.POINTER(eagle3_tree), C.POINTER(eagle3_pool), _P]),
+    "eagle3_next_rows": (C.c_int, [_P, C.c_int, _P, _P, _P, _P, _P]),
     "eagle3_build_tree": (C.c_int, [_P, C.c_int, C.c_int, _P, _P, _P, _P, _P, _P,
                                     C.POINTER(eagle3_tree), _P]),
     "eagle3_verify": (C.c_int, [_P, C.c_int, C.POINTER(eagle3_tree), C.POINTER(eagle3_kv), C.c_int,
                                 C.c_float, C.c_ulonglong, C.c_ulonglong, _P, _P, _P,
                                 C.POINTER(eagle3_verify_stats), _P]),
     "eagle3_graph_capture": (C.c_int, [_P, C.c_int, C.c_int, _P, _P, C.POINTER(eagle3_kv),
-                                       C.POINTER(eagle3_tree), C.c_int, C.c_float, C.c_ulonglong,
-                                       _P, _P, _P, _P]),
+                                       C.POINTER(eagle3_tree), C.c_int, C.c_int, C.c_float,
+                                       C.c_ulonglong, _P, _P, _P, _P]),
     "eagle3_graph_launch": (C.c_int, [_P, C.c_ulonglong, _P]),
     "eagle3_lm_head_topk": (C.c_int, [_P, C.c_int, _P, _P, _P, _P, _P]),
     "eagle3_lm_head_topk_noalloc": (C.c_int, [C.c_int, C.c_int, C.c_int, C.c_int, _P, C.c_int, _P,
@@ -127,6 +130,16 @@ def eagle3_draft_round(ctx, B, n_new, feats_new, tokens_new, kv: eagle3_kv, tree
                                   _ref(pool), stream)
 
 
+def eagle3_draft_round_ragged(ctx, B, total_new, cu_new, feats_new, tokens_new, kv: eagle3_kv,
+                              tree: eagle3_tree, pool: eagle3_pool | None = None, stream=0) -> int:
+    return lib.eagle3_draft_round_ragged(ctx, B, total_new, cu_new, feats_new, tokens_new, C.byref(kv),
+                                         C.byref(tree), _ref(pool), stream)
+
+
+def eagle3_next_rows(ctx, B, accept_len, out_tokens, cu_new, tokens_new, stream=0) -> int:
+    return lib.eagle3_next_rows(ctx, B, accept_len, out_tokens, cu_new, tokens_new, stream)
+
+
 def eagle3_build_tree(ctx, B, pool_n, pool_tok, pool_parent, pool_score, pool_depth, root_tok,
                       root_pos, tree: eagle3_tree, stream=0) -> int:
     return lib.eagle3_build_tree(ctx, B, pool_n, pool_tok, pool_parent, pool_score, pool_depth,
@@ -140,10 +153,12 @@ def eagle3_verify(ctx, B, tree: eagle3_tree, kv: eagle3_kv, mode, temperature, s
                              accept_len, path, out_tokens, _ref(stats), stream)
 
 
-def eagle3_graph_capture(ctx, B, n_new, feats_new, tokens_new, kv: eagle3_kv, tree: eagle3_tree, mode,
-                         temperature, seed, accept_len, path, out_tokens, stream) -> int:
+def eagle3_graph_capture(ctx, B, n_new, feats_new, tokens_new, kv: eagle3_kv, tree: eagle3_tree,
+                         with_verify, mode, temperature, seed, accept_len, path, out_tokens,
+                         stream) -> int:
     return lib.eagle3_graph_capture(ctx, B, n_new, feats_new, tokens_new, C.byref(kv), C.byref(tree),
-                                    mode, temperature, seed, accept_len, path, out_tokens, stream)
+                                    with_verify, mode, temperature, seed, accept_len, path,
+                                    out_tokens, stream)
 
 
 def eagle3_graph_launch(ctx, round_id, stream) -> int:

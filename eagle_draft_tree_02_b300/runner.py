@@ -71,7 +71,8 @@ class PoolOut:
 class Engine:
     """One context plus the device copies of one round's inputs and its KV cache."""
 
-    def __init__(self, inputs: RoundInputs, device="cuda", max_new: int = 1, with_target=True):
+    def __init__(self, inputs: RoundInputs, device="cuda", max_new: int = 1, with_target=True,
+                 max_prefix_extra: int = 0):
         self.inp = inputs
         cfg = self.cfg = inputs.cfg
         self.device = torch.device(device)
@@ -79,7 +80,8 @@ class Engine:
         self.B = cfg.batch
         self.w = {k: to_device(v, dev) for k, v in inputs.w.items()
                   if with_target or k != "w_target"}
-        self.max_prefix = int(inputs.prefix_lens.max())
+        # contiguous cache: room for the prefix plus rows later rounds commit
+        self.max_prefix = int(inputs.prefix_lens.max()) + max_prefix_extra
         if cfg.page_size:
             self.max_prefix = inputs.page_table.shape[1] * cfg.page_size
         ws = E.eagle3_weights()
@@ -181,8 +183,8 @@ class Engine:
         E.check(self.ctx, s)
         return self.accept_len, self.path, self.out_tokens
 
-    def capture(self, temperature=0.0, seed=0, stream=None):
-        """Capture one step (draft round + verify) into the context's CUDA graph.
+    def capture(self, temperature=0.0, seed=0, stream=None, with_verify=True):
+        """Capture one step (draft round, + verify) into the context's CUDA graph.
 
         Needs an eager draft round first and a non-default stream; replays read
         the same input and output buffers (self.feats_new, self.tokens_new,
@@ -190,7 +192,8 @@ class Engine:
         mode = 0 if temperature == 0 else 1
         st = stream if stream is not None else self.stream()
         s = E.eagle3_graph_capture(self.ctx, self.B, 1, self.feats_new.data_ptr(),
-                                   self.tokens_new.data_ptr(), self.kv, self._tree_s, mode,
+                                   self.tokens_new.data_ptr(), self.kv, self._tree_s,
+                                   1 if with_verify else 0, mode,
                                    float(temperature or 1.0), seed, self.accept_len.data_ptr(),
                                    self.path.data_ptr(), self.out_tokens.data_ptr(), st)
         E.check(self.ctx, s)

@@ -172,6 +172,30 @@ eagle3_status eagle3_draft_round(eagle3_ctx* ctx, int B, int n_new, const void* 
                                  const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
                                  eagle3_pool* pool_out, eagle3_stream stream);
 
+/* The same round with a different number of new rows per request, as in
+ * steady-state decoding: request b's new rows are rows cu_new[b] ..
+ * cu_new[b+1] - 1 of feats_new [total_new, 3d] / tokens_new [total_new]
+ * (device), at positions seq_lens[b] onward; the last is the request's root.
+ * cu_new [B+1] (int32, device) with cu_new[0] = 0, cu_new[B] = total_new and
+ * 1 <= cu_new[b+1] - cu_new[b] <= max_new.  A count outside that range is
+ * clamped and raises a device flag (EAGLE3_ERR_DEVICE_ASSERT from eagle3_check). */
+eagle3_status eagle3_draft_round_ragged(eagle3_ctx* ctx, int B, int total_new, const int* cu_new,
+                                        const void* feats_new, const int* tokens_new,
+                                        const eagle3_kv* kv, eagle3_tree* out, eagle3_pool* pool_out,
+                                        eagle3_stream stream);
+
+/* The token rows of the next round from a verification, without a host round
+ * trip ("EAGLE-3 精读" §2: the drafter continues from the target's accepted
+ * sequence).  Request b contributes accept_len[b] + 1 rows: its accepted
+ * tokens then the bonus token, out_tokens[b][0 .. accept_len[b]] of
+ * eagle3_verify.  Writes cu_new [B+1] and tokens_new [sum of rows] (int32,
+ * device) for eagle3_draft_round_ragged.  The caller supplies the rows'
+ * target features and, once the previous round's rows are committed,
+ * advances seq_lens by that round's row counts.  B <= 1024; max_new should be
+ * at least D + 1. */
+eagle3_status eagle3_next_rows(eagle3_ctx* ctx, int B, const int* accept_len, const int* out_tokens,
+                               int* cu_new, int* tokens_new, eagle3_stream stream);
+
 /* Tree builder alone (for tests and outside drafters): keeps the top-M of a
  * pool by (score desc, depth asc, pool index asc) and writes the canonical
  * tree.  pool arrays [B, pool_n] (device; parent = pool index or -1), root_tok
@@ -197,8 +221,9 @@ eagle3_status eagle3_verify(eagle3_ctx* ctx, int B, const eagle3_tree* tree, con
                             unsigned long long round_id, int* accept_len, int* path,
                             int* out_tokens, eagle3_verify_stats* stats, eagle3_stream stream);
 
-/* Record one whole step -- eagle3_draft_round followed by eagle3_verify, with
- * the same arguments as those two calls (no pool or stats outputs) -- into a
+/* Record one whole step -- eagle3_draft_round followed, if with_verify, by
+ * eagle3_verify, with the same arguments as those two calls (no pool or stats
+ * outputs; the verify arguments are ignored without with_verify) -- into a
  * CUDA graph kept by the context, replacing any earlier one.  The step's
  * pointers (new rows, KV descriptor, tree and verification outputs) are fixed
  * in the graph: refill the same buffers before each replay.  The round id is
@@ -207,9 +232,9 @@ eagle3_status eagle3_verify(eagle3_ctx* ctx, int B, const eagle3_tree* tree, con
  * other than the legacy default stream.  Nothing runs during the capture. */
 eagle3_status eagle3_graph_capture(eagle3_ctx* ctx, int B, int n_new, const void* feats_new,
                                    const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
-                                   int mode, float temperature, unsigned long long seed,
-                                   int* accept_len, int* path, int* out_tokens,
-                                   eagle3_stream stream);
+                                   int with_verify, int mode, float temperature,
+                                   unsigned long long seed, int* accept_len, int* path,
+                                   int* out_tokens, eagle3_stream stream);
 
 /* Replay the captured step on `stream` with the given round id (the Philox
  * counter of the sampling draws).  EAGLE3_ERR_STATE if nothing was captured.

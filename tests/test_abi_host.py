@@ -90,4 +90,4 @@ def test_noalloc_head_rejects_bad_requests_before_launch(E):
 def test_graph_calls_need_a_context(E):
     kv, tree = E.eagle3_kv(), E.eagle3_tree()
     assert E.eagle3_graph_launch(0, 0, 0) == E.ERR_INVALID_ARG
-    assert E.eagle3_graph_capture(0, 1, 1, 1, 1, kv, tree, 0, 1.0, 0, 1, 1, 1, 0) == E.ERR_INVALID_ARG
+    assert E.eagle3_graph_capture(0, 1, 1, 1, 1, kv, tree, 1, 0, 1.0, 0, 1, 1, 1, 0) == E.ERR_INVALID_ARG
