@@ -40,6 +40,9 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefix-scale", type=float, default=1.0,
+                    help="scale the prefix lengths (a small case of the same kernels for profiling; "
+                         "the bench line is only valid at 1.0)")
     return ap.parse_args()
 
 
@@ -180,6 +183,12 @@ def main():
     args = parse()
     from eagle_draft_tree_02_b300.configs import by_name
     cfg = by_name(args.config)
+    if args.prefix_scale != 1.0:
+        sc = args.prefix_scale
+        rng = cfg.prefix_range
+        cfg = cfg.scaled(prefix=max(2, int(cfg.prefix * sc)),
+                         prefix_range=None if rng is None else (max(2, int(rng[0] * sc)),
+                                                                max(2, int(rng[1] * sc))))
     if args.impl == "reference":
         run_reference(args, cfg)
         return
@@ -330,6 +339,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "data": "synthetic (seeded weights, features, tokens; no trained model)",
         "config": {"workload": cfg.name, "batch": cfg.batch, "prefix": cfg.prefix, "d": cfg.d,
+                   "prefix_scale": args.prefix_scale,
                    "vocab": cfg.vocab, "depth": cfg.depth, "topk": cfg.topk, "n_verify": cfg.n_verify,
                    "verify": f"T={T}" if T else "greedy",
                    "l2": f"inputs larger than L2: {rb['step'] / 1e9:.2f} GB of weights/KV streamed per step"},

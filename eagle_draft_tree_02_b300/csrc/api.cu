@@ -302,7 +302,8 @@ void draft_head_lowrank(eagle3_ctx* c, const void* H, int R, bool split, int* to
   la.R = R;
   la.H = H;
   la.h_split = split;
-  la.t_split = use_split(c, R);
+  // t only ranks the candidates (their log q comes from the exact head): one bf16
+  la.t_split = false;
   la.tok = tok;
   la.logq = logq;
   la.lse = lse;

@@ -972,7 +972,7 @@ struct Launch {
   size_t smem;
 };
 
-Launch plan_launch(int R) {
+Launch plan_launch(int R, int n_kb) {
   Launch L;
   L.n_tiles = cdiv(std::max(R, 1), 256);
   L.ntile = std::max(16, cdiv(cdiv(std::max(R, 1), L.n_tiles), 16) * 16);
@@ -982,8 +982,10 @@ Launch plan_launch(int R) {
   const size_t stage = A_STAGE + (size_t)L.ntile * BK * 2;
   const size_t fixed = 1024 + 64;
   // A wide activation tile (a stage of more than 24 KB) would leave two CTAs
-  // with 2-3 stages each; one CTA with the whole shared memory keeps 4+.
-  const size_t budget = stage > 24 * 1024 ? kSmemBudgetWide : kSmemBudget;
+  // with 2-3 stages each; one CTA with the whole shared memory keeps 4+ --
+  // worth it only for a long K loop (a short one, like the low-rank head's
+  // 4 k-blocks, is better served by two CTAs per SM).
+  const size_t budget = (stage > 24 * 1024 && n_kb >= 16) ? kSmemBudgetWide : kSmemBudget;
   L.stages = (int)std::max<size_t>(2, std::min<size_t>(8, (budget - fixed) / stage));
   L.smem = fixed + L.stages * stage + 16 * L.stages + 16;
   return L;
@@ -1002,7 +1004,7 @@ bool launch(TcGemm* t, const CUtensorMap* a0, const CUtensorMap* a1, const CUten
             const void* X, int ldx, int K, int R, bool split, int S, TcArgs& args, int grid_x,
             cudaStream_t st) {
   const int ncols = split ? 2 * R : R;
-  Launch L = plan_launch(ncols);
+  Launch L = plan_launch(ncols, cdiv(K, BK));
   CUtensorMap mb;
   if (!encode_map(t->encode, &mb, X, ncols, K, (size_t)ldx * 2, L.ntile)) return false;
   args.R = R;

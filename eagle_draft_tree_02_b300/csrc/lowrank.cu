@@ -236,12 +236,24 @@ __global__ void __launch_bounds__(kSelThreads) lowrank_select_kernel(LowRankArgs
   const int nw = blockDim.x >> 5, C = a.C;
 
   const int n = a.cnt[r];
-  if (n <= kLrCap) {
-    int P = 128;
-    while (P < n) P <<= 1;
-    for (int i = tid; i < P; i += blockDim.x)
-      key[i] = i < n ? lr_key(a.cval[(size_t)r * kLrCap + i], a.ctok[(size_t)r * kLrCap + i]) : 0ull;
-    sort_keys_desc(key, P);
+  if (n <= kLrCap - 128) {
+    // the buffer's keys are distinct (one per token): the key of rank i (by
+    // count of larger keys) goes to top[i] for i < C.  top[] sits past the
+    // n buffered keys (n <= kLrCap - 128 here, see the overflow test below).
+    for (int i = tid; i < n; i += blockDim.x)
+      key[i] = lr_key(a.cval[(size_t)r * kLrCap + i], a.ctok[(size_t)r * kLrCap + i]);
+    unsigned long long* top = key + (kLrCap - 128);
+    for (int i = tid; i < 128; i += blockDim.x) top[i] = 0ull;
+    __syncthreads();
+    for (int i = tid; i < n; i += blockDim.x) {
+      const unsigned long long ki = key[i];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += key[j] > ki;
+      if (rank < C) top[rank] = ki;
+    }
+    __syncthreads();
+    for (int i = tid; i < C; i += blockDim.x) key[i] = top[i];
+    __syncthreads();
   } else {
     for (int j = tid; j < a.r; j += blockDim.x) t_s[j] = act_at((const T*)a.t, r, a.r, j, a.t_split);
     __syncthreads();
@@ -256,7 +268,9 @@ __global__ void __launch_bounds__(kSelThreads) lowrank_select_kernel(LowRankArgs
     int* dst = a.cand_out + ((size_t)b * a.cand_n_exp + a.cand_slot0 + j) * C;
     for (int i = tid; i < C; i += blockDim.x) dst[i] = ctk[i];
   }
-  // exact logits of the candidates: one warp per candidate
+  // exact logits of the candidates: one warp per candidate, 16-byte loads of
+  // the head row (8 bf16 or 4 fp32 per lane and step)
+  constexpr int VEC = 16 / sizeof(T);
   for (int c = wid; c < C; c += nw) {
     if (ctk[c] < 0 || ctk[c] >= a.V) {  // only after an aborted low-rank pass
       if (lane == 0) {
@@ -267,7 +281,16 @@ __global__ void __launch_bounds__(kSelThreads) lowrank_select_kernel(LowRankArgs
     }
     const T* w = (const T*)a.W + (size_t)ctk[c] * a.d;
     float acc = 0.f;
-    for (int j = lane; j < a.d; j += 32) acc = fmaf(ldf(w + j), h_s[j], acc);
+    if (a.d % VEC == 0 && ((uintptr_t)w & 15) == 0) {
+      for (int j = lane * VEC; j < a.d; j += 32 * VEC) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(w + j);
+        const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+        for (int u = 0; u < VEC; ++u) acc = fmaf(ldf(e + u), h_s[j + u], acc);
+      }
+    } else {
+      for (int j = lane; j < a.d; j += 32) acc = fmaf(ldf(w + j), h_s[j], acc);
+    }
     acc = warp_sum(acc);
     if (lane == 0) ex[c] = acc;
   }
