@@ -153,15 +153,32 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// The load and its wait sit in one asm statement, so that no use of the
+// registers can be scheduled before the data has arrived.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
         "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
 }
 
 // ----------------------------------------------------------------------------- epilogues
@@ -470,7 +487,7 @@ __device__ __forceinline__ void list_merge(float* vals, int* idx, int k, unsigne
 }
 
 // draft head: fold this warp's 32 tokens of one row into the row's top-k list
-// (the log-sum-exp part is ph_lse_rows).  state: [0] max, [1] sum exp,
+// (the log-sum-exp part is draft_chunk).  state: [0] max, [1] sum exp,
 // [2, 2+k) values, [2+k, 2+2k) tokens (int bits), the list sorted by
 // (value desc, token asc)
 __device__ __forceinline__ void ph_fold_draft(float* st, int k, float x, int tok, bool valid,
@@ -499,106 +516,230 @@ __device__ __forceinline__ void ph_fold_draft(float* st, int k, float x, int tok
   list_merge(vals, idx, k, warp_sort_desc(q ? mine : 0ull, lane), lane);
 }
 
-// verify head: state [0] best z, [1] its token, [2] max z/T, [3] sum exp, [4] best
-// Gumbel score, [5] its token.  Four rows at once, so that the warp
-// reductions of the rows interleave and their shuffle latencies overlap:
-// row q (< nr) has state st[q], global row r[q], child tokens ct[q] (shared
-// memory), logit z[q] at this lane's token x, and Gumbel noise g[q].
-__device__ __forceinline__ void ph_fold_verify4(float* const (&st)[4], const VerifyHeadArgs& va,
-                                                const int (&r)[4], const int* const (&ct)[4],
-                                                const float (&z)[4], int nr, int x, bool valid,
-                                                const float (&g)[4], int lane) {
-  float zb[4], t[4], gb[4], m[4], sl[4];
-  int zi[4], gi[4];
+// Warp-wide maximum of one float per lane, returned to every lane.
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Sums over the warp of 16 values per lane.  Each step keeps half of a lane's
+// values and adds the partner lane's copy of them, handing over the other
+// half, so lane l ends with the total of value (l >> 1) & 15: 31 shuffles
+// for 16 sums instead of 80.
+__device__ __forceinline__ float warp_sum16_scatter(const float (&v)[16], int lane) {
+  float a[8], b[4], c[2];
+  bool u = (lane & 16) != 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const bool ok = valid && q < nr;
-    zb[q] = ok ? z[q] : -INFINITY;
-    zi[q] = ok ? x : 0x7fffffff;
-    t[q] = ok ? z[q] * va.inv_t : -INFINITY;
-    gb[q] = -INFINITY;
-    gi[q] = 0x7fffffff;
-    if (ok) {
-      bool child = false;
-      for (int c = 0; c < va.kmax; ++c) {
-        if (ct[q][c] == x) {
-          child = true;
-          va.child_z[(size_t)r[q] * va.kmax + c] = z[q];
-        }
-      }
-      if (va.sampling && !child) {
-        gb[q] = t[q] + g[q];
-        gi[q] = x;
+  for (int j = 0; j < 8; ++j)
+    a[j] = (u ? v[j + 8] : v[j]) + __shfl_xor_sync(0xffffffffu, u ? v[j] : v[j + 8], 16);
+  u = (lane & 8) != 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    b[j] = (u ? a[j + 4] : a[j]) + __shfl_xor_sync(0xffffffffu, u ? a[j] : a[j + 4], 8);
+  u = (lane & 4) != 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    c[j] = (u ? b[j + 2] : b[j]) + __shfl_xor_sync(0xffffffffu, u ? b[j] : b[j + 2], 4);
+  u = (lane & 2) != 0;
+  const float d = (u ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, u ? c[0] : c[1], 2);
+  return d + __shfl_xor_sync(0xffffffffu, d, 1);
+}
+
+__device__ __forceinline__ float sel16(const float (&v)[16], int q) {
+  float r = v[0];
+#pragma unroll
+  for (int j = 1; j < 16; ++j) r = q == j ? v[j] : r;
+  return r;
+}
+
+// This lane's logits of rows r0 .. r0 + 15 from the accumulator at taddr
+// (split: columns 2r and 2r + 1 hold row r's hi and lo halves); -inf for rows
+// >= r0 + nr and for tokens beyond the vocabulary.  Only columns below ncols,
+// which the tile allocation covers, are read.
+__device__ __forceinline__ void load_rows16(uint32_t taddr, int r0, bool split, int ncols, int nr,
+                                            bool valid, float (&x)[16]) {
+  if (split) {
+    if (2 * r0 + 16 < ncols) {
+      uint32_t v[32];
+      tmem_ld32(taddr + (uint32_t)(2 * r0), v);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) x[q] = __uint_as_float(v[2 * q]) + __uint_as_float(v[2 * q + 1]);
+    } else {
+      uint32_t v[16];
+      tmem_ld16(taddr + (uint32_t)(2 * r0), v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        x[q] = __uint_as_float(v[2 * q]) + __uint_as_float(v[2 * q + 1]);
+        x[q + 8] = -INFINITY;
       }
     }
-    m[q] = t[q];
+  } else {
+    uint32_t v[16];
+    tmem_ld16(taddr + (uint32_t)r0, v);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) x[q] = __uint_as_float(v[q]);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
+  for (int q = 0; q < 16; ++q)
+    if (!valid || q >= nr) x[q] = -INFINITY;
+}
+
+// Draft head, one chunk of 16 rows (nr of them real) over this warp's 32
+// tokens: fold each row's (max, sum exp) into its running state, and its new
+// top-k entries into its sorted list.  Lane l (even) owns row (l >> 1) & 15
+// for the log-sum-exp; with k = 1 it also keeps the row's best token, the
+// first lane that holds the row maximum.  With k > 1 a row whose k-th best
+// no token of the chunk beats is skipped: the tokens arrive in increasing
+// order, so a tie never displaces an entry.
+__device__ __forceinline__ void draft_chunk(float* mine, int sw, int k, int r0, int nr,
+                                            const float (&x)[16], int tok0, int lane) {
+  const int qo = (lane >> 1) & 15;
+  float ex[16], Mo = -INFINITY;
+  unsigned bo = 0u;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], o));
-#pragma unroll
-  for (int q = 0; q < 4; ++q) sl[q] = t[q] == -INFINITY ? 0.f : expf(t[q] - m[q]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      sl[q] += __shfl_xor_sync(0xffffffffu, sl[q], o);
-      const float ozb = __shfl_xor_sync(0xffffffffu, zb[q], o);
-      const int ozi = __shfl_xor_sync(0xffffffffu, zi[q], o);
-      if (better(ozb, ozi, zb[q], zi[q])) {
-        zb[q] = ozb;
-        zi[q] = ozi;
-      }
-      const float ogb = __shfl_xor_sync(0xffffffffu, gb[q], o);
-      const int ogi = __shfl_xor_sync(0xffffffffu, gi[q], o);
-      if (better(ogb, ogi, gb[q], gi[q])) {
-        gb[q] = ogb;
-        gi[q] = ogi;
+  for (int q = 0; q < 16; ++q) {
+    ex[q] = 0.f;
+    if (q < nr) {
+      const float M = warp_max_f32(x[q]);
+      if (x[q] != -INFINITY) ex[q] = __expf(x[q] - M);
+      const unsigned b = __ballot_sync(0xffffffffu, x[q] == M && x[q] != -INFINITY);
+      if (q == qo) {
+        Mo = M;
+        bo = b;
       }
     }
-  if (lane == 0) {
+  }
+  const float S = warp_sum16_scatter(ex, lane);
+  if ((lane & 1) == 0 && qo < nr && bo) {
+    float* st = mine + (size_t)(r0 + qo) * sw;
+    lse_fold_dev(st[0], st[1], Mo, S);
+    if (k == 1) {
+      const int t = tok0 + __ffs(bo) - 1;
+      if (better(Mo, t, st[2], __float_as_int(st[3]))) {
+        st[2] = Mo;
+        st[3] = __int_as_float(t);
+      }
+    }
+  }
+  if (k > 1) {
+    __syncwarp();
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 16; ++q) {
       if (q >= nr) break;
-      float* s = st[q];
-      if (better(zb[q], zi[q], s[0], __float_as_int(s[1]))) {
-        s[0] = zb[q];
-        s[1] = __int_as_float(zi[q]);
-      }
-      lse_fold_dev(s[2], s[3], m[q], sl[q]);
-      if (better(gb[q], gi[q], s[4], __float_as_int(s[5]))) {
-        s[4] = gb[q];
-        s[5] = __int_as_float(gi[q]);
-      }
+      float* st = mine + (size_t)(r0 + q) * sw;
+      if (__any_sync(0xffffffffu, x[q] > st[1 + k]))
+        ph_fold_draft(st, k, x[q], tok0 + lane, x[q] != -INFINITY, lane);
     }
   }
   __syncwarp();
 }
 
-// draft head, first part for several rows at once: the online log-sum-exp of
-// each row's 32 values, with the rows' reductions interleaved
-template <int N>
-__device__ __forceinline__ void ph_lse_rows(float* const (&st)[N], const float (&x)[N], int nr,
-                                            int lane) {
-  float m[N], sl[N];
-#pragma unroll
-  for (int q = 0; q < N; ++q) m[q] = x[q];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-    for (int q = 0; q < N; ++q) m[q] = fmaxf(m[q], __shfl_xor_sync(0xffffffffu, m[q], o));
-#pragma unroll
-  for (int q = 0; q < N; ++q) sl[q] = x[q] == -INFINITY ? 0.f : expf(x[q] - m[q]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-    for (int q = 0; q < N; ++q) sl[q] += __shfl_xor_sync(0xffffffffu, sl[q], o);
-  if (lane == 0) {
-#pragma unroll
-    for (int q = 0; q < N; ++q)
-      if (q < nr) lse_fold_dev(st[q][0], st[q][1], m[q], sl[q]);
+// Verify head, one chunk of 16 rows (nr of them real) over this warp's 32
+// tokens.  State of a row: [0] best z, [1] its token, [2] max z/T, [3] sum
+// exp, [4] best Gumbel score z/T + g over the non-child tokens, [5] its
+// token.  evs holds this CTA's child events (local row * kmax + child, token):
+// a child among these tokens has its logit stored in child_z and takes no
+// Gumbel score.  Gumbel words: lane l draws the Philox block of row 4 j +
+// l / 8 for tokens tok0 + 4 (l % 8) .. + 3, and each lane takes its token's
+// word from lane 8 (q % 4) + l / 4.
+__device__ __forceinline__ void verify_chunk(float* mine, const VerifyHeadArgs& va, int R, int r_off,
+                                             int r0, int nr, const float (&x)[16], int tok0,
+                                             int lane, const int2* evs, int n_ev) {
+  const int qo = (lane >> 1) & 15;
+  const int kmax = va.kmax;
+  uint32_t excl = 0u;
+  for (int b0 = 0; b0 < n_ev; b0 += 32) {
+    int2 ev = make_int2(-1, -1);
+    if (b0 + lane < n_ev) ev = evs[b0 + lane];
+    const int rr = ev.x >= 0 ? ev.x / kmax - r0 : -1;
+    const bool hit = ev.x >= 0 && (unsigned)(ev.y - tok0) < 32u && (unsigned)rr < 16u;
+    unsigned hb = __ballot_sync(0xffffffffu, hit);
+    while (hb) {
+      const int src = __ffs(hb) - 1;
+      hb &= hb - 1;
+      const int qh = __shfl_sync(0xffffffffu, rr, src);
+      const int lh = __shfl_sync(0xffffffffu, ev.y - tok0, src);
+      const int ix = __shfl_sync(0xffffffffu, ev.x, src);
+      const float zv = __shfl_sync(0xffffffffu, sel16(x, qh), lh);
+      if (lane == 0) va.child_z[(size_t)r_off * kmax + ix] = zv;
+      if (lane == lh) excl |= 1u << qh;
+    }
   }
+  float g[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) g[q] = 0.f;
+  if (va.sampling) {
+    const unsigned long long rid = va.round_ptr ? *va.round_ptr : va.round_id;
+#pragma unroll
+    for (int g4 = 0; g4 < 16; g4 += 4) {
+      if (g4 < nr) {
+        uint32_t m[4] = {0u, 0u, 0u, 0u};
+        const int rq = r0 + g4 + (lane >> 3);
+        if (rq < R) {
+          uint64_t w[4];
+          const int rg = r_off + rq;
+          gumbel_block(va.seed, rid, rg / va.M1, rg % va.M1, (uint64_t)((tok0 >> 2) + (lane & 7)), w);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) m[j] = (uint32_t)(w[j] >> 40);
+        }
+        const int sel = lane & 3;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int src = q * 8 + (lane >> 2);
+          const uint32_t m0 = __shfl_sync(0xffffffffu, m[0], src);
+          const uint32_t m1 = __shfl_sync(0xffffffffu, m[1], src);
+          const uint32_t m2 = __shfl_sync(0xffffffffu, m[2], src);
+          const uint32_t m3 = __shfl_sync(0xffffffffu, m[3], src);
+          g[g4 + q] = gumbel_from_u24(sel == 0 ? m0 : sel == 1 ? m1 : sel == 2 ? m2 : m3);
+        }
+      }
+    }
+  }
+  float ex[16], Mo = -INFINITY, Go = -INFINITY;
+  unsigned bz = 0u, bg = 0u;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    ex[q] = 0.f;
+    if (q < nr) {
+      const float M = warp_max_f32(x[q]);
+      if (x[q] != -INFINITY) ex[q] = __expf((x[q] - M) * va.inv_t);
+      const unsigned b = __ballot_sync(0xffffffffu, x[q] == M && x[q] != -INFINITY);
+      if (q == qo) {
+        Mo = M;
+        bz = b;
+      }
+      if (va.sampling) {
+        const float s = (x[q] == -INFINITY || ((excl >> q) & 1u)) ? -INFINITY : x[q] * va.inv_t + g[q];
+        const float G = warp_max_f32(s);
+        const unsigned bs = __ballot_sync(0xffffffffu, s == G && s != -INFINITY);
+        if (q == qo) {
+          Go = G;
+          bg = bs;
+        }
+      }
+    }
+  }
+  const float S = warp_sum16_scatter(ex, lane);
+  if ((lane & 1) == 0 && qo < nr) {
+    float* st = mine + (size_t)(r0 + qo) * 6;
+    if (bz) {
+      const int t = tok0 + __ffs(bz) - 1;
+      if (better(Mo, t, st[0], __float_as_int(st[1]))) {
+        st[0] = Mo;
+        st[1] = __int_as_float(t);
+      }
+      lse_fold_dev(st[2], st[3], Mo * va.inv_t, S);
+    }
+    if (bg) {
+      const int t = tok0 + __ffs(bg) - 1;
+      if (better(Go, t, st[4], __float_as_int(st[5]))) {
+        st[4] = Go;
+        st[5] = __int_as_float(t);
+      }
+    }
+  }
+  __syncwarp();
 }
 
 #ifndef E3_HEAD_CTAS_PER_SM
@@ -623,7 +764,8 @@ __global__ void __launch_bounds__(192, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gen);
   volatile int* abort_f = reinterpret_cast<volatile int*>(gen + 4);
   float* state = reinterpret_cast<float*>(gen + 16);  // [4][R][sw]
-  int* child_s = reinterpret_cast<int*>(state + (size_t)4 * a.R * a.sw);  // verify: [R][kmax]
+  int* n_ev_s = reinterpret_cast<int*>(gen + 8);
+  int2* evs = reinterpret_cast<int2*>(state + (size_t)4 * a.R * a.sw);  // verify: <= R kmax events
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -660,9 +802,16 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   pdl_begin();  // set-up above overlaps the previous kernel's tail
-  if (MODE == 2) {  // this launch's rows' child tokens, read by every tile's epilogue
-    for (int i = threadIdx.x; i < a.R * a.va.kmax; i += blockDim.x)
-      child_s[i] = a.va.child_tok[(size_t)a.r_off * a.va.kmax + i];
+  if (MODE == 2) {
+    // child events of the tiles this CTA owns: (local row * kmax + child, token)
+    if (threadIdx.x == 0) *n_ev_s = 0;
+    __syncthreads();
+    const int kmax = a.va.kmax;
+    for (int j = threadIdx.x; j < a.R * kmax; j += blockDim.x) {
+      const int t = a.va.child_tok[(size_t)a.r_off * kmax + j];
+      if (t >= 0 && t < a.V && (t / BM) % (int)gridDim.x == (int)blockIdx.x)
+        evs[atomicAdd(n_ev_s, 1)] = make_int2(j, t);
+    }
     __syncthreads();
   }
 
@@ -715,106 +864,23 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------- epilogue: TMEM lanes 32 (warp % 4) .. +31 are this warp's tokens
     const int e = warp - 2, lg = warp & 3;
     float* mine = state + (size_t)e * a.R * a.sw;
+    const int n_ev = MODE == 2 ? *n_ev_s : 0;
     int i = 0;
     for (int mt = blockIdx.x; mt < a.n_mtiles; mt += gridDim.x, ++i) {
       const int ab = i & 1;
       if (!mbar_wait(tfull0 + 8 * ab, (uint32_t)(i >> 1) & 1u, abort_f, a.flags)) break;
       tc_fence_after();
-      const int tok = mt * BM + lg * 32 + lane;
-      const bool valid = tok < a.V;
-      const uint32_t taddr = tmem + (uint32_t)ab * a.acc_cols + ((uint32_t)(lg * 32) << 16);
       const int tok0 = mt * BM + lg * 32;  // this warp's first token
-      for (int c0 = 0; c0 < a.ntile; c0 += 16) {
-        if (c0 >= a.ncols) break;
-        uint32_t v[16];
-        tmem_ld16(taddr + (uint32_t)c0, v);
-        if (MODE == 1) {
-          // the chunk's rows: 8 split rows (column pairs) or 16 plain rows
-          if (a.split) {
-            float xv[8];
-            float* stp[8];
-            const int r0 = c0 >> 1, nr = min(8, a.R - r0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              xv[q] = (valid && q < nr) ? __uint_as_float(v[2 * q]) + __uint_as_float(v[2 * q + 1])
-                                        : -INFINITY;
-              stp[q] = mine + (size_t)(r0 + (q < nr ? q : 0)) * a.sw;
-            }
-            ph_lse_rows<8>(stp, xv, nr, lane);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (q < nr) ph_fold_draft(stp[q], a.hp.k, xv[q], tok, valid, lane);
-          } else {
-            float xv[16];
-            float* stp[16];
-            const int r0 = c0, nr = min(16, a.R - r0);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              xv[q] = (valid && q < nr) ? __uint_as_float(v[q]) : -INFINITY;
-              stp[q] = mine + (size_t)(r0 + (q < nr ? q : 0)) * a.sw;
-            }
-            ph_lse_rows<16>(stp, xv, nr, lane);
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-              if (q < nr) ph_fold_draft(stp[q], a.hp.k, xv[q], tok, valid, lane);
-          }
-        } else {
-          // rows in groups of 4: lane l computes the Philox block of row
-          // (l / 8) of the group for tokens tok0 + 4 (l % 8) .. + 3, and each
-          // lane takes its token's word from lane 8 q + lane / 4
-          auto group = [&](int r0, int nr, auto value_of) {
-            uint64_t w[4] = {0ull, 0ull, 0ull, 0ull};
-            if (a.va.sampling) {
-              const int rq = r0 + (lane >> 3);
-              if (rq < a.R) {
-                const int rg = a.r_off + rq;
-                const unsigned long long rid = a.va.round_ptr ? *a.va.round_ptr : a.va.round_id;
-                gumbel_block(a.va.seed, rid, rg / a.va.M1, rg % a.va.M1,
-                             (uint64_t)((tok0 >> 2) + (lane & 7)), w);
-              }
-            }
-            float g[4] = {0.f, 0.f, 0.f, 0.f}, zq[4];
-            int rq[4];
-            float* stp[4];
-            const int* ctp[4];
-            const int nrr = min(nr, a.R - r0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (a.va.sampling) {
-                const int src = q * 8 + (lane >> 2);
-                const uint64_t w0 = __shfl_sync(0xffffffffu, w[0], src);
-                const uint64_t w1 = __shfl_sync(0xffffffffu, w[1], src);
-                const uint64_t w2 = __shfl_sync(0xffffffffu, w[2], src);
-                const uint64_t w3 = __shfl_sync(0xffffffffu, w[3], src);
-                const int sel = lane & 3;
-                g[q] = gumbel_from_word(sel == 0 ? w0 : sel == 1 ? w1 : sel == 2 ? w2 : w3);
-              }
-              const int rr = r0 + (q < nrr ? q : 0);
-              zq[q] = value_of(q);
-              rq[q] = a.r_off + rr;
-              stp[q] = mine + (size_t)rr * a.sw;
-              ctp[q] = child_s + (size_t)rr * a.va.kmax;
-            }
-            ph_fold_verify4(stp, a.va, rq, ctp, zq, nrr, tok, valid, g, lane);
-          };
-          if (a.split) {  // 8 rows in this chunk
-#pragma unroll
-            for (int g4 = 0; g4 < 8; g4 += 4) {
-              const int r0 = (c0 >> 1) + g4;
-              if (r0 >= a.R) break;
-              group(r0, 4, [&](int q) {
-                return __uint_as_float(v[2 * (g4 + q)]) + __uint_as_float(v[2 * (g4 + q) + 1]);
-              });
-            }
-          } else {  // 16 rows in this chunk
-#pragma unroll
-            for (int g4 = 0; g4 < 16; g4 += 4) {
-              const int r0 = c0 + g4;
-              if (r0 >= a.R) break;
-              group(r0, 4, [&](int q) { return __uint_as_float(v[g4 + q]); });
-            }
-          }
-        }
+      const bool valid = tok0 + lane < a.V;
+      const uint32_t taddr = tmem + (uint32_t)ab * a.acc_cols + ((uint32_t)(lg * 32) << 16);
+      for (int r0 = 0; r0 < a.R; r0 += 16) {
+        const int nr = min(16, a.R - r0);
+        float x[16];
+        load_rows16(taddr, r0, a.split != 0, a.ncols, nr, valid, x);
+        if (MODE == 1)
+          draft_chunk(mine, a.sw, a.hp.k, r0, nr, x, tok0, lane);
+        else
+          verify_chunk(mine, a.va, a.R, a.r_off, r0, nr, x, tok0, lane, evs, n_ev);
       }
       tc_fence_before();
       __syncwarp();
@@ -1039,7 +1105,7 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
   uint32_t acc = 32;
   while (acc < (uint32_t)ntile) acc <<= 1;
   const int sw = MODE == 1 ? 2 + 2 * args.hp.k : 6;
-  const size_t state = (size_t)4 * R * sw * 4 + (MODE == 2 ? (size_t)R * args.va.kmax * 4 : 0);
+  const size_t state = (size_t)4 * R * sw * 4 + (MODE == 2 ? (size_t)R * args.va.kmax * 8 : 0);
   const size_t stage = A_STAGE + (size_t)ntile * BK * 2;
   // CTAs per SM: as configured, but their double-buffered accumulators must
   // share the SM's 512 TMEM columns (an allocation beyond them would wait)

@@ -75,8 +75,7 @@ __device__ __forceinline__ float verify_uniform(unsigned long long seed, unsigne
 // so U' never rounds to 1.  The outer log uses the fast intrinsic: its error
 // (about 1e-6 relative) can only move a Gumbel argmax whose two best scores
 // are that close, a near-tie that the parity rule counts.
-__device__ __forceinline__ float gumbel_from_word(uint64_t w) {
-  const uint32_t m = (uint32_t)(w >> 40);
+__device__ __forceinline__ float gumbel_from_u24(uint32_t m) {  // m = word >> 40
   float e;
   if (m < (1u << 23)) {
     float u = ((float)m + 0.5f) * 5.9604644775390625e-08f;
@@ -86,6 +85,9 @@ __device__ __forceinline__ float gumbel_from_word(uint64_t w) {
     e = -log1pf(-t);
   }
   return -__logf(e);
+}
+__device__ __forceinline__ float gumbel_from_word(uint64_t w) {
+  return gumbel_from_u24((uint32_t)(w >> 40));
 }
 
 // the Philox block that holds the Gumbel words of tokens 4 blk .. 4 blk + 3
