@@ -34,6 +34,7 @@ namespace {
 constexpr int QG = 32;   // query heads per block (CUDA-core kernel)
 constexpr int QGM = 64;  // queries per block (tensor-core kernel: 4 warps x 16)
 constexpr int KC = 64;   // keys per chunk
+constexpr int KST = 3;   // prefix stages in flight (tensor-core kernel)
 constexpr int NT = 256;  // threads (CUDA-core kernel)
 }
 
@@ -249,14 +250,41 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+// One-dimensional bulk copy global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void att_mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void att_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void att_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Bounded wait for the phase with the given parity: false (and the timeout
+// flag) after about two seconds.
+__device__ __forceinline__ bool att_wait(uint32_t bar, uint32_t parity, int* flags) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 63) == 63 && clock64() - t0 > 4000000000LL) {
+      raise_flag(flags, FLAG_TIMEOUT);
+      return false;
+    }
+  }
 }
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -285,8 +313,9 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
   constexpr int NKS = DH / 16;     // k16 steps over dh
   constexpr int PIECES = DH / 8;   // 16-byte pieces per K or V row
   extern __shared__ __align__(16) unsigned char att_smem[];
-  bf16* Ks = reinterpret_cast<bf16*>(att_smem);  // [2][KC][LD]
-  bf16* Vs = Ks + 2 * KC * LD;                   // [2][KC][LD]
+  bf16* Ks = reinterpret_cast<bf16*>(att_smem);  // [KST][KC][LD]
+  bf16* Vs = Ks + KST * KC * LD;                 // [KST][KC][LD]
+  const uint32_t bar0 = smem_u32(Vs + KST * KC * LD);  // [KST] mbarriers
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv, split = blockIdx.z;
@@ -345,24 +374,40 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   const bool active = qw < nq;
 
-  auto load_chunk = [&](int c0, int buf) {
-    for (int i = tid; i < KC * PIECES; i += blockDim.x) {
-      const int kk = i / PIECES, piece = i % PIECES, key = c0 + kk;
-      const bf16 *kp = nullptr, *vp = nullptr;
-      if (key < key_hi) {
-        kp = kv_row_ptr<bf16>(a, a.cache_k, b, key, kvh);
-        vp = kv_row_ptr<bf16>(a, a.cache_v, b, key, kvh);
-        if (!kp || !vp) {
-          if (piece == 0) raise_flag(a.flags, FLAG_PAGE_RANGE);
-          kp = vp = nullptr;
-        }
-      }
-      const uint32_t dk = smem_u32(Ks + (size_t)(buf * KC + kk) * LD + piece * 8);
-      const uint32_t dv = smem_u32(Vs + (size_t)(buf * KC + kk) * LD + piece * 8);
-      cp_async16(dk, kp ? (const void*)(kp + piece * 8) : a.cache_k, kp ? 16 : 0);
-      cp_async16(dv, vp ? (const void*)(vp + piece * 8) : a.cache_v, vp ? 16 : 0);
+  // Prefix chunks stream through a ring of KST stages.  Thread t copies one
+  // row of every chunk -- key t % KC of K (t < KC) or of V -- with a bulk copy
+  // that completes on the stage's mbarrier; a key past the split's end, or on
+  // a bad page, gets a zero row instead.  Its page-table entry is fetched one
+  // chunk ahead of the copy.
+  const int ck = tid % KC;
+  const bf16* ccache = reinterpret_cast<const bf16*>(tid < KC ? a.cache_k : a.cache_v);
+  bf16* crow = (tid < KC ? Ks : Vs) + (size_t)ck * LD;
+  auto page_of = [&](int ci) -> int {
+    const int pos = key_lo + ci * KC + ck;
+    if (!a.page_table || ci >= n_chunks || pos >= key_hi) return 0;
+    return a.page_table[(size_t)b * a.max_pages + pos / a.page_size];
+  };
+  auto issue = [&](int ci, int pg) {
+    const int st = ci % KST, pos = key_lo + ci * KC + ck;
+    const uint32_t dst = smem_u32(crow + (size_t)st * KC * LD), bar = bar0 + 8u * st;
+    long long row = -1;
+    if (pos < key_hi) {
+      if (!a.page_table)
+        row = (long long)b * a.max_prefix + pos;
+      else if (pg >= 0 && pg < a.n_pages)
+        row = (long long)pg * a.page_size + pos % a.page_size;
+      else
+        raise_flag(a.flags, FLAG_PAGE_RANGE);
     }
-    cp_async_commit();
+    if (row >= 0) {
+      att_arrive_tx(bar, DH * 2);
+      bulk_g2s(dst, ccache + ((size_t)row * a.Hkv + kvh) * DH, DH * 2, bar);
+    } else {
+#pragma unroll
+      for (int p = 0; p < PIECES; ++p)
+        *reinterpret_cast<uint4*>(crow + (size_t)st * KC * LD + p * 8) = make_uint4(0u, 0u, 0u, 0u);
+      att_arrive(bar);
+    }
   };
   // tree chunk: buffer 0 holds hi, buffer 1 lo, of K and of V
   auto load_tree = [&]() {
@@ -396,23 +441,37 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
     }
   };
 
-  if (n_chunks > 0) {
-    if (tree)
-      load_tree();
-    else
-      load_chunk(key_lo, 0);
-  }
-  for (int ci = 0; ci < n_chunks; ++ci) {
-    const int c0 = key_lo + ci * KC, buf = tree ? 0 : (ci & 1);
-    if (!tree) {
-      if (ci + 1 < n_chunks) {
-        load_chunk(c0 + KC, buf ^ 1);
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
+  int pg_next = 0;
+  if (tree) {
+    if (n_chunks > 0) load_tree();
+  } else {
+    if (tid == 0) {
+      for (int st = 0; st < KST; ++st) att_mbar_init(bar0 + 8u * st, blockDim.x);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    for (int ci = 0; ci < KST - 1 && ci < n_chunks; ++ci) issue(ci, page_of(ci));
+    pg_next = page_of(KST - 1);
+  }
+  for (int ci = 0; ci < n_chunks; ++ci) {
+    const int c0 = key_lo + ci * KC, buf = tree ? 0 : ci % KST;
+    if (!tree) {
+      // refill the stage that the previous chunk used, then wait for this one
+      const int cn = ci + KST - 1;
+      if (cn < n_chunks) {
+        issue(cn, pg_next);
+        pg_next = page_of(cn + 1);
+      }
+      const bool ok = att_wait(bar0 + 8u * buf, (uint32_t)(ci / KST) & 1u, a.flags);
+      if (!__syncthreads_and(ok)) {
+        // a copy never landed: let the ones still in flight land before leaving
+        for (int c = ci + 1; c < n_chunks && c < ci + KST; ++c)
+          att_wait(bar0 + 8u * (c % KST), (uint32_t)(c / KST) & 1u, a.flags);
+        break;
+      }
+    } else {
+      __syncthreads();
+    }
     if (active) {
       const bf16* kb = Ks + (size_t)buf * KC * LD;
       const bf16* vb = Vs + (size_t)buf * KC * LD;
@@ -513,7 +572,7 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
         }
       }
     }
-    __syncthreads();  // this buffer is refilled two chunks later
+    __syncthreads();  // this stage is refilled at the next chunk
   }
   // partials: unnormalised o, running max, and the quad's sum of exp
 #pragma unroll
@@ -634,6 +693,9 @@ __global__ void attention_combine_kernel(AttnArgs a) {
   }
 }
 
+// K and V rings of the tensor-core kernel, then one mbarrier per stage
+static int mma_smem(int dh) { return 2 * KST * KC * (dh + 8) * 2 + 8 * KST; }
+
 template <typename T>
 void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
   int R = a.B * a.rows_per_req;
@@ -648,18 +710,18 @@ void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
     cudaFuncSetAttribute(tree_attention_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          160 * 1024);
     cudaFuncSetAttribute(prefix_attention_mma_kernel<64, 1>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * KC * (64 + 8) * 2);
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem(64));
     cudaFuncSetAttribute(prefix_attention_mma_kernel<128, 1>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * KC * (128 + 8) * 2);
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem(128));
     cudaFuncSetAttribute(prefix_attention_mma_kernel<64, 4>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * KC * (64 + 8) * 2);
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem(64));
     cudaFuncSetAttribute(prefix_attention_mma_kernel<128, 4>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * KC * (128 + 8) * 2);
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem(128));
     attr_set[ti] = true;
   }
   if (mma) {  // prefix and tree splits in one launch
     dim3 gp(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, true), n_splits);
-    const size_t sm2 = (size_t)4 * KC * (a.dh + 8) * 2;
+    const size_t sm2 = mma_smem(a.dh);
     const bool kw4 = attention_kw(a.rows_per_req, a.Hq, a.Hkv) == 4;
     if (a.dh == 128) {
       if (kw4)
