@@ -396,6 +396,9 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
 
   // bf16: the tcgen05 LM head takes at most 256 rows per launch
   if (f.dtype == EAGLE3_BF16 && f.max_batch * f.topk > 256) return EAGLE3_ERR_UNSUPPORTED;
+  // Kernels request weight tiles before waiting for the preceding kernel on
+  // their stream, so every write of the weights must be complete from here on.
+  if (cudaDeviceSynchronize() != cudaSuccess) return EAGLE3_ERR_CUDA;
   eagle3_ctx* c = new eagle3_ctx();
   c->cfg = f;
   c->w = *w;

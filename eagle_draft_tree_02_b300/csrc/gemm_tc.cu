@@ -292,19 +292,32 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // The weights (operand A) do not depend on earlier kernels: the first ring
+  // of them is requested before the wait for the previous kernel, so their
+  // latency overlaps its tail.  The activations follow after the wait.
+  const CUtensorMap* mA = seg == 0 ? &mA0 : (seg == 1 ? &mA1 : &mA2);
+  const int pre = (nkb > 0 && warp == 0 && lane == 0) ? min(S, nkb) : 0;
+  if (pre) {
+    const uint64_t pw = policy_evict_first();
+    for (int i = 0; i < pre; ++i) {
+      mbar_arrive_tx(full0 + 8 * i, A_STAGE + B_STAGE);
+      tma_load_2d(sA + i * A_STAGE, mA, full0 + 8 * i, (kb0 + i) * BK, m0, pw);
+    }
+  }
   pdl_begin();  // set-up above overlaps the previous kernel's tail
 
   if (nkb > 0 && warp == 0 && lane == 0) {
     // ---------------- TMA producer
-    const CUtensorMap* mA = seg == 0 ? &mA0 : (seg == 1 ? &mA1 : &mA2);
     const uint64_t pw = policy_evict_first(), px = policy_evict_last();
     for (int i = 0; i < nkb; ++i) {
       const int s = i % S;
       const uint32_t ph = (uint32_t)(i / S) & 1u;
-      if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_f, a.flags)) break;
-      mbar_arrive_tx(full0 + 8 * s, A_STAGE + B_STAGE);
       const int kx = (kb0 + i) * BK;
-      tma_load_2d(sA + s * A_STAGE, mA, full0 + 8 * s, kx, m0, pw);
+      if (i >= pre) {
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_f, a.flags)) break;
+        mbar_arrive_tx(full0 + 8 * s, A_STAGE + B_STAGE);
+        tma_load_2d(sA + s * A_STAGE, mA, full0 + 8 * s, kx, m0, pw);
+      }
       tma_load_2d(sB + s * B_STAGE, &mB, full0 + 8 * s, kx, n0, px);
     }
   } else if (nkb > 0 && warp == 1 && lane == 0) {
@@ -801,6 +814,16 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  // the first ring of weight stages (of this CTA's first tile) is requested
+  // before the wait for the previous kernel; its activations follow after it
+  const int pre = (warp == 0 && lane == 0 && (int)blockIdx.x < a.n_mtiles) ? min(S, a.n_kb) : 0;
+  if (pre) {
+    const uint64_t pw = policy_evict_first();
+    for (int c = 0; c < pre; ++c) {
+      mbar_arrive_tx(full0 + 8 * c, A_STAGE + B_STAGE);
+      tma_load_2d(sA + c * A_STAGE, &mA, full0 + 8 * c, c * BK, (int)blockIdx.x * BM, pw);
+    }
+  }
   pdl_begin();  // set-up above overlaps the previous kernel's tail
   if (MODE == 2) {
     // child events of the tiles this CTA owns: (local row * kmax + child, token)
@@ -824,12 +847,14 @@ __global__ void __launch_bounds__(192, 1)
       for (int kb = 0; kb < a.n_kb; ++kb, ++c) {
         const int s = c % S;
         const uint32_t ph = (uint32_t)(c / S) & 1u;
-        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_f, a.flags)) {
-          ok = false;
-          break;
+        if (c >= pre) {
+          if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_f, a.flags)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_tx(full0 + 8 * s, A_STAGE + B_STAGE);
+          tma_load_2d(sA + s * A_STAGE, &mA, full0 + 8 * s, kb * BK, mt * BM, pw);
         }
-        mbar_arrive_tx(full0 + 8 * s, A_STAGE + B_STAGE);
-        tma_load_2d(sA + s * A_STAGE, &mA, full0 + 8 * s, kb * BK, mt * BM, pw);
         tma_load_2d(sB + s * B_STAGE, &mB, full0 + 8 * s, kb * BK, 0, px);
       }
     }

@@ -144,7 +144,10 @@ typedef struct {
 
 /* Create a context: checks the config, borrows the weights, allocates the
  * workspace for max_batch requests once (nothing is allocated later) and
- * prepares the kernels' tensor maps.  Returns EAGLE3_ERR_OOM if the workspace
+ * prepares the kernels' tensor maps.  It synchronizes the device first: the
+ * weights must be fully written before the call and stay unchanged while the
+ * context exists (kernels start reading weight tiles before the preceding
+ * kernel on their stream has finished).  Returns EAGLE3_ERR_OOM if the workspace
  * does not fit, EAGLE3_ERR_UNSUPPORTED for shapes outside the limits above. */
 eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, eagle3_ctx** out);
 
