@@ -760,8 +760,15 @@ __device__ __forceinline__ void verify_chunk(float* mine, const VerifyHeadArgs& 
 #endif
 constexpr int kHeadCtasPerSm = E3_HEAD_CTAS_PER_SM;
 
+// Warps 2 .. 2 + kHeadEpiWarps - 1 run the epilogue: two per TMEM lane
+// quarter, each taking every other chunk of 16 rows, so that the long
+// dependent chains of a chunk (warp reductions, the Philox rounds of the
+// Gumbel noise) of two chunks overlap.
+constexpr int kHeadEpiWarps = 8;
+constexpr int kHeadThreads = 64 + 32 * kHeadEpiWarps;
+
 template <int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kHeadThreads, 2)
     tc_head_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
                    const PhArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -788,15 +795,14 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(tfull0 + 8 * j, 1);
-      mbar_init(tempty0 + 8 * j, 4);
+      mbar_init(tempty0 + 8 * j, kHeadEpiWarps);
     }
     *abort_f = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tmem_alloc(su32(tslot), a.tmem_cols);
-  if (warp >= 2) {  // running state of this epilogue warp's rows
-    float* mine = state + (size_t)(warp - 2) * a.R * a.sw;
-    for (int i = lane; i < a.R * a.sw; i += 32) {
+  if (warp >= 2) {  // running state [lane quarter][row][field]
+    for (int i = threadIdx.x - 64; i < 4 * a.R * a.sw; i += 32 * kHeadEpiWarps) {
       const int f = i % a.sw;
       float v;
       if (MODE == 1) {
@@ -807,7 +813,7 @@ __global__ void __launch_bounds__(192, 1)
         v = (f == 0 || f == 2 || f == 4) ? -INFINITY
             : (f == 3 ? 0.f : __int_as_float(0x7fffffff));
       }
-      mine[i] = v;
+      state[i] = v;
     }
   }
   tc_fence_before();
@@ -886,9 +892,11 @@ __global__ void __launch_bounds__(192, 1)
       if (ok) mma_commit(tfull0 + 8 * ab);
     }
   } else if (warp >= 2) {
-    // ---------------- epilogue: TMEM lanes 32 (warp % 4) .. +31 are this warp's tokens
+    // ---------------- epilogue: TMEM lanes 32 (warp % 4) .. +31 are this warp's tokens;
+    // warp e takes the row chunks r0 = 16 (e / 4) (mod 32) and keeps their
+    // state in its lane quarter's rows
     const int e = warp - 2, lg = warp & 3;
-    float* mine = state + (size_t)e * a.R * a.sw;
+    float* mine = state + (size_t)(e & 3) * a.R * a.sw;
     const int n_ev = MODE == 2 ? *n_ev_s : 0;
     int i = 0;
     for (int mt = blockIdx.x; mt < a.n_mtiles; mt += gridDim.x, ++i) {
@@ -898,7 +906,7 @@ __global__ void __launch_bounds__(192, 1)
       const int tok0 = mt * BM + lg * 32;  // this warp's first token
       const bool valid = tok0 + lane < a.V;
       const uint32_t taddr = tmem + (uint32_t)ab * a.acc_cols + ((uint32_t)(lg * 32) << 16);
-      for (int r0 = 0; r0 < a.R; r0 += 16) {
+      for (int r0 = 16 * (e >> 2); r0 < a.R; r0 += 16 * (kHeadEpiWarps / 4)) {
         const int nr = min(16, a.R - r0);
         float x[16];
         load_rows16(taddr, r0, a.split != 0, a.ncols, nr, valid, x);
@@ -911,13 +919,13 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * ab);
     }
-    // combine the four epilogue warps' states; warp e takes rows r = e (mod 4)
-    // and writes one partial per (CTA, row)
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    // combine the four lane quarters' states; warp e takes rows r = e (mod
+    // kHeadEpiWarps) and writes one partial per (CTA, row)
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kHeadEpiWarps) : "memory");
     if (!*abort_f) {
       const int part = blockIdx.x;
-      for (int r = e; r < a.R; r += 4) {
-        float* st = state + (size_t)r * a.sw;  // warp 0's state of row r gathers the others
+      for (int r = e; r < a.R; r += kHeadEpiWarps) {
+        float* st = state + (size_t)r * a.sw;  // quarter 0's state of row r gathers the others
         for (int o = 1; o < 4; ++o) {
           const float* so = state + ((size_t)o * a.R + r) * a.sw;
           if (MODE == 1) {
@@ -1164,7 +1172,7 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
                          232448);
     attr = true;
   }
-  launch_pdl(tc_head_kernel<MODE>, dim3(grid), dim3(192), smem, st, *wmap, mb, args);
+  launch_pdl(tc_head_kernel<MODE>, dim3(grid), dim3(kHeadThreads), smem, st, *wmap, mb, args);
   n_parts = grid;  // one partial per CTA
   return true;
 }
