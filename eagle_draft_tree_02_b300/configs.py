@@ -36,6 +36,9 @@ class RoundConfig:
     lr_rank: int = 0        # two-stage head rank r (0 = single-stage head)
     lr_cand: int = 0        # two-stage head candidate count
     temperatures: tuple = (0.0,)  # verify modes: 0.0 = greedy, >0 = sampling at T
+    fc_norm: bool = False   # drafter variant: RMSNorm (gain g_fc) on the fused feature
+    post_norm: bool = False # drafter variant: norms after the residual adds
+    gain_std: float = 0.0   # RMSNorm gains ~ 1 + N(0, gain_std^2) (0: all gains 1)
 
     @property
     def pool_size(self) -> int:

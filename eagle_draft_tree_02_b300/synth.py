@@ -18,6 +18,8 @@ Recipe (every config):
   * two-stage head: U ~ N(0, (1/16)^2) [V, r], V_lr ~ N(0, 0.02^2) [r, d],
     ``W_lm = round(U V_lr + 0.5 * N(0, 0.02^2))`` (the low-rank part carries 80%
     of the variance, total std about 0.022);
+  * RMSNorm gains are 1, except in the drafter-variant cases, which draw them
+    as 1 + N(0, gain_std^2) so that a dropped or misplaced gain shows;
   * ragged prefixes: P_b ~ U{lo..hi}; a paged cache gets its physical pages in a
     random permutation so the page table is exercised.
 """
@@ -35,7 +37,7 @@ _CHUNK = 1 << 23
 
 # tensor ids (fixed: they are part of the recipe)
 T_WFC, T_EMB, T_WQ, T_WK, T_WV, T_WO, T_WG, T_WU, T_WD, T_WLM, T_G, T_FEAT, T_TOK, T_PLEN, \
-    T_PAGES, T_LRU, T_LRV, T_LRN = range(18)
+    T_PAGES, T_LRU, T_LRV, T_LRN, T_GAIN = range(19)
 
 
 def bf16_bits_from_f64(x: np.ndarray) -> np.ndarray:
@@ -123,9 +125,12 @@ def make_inputs(cfg: RoundConfig, seed: int | None = None, threads: int | None =
         "w_up": W(T_WU, cfg.ffn, d),
         "w_down": W(T_WD, d, cfg.ffn),
     }
-    one = np.ones(d, dtype=np.float64)
-    for g in ("g_emb", "g_hid", "g_post", "g_final"):
-        w[g] = bf16_bits_from_f64(one) if dt == "bf16" else one.astype(np.float32)
+    gains = ("g_emb", "g_hid", "g_post", "g_final") + (("g_fc",) if cfg.fc_norm else ())
+    for i, g in enumerate(gains):
+        v = np.ones(d, dtype=np.float64)
+        if cfg.gain_std > 0:
+            v = v + cfg.gain_std * _rng(seed, T_GAIN * 1000 + i).standard_normal(d)
+        w[g] = bf16_bits_from_f64(v) if dt == "bf16" else v.astype(np.float32)
 
     if cfg.lr_rank:
         r = cfg.lr_rank

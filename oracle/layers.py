@@ -23,6 +23,11 @@ Readings where the pages are silent (listed again in the design notes):
       float64, no frequency scaling;
   R-6 pre-norm layer: r = hid + W_o attn(x); s = r + W_down(silu(W_g z) * W_u z)
       with z = rms(r); h = rms(s) feeds the LM head.
+  R-15 drafter variants named by the EAGLE-4 blog (section 在EAGLE4中: the
+      drafter keeps EAGLE-3.1's FC Norm and Post-norm), with no formula there:
+      FC norm g = rms(W_fc f; g_fc); post-norm r = rms(hid + W_o attn(x); g_post),
+      s = rms(r + W_down(silu(W_g r) * W_u r); g_final), and s is both the LM
+      head's input and the state fed to children.
 
 ORACLE / TEST INFRASTRUCTURE ONLY.
 """
@@ -76,6 +81,15 @@ def fuse(feats: np.ndarray, w_fc: np.ndarray) -> np.ndarray:
     return linear(feats, w_fc)
 
 
+def fused_feature(w: dict, cfg, feats: np.ndarray) -> np.ndarray:
+    """The decoder's hid for prefix rows: g = W_fc f, or rms(W_fc f; g_fc) with the
+    FC-norm variant (R-15)."""
+    g = fuse(feats, w["w_fc"])
+    if getattr(cfg, "fc_norm", False):
+        g = rmsnorm(g, w["g_fc"], cfg.rms_eps)
+    return g
+
+
 def decoder_input(w: dict, cfg, tokens: np.ndarray, hid: np.ndarray) -> np.ndarray:
     """x = [rms(E[y]; g_emb); rms(hid; g_hid)]  -> [n, 2d]."""
     e = f64(w["embed"][np.asarray(tokens)])
@@ -113,7 +127,14 @@ def layer_tail(w: dict, cfg, hid: np.ndarray, o: np.ndarray):
     """O-projection, residual, SwiGLU FFN and the final norm.
 
     Returns (s, h): s is the pre-final-norm state fed to children, h = rms(s).
+    With the post-norm variant (R-15) both sums are normalised after the add and
+    s = h.
     """
+    if getattr(cfg, "post_norm", False):
+        r = rmsnorm(f64(hid) + linear(o, w["w_o"]), w["g_post"], cfg.rms_eps)
+        s = rmsnorm(r + linear(silu(linear(r, w["w_gate"])) * linear(r, w["w_up"]), w["w_down"]),
+                    w["g_final"], cfg.rms_eps)
+        return s, s
     r = f64(hid) + linear(o, w["w_o"])
     z = rmsnorm(r, w["g_post"], cfg.rms_eps)
     s = r + linear(silu(linear(z, w["w_gate"])) * linear(z, w["w_up"]), w["w_down"])

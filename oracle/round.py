@@ -92,7 +92,7 @@ def prefix_kv(w, cfg, feats, tokens, rows=None):
     feats [P, 3d], tokens [P].  Row i has position i, hid = g_i (R-2, R-4).
     """
     rows = np.arange(feats.shape[0]) if rows is None else np.asarray(rows)
-    g = L.fuse(feats[rows], w["w_fc"])
+    g = L.fused_feature(w, cfg, feats[rows])
     x = L.decoder_input(w, cfg, tokens[rows], g)
     _, k, v = L.qkv(w, cfg, x, rows)
     return k, v
@@ -100,7 +100,7 @@ def prefix_kv(w, cfg, feats, tokens, rows=None):
 
 def root_forward(w, cfg, K, V, feat_root, tok_root, root_pos):
     """Pass 0: the root row attends to prefix rows 0..root_pos (its own K/V included)."""
-    g = L.fuse(feat_root[None], w["w_fc"])
+    g = L.fused_feature(w, cfg, feat_root[None])
     x = L.decoder_input(w, cfg, np.array([tok_root]), g)
     q, _, _ = L.qkv(w, cfg, x, np.array([root_pos]))
     o = L.attend(q[0], K[:root_pos + 1], V[:root_pos + 1], cfg)

@@ -19,7 +19,12 @@ independent library routine, a closed form, an invariant or brute force:
   correction) that the same test rejects;
 * Philox4x64-10 vs numpy.random.Philox (an independent implementation);
 * two-stage head: with all tokens as candidates it equals the single-stage
-  head; with an exactly low-rank head the candidates are the true top-c.
+  head; with an exactly low-rank head the candidates are the true top-c;
+* drafter variants (EAGLE-4 blog, 在EAGLE4中: FC Norm and Post-norm): the
+  scale invariances that only a norm in the stated place gives (a post-norm
+  layer is unchanged when hid and the attention output are scaled together; an
+  FC-normed round is unchanged when every target feature is scaled), unit RMS
+  of the normalised rows, and the tree/path equivalence with the variants on.
 """
 import numpy as np
 import pytest
@@ -142,7 +147,7 @@ def _brute_path_states(w, cfg, f, tok, P, pool, node):
     prefix rows 0..P-1 and then the root-to-node path; returns (s, h) of the last row."""
     Ks, Vs = [], []
     path = pool.ancestors_or_self(node) if node is not None else []
-    rows = [(tok[i], L.fuse(f[i][None], w["w_fc"])[0]) for i in range(P)]
+    rows = [(tok[i], L.fused_feature(w, cfg, f[i][None])[0]) for i in range(P)]
     for t, i in enumerate(path):
         rows.append((pool.tok[i], None))
     s = h = None
@@ -416,3 +421,78 @@ def test_inputs_are_deterministic():
     for k in a.w:
         assert np.array_equal(a.w[k], b.w[k]), k
     assert np.array_equal(a.feats, b.feats) and np.array_equal(a.tokens, b.tokens)
+
+
+# ----------------------------------------------------------------------------- drafter variants
+def _variant_cfg(**kw):
+    return CONFIGS[0].scaled(name="variant_pin", prefix=24, depth=3, topk=3, n_verify=8,
+                             gain_std=0.1, **kw)
+
+
+def test_post_norm_layer_is_scale_invariant_and_unit_rms():
+    cfg = _variant_cfg(post_norm=True, rms_eps=0.0)
+    w = R.weights_f32(make_inputs(cfg, seed=21))
+    rng = np.random.default_rng(5)
+    hid = rng.standard_normal((3, cfg.d))
+    o = rng.standard_normal((3, cfg.n_q_heads * cfg.head_dim))
+    s1, h1 = L.layer_tail(w, cfg, hid, o)
+    s2, h2 = L.layer_tail(w, cfg, 3.7 * hid, 3.7 * o)
+    np.testing.assert_allclose(s2, s1, rtol=1e-10, atol=1e-12)
+    np.testing.assert_array_equal(s1, h1)  # the state fed to children is the head's input
+    ms = np.mean((s1 / w["g_final"].astype(np.float64)) ** 2, axis=-1)
+    np.testing.assert_allclose(ms, 1.0, rtol=1e-12)
+    # the pre-norm layer has neither property
+    pre = _variant_cfg(rms_eps=0.0)
+    p1, q1 = L.layer_tail(w, pre, hid, o)
+    p2, _ = L.layer_tail(w, pre, 3.7 * hid, 3.7 * o)
+    assert np.abs(p2 - p1).max() > 1e-3 and np.abs(p1 - q1).max() > 1e-3
+
+
+def test_fc_norm_feature_is_scale_invariant_with_unit_rms():
+    cfg = _variant_cfg(fc_norm=True, rms_eps=0.0)
+    w = R.weights_f32(make_inputs(cfg, seed=22))
+    f = np.random.default_rng(6).standard_normal((4, 3 * cfg.d))
+    g = L.fused_feature(w, cfg, f)
+    np.testing.assert_allclose(L.fused_feature(w, cfg, 0.25 * f), g, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(np.mean((g / w["g_fc"].astype(np.float64)) ** 2, axis=-1), 1.0,
+                               rtol=1e-12)
+    plain = L.fused_feature(w, _variant_cfg(), f)
+    np.testing.assert_allclose(plain, L.fuse(f, w["w_fc"]), rtol=0, atol=0)
+
+
+def test_fc_norm_round_is_invariant_to_feature_scale():
+    """With the FC norm every use of g (prefix rows, root) sees a normalised
+    feature, so scaling all target features leaves the whole round unchanged;
+    without it the round changes."""
+    for fc, expect_same in ((True, True), (False, False)):
+        cfg = _variant_cfg(fc_norm=fc, post_norm=True, rms_eps=0.0)
+        inp = make_inputs(cfg, seed=23)
+        w = R.weights_f32(inp)
+        f = inp.feats_f32().astype(np.float64)
+        P = int(inp.prefix_lens[0])
+        outs = []
+        for a in (1.0, 2.5):
+            K, V = R.prefix_kv(w, cfg, a * f[:P], inp.tokens[:P])
+            rr = R.round_request(w, cfg, K, V, a * f[P - 1], inp.tokens[P - 1], P - 1,
+                                 temperatures=(0.0,))
+            outs.append(rr)
+        same = (np.array_equal(outs[0].tree.tok, outs[1].tree.tok)
+                and np.allclose(outs[0].draft.pool.logq, outs[1].draft.pool.logq, rtol=0,
+                                atol=1e-9))
+        assert same == expect_same, (fc, same)
+
+
+@pytest.fixture(scope="module")
+def variant_round():
+    cfg = _variant_cfg(fc_norm=True, post_norm=True)
+    inp = make_inputs(cfg, seed=24)
+    w = R.weights_f32(inp)
+    f = inp.feats_f32()
+    P = int(inp.prefix_lens[0])
+    K, V = R.prefix_kv(w, cfg, f[:P], inp.tokens[:P])
+    rr = R.round_request(w, cfg, K, V, f[P - 1], inp.tokens[P - 1], P - 1, temperatures=(0.0,))
+    return cfg, inp, w, f, P, K, V, rr
+
+
+def test_variant_tree_states_equal_sequential_path_forward(variant_round):
+    test_tree_states_equal_sequential_path_forward(variant_round)
