@@ -169,7 +169,11 @@ void kv_rows(eagle3_ctx* c, int R, const void* feats, bool has_q, const float* h
   if (feats) {  // the caller's features are exact storage values: never split
     int S = splits_for(c, R, d, 3 * d);
     gemm1(c, TCW_FC, feats, 3 * d, c->w.w_fc, d, 3 * d, c->part, d, R, false, S, (size_t)R * d, st);
-    launch_reduce_parts(R, d, S, c->part, c->g, st);
+    if (f.variant & EAGLE3_FC_NORM) {
+      DISPATCH(c, launch_reduce_norm, R, d, S, f.rms_eps, c->part, c->w.g_fc, c->g, st);
+    } else {
+      launch_reduce_parts(R, d, S, c->part, c->g, st);
+    }
     c->launches++;
     hid_base = c->g;
   }
@@ -273,8 +277,9 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   // r = hid + W_o o ; z = rms(r)
   int S = splits_for(c, R, d, qd);
   gemm1(c, TCW_O, c->o, qd, c->w.w_o, d, qd, c->part, d, R, split, S, (size_t)R * d, st);
+  const bool post = (f.variant & EAGLE3_POST_NORM) != 0;
   DISPATCH(c, launch_o_epilogue, R, d, S, f.rms_eps, c->part, hid_base, c->rp.t_hid, c->w.g_post,
-           c->r, c->z, split, st);
+           c->r, c->z, split, post, st);
   c->launches++;
   // a = silu(W_g z) * W_u z  (gate and up in one GEMM: columns [0, F) and [F, 2F))
   const int F = f.ffn;
@@ -287,7 +292,7 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   int Sd = splits_for(c, R, d, F);
   gemm1(c, TCW_DOWN, c->a, F, c->w.w_down, d, F, c->part, d, R, split, Sd, (size_t)R * d, st);
   DISPATCH(c, launch_down_epilogue, R, d, Sd, f.rms_eps, c->part, c->r, c->w.g_final, c->rp.t_sdst,
-           c->S, c->rp.t_out, h_base, split, st);
+           c->S, c->rp.t_out, h_base, split, post, st);
   c->launches++;
 }
 
@@ -390,6 +395,8 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
     return EAGLE3_ERR_INVALID_ARG;
   // bf16 streams U [V, r] in 64-column TMA boxes
   if (f.lr_rank > 0 && f.dtype == EAGLE3_BF16 && f.lr_rank % 64) return EAGLE3_ERR_UNSUPPORTED;
+  if ((f.variant & ~(EAGLE3_FC_NORM | EAGLE3_POST_NORM)) || ((f.variant & EAGLE3_FC_NORM) && !w->g_fc))
+    return EAGLE3_ERR_INVALID_ARG;
   if (!w->w_fc || !w->embed || !w->w_q || !w->w_k || !w->w_v || !w->w_o || !w->w_gate || !w->w_up ||
       !w->w_down || !w->g_emb || !w->g_hid || !w->g_post || !w->g_final || !w->w_lm)
     return EAGLE3_ERR_INVALID_ARG;

@@ -64,6 +64,26 @@ __global__ void reduce_parts_kernel(int R, int N, int S, const float* __restrict
     out[i] = sum_parts(part + i, n, S);
 }
 
+// g = rms(sum of fusion partials) * g_fc: the FC-norm variant, one block per row
+template <typename T>
+__global__ void reduce_norm_kernel(int R, int N, int S, float eps, const float* __restrict__ part,
+                                   const T* __restrict__ g_fc, float* __restrict__ out) {
+  pdl_begin();
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const size_t n = (size_t)R * N;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < N; j += blockDim.x) {
+    const float v = sum_parts(part + (size_t)r * N + j, n, S);
+    out[(size_t)r * N + j] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / N + eps);
+  for (int j = threadIdx.x; j < N; j += blockDim.x)
+    out[(size_t)r * N + j] *= inv * ldf(g_fc + j);
+}
+
 // ----------------------------------------------------------------------------- RoPE + KV write
 // One thread per rotate-half pair (j, j + dh/2) of one head.  Heads are laid
 // out [q heads | k heads | v heads] in the partials when has_q, else [k | v].
@@ -144,7 +164,7 @@ template <typename T>
 __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* __restrict__ part,
                                   const float* __restrict__ hid_base, const int* __restrict__ hid_row,
                                   const T* __restrict__ g_post, float* __restrict__ r_out,
-                                  T* __restrict__ z_out, bool split) {
+                                  T* __restrict__ z_out, bool split, bool post) {
   pdl_begin();
   __shared__ float red[32];
   int r = blockIdx.x;
@@ -159,8 +179,11 @@ __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* _
   ss = block_sum(ss, red);
   float inv = rsqrtf(ss / d + eps);
   T* zr = z_out + act_row(r, d, split);
-  for (int j = threadIdx.x; j < d; j += blockDim.x)
-    st_act(zr, d, j, r_out[(size_t)r * d + j] * inv * ldf(g_post + j), split);
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    const float z = r_out[(size_t)r * d + j] * inv * ldf(g_post + j);
+    if (post) r_out[(size_t)r * d + j] = z;  // post-norm: the residual stream is normalised too
+    st_act(zr, d, j, z, split);
+  }
 }
 
 // ----------------------------------------------------------------------------- a = silu(W_g z) * (W_u z)
@@ -186,7 +209,7 @@ __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float
                                      const float* __restrict__ r_in, const T* __restrict__ g_final,
                                      const int* __restrict__ s_dst, float* __restrict__ s_base,
                                      const int* __restrict__ h_dst, T* __restrict__ h_base,
-                                     bool split) {
+                                     bool split, bool post) {
   pdl_begin();
   __shared__ float red[32];
   extern __shared__ float srow[];
@@ -204,8 +227,9 @@ __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float
   int hd = h_dst ? h_dst[r] : r;
   T* hr = h_base + act_row(hd, d, split);
   for (int j = threadIdx.x; j < d; j += blockDim.x) {
-    if (sd >= 0) s_base[(size_t)sd * d + j] = srow[j];
-    st_act(hr, d, j, srow[j] * inv * ldf(g_final + j), split);
+    const float h = srow[j] * inv * ldf(g_final + j);
+    if (sd >= 0) s_base[(size_t)sd * d + j] = post ? h : srow[j];  // post-norm: the state is h
+    st_act(hr, d, j, h, split);
   }
 }
 
@@ -232,6 +256,14 @@ void launch_reduce_parts(int R, int N, int S, const float* part, float* out, cud
 }
 
 template <typename T>
+void launch_reduce_norm(int R, int N, int S, float eps, const float* part, const void* g_fc,
+                        float* out, cudaStream_t st) {
+  if (R <= 0) return;
+  launch_pdl(reduce_norm_kernel<T>, dim3(R), dim3(kRowThreads), 0, st, R, N, S, eps, part,
+             (const T*)g_fc, out);
+}
+
+template <typename T>
 void launch_qkv_epilogue(const QkvEpi& p, cudaStream_t st) {
   if (p.R <= 0) return;
   int nh = (p.has_q ? p.Hq : 0) + 2 * p.Hkv;
@@ -243,10 +275,10 @@ void launch_qkv_epilogue(const QkvEpi& p, cudaStream_t st) {
 template <typename T>
 void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const float* hid_base,
                        const int* hid_row, const void* g_post, float* r_out, void* z_out,
-                       bool split, cudaStream_t st) {
+                       bool split, bool post, cudaStream_t st) {
   if (R <= 0) return;
-  launch_pdl(o_epilogue_kernel<T>, dim3(R), dim3(kRowThreads), 0, st, R, d, S, eps, part, hid_base, hid_row, (const T*)g_post,
-                                          r_out, (T*)z_out, split);
+  launch_pdl(o_epilogue_kernel<T>, dim3(R), dim3(kRowThreads), 0, st, R, d, S, eps, part, hid_base,
+             hid_row, (const T*)g_post, r_out, (T*)z_out, split, post);
 }
 
 template <typename T>
@@ -261,11 +293,10 @@ void launch_swiglu(int R, int F, int S, const float* part, void* a, bool split, 
 template <typename T>
 void launch_down_epilogue(int R, int d, int S, float eps, const float* part, const float* r_in,
                           const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
-                          void* h_base, bool split, cudaStream_t st) {
+                          void* h_base, bool split, bool post, cudaStream_t st) {
   if (R <= 0) return;
-  launch_pdl(down_epilogue_kernel<T>, dim3(R), dim3(kRowThreads), d * sizeof(float), st, R, d, S, eps, part, r_in,
-                                                            (const T*)g_final, s_dst, s_base, h_dst,
-                                                            (T*)h_base, split);
+  launch_pdl(down_epilogue_kernel<T>, dim3(R), dim3(kRowThreads), d * sizeof(float), st, R, d, S,
+             eps, part, r_in, (const T*)g_final, s_dst, s_base, h_dst, (T*)h_base, split, post);
 }
 
 #define E3_INST(T)                                                                                   \
@@ -273,12 +304,14 @@ void launch_down_epilogue(int R, int d, int S, float eps, const float* part, con
                                       const void*, const void*, const void*, void*, bool, int*,     \
                                       cudaStream_t);                                                 \
   template void launch_qkv_epilogue<T>(const QkvEpi&, cudaStream_t);                                 \
+  template void launch_reduce_norm<T>(int, int, int, float, const float*, const void*, float*,     \
+                                      cudaStream_t);                                                 \
   template void launch_o_epilogue<T>(int, int, int, float, const float*, const float*, const int*,  \
-                                     const void*, float*, void*, bool, cudaStream_t);                \
+                                     const void*, float*, void*, bool, bool, cudaStream_t);          \
   template void launch_swiglu<T>(int, int, int, const float*, void*, bool, cudaStream_t);            \
   template void launch_down_epilogue<T>(int, int, int, float, const float*, const float*,           \
                                         const void*, const int*, float*, const int*, void*, bool,   \
-                                        cudaStream_t);
+                                        bool, cudaStream_t);
 E3_INST(float)
 E3_INST(bf16)
 #undef E3_INST

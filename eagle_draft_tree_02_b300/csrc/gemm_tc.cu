@@ -766,6 +766,13 @@ constexpr int kHeadCtasPerSm = E3_HEAD_CTAS_PER_SM;
 // Gumbel noise) of two chunks overlap.
 constexpr int kHeadEpiWarps = 8;
 constexpr int kHeadThreads = 64 + 32 * kHeadEpiWarps;
+// A ring stage holds kHeadKSub swizzle-row sub-tiles (64 K-columns each) of
+// both operands, so a weight row is read in runs of kHeadKSub * 128 bytes.
+#ifndef E3_HEAD_KSUB
+#define E3_HEAD_KSUB 1
+#endif
+constexpr int kHeadKSub = E3_HEAD_KSUB;
+constexpr int kHeadBK = BK * kHeadKSub;
 
 template <int MODE>
 __global__ void __launch_bounds__(kHeadThreads, 2)
@@ -776,9 +783,10 @@ __global__ void __launch_bounds__(kHeadThreads, 2)
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   const uint32_t sA = raw + pad;
   const int S = a.stages;
-  const uint32_t B_STAGE = (uint32_t)a.ntile * BK * 2;
-  const uint32_t sB = sA + S * A_STAGE;
-  const uint32_t bars = sB + S * B_STAGE;
+  const uint32_t B_SUB = (uint32_t)a.ntile * BK * 2;             // one sub-tile of B
+  const uint32_t A_ST = A_STAGE * kHeadKSub, B_ST = B_SUB * kHeadKSub;  // one stage
+  const uint32_t sB = sA + S * A_ST;
+  const uint32_t bars = sB + S * B_ST;
   const uint32_t full0 = bars, empty0 = bars + 8 * S, tfull0 = bars + 16 * S, tempty0 = tfull0 + 16;
   uint8_t* gen = smem_raw + pad + (bars - sA) + 16 * S + 32;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gen);
@@ -826,8 +834,10 @@ __global__ void __launch_bounds__(kHeadThreads, 2)
   if (pre) {
     const uint64_t pw = policy_evict_first();
     for (int c = 0; c < pre; ++c) {
-      mbar_arrive_tx(full0 + 8 * c, A_STAGE + B_STAGE);
-      tma_load_2d(sA + c * A_STAGE, &mA, full0 + 8 * c, c * BK, (int)blockIdx.x * BM, pw);
+      mbar_arrive_tx(full0 + 8 * c, A_ST + B_ST);
+      for (int h = 0; h < kHeadKSub; ++h)
+        tma_load_2d(sA + c * A_ST + h * A_STAGE, &mA, full0 + 8 * c, c * kHeadBK + h * BK,
+                    (int)blockIdx.x * BM, pw);
     }
   }
   pdl_begin();  // set-up above overlaps the previous kernel's tail
@@ -858,10 +868,13 @@ __global__ void __launch_bounds__(kHeadThreads, 2)
             ok = false;
             break;
           }
-          mbar_arrive_tx(full0 + 8 * s, A_STAGE + B_STAGE);
-          tma_load_2d(sA + s * A_STAGE, &mA, full0 + 8 * s, kb * BK, mt * BM, pw);
+          mbar_arrive_tx(full0 + 8 * s, A_ST + B_ST);
+          for (int h = 0; h < kHeadKSub; ++h)
+            tma_load_2d(sA + s * A_ST + h * A_STAGE, &mA, full0 + 8 * s, kb * kHeadBK + h * BK,
+                        mt * BM, pw);
         }
-        tma_load_2d(sB + s * B_STAGE, &mB, full0 + 8 * s, kb * BK, 0, px);
+        for (int h = 0; h < kHeadKSub; ++h)
+          tma_load_2d(sB + s * B_ST + h * B_SUB, &mB, full0 + 8 * s, kb * kHeadBK + h * BK, 0, px);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -881,12 +894,15 @@ __global__ void __launch_bounds__(kHeadThreads, 2)
           break;
         }
         tc_fence_after();
-        const uint64_t ad = sw128_desc(sA + s * A_STAGE);
-        const uint64_t bd = sw128_desc(sB + s * B_STAGE);
 #pragma unroll
-        for (int k = 0; k < BK / UK; ++k)
-          mma_bf16(d, ad + (uint64_t)(k * UK * 2 / 16), bd + (uint64_t)(k * UK * 2 / 16), a.idesc,
-                   (kb > 0 || k > 0) ? 1u : 0u);
+        for (int h = 0; h < kHeadKSub; ++h) {
+          const uint64_t ad = sw128_desc(sA + s * A_ST + h * A_STAGE);
+          const uint64_t bd = sw128_desc(sB + s * B_ST + h * B_SUB);
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k)
+            mma_bf16(d, ad + (uint64_t)(k * UK * 2 / 16), bd + (uint64_t)(k * UK * 2 / 16), a.idesc,
+                     (kb > 0 || h > 0 || k > 0) ? 1u : 0u);
+        }
         mma_commit(empty0 + 8 * s);
       }
       if (ok) mma_commit(tfull0 + 8 * ab);
@@ -1139,7 +1155,7 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
   while (acc < (uint32_t)ntile) acc <<= 1;
   const int sw = MODE == 1 ? 2 + 2 * args.hp.k : 6;
   const size_t state = (size_t)4 * R * sw * 4 + (MODE == 2 ? (size_t)R * args.va.kmax * 8 : 0);
-  const size_t stage = A_STAGE + (size_t)ntile * BK * 2;
+  const size_t stage = (A_STAGE + (size_t)ntile * BK * 2) * kHeadKSub;
   // CTAs per SM: as configured, but their double-buffered accumulators must
   // share the SM's 512 TMEM columns (an allocation beyond them would wait)
   const int ctas = std::max(1, std::min(kHeadCtasPerSm, (int)(512 / (2 * acc))));
@@ -1156,7 +1172,7 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
   args.R_total = R_total < 0 ? R : R_total;
   args.ncols = ncols;
   args.split = split ? 1 : 0;
-  args.n_kb = cdiv(K, BK);
+  args.n_kb = cdiv(K, kHeadBK);
   args.ntile = ntile;
   args.stages = stages;
   args.n_mtiles = n_mtiles;

@@ -27,18 +27,24 @@ void launch_build_input(int R, int d, int V, float eps, const int* tok, const fl
                         const int* hid_row, const void* E, const void* g_emb, const void* g_hid,
                         void* x, bool split, int* flags, cudaStream_t st);
 void launch_reduce_parts(int R, int N, int S, const float* part, float* out, cudaStream_t st);
+// g = rms(sum of fusion partials) * g_fc (the FC-norm variant), fp32 [R, N]
+template <typename T>
+void launch_reduce_norm(int R, int N, int S, float eps, const float* part, const void* g_fc,
+                        float* out, cudaStream_t st);
 template <typename T> void launch_qkv_epilogue(const QkvEpi& p, cudaStream_t st);
+// post = false: r = hid + W_o o, z = rms(r) g_post; true (post-norm): r = z = rms(hid + W_o o) g_post
 template <typename T>
 void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const float* hid_base,
                        const int* hid_row, const void* g_post, float* r_out, void* z_out,
-                       bool split, cudaStream_t st);
+                       bool split, bool post, cudaStream_t st);
 // part: [S][R][2F] with the gate in columns [0, F) and up in [F, 2F)
 template <typename T>
 void launch_swiglu(int R, int F, int S, const float* part, void* a, bool split, cudaStream_t st);
+// post = false: s = r + W_down a, h = rms(s) g_final; true (post-norm): s = h = rms(r + W_down a) g_final
 template <typename T>
 void launch_down_epilogue(int R, int d, int S, float eps, const float* part, const float* r_in,
                           const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
-                          void* h_base, bool split, cudaStream_t st);
+                          void* h_base, bool split, bool post, cudaStream_t st);
 
 // ----------------------------------------------------------------------------- gemm_simt.cu
 // Y[s][r][col0 + n] = sum_{k in split s} X[r][k] W[n][k]  (fp32 accumulate)

@@ -29,11 +29,12 @@ class eagle3_config(C.Structure):
                                        "lr_rank", "lr_cand")] + \
                [("rope_theta", C.c_float), ("rms_eps", C.c_float)] + \
                [(n, C.c_int) for n in ("dtype", "depth", "topk", "n_verify", "page_size",
-                                       "max_batch", "max_prefix", "max_new")]
+                                       "max_batch", "max_prefix", "max_new", "variant")]
 
 
 WEIGHT_NAMES = ("w_fc", "embed", "w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down",
-                "g_emb", "g_hid", "g_post", "g_final", "w_lm", "w_target", "lr_u", "lr_v")
+                "g_emb", "g_hid", "g_post", "g_final", "w_lm", "w_target", "lr_u", "lr_v", "g_fc")
+FC_NORM, POST_NORM = 1, 2  # eagle3_config.variant bits
 
 
 class eagle3_weights(C.Structure):

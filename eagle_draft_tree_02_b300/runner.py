@@ -30,6 +30,7 @@ def make_config(cfg: RoundConfig, max_prefix: int, max_new: int = 1, max_batch: 
     c.depth, c.topk, c.n_verify, c.page_size = cfg.depth, cfg.topk, cfg.n_verify, cfg.page_size
     c.max_batch = max_batch or cfg.batch
     c.max_prefix, c.max_new = max_prefix, max_new
+    c.variant = (E.FC_NORM if cfg.fc_norm else 0) | (E.POST_NORM if cfg.post_norm else 0)
     return c
 
 

@@ -59,6 +59,20 @@ typedef enum {
 
 enum { EAGLE3_FP32 = 0, EAGLE3_BF16 = 1 };
 
+/* Drafter variants (eagle3_config.variant, bits).  The EAGLE-4 blog (section
+ * 在EAGLE4中) states that its one-layer drafter keeps EAGLE-3.1's "FC Norm" and
+ * "Post-norm"; the pages give no formula, so the plainest readings are used:
+ *   EAGLE3_FC_NORM:   g = rms(W_fc [low; mid; high]) * g_fc (an RMSNorm with
+ *                     gain g_fc on the fused feature, before it enters the
+ *                     decoder input and its residual stream);
+ *   EAGLE3_POST_NORM: each residual sum is normalised after the add:
+ *                     r = rms(hid + W_o attn) * g_post,
+ *                     s = rms(r + W_down(silu(W_gate r) * W_up r)) * g_final,
+ *                     and s is both the LM head's input and the state fed to
+ *                     the node's children (no separate final norm).
+ * 0 is the EAGLE-3 pre-norm drafter: z = rms(r) feeds the FFN, h = rms(s). */
+enum { EAGLE3_FC_NORM = 1, EAGLE3_POST_NORM = 2 };
+
 /* Shapes of the draft model and of the round.  All sizes in elements. */
 typedef struct {
   int d;           /* model width */
@@ -80,6 +94,7 @@ typedef struct {
   int max_batch;   /* largest B of any call */
   int max_prefix;  /* rows one request may hold in the cache (contiguous layout stride) */
   int max_new;     /* largest n_new of a draft round */
+  int variant;     /* EAGLE3_FC_NORM | EAGLE3_POST_NORM bits, 0 = EAGLE-3 pre-norm */
 } eagle3_config;
 
 /* Device pointers of the draft weights (row-major [out, in], config dtype).
@@ -87,11 +102,13 @@ typedef struct {
  *   w_o [d, Hq*dh]; w_gate, w_up [F, d]; w_down [d, F];
  *   g_emb, g_hid, g_post, g_final [d] RMSNorm gains;
  *   w_lm [V, d] draft LM head; w_target [V, d] synthetic target head used by
- *   eagle3_verify; lr_u [V, r], lr_v [r, d] the two-stage head (else NULL). */
+ *   eagle3_verify; lr_u [V, r], lr_v [r, d] the two-stage head (else NULL);
+ *   g_fc [d] gain of the FC norm (EAGLE3_FC_NORM only, else NULL). */
 typedef struct {
   const void *w_fc, *embed, *w_q, *w_k, *w_v, *w_o, *w_gate, *w_up, *w_down;
   const void *g_emb, *g_hid, *g_post, *g_final;
   const void *w_lm, *w_target, *lr_u, *lr_v;
+  const void* g_fc;
 } eagle3_weights;
 
 /* Draft KV cache, caller-owned, config dtype, K after RoPE.

@@ -44,7 +44,7 @@ def _run(cfg, requests=None, conditioned_kv=False, kv_rows_checked=0):
             rows = np.sort(rng.choice(P, size=min(P, kv_rows_checked), replace=False))
             # sampled rows at their true positions
             from oracle import layers as L
-            g = L.fuse(f[lo:hi][rows], w["w_fc"])
+            g = L.fused_feature(w, cfg, f[lo:hi][rows])
             x = L.decoder_input(w, cfg, inp.tokens[lo:hi][rows], g)
             _, k, v = L.qkv(w, cfg, x, rows)
             tol = TOL[cfg.dtype]["logit"]

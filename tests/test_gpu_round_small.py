@@ -34,6 +34,11 @@ CASES = {
     "small_bf16": (SMALL_BF16, 6),
     "two_stage_fp32": (TWO_STAGE_FP32, 8),
     "two_stage_bf16_v40k": (TWO_STAGE_BF16, 9),
+    # drafter variants (FC norm, post-norm) with non-unit gains
+    "variant_fc_norm_fp32": (C0.scaled(name="fc_norm_fp32", fc_norm=True, gain_std=0.1), 10),
+    "variant_post_norm_fp32": (C0.scaled(name="post_norm_fp32", post_norm=True, gain_std=0.1), 11),
+    "variant_fc_post_bf16": (SMALL_BF16.scaled(name="fc_post_bf16", fc_norm=True, post_norm=True,
+                                               gain_std=0.1), 12),
 }
 
 
