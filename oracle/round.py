@@ -36,6 +36,22 @@ target mass of the children already rejected at that node; if none is accepted
 (or the node is a leaf) the bonus token is the Gumbel-argmax of z/T over the
 tokens that are not children of the node, an exact draw from the residual.
 
+Per-request control (R-16; EAGLE-4 blog, EAGLE-Harness paragraph, and
+几条技术路线正在收敛, second trend): a request b may carry caps -- depth D_b,
+branch count k_b, verify count M_b -- and three cost-aware rules, each of the
+form "expected extra accepted tokens / extra time >= threshold":
+  * another draft layer (pass t+1) runs only while the confidence mass of the
+    next frontier, sum of exp(score), is at least tau_depth * growth**(t+1) *
+    pass_us[t+1] (a threshold that rises with depth);
+  * the kept set is the longest prefix of the score order whose i-th node has
+    exp(score_i) >= tau_verify * (verify_us[i] - verify_us[i-1]) (at least one
+    node);
+  * a node expands at most k_light children when B <= light_batch, else
+    k_heavy.
+A node that a cap or rule leaves out is not created: its pool slot holds token
+-1, parent -1, score and log q -inf.  Tree slots past the kept count hold
+token -1, parent -1, depth 0, score -inf and only their own mask bit.
+
 Every decision goes through a ``Decisions`` object.  The plain class takes the
 oracle's own choice; tests may pass a subclass that, where the oracle's margin
 is inside a stated tolerance, adopts another valid choice (conditioned mode).
@@ -83,6 +99,51 @@ class Decisions:
     def bonus(self, b, node, scores):
         """Gumbel-argmax (scores already hold -inf at excluded tokens)."""
         return int(np.argmax(scores))
+
+    def keep_drafting(self, b, t, mass, threshold):
+        """Cost-aware depth rule: run pass t (mass = the frontier's sum of exp(score))."""
+        return mass >= threshold
+
+    def verify_count(self, b, gains, costs, m_cap):
+        """Kept-set size: the longest prefix (at least 1) with gains[i] >= costs[i]."""
+        m = 1
+        while m < m_cap and gains[m] >= costs[m]:
+            m += 1
+        return m
+
+
+@dataclass
+class Control:
+    """Per-request caps and the cost-aware rules of one round (R-16).
+
+    Caps are lists over requests (None = the config's value).  A rule is off
+    while its threshold is 0 (light_batch 0 turns the branch rule off).
+    pass_us[t] is the cost of draft pass t, verify_us[m] that of verifying m
+    nodes (verify_us[0] = 0), both from the latency table at the call's shape.
+    """
+    depth_cap: list | None = None
+    topk_cap: list | None = None
+    verify_cap: list | None = None
+    tau_depth: float = 0.0
+    depth_growth: float = 1.0
+    tau_verify: float = 0.0
+    light_batch: int = 0
+    k_light: int = 8
+    k_heavy: int = 4
+    pass_us: list | None = None
+    verify_us: list | None = None
+
+    def k_for(self, b, B, k):
+        kb = k if self.topk_cap is None else min(k, int(self.topk_cap[b]))
+        if self.light_batch > 0:
+            kb = min(kb, self.k_light if B <= self.light_batch else self.k_heavy)
+        return kb
+
+    def d_for(self, b, D):
+        return D if self.depth_cap is None else min(D, int(self.depth_cap[b]))
+
+    def m_for(self, b, M):
+        return M if self.verify_cap is None else min(M, int(self.verify_cap[b]))
 
 
 # --------------------------------------------------------------------------- prefix
@@ -159,12 +220,19 @@ def _tree_pass(w, cfg, K, V, root_pos, pool, nodes, states, s_root, tree_kv):
     return L.layer_tail(w, cfg, hid, o)
 
 
-def draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec: Decisions, b=0):
-    """Draft passes and pool of one request (steps 2-4 up to the kept set)."""
+def draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec: Decisions, b=0,
+                  ctl: Control | None = None, B=1):
+    """Draft passes and pool of one request (steps 2-4 up to the kept set).
+
+    With ``ctl`` the request's branch and depth caps and the depth rule apply
+    (R-16); the pool keeps its layout, with uncreated nodes as -inf slots."""
     k_, D = cfg.topk, cfg.depth
+    kb = ctl.k_for(b, B, k_) if ctl else k_
+    db = ctl.d_for(b, D) if ctl else D
     s_root, h_root = root_forward(w, cfg, K, V, feat_root, tok_root, root_pos)
     pool = Pool()
     states, hs, node_logq, frontiers, tree_kv = {}, {}, {}, [], {}
+    ninf = -np.inf
 
     def expand(depth, nodes, h_rows):
         """LM head on a pass's rows (one call), then each node's k children."""
@@ -177,12 +245,28 @@ def draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec: Decisions, b
                 cand, logq = order, ell - L.logsumexp(ell)
             node_logq[(depth, rank)] = (np.asarray(cand), logq)
             base = 0.0 if parent < 0 else pool.score[parent]
-            for j in dec.children(b, depth, rank, cand, logq, k_):
-                pool.add(cand[j], parent, base + logq[j], depth + 1, logq[j])
+            for jr, j in enumerate(dec.children(b, depth, rank, cand, logq, k_)):
+                if jr < kb:
+                    pool.add(cand[j], parent, base + logq[j], depth + 1, logq[j])
+                else:
+                    pool.add(-1, -1, ninf, depth + 1, ninf)
+
+    def empty_level(depth, n):
+        for _ in range(n):
+            pool.add(-1, -1, ninf, depth + 1, ninf)
 
     expand(0, [-1], h_root[None])
-    frontier = list(range(k_)) if D >= 2 else []
+    frontier = [i for i in range(k_) if np.isfinite(pool.score[i])] if D >= 2 else []
     for t in range(1, D):
+        if ctl is not None and t < db and ctl.tau_depth > 0 and frontier:
+            mass = float(np.sum(np.exp([pool.score[i] for i in frontier])))
+            thr = ctl.tau_depth * ctl.depth_growth ** t * float(ctl.pass_us[t])
+            if not dec.keep_drafting(b, t, mass, thr):
+                db = t
+        if t >= db or not frontier:
+            frontiers.append([])
+            empty_level(t, k_ * k_)
+            continue
         for r, i in enumerate(frontier):
             pool.fwd[i] = (t - 1) * k_ + r
         frontiers.append(list(frontier))
@@ -191,9 +275,11 @@ def draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec: Decisions, b
         for r, i in enumerate(frontier):
             states[i], hs[i] = s[r], h[r]
         expand(t, frontier, h)
+        empty_level(t, (k_ - len(frontier)) * k_)   # frontier slots with no node
         if t + 1 < D:
             sc = np.array(pool.score[base:])
-            frontier = [base + int(j) for j in dec.frontier(b, t + 1, sc, k_)]
+            fin = int(np.isfinite(sc).sum())
+            frontier = [base + int(j) for j in dec.frontier(b, t + 1, sc, k_)][:fin]
     return DraftResult(pool, s_root, h_root, states, hs, node_logq, frontiers)
 
 
@@ -212,14 +298,30 @@ class Tree:
     def children(self, u):
         return [int(c) for c in np.nonzero(self.parent == u)[0]]
 
+    @property
+    def n_real(self) -> int:
+        """Root plus kept nodes (the slots after them are padding)."""
+        return int(np.sum(self.tok >= 0))
+
 
 def build_tree(pool_tok, pool_parent, pool_score, pool_depth, tok_root, root_pos, m,
-               dec: Decisions | None = None, b=0) -> Tree:
-    """Global top-M of the pool, ancestor-closed, in canonical order, with its mask."""
+               dec: Decisions | None = None, b=0, ctl: Control | None = None) -> Tree:
+    """Global top-M of the pool, ancestor-closed, in canonical order, with its mask.
+
+    With ``ctl``: at most the request's verify cap, never an uncreated node, and
+    the verify rule of R-16; the tree is padded to M + 1 slots."""
     dec = dec or Decisions()
     score = np.asarray(pool_score, dtype=np.float64)
     depth = np.asarray(pool_depth)
+    m_slots = m
+    if ctl is not None:
+        m = min(ctl.m_for(b, m), int(np.isfinite(score).sum()))
     sel = [int(i) for i in dec.select(b, score, depth, m)]
+    if ctl is not None and ctl.tau_verify > 0 and len(sel) > 1:
+        gains = np.exp(score[sel])
+        vu = np.asarray(ctl.verify_us, dtype=np.float64)
+        costs = ctl.tau_verify * (vu[1:len(sel) + 1] - vu[:len(sel)])
+        sel = sel[:dec.verify_count(b, gains, costs, len(sel))]
     rank = {p: r for r, p in enumerate(sel)}
     order = sorted(sel, key=lambda p: (depth[p], rank[p]))
     tidx = {p: t + 1 for t, p in enumerate(order)}
@@ -233,27 +335,34 @@ def build_tree(pool_tok, pool_parent, pool_score, pool_depth, tok_root, root_pos
         if pp >= 0 and pp not in tidx:
             raise ValueError("kept set is not ancestor-closed")
         tok[t], par[t], dep[t], sc[t], pidx[t] = pool_tok[p], (0 if pp < 0 else tidx[pp]), depth[p], score[p], p
+    if ctl is not None and n < m_slots + 1:  # padding slots
+        pad = m_slots + 1 - n
+        tok = np.concatenate([tok, np.full(pad, -1)]); par = np.concatenate([par, np.full(pad, -1)])
+        dep = np.concatenate([dep, np.zeros(pad, dtype=np.int64)])
+        sc = np.concatenate([sc, np.full(pad, -np.inf)]); pidx = np.concatenate([pidx, np.full(pad, -1)])
+        n = m_slots + 1
     mask = np.zeros((n, n), dtype=bool)
     for i in range(n):
         j = i
         while j >= 0:
             mask[i, j] = True
-            j = par[j]
+            j = par[j] if (i == 0 or tok[i] >= 0) else -1
     return Tree(tok, par, dep, root_pos + dep, sc, pidx, mask)
 
 
 # --------------------------------------------------------------------------- verify
 def verify_logits(w, cfg, K, V, root_pos, tree: Tree, draft: DraftResult):
-    """Target logits z [M+1, V] of the synthetic target over the kept nodes (R-8)."""
-    n = len(tree.tok)
+    """Target logits z [n, V] of the synthetic target over the root and the kept
+    nodes (R-8); padding slots are not evaluated."""
+    n = tree.n_real
     h = np.empty((n, cfg.d))
     h[0] = draft.h_root
     if n > 1:
         nodes = np.arange(1, n)
         hid = np.stack([draft.s_root if tree.parent[u] == 0 else
                         draft.states[int(tree.pool_index[tree.parent[u]])] for u in nodes])
-        x = L.decoder_input(w, cfg, tree.tok[1:], hid)
-        q, k, v = L.qkv(w, cfg, x, tree.pos[1:])
+        x = L.decoder_input(w, cfg, tree.tok[1:n], hid)
+        q, k, v = L.qkv(w, cfg, x, tree.pos[1:n])
         o = np.empty((n - 1, cfg.n_q_heads * cfg.head_dim))
         for j, u in enumerate(nodes):
             anc = [a - 1 for a in np.nonzero(tree.mask[u])[0] if a > 0]
@@ -319,11 +428,13 @@ class RequestRound:
 
 
 def round_request(w, cfg, K, V, feat_root, tok_root, root_pos, temperatures=(0.0,), seed=0,
-                  round_id=0, dec: Decisions | None = None, b=0, with_verify=True):
+                  round_id=0, dec: Decisions | None = None, b=0, with_verify=True,
+                  ctl: Control | None = None, B=1):
     dec = dec or Decisions()
-    dr = draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec, b)
+    dr = draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec, b, ctl, B)
     p = dr.pool
-    tree = build_tree(p.tok, p.parent, p.score, p.depth, tok_root, root_pos, cfg.n_verify, dec, b)
+    tree = build_tree(p.tok, p.parent, p.score, p.depth, tok_root, root_pos, cfg.n_verify, dec, b,
+                      ctl)
     z, out = None, {}
     if with_verify:
         z, _ = verify_logits(w, cfg, K, V, root_pos, tree, dr)

@@ -496,3 +496,109 @@ def variant_round():
 
 def test_variant_tree_states_equal_sequential_path_forward(variant_round):
     test_tree_states_equal_sequential_path_forward(variant_round)
+
+
+# ----------------------------------------------------------------------------- per-request control
+def _ctl_setup(seed=31, **kw):
+    cfg = CONFIGS[0].scaled(name="ctl_pin", prefix=24, depth=4, topk=3, n_verify=10, **kw)
+    inp = make_inputs(cfg, seed=seed)
+    w = R.weights_f32(inp)
+    f = inp.feats_f32()
+    P = int(inp.prefix_lens[0])
+    K, V = R.prefix_kv(w, cfg, f[:P], inp.tokens[:P])
+
+    def run(ctl=None, B=1):
+        return R.round_request(w, cfg, K, V, f[P - 1], inp.tokens[P - 1], P - 1, temperatures=(0.0,),
+                               ctl=ctl, B=B)
+    return cfg, run
+
+
+def test_control_with_full_caps_and_no_rules_is_the_plain_round():
+    cfg, run = _ctl_setup()
+    a = run()
+    b = run(R.Control(depth_cap=[cfg.depth], topk_cap=[cfg.topk], verify_cap=[cfg.n_verify]))
+    assert a.draft.pool.tok == b.draft.pool.tok and a.draft.pool.fwd == b.draft.pool.fwd
+    np.testing.assert_array_equal(a.tree.tok, b.tree.tok)
+    np.testing.assert_array_equal(a.tree.mask, b.tree.mask)
+    assert a.verify[0.0].out_tokens == b.verify[0.0].out_tokens
+
+
+def test_depth_and_branch_caps_prune_the_pool():
+    cfg, run = _ctl_setup()
+    full = run()
+    d1 = run(R.Control(depth_cap=[1]))
+    made = [i for i, t in enumerate(d1.draft.pool.tok) if t >= 0]
+    assert made == list(range(cfg.topk))                  # only the root's children
+    assert all(np.isneginf(d1.draft.pool.score[i]) for i in range(cfg.topk, len(d1.draft.pool.tok)))
+    assert set(d1.tree.depth[1:d1.tree.n_real]) == {1} and d1.tree.n_real == 1 + cfg.topk
+    k2 = run(R.Control(topk_cap=[2]))
+    p = k2.draft.pool
+    kids = {}
+    for i, (t, par) in enumerate(zip(p.tok, p.parent)):
+        if t >= 0:
+            kids.setdefault(par, []).append(i)
+    assert all(len(v) <= 2 for v in kids.values())
+    # each node keeps its two best children of the uncapped round (same tokens, same order)
+    assert [p.tok[i] for i in kids[-1]] == full.draft.pool.tok[:2]
+
+
+def test_verify_cap_and_rule_keep_a_prefix_of_the_selection_order():
+    cfg, run = _ctl_setup()
+    full = run()
+    p = full.draft.pool
+    order = R.Decisions().select(0, np.asarray(p.score), np.asarray(p.depth), cfg.n_verify)
+    for m in (1, 4, 7):
+        t = run(R.Control(verify_cap=[m])).tree
+        assert t.n_real == m + 1 and len(t.tok) == cfg.n_verify + 1
+        assert sorted(t.pool_index[1:m + 1]) == sorted(int(i) for i in order[:m])
+        assert (t.tok[m + 1:] == -1).all() and (t.parent[m + 1:] == -1).all()
+        assert all(t.mask[u].sum() == 1 and t.mask[u, u] for u in range(m + 1, len(t.tok)))
+    vu = list(np.arange(cfg.n_verify + 1, dtype=np.float64))   # one unit per node
+    assert run(R.Control(tau_verify=1e9, verify_us=vu)).tree.n_real == 2
+    assert run(R.Control(tau_verify=1e-30, verify_us=vu)).tree.n_real == cfg.n_verify + 1
+    # a mid threshold keeps exactly the nodes whose exp(score) clears it, as a prefix
+    sc = np.exp(np.asarray(p.score)[order])
+    thr = float(np.sqrt(sc[3] * sc[4]))
+    if sc[3] > sc[4]:
+        assert run(R.Control(tau_verify=thr, verify_us=vu)).tree.n_real == 1 + 4
+
+
+def test_depth_rule_stops_where_the_frontier_mass_falls_short():
+    cfg, run = _ctl_setup()
+    full = run()
+    p = full.draft.pool
+    masses = [float(np.exp([p.score[i] for i in fr]).sum()) for fr in full.draft.frontiers]
+    pu = [100.0] * cfg.depth
+    assert len(run(R.Control(tau_depth=1e9, pass_us=pu)).draft.frontiers[0]) == 0
+    r = run(R.Control(tau_depth=1e-30, pass_us=pu))
+    assert r.draft.pool.tok == p.tok
+    # threshold between the masses of the frontiers of depth 1 and 2 (growth 1): pass 1 runs, pass 2 not
+    if masses[0] > masses[1]:
+        tau = float(np.sqrt(masses[0] * masses[1])) / 100.0
+        r = run(R.Control(tau_depth=tau, pass_us=pu))
+        assert r.draft.frontiers[0] == full.draft.frontiers[0] and r.draft.frontiers[1] == []
+        assert max(d for d, t in zip(r.draft.pool.depth, r.draft.pool.tok) if t >= 0) == 2
+
+
+def test_branch_rule_uses_the_light_and_heavy_caps():
+    cfg, run = _ctl_setup()
+    ctl = R.Control(light_batch=1, k_light=2, k_heavy=1)
+    for B, k in ((1, 2), (2, 1)):
+        p = run(ctl, B=B).draft.pool
+        assert sum(1 for t in p.tok[:cfg.topk] if t >= 0) == k
+
+
+def test_greedy_on_a_capped_tree_is_the_longest_matching_path():
+    cfg, run = _ctl_setup()
+    tr = run(R.Control(verify_cap=[6], topk_cap=[2])).tree
+    rng = np.random.default_rng(9)
+    z = rng.standard_normal((tr.n_real, cfg.vocab))
+    for u in range(tr.n_real):
+        kids = tr.children(u)
+        if kids:
+            z[u, tr.tok[kids[0]]] = 50.0
+    res = R.verify_greedy(tr, z)
+    best = max((q for q in _all_paths(tr)
+                if all(tr.tok[c] == np.argmax(z[0 if i == 0 else q[i - 1]]) for i, c in enumerate(q))),
+               key=len)
+    assert res.path == best
