@@ -69,6 +69,12 @@ struct eagle3_ctx {
   float *child_z, *vpart, *z_max, *lse, *g_max;
   int n_vparts;
   int* flags;
+  // per-request caps and cost-aware rules (eagle3_set_control)
+  CtlDev ctl{};
+  eagle3_control ctl_host{};
+  float *d_pass_us = nullptr, *d_verify_us = nullptr;
+  int *d_deff = nullptr, *d_active = nullptr;
+  const int* skip = nullptr;  // set while a draft pass t >= 1 is launched: &d_active[t]
   // tcgen05 GEMM plans
   TcGemm* tc = nullptr;
   // CUDA graph of one step (draft round + verify), replayed by eagle3_graph_launch
@@ -88,6 +94,44 @@ struct eagle3_ctx {
 namespace {
 
 bool use_split(const eagle3_ctx* c, int R) { return c->bf && R <= kSplitMaxRows; }
+
+// The control of one call: the context's setting plus the branch cap of this batch size.
+CtlDev round_control(const eagle3_ctx* c, int B) {
+  CtlDev d = c->ctl;
+  if (!d.on) return d;
+  const eagle3_control& h = c->ctl_host;
+  int kc = c->k;
+  if (h.light_batch > 0) kc = std::min(kc, B <= h.light_batch ? h.k_light : h.k_heavy);
+  d.k_call = std::max(1, kc);
+  return d;
+}
+
+// position of x on an ascending grid: index i and weight w of g[i+1] (clamped)
+void grid_pos(const int* g, int n, double x, int& i, double& w) {
+  if (n <= 1 || x <= g[0]) { i = 0; w = 0.0; return; }
+  if (x >= g[n - 1]) { i = n - 2; w = 1.0; return; }
+  i = 0;
+  while (g[i + 1] < x) ++i;
+  w = (x - g[i]) / (double)(g[i + 1] - g[i]);
+}
+
+double table_at(const eagle3_latency_table* t, const float* v, int B, int P, int n) {
+  int ib, ip, in;
+  double wb, wp, wn;
+  grid_pos(t->batch, t->n_batch, B, ib, wb);
+  grid_pos(t->prefix, t->n_prefix, P, ip, wp);
+  grid_pos(t->tokens, t->n_tokens, n, in, wn);
+  double acc = 0.0;
+  for (int a = 0; a < 2; ++a)
+    for (int b = 0; b < 2; ++b)
+      for (int e = 0; e < 2; ++e) {
+        const int xb = std::min(ib + a, t->n_batch - 1), xp = std::min(ip + b, t->n_prefix - 1);
+        const int xn = std::min(in + e, t->n_tokens - 1);
+        const double w = (a ? wb : 1.0 - wb) * (b ? wp : 1.0 - wp) * (e ? wn : 1.0 - wn);
+        if (w != 0.0) acc += w * v[((size_t)xb * t->n_prefix + xp) * t->n_tokens + xn];
+      }
+  return acc;
+}
 
 eagle3_status fail(eagle3_ctx* c, eagle3_status s, const std::string& msg) {
   if (c) c->err = msg;
@@ -137,7 +181,8 @@ void tc_error(eagle3_ctx* c, const char* what);
 void gemm(eagle3_ctx* c, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
           int ldy, int R, bool split, int S, size_t split_stride, cudaStream_t st) {
   if (c->bf) {
-    if (!tc_gemm(c->tc, segs, nseg, X, ldx, K, Y, ldy, R, split, S, split_stride, c->flags, st))
+    if (!tc_gemm(c->tc, segs, nseg, X, ldx, K, Y, ldy, R, split, S, split_stride, c->flags, st,
+                 c->skip))
       tc_error(c, "tcgen05 GEMM rejected its arguments");
     c->launches++;
     return;
@@ -272,6 +317,7 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   a.out = c->o;
   a.split = split;
   a.flags = c->flags;
+  a.skip = c->skip;
   DISPATCH(c, launch_tree_attention, a, st);
   c->launches += 2;
   // r = hid + W_o o ; z = rms(r)
@@ -343,6 +389,7 @@ void draft_head(eagle3_ctx* c, const void* H, int R, bool split, int* tok, float
   }
   HeadParts hp = c->hp;
   hp.R = R;
+  hp.skip = c->skip;
   if (c->bf) {
     if (!tc_lm_head(c->tc, H, R, split, hp, c->flags, st))
       tc_error(c, "tcgen05 LM head rejected its arguments");
@@ -539,6 +586,10 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
   }
   add((void**)&c->d_round, 8);
   add((void**)&c->flags, 64);
+  add((void**)&c->d_pass_us, (size_t)f.depth * 4);
+  add((void**)&c->d_verify_us, (size_t)(f.n_verify + 1) * 4);
+  add((void**)&c->d_deff, (size_t)B * 4);
+  add((void**)&c->d_active, (size_t)(f.depth + 1) * 4);
   size_t total = 0;
   for (auto& p : plan) total += align_up(p.second, 256);
   if (cudaMalloc(&c->arena, total) != cudaSuccess) {
@@ -652,20 +703,25 @@ eagle3_status draft_round_impl(eagle3_ctx* c, int B, int n_new, const int* cu_ne
           use_split(c, total_new), st);
   tail_rows(c, B, 1, c->g, kv, KvTarget{nullptr, nullptr, 0}, c->h_root, sp0, st);
   draft_head(c, c->h_root, B, sp0, c->top_tok, c->top_logq, c->top_lse, st, 0, 1);
-  launch_expand(B, 0, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
+  CtlDev ctl = round_control(c, B);
+  if (ctl.on) cudaMemsetAsync(c->d_active, 0, (size_t)(D + 1) * 4, st);
+  launch_expand(ctl, B, 0, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
                 c->slot_words, c->root_pos, c->n_slots, c->rp, st);
   c->launches++;
-  // passes 1..D-1: the frontier of each depth with the parent's state as hid
+  // passes 1..D-1: the frontier of each depth with the parent's state as hid; with
+  // control on, the heavy kernels of a pass that no request takes part in return at once
   KvTarget tree{c->tk, c->tv, c->n_slots};
   for (int t = 1; t < D; ++t) {
+    c->skip = ctl.on ? c->d_active + t : nullptr;
     kv_rows(c, B * k, nullptr, true, c->S, kv, tree, spk, st);
     tail_rows(c, B, k, c->S, kv, tree, c->h, spk, st);
     draft_head(c, c->h, B * k, spk, c->top_tok, c->top_logq, c->top_lse, st, 1 + (t - 1) * k, k);
-    launch_expand(B, t, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
+    launch_expand(ctl, B, t, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
                   c->slot_words, c->root_pos, c->n_slots, c->rp, st);
     c->launches++;
   }
-  launch_build_tree(B, c->pool_n, c->M, c->pool.tok, c->pool.parent, c->pool.score, c->pool.depth,
+  c->skip = nullptr;
+  launch_build_tree(ctl, B, c->pool_n, c->M, c->pool.tok, c->pool.parent, c->pool.score, c->pool.depth,
                     c->root_tok, c->root_pos, out->tokens, out->parent, out->depth, out->pos,
                     out->pool_index, out->score, out->mask, c->flags, st);
   c->launches++;
@@ -749,7 +805,8 @@ eagle3_status eagle3_build_tree(eagle3_ctx* c, int B, int pool_n, const int* poo
   if (!tree_ok(out)) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad tree output");
   cudaStream_t st = (cudaStream_t)stream;
   c->last = st;
-  launch_build_tree(B, pool_n, c->M, pool_tok, pool_parent, pool_score, pool_depth, root_tok,
+  launch_build_tree(round_control(c, B), B, pool_n, c->M, pool_tok, pool_parent, pool_score,
+                    pool_depth, root_tok,
                     root_pos, out->tokens, out->parent, out->depth, out->pos, out->pool_index,
                     out->score, out->mask, c->flags, st);
   c->launches++;
@@ -972,5 +1029,73 @@ const char* eagle3_last_error(const eagle3_ctx* c) { return c ? c->err.c_str() :
 size_t eagle3_workspace_bytes(const eagle3_ctx* c) { return c ? c->arena_bytes : 0; }
 
 int eagle3_last_launch_count(const eagle3_ctx* c) { return c ? c->launches : 0; }
+
+eagle3_status eagle3_set_control(eagle3_ctx* c, const eagle3_control* ctl) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  if (!ctl) {
+    c->ctl = CtlDev{};
+    c->ctl_host = eagle3_control{};
+    return EAGLE3_OK;
+  }
+  const eagle3_control& h = *ctl;
+  auto ok_f = [](float x) { return x >= 0.f && x < 3.0e38f; };
+  if (!ok_f(h.tau_depth) || !ok_f(h.tau_verify) || !(h.depth_growth > 0.f) || !ok_f(h.depth_growth) ||
+      h.light_batch < 0 || (h.light_batch > 0 && (h.k_light < 1 || h.k_heavy < 1)) ||
+      (h.tau_depth > 0.f && !h.pass_us) || (h.tau_verify > 0.f && !h.verify_us))
+    return fail(c, EAGLE3_ERR_INVALID_ARG, "bad control");
+  if (h.tau_depth > 0.f)
+    for (int t = 0; t < c->D; ++t)
+      if (!ok_f(h.pass_us[t])) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad pass_us");
+  if (h.tau_verify > 0.f)
+    for (int m = 0; m <= c->M; ++m)
+      if (!ok_f(h.verify_us[m])) return fail(c, EAGLE3_ERR_INVALID_ARG, "bad verify_us");
+  if (h.tau_depth > 0.f &&
+      cudaMemcpy(c->d_pass_us, h.pass_us, (size_t)c->D * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+    return fail(c, EAGLE3_ERR_CUDA, "control copy");
+  if (h.tau_verify > 0.f &&
+      cudaMemcpy(c->d_verify_us, h.verify_us, (size_t)(c->M + 1) * 4, cudaMemcpyHostToDevice) !=
+          cudaSuccess)
+    return fail(c, EAGLE3_ERR_CUDA, "control copy");
+  CtlDev d{};
+  d.on = 1;
+  d.depth_cap = h.depth_cap;
+  d.topk_cap = h.topk_cap;
+  d.verify_cap = h.verify_cap;
+  d.k_call = c->k;
+  d.tau_depth = h.tau_depth;
+  d.depth_growth = h.depth_growth;
+  d.tau_verify = h.tau_verify;
+  d.pass_us = c->d_pass_us;
+  d.verify_us = c->d_verify_us;
+  d.d_eff = c->d_deff;
+  d.active = c->d_active;
+  c->ctl = d;
+  c->ctl_host = h;
+  c->ctl_host.pass_us = nullptr;  // copied; the caller's arrays are not kept
+  c->ctl_host.verify_us = nullptr;
+  return EAGLE3_OK;
+}
+
+eagle3_status eagle3_latency_costs(const eagle3_latency_table* t, int B, int P, int depth,
+                                   int topk, int n_verify, float* pass_us, float* verify_us) {
+  if (!t || !pass_us || !verify_us || depth < 1 || topk < 1 || n_verify < 0 || t->n_batch < 1 ||
+      t->n_prefix < 1 || t->n_tokens < 1 || !t->batch || !t->prefix || !t->tokens ||
+      !t->draft_us || !t->verify_us)
+    return EAGLE3_ERR_INVALID_ARG;
+  auto ascending = [](const int* g, int n) {
+    for (int i = 1; i < n; ++i)
+      if (g[i] <= g[i - 1]) return false;
+    return true;
+  };
+  if (!ascending(t->batch, t->n_batch) || !ascending(t->prefix, t->n_prefix) ||
+      !ascending(t->tokens, t->n_tokens))
+    return EAGLE3_ERR_INVALID_ARG;
+  for (int i = 0; i < depth; ++i)
+    pass_us[i] = (float)table_at(t, t->draft_us, B, P, i == 0 ? 1 : topk);
+  verify_us[0] = 0.f;
+  for (int m = 1; m <= n_verify; ++m) verify_us[m] = (float)table_at(t, t->verify_us, B, P, m);
+  return EAGLE3_OK;
+}
 
 }  // extern "C"

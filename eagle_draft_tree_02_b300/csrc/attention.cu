@@ -68,6 +68,7 @@ __device__ __forceinline__ const T* kv_row_ptr(const AttnArgs& a, const void* ca
 template <typename T>
 __global__ void __launch_bounds__(NT) tree_attention_kernel(AttnArgs a, int z_off) {
   pdl_begin();
+  if (a.skip && *a.skip == 0) return;
   extern __shared__ float sm[];
   const int dh = a.dh;
   const int G = a.Hq / a.Hkv;
@@ -307,6 +308,7 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 template <int DH, int KW>
 __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
   pdl_begin();
+  if (a.skip && *a.skip == 0) return;
   constexpr int LD = DH + 8;       // shared row stride (bf16): conflict-free fragment loads
   constexpr int NKT = KC / 8 / KW; // key tiles of 8 per chunk and warp
   constexpr int NDT = DH / 8;      // output tiles of 8 dims
@@ -649,6 +651,7 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
 template <typename T>
 __global__ void attention_combine_kernel(AttnArgs a) {
   pdl_begin();
+  if (a.skip && *a.skip == 0) return;
   __shared__ float wts[256];  // per split: its weight e^{m_s - m} / l
   __shared__ float red[32];
   const int row = blockIdx.x, head = blockIdx.y, tid = threadIdx.x;

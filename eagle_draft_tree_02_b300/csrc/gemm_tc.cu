@@ -52,6 +52,7 @@ struct TcArgs {
   VerifyHeadArgs va;
   LowRankArgs la;
   int* flags;
+  const int* skip;  // if set and *skip == 0 (no request active in the pass), the kernel returns
 };
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(128, 1)
   // of them is requested before the wait for the previous kernel, so their
   // latency overlaps its tail.  The activations follow after the wait.
   const CUtensorMap* mA = seg == 0 ? &mA0 : (seg == 1 ? &mA1 : &mA2);
-  const int pre = (nkb > 0 && warp == 0 && lane == 0) ? min(S, nkb) : 0;
+  const int pre = (nkb > 0 && warp == 0 && lane == 0 && !a.skip) ? min(S, nkb) : 0;
   if (pre) {
     const uint64_t pw = policy_evict_first();
     for (int i = 0; i < pre; ++i) {
@@ -305,6 +306,15 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
   pdl_begin();  // set-up above overlaps the previous kernel's tail
+  if (a.skip && *a.skip == 0) {  // a pass no request takes part in (nothing was requested)
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      __syncwarp();
+      tmem_dealloc(tmem, a.tmem_cols);
+    }
+    return;
+  }
 
   if (nkb > 0 && warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -830,7 +840,8 @@ __global__ void __launch_bounds__(kHeadThreads, 2)
   const uint32_t tmem = *tslot;
   // the first ring of weight stages (of this CTA's first tile) is requested
   // before the wait for the previous kernel; its activations follow after it
-  const int pre = (warp == 0 && lane == 0 && (int)blockIdx.x < a.n_mtiles) ? min(S, a.n_kb) : 0;
+  const int pre =
+      (warp == 0 && lane == 0 && (int)blockIdx.x < a.n_mtiles && !a.hp.skip) ? min(S, a.n_kb) : 0;
   if (pre) {
     const uint64_t pw = policy_evict_first();
     for (int c = 0; c < pre; ++c) {
@@ -841,6 +852,15 @@ __global__ void __launch_bounds__(kHeadThreads, 2)
     }
   }
   pdl_begin();  // set-up above overlaps the previous kernel's tail
+  if (MODE == 1 && a.hp.skip && *a.hp.skip == 0) {  // a pass no request takes part in
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      __syncwarp();
+      tmem_dealloc(tmem, a.tmem_cols);
+    }
+    return;
+  }
   if (MODE == 2) {
     // child events of the tiles this CTA owns: (local row * kmax + child, token)
     if (threadIdx.x == 0) *n_ev_s = 0;
@@ -1195,9 +1215,11 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
 }  // namespace
 
 bool tc_gemm(TcGemm* t, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
-             int ldy, int R, bool split, int S, size_t split_stride, int* flags, cudaStream_t st) {
+             int ldy, int R, bool split, int S, size_t split_stride, int* flags, cudaStream_t st,
+             const int* skip) {
   if (!t || nseg < 1 || nseg > 3 || R <= 0) return false;
   TcArgs args{};
+  args.skip = skip;
   const CUtensorMap* maps[3];
   int tiles = 0;
   for (int i = 0; i < nseg; ++i) {

@@ -38,8 +38,10 @@ int tc_head_parts(int V);
 // `split`, X holds each row r as a (hi, lo) pair of bf16 rows 2r, 2r+1 (see
 // st_act) and the product is taken on their sum.  Returns false (and nothing
 // is launched) on an unusable argument.
+// skip (may be NULL): the launch returns at once if *skip == 0 when it runs
 bool tc_gemm(TcGemm* t, const GemmSeg* segs, int nseg, const void* X, int ldx, int K, float* Y,
-             int ldy, int R, bool split, int S, size_t split_stride, int* flags, cudaStream_t st);
+             int ldy, int R, bool split, int S, size_t split_stride, int* flags, cudaStream_t st,
+             const int* skip = nullptr);
 // The vocabulary heads.  hp.n_parts / a.n_parts must hold at least
 // tc_head_parts(V) partials; on return they give the number written, which
 // the merge kernels read.

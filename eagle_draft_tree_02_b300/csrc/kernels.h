@@ -71,6 +71,7 @@ struct AttnArgs {
   void* out;               // [R][Hq dh] storage type (split rows: see st_act)
   bool split;
   int* flags;
+  const int* skip;  // if set and *skip == 0 (no request active in the pass), the kernels return
 };
 // Launches the key splits (prefix and tree) and their merge: 2 launches.
 template <typename T> void launch_tree_attention(const AttnArgs& a, cudaStream_t st);
@@ -85,6 +86,7 @@ struct HeadParts {
   float* ms;     // [n_parts][R][2]    running max, sum exp
   float* val;    // [n_parts][R][k]
   int* idx;      // [n_parts][R][k]
+  const int* skip;  // if set and *skip == 0 (no request active in the pass), the kernels return
 };
 template <typename T>
 void launch_lm_head_simt(const void* H, const void* W, int R, int V, int d, const HeadParts& hp,
@@ -124,6 +126,17 @@ struct PoolDev {
   float *score, *logq;
   int n;  // pool_n
 };
+// Per-request caps and cost-aware rules of a round (all off when `on` is 0).
+struct CtlDev {
+  int on;
+  const int *depth_cap, *topk_cap, *verify_cap;  // [B] or NULL
+  int k_call;           // branch cap of this call's batch size (the light/heavy rule), <= k
+  float tau_depth, depth_growth, tau_verify;
+  const float* pass_us;    // [D]
+  const float* verify_us;  // [M+1]
+  int* d_eff;           // [B] depth the request runs to (set at pass 0, lowered by the rule)
+  int* active;          // [D + 1] requests active at pass t
+};
 // pass 0 rows: n_new rows per request, or the ragged rows given by cu_new [B+1]
 void launch_plan_root(int B, int n_new, const int* cu_new, int total, int max_new,
                       const int* tokens_new, const int* seq_lens, int n_slots, const RowPlan& rp,
@@ -133,10 +146,10 @@ void launch_next_rows(int B, int D, const int* accept_len, const int* out_tokens
                       int* tokens_new, int* flags, cudaStream_t st);
 void launch_plan_prefill(int rows, int r0, int B, const int* cu_rows, const int* tokens,
                          const int* seq_lens, const RowPlan& rp, cudaStream_t st);
-void launch_expand(int B, int t, int k, int D, const int* top_tok, const float* top_logq,
+void launch_expand(const CtlDev& ctl, int B, int t, int k, int D, const int* top_tok, const float* top_logq,
                    const PoolDev& pool, int* frontier, uint32_t* slot_mask, int slot_words,
                    const int* root_pos, int n_slots, const RowPlan& rp, cudaStream_t st);
-void launch_build_tree(int B, int pool_n, int M, const int* tok, const int* parent,
+void launch_build_tree(const CtlDev& ctl, int B, int pool_n, int M, const int* tok, const int* parent,
                        const float* score, const int* depth, const int* root_tok,
                        const int* root_pos, int* t_tok, int* t_parent, int* t_depth, int* t_pos,
                        int* t_pidx, float* t_score, uint32_t* t_mask, int* flags, cudaStream_t st);

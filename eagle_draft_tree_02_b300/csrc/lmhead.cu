@@ -146,6 +146,7 @@ template <int K>
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(HeadParts hp, int* tok, float* logq,
                                                                    float* lse_out) {
   pdl_begin();
+  if (hp.skip && *hp.skip == 0) return;
   __shared__ float red_m[32], red_s[32];
   __shared__ int red_i[32];
   __shared__ float win_v;

@@ -133,13 +133,14 @@ void launch_plan_prefill(int rows, int r0, int B, const int* cu_rows, const int*
 // depth-t frontier, k rows per request): append the children to the pool,
 // choose the depth-(t+1) frontier if another pass follows, and write that
 // pass's row plan.
-__global__ void expand_kernel(int B, int t, int k, int D, const int* __restrict__ top_tok,
+__global__ void expand_kernel(CtlDev ctl, int B, int t, int k, int D, const int* __restrict__ top_tok,
                               const float* __restrict__ top_logq, PoolDev pool, int* frontier,
                               uint32_t* slot_mask, int slot_words, const int* root_pos,
                               int n_slots, RowPlan rp) {
   pdl_begin();
   __shared__ float sc[256];
   __shared__ int nf[16];
+  __shared__ int s_deff;
   int b = blockIdx.x, tid = threadIdx.x;
   int* ptok = pool.tok + (size_t)b * pool.n;
   int* ppar = pool.parent + (size_t)b * pool.n;
@@ -148,22 +149,51 @@ __global__ void expand_kernel(int B, int t, int k, int D, const int* __restrict_
   float* psc = pool.score + (size_t)b * pool.n;
   float* plq = pool.logq + (size_t)b * pool.n;
   int* fr = frontier + b * k;
+  // depth this request runs to, and its branch cap
+  int kb = k;
+  if (tid == 0) {
+    int de = D;
+    if (ctl.on) {
+      if (t == 0) {
+        if (ctl.depth_cap) de = max(1, min(D, ctl.depth_cap[b]));
+        ctl.d_eff[b] = de;
+      } else {
+        de = ctl.d_eff[b];
+      }
+    }
+    s_deff = de;
+  }
+  if (ctl.on) {
+    kb = ctl.k_call;
+    if (ctl.topk_cap) kb = max(1, min(kb, ctl.topk_cap[b]));
+  }
+  __syncthreads();
+  const bool run = t < s_deff;  // this pass expands the request's frontier
   int n_new = (t == 0) ? k : k * k;
   int base = (t == 0) ? 0 : k + (t - 1) * k * k;
   if (tid < n_new) {
     int i = tid / k, j = tid % k;  // parent's frontier rank, child rank
     int row = (t == 0) ? b : b * k + i;
     int parent = (t == 0) ? -1 : fr[i];
-    float lq = top_logq[(size_t)row * k + j];
-    float s = (parent < 0 ? 0.f : psc[parent]) + lq;
+    const bool real = run && j < kb && (t == 0 || psc[parent] != -INFINITY);
     int idx = base + tid;
-    ptok[idx] = top_tok[(size_t)row * k + j];
-    ppar[idx] = parent;
     pdep[idx] = t + 1;
     pfwd[idx] = -1;
-    psc[idx] = s;
-    plq[idx] = lq;
-    sc[tid] = s;
+    if (real) {
+      float lq = top_logq[(size_t)row * k + j];
+      float s = (parent < 0 ? 0.f : psc[parent]) + lq;
+      ptok[idx] = top_tok[(size_t)row * k + j];
+      ppar[idx] = parent;
+      psc[idx] = s;
+      plq[idx] = lq;
+      sc[tid] = s;
+    } else {  // not created: a cap, the depth rule or an empty frontier slot
+      ptok[idx] = -1;
+      ppar[idx] = -1;
+      psc[idx] = -INFINITY;
+      plq[idx] = -INFINITY;
+      sc[tid] = -INFINITY;
+    }
   }
   __syncthreads();
   if (t + 1 > D - 1) return;  // no further pass
@@ -177,18 +207,44 @@ __global__ void expand_kernel(int B, int t, int k, int D, const int* __restrict_
     if (rank < k) nf[rank] = base + tid;
   }
   __syncthreads();
+  if (tid == 0 && ctl.on) {
+    // the depth rule: draft pass t+1 only while the frontier's confidence mass
+    // pays for the pass; an empty frontier ends the request's drafting too
+    int de = s_deff;
+    float mass = 0.f;
+    for (int r = 0; r < k; ++r) {
+      const float s = psc[nf[r]];
+      if (s != -INFINITY) mass += expf(s);
+    }
+    if (t + 1 < de) {
+      if (mass == 0.f) de = t + 1;
+      else if (ctl.tau_depth > 0.f &&
+               !(mass >= ctl.tau_depth * powf(ctl.depth_growth, (float)(t + 1)) * ctl.pass_us[t + 1]))
+        de = t + 1;
+    }
+    ctl.d_eff[b] = de;
+    s_deff = de;
+    if (t + 1 < de) atomicAdd(ctl.active + t + 1, 1);
+  }
+  __syncthreads();
+  const bool next = t + 1 < s_deff;
   if (tid < k) {
     int r = tid;
     int node = nf[r];
     int slot = t * k + r;  // frontier slot of depth t+1, rank r
-    pfwd[node] = slot;
-    fr[r] = node;
-    int parent = ppar[node];
+    const bool real = next && psc[node] != -INFINITY;
+    int parent = real ? ppar[node] : -1;
+    if (real) {
+      pfwd[node] = slot;
+      fr[r] = node;
+    } else {
+      fr[r] = node;  // an empty slot: its row runs on a placeholder and makes no children
+    }
     int srow_base = b * (1 + n_slots);
     int hid = parent < 0 ? srow_base : srow_base + 1 + pfwd[parent];
     int row = b * k + r;
     rp.kv_b[row] = b;
-    rp.kv_tok[row] = ptok[node];
+    rp.kv_tok[row] = real ? ptok[node] : 0;
     rp.kv_hid[row] = hid;
     rp.kv_pos[row] = root_pos[b] + t + 1;
     rp.kv_dst[row] = slot;
@@ -211,18 +267,18 @@ __global__ void expand_kernel(int B, int t, int k, int D, const int* __restrict_
   }
 }
 
-void launch_expand(int B, int t, int k, int D, const int* top_tok, const float* top_logq,
+void launch_expand(const CtlDev& ctl, int B, int t, int k, int D, const int* top_tok, const float* top_logq,
                    const PoolDev& pool, int* frontier, uint32_t* slot_mask, int slot_words,
                    const int* root_pos, int n_slots, const RowPlan& rp, cudaStream_t st) {
-  launch_pdl(expand_kernel, dim3(B), dim3(256), 0, st, B, t, k, D, top_tok, top_logq, pool, frontier, slot_mask,
-                                   slot_words, root_pos, n_slots, rp);
+  launch_pdl(expand_kernel, dim3(B), dim3(256), 0, st, ctl, B, t, k, D, top_tok, top_logq, pool,
+             frontier, slot_mask, slot_words, root_pos, n_slots, rp);
 }
 
 // ----------------------------------------------------------------------------- tree builder
 // One block per request.  Rank of node i = number of nodes ahead of it in
 // (score desc, depth asc, index asc); the kept set is rank < M.  Canonical
 // position among the kept nodes: (depth asc, rank asc).
-__global__ void build_tree_kernel(int pool_n, int M, const int* __restrict__ tok,
+__global__ void build_tree_kernel(CtlDev ctl, int pool_n, int M, const int* __restrict__ tok,
                                   const int* __restrict__ parent, const float* __restrict__ score,
                                   const int* __restrict__ depth, const int* root_tok,
                                   const int* root_pos, int* t_tok, int* t_parent, int* t_depth,
@@ -253,11 +309,31 @@ __global__ void build_tree_kernel(int pool_n, int M, const int* __restrict__ tok
     }
     if (rank < M) sel[rank] = i;
   }
+  __shared__ int s_mb;
+  if (tid == 0) s_mb = M;
   __syncthreads();
-  for (int q = tid; q < M; q += nt) {
+  if (ctl.on && tid == 0) {
+    // kept count: the request's verify cap, created nodes only, then the
+    // verify rule over the selection order (at least one node)
+    int mb = M;
+    if (ctl.verify_cap) mb = max(1, min(mb, ctl.verify_cap[b]));
+    int nfin = 0;
+    for (int i = 0; i < pool_n; ++i) nfin += ssc[i] != -INFINITY;
+    mb = max(1, min(mb, nfin));
+    if (ctl.tau_verify > 0.f) {
+      int m = 1;
+      while (m < mb && expf(ssc[sel[m]]) >= ctl.tau_verify * (ctl.verify_us[m + 1] - ctl.verify_us[m]))
+        ++m;
+      mb = m;
+    }
+    s_mb = mb;
+  }
+  __syncthreads();
+  const int Mb = s_mb;
+  for (int q = tid; q < Mb; q += nt) {
     int node = sel[q], dd = sdep[node];
     int p = 0;
-    for (int q2 = 0; q2 < M; ++q2) {
+    for (int q2 = 0; q2 < Mb; ++q2) {
       int d2 = sdep[sel[q2]];
       p += (d2 < dd) || (d2 == dd && q2 < q);
     }
@@ -267,7 +343,16 @@ __global__ void build_tree_kernel(int pool_n, int M, const int* __restrict__ tok
   const int M1 = M + 1;
   const size_t tb = (size_t)b * M1;
   int rp = root_pos[b];
-  for (int q = tid; q < M; q += nt) {
+  for (int u = Mb + 1 + tid; u <= M; u += nt) {  // slots past the kept count
+    tpar[u] = -1;
+    t_tok[tb + u] = -1;
+    t_parent[tb + u] = -1;
+    t_depth[tb + u] = 0;
+    t_pos[tb + u] = rp;
+    t_pidx[tb + u] = -1;
+    t_score[tb + u] = -INFINITY;
+  }
+  for (int q = tid; q < Mb; q += nt) {
     int node = sel[q];
     int u = tidx[node];
     int pp = parent[pb + node];
@@ -310,7 +395,7 @@ __global__ void build_tree_kernel(int pool_n, int M, const int* __restrict__ tok
   }
 }
 
-void launch_build_tree(int B, int pool_n, int M, const int* tok, const int* parent,
+void launch_build_tree(const CtlDev& ctl, int B, int pool_n, int M, const int* tok, const int* parent,
                        const float* score, const int* depth, const int* root_tok,
                        const int* root_pos, int* t_tok, int* t_parent, int* t_depth, int* t_pos,
                        int* t_pidx, float* t_score, uint32_t* t_mask, int* flags, cudaStream_t st) {
@@ -320,7 +405,7 @@ void launch_build_tree(int B, int pool_n, int M, const int* tok, const int* pare
     cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
     attr = true;
   }
-  launch_pdl(build_tree_kernel, dim3(B), dim3(512), smem, st, pool_n, M, tok, parent, score, depth, root_tok, root_pos,
+  launch_pdl(build_tree_kernel, dim3(B), dim3(512), smem, st, ctl, pool_n, M, tok, parent, score, depth, root_tok, root_pos,
                                           t_tok, t_parent, t_depth, t_pos, t_pidx, t_score, t_mask,
                                           flags);
 }
@@ -354,7 +439,7 @@ __global__ void plan_verify_kernel(int M, int kmax, const int* t_tok, const int*
       hid += 1 + f;
     }
     rp.kv_b[row] = b;
-    rp.kv_tok[row] = t_tok[tb + u];
+    rp.kv_tok[row] = max(t_tok[tb + u], 0);  // a padding slot (token -1) runs on a placeholder
     rp.kv_hid[row] = hid;
     rp.kv_pos[row] = t_pos[tb + u];
     rp.kv_dst[row] = u;

@@ -55,6 +55,20 @@ class eagle3_pool(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("tok", "parent", "depth", "fwd", "score", "logq", "cand")]
 
 
+class eagle3_control(C.Structure):
+    _fields_ = [("depth_cap", C.c_void_p), ("topk_cap", C.c_void_p), ("verify_cap", C.c_void_p),
+                ("tau_depth", C.c_float), ("depth_growth", C.c_float), ("tau_verify", C.c_float),
+                ("light_batch", C.c_int), ("k_light", C.c_int), ("k_heavy", C.c_int),
+                ("pass_us", C.POINTER(C.c_float)), ("verify_us", C.POINTER(C.c_float))]
+
+
+class eagle3_latency_table(C.Structure):
+    _fields_ = [("n_batch", C.c_int), ("n_prefix", C.c_int), ("n_tokens", C.c_int),
+                ("batch", C.POINTER(C.c_int)), ("prefix", C.POINTER(C.c_int)),
+                ("tokens", C.POINTER(C.c_int)), ("draft_us", C.POINTER(C.c_float)),
+                ("verify_us", C.POINTER(C.c_float))]
+
+
 class eagle3_verify_stats(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("z_max", "lse", "z_argmax", "g_argmax")]
 
@@ -86,6 +100,10 @@ _sig = {
     "eagle3_last_error": (C.c_char_p, [_P]),
     "eagle3_workspace_bytes": (C.c_size_t, [_P]),
     "eagle3_last_launch_count": (C.c_int, [_P]),
+    "eagle3_set_control": (C.c_int, [_P, C.POINTER(eagle3_control)]),
+    "eagle3_latency_costs": (C.c_int, [C.POINTER(eagle3_latency_table), C.c_int, C.c_int, C.c_int,
+                                       C.c_int, C.c_int, C.POINTER(C.c_float),
+                                       C.POINTER(C.c_float)]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(lib, _name)
@@ -195,6 +213,43 @@ def eagle3_workspace_bytes(ctx) -> int:
 
 def eagle3_last_launch_count(ctx) -> int:
     return lib.eagle3_last_launch_count(ctx)
+
+
+def eagle3_set_control(ctx, ctl: eagle3_control | None) -> int:
+    return lib.eagle3_set_control(_P(ctx), C.byref(ctl) if ctl is not None else None)
+
+
+def make_control(depth_cap=None, topk_cap=None, verify_cap=None, tau_depth=0.0, depth_growth=1.0,
+                 tau_verify=0.0, light_batch=0, k_light=8, k_heavy=4, pass_us=None,
+                 verify_us=None) -> eagle3_control:
+    """Marshal the control: caps are device pointers (int or None), costs host sequences."""
+    c = eagle3_control()
+    c.depth_cap, c.topk_cap, c.verify_cap = depth_cap, topk_cap, verify_cap
+    c.tau_depth, c.depth_growth, c.tau_verify = tau_depth, depth_growth, tau_verify
+    c.light_batch, c.k_light, c.k_heavy = light_batch, k_light, k_heavy
+    if pass_us is not None:
+        c._pass = (C.c_float * len(pass_us))(*pass_us)
+        c.pass_us = C.cast(c._pass, C.POINTER(C.c_float))
+    if verify_us is not None:
+        c._verify = (C.c_float * len(verify_us))(*verify_us)
+        c.verify_us = C.cast(c._verify, C.POINTER(C.c_float))
+    return c
+
+
+def eagle3_latency_costs(batch, prefix, tokens, draft_us, verify_us, B, P, depth, topk, n_verify):
+    """Host lookup of one round's costs from a latency table (grids and [nb][np][nt] arrays)."""
+    import numpy as _np
+    t = eagle3_latency_table()
+    g = [(_np.ascontiguousarray(x, dtype=_np.int32)) for x in (batch, prefix, tokens)]
+    v = [(_np.ascontiguousarray(x, dtype=_np.float32)) for x in (draft_us, verify_us)]
+    t.n_batch, t.n_prefix, t.n_tokens = (len(x) for x in g)
+    ip, fp = C.POINTER(C.c_int), C.POINTER(C.c_float)
+    t.batch, t.prefix, t.tokens = (x.ctypes.data_as(ip) for x in g)
+    t.draft_us, t.verify_us = (x.ctypes.data_as(fp) for x in v)
+    pu = (C.c_float * depth)()
+    vu = (C.c_float * (n_verify + 1))()
+    s = lib.eagle3_latency_costs(C.byref(t), B, P, depth, topk, n_verify, pu, vu)
+    return s, list(pu), list(vu)
 
 
 def check(ctx, status: int) -> None:

@@ -167,6 +167,20 @@ class Engine:
         E.check(self.ctx, s)
         self.seq_lens.copy_(torch.from_numpy(self.inp.prefix_lens - 1).to(self.device))
 
+    def set_control(self, depth_cap=None, topk_cap=None, verify_cap=None, **rules):
+        """Per-request caps (host int sequences, copied to the device) and the
+        cost-aware rules (keyword arguments of eagle3_control); no arguments: off."""
+        if depth_cap is None and topk_cap is None and verify_cap is None and not rules:
+            E.check(self.ctx, E.eagle3_set_control(self.ctx, None))
+            return
+        caps = {}
+        for name, v in (("depth_cap", depth_cap), ("topk_cap", topk_cap), ("verify_cap", verify_cap)):
+            if v is not None:
+                caps[name] = torch.tensor(list(v), dtype=torch.int32, device=self.device)
+        self._caps = caps  # kept alive while the control is set
+        ctl = E.make_control(**{k: t.data_ptr() for k, t in caps.items()}, **rules)
+        E.check(self.ctx, E.eagle3_set_control(self.ctx, ctl))
+
     def draft_round(self, with_pool=True, feats_new=None, tokens_new=None):
         f = self.feats_new if feats_new is None else feats_new
         t = self.tokens_new if tokens_new is None else tokens_new

@@ -159,6 +159,61 @@ typedef struct {
   int *z_argmax, *g_argmax;
 } eagle3_verify_stats;
 
+/* Per-request control of the round: caps and the cost-aware rules of the
+ * EAGLE-4 blog's "EAGLE-Harness" paragraph (a warm-up measures draft and
+ * verify times into a lookup table; each round then asks, in three places,
+ * whether the expected extra accepted tokens per extra time clear a
+ * threshold: another draft layer, how many nodes to verify, and how many
+ * branches a node expands -- 8 under light load, 4 under heavy load) and of
+ * its remark that confidence is the product of draft probabilities with a
+ * threshold that rises with depth.  Readings (the blog gives no formula):
+ *   depth:   pass t (t >= 1) runs for request b only while the confidence
+ *            mass of its frontier, sum of exp(score), is at least
+ *            tau_depth * depth_growth^t * pass_us[t];
+ *   verify:  the kept set is the longest prefix of the score order whose i-th
+ *            node has exp(score_i) >= tau_verify * (verify_us[i] -
+ *            verify_us[i-1]), at least one node;
+ *   branch:  a node makes at most k_light children when B <= light_batch,
+ *            else k_heavy.
+ * The caps depth_cap / topk_cap / verify_cap ([max_batch] int32 device arrays,
+ * read when the round runs; NULL = the config's D, k, M) bound each request as
+ * well, so one batch can mix requests of different D, k and M.  A pool node
+ * that is not created has token -1, parent -1 and score / log q -inf; tree
+ * slots past a request's kept count have token -1, parent -1, depth 0, score
+ * -inf and only their own mask bit, and verification ignores them.  A rule is
+ * off while its threshold is 0 (light_batch 0: no branch rule).  When no
+ * request takes part in a pass, its GEMMs, attention and LM head return at
+ * once. */
+typedef struct {
+  const int *depth_cap, *topk_cap, *verify_cap;
+  float tau_depth, depth_growth, tau_verify;
+  int light_batch, k_light, k_heavy;
+  const float* pass_us;   /* host [D]: cost of draft pass t in microseconds (tau_depth > 0) */
+  const float* verify_us; /* host [M+1]: cost of verifying m nodes, verify_us[0] = 0 (tau_verify > 0) */
+} eagle3_control;
+
+/* Set (ctl != NULL) or clear (NULL) the control of later rounds and tree
+ * builds.  The cost arrays are copied (the call synchronizes the device); the
+ * cap arrays are borrowed.  A captured graph keeps the control it was
+ * captured with: capture again after a change. */
+eagle3_status eagle3_set_control(eagle3_ctx* ctx, const eagle3_control* ctl);
+
+/* The warm-up's lookup table: times on ascending grids of batch size B,
+ * prefix length P and tokens per request n (rows of a draft pass, or nodes
+ * verified), [n_batch][n_prefix][n_tokens] row-major, microseconds. */
+typedef struct {
+  int n_batch, n_prefix, n_tokens;
+  const int *batch, *prefix, *tokens;
+  const float *draft_us, *verify_us;
+} eagle3_latency_table;
+
+/* Costs of one round at (B, P) from the table, by trilinear interpolation
+ * (clamped at the grid's ends): pass_us[0] = draft(B, P, 1) (the root pass),
+ * pass_us[t] = draft(B, P, topk) for t = 1..depth-1; verify_us[0] = 0 and
+ * verify_us[m] = verify(B, P, m) for m = 1..n_verify.  Host-only; no GPU. */
+eagle3_status eagle3_latency_costs(const eagle3_latency_table* table, int B, int P, int depth,
+                                   int topk, int n_verify, float* pass_us, float* verify_us);
+
 /* Create a context: checks the config, borrows the weights, allocates the
  * workspace for max_batch requests once (nothing is allocated later) and
  * prepares the kernels' tensor maps.  It synchronizes the device first: the

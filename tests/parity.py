@@ -105,26 +105,58 @@ class Follow(R.Decisions):
     def children(self, b, depth, rank, cand_tokens, logq_row, k):
         own = super().children(b, depth, rank, cand_tokens, logq_row, k)
         base = 0 if depth == 0 else k + (depth - 1) * k * k + rank * k
-        gtok = self.g.pool["tok"][b, base:base + k]
+        gtok = [int(t) for t in self.g.pool["tok"][b, base:base + k] if t >= 0]  # created ones
         pos = {int(t): i for i, t in enumerate(np.asarray(cand_tokens))}
-        if any(int(t) not in pos for t in gtok):
+        if any(t not in pos for t in gtok):
             self.rep.failures.append(("children-token", b, depth, rank))
             return own
-        return self._adopt(("children", b, depth, rank), own, [pos[int(t)] for t in gtok], logq_row, self.tol)
+        n = len(gtok)
+        got = self._adopt(("children", b, depth, rank), [int(x) for x in own[:n]],
+                          [pos[t] for t in gtok], logq_row, self.tol)
+        return list(got) + [int(x) for x in own[n:] if int(x) not in got][:k - n]
 
     def frontier(self, b, depth, scores, k):
         own = super().frontier(b, depth, scores, k)
         base = k + (depth - 2) * k * k
         fwd = self.g.pool["fwd"][b, base:base + k * k]
-        chosen = sorted((int(f), i) for i, f in enumerate(fwd) if f >= 0)
-        return self._adopt(("frontier", b, depth), own, [i for _, i in chosen], scores,
-                           self.tol * depth)
+        chosen = [i for _, i in sorted((int(f), i) for i, f in enumerate(fwd) if f >= 0)]
+        if not chosen:  # the GPU expanded none of them (the request stopped drafting)
+            return own
+        own_real = [int(i) for i in own if np.isfinite(scores[i])]
+        got = self._adopt(("frontier", b, depth), own_real, chosen, scores, self.tol * depth)
+        return got + [int(i) for i in own if not np.isfinite(scores[i])]
+
+    def keep_drafting(self, b, t, mass, threshold):
+        own = super().keep_drafting(b, t, mass, threshold)
+        k = self.cfg.topk
+        lo, hi = (0, k) if t == 1 else (k + (t - 2) * k * k, k + (t - 1) * k * k)
+        gpu = bool((self.g.pool["fwd"][b, lo:hi] >= 0).any())
+        if gpu == own:
+            return own
+        if abs(np.log(max(mass, 1e-300)) - np.log(max(threshold, 1e-300))) < self.tol * t:
+            self.rep.near_ties.append(("keep_drafting", b, t))
+            return gpu
+        self.rep.failures.append(("keep_drafting", b, t, float(mass), float(threshold)))
+        return own
+
+    def verify_count(self, b, gains, costs, m_cap):
+        own = super().verify_count(b, gains, costs, m_cap)
+        gpu = int((self.g.tree["tokens"][b, 1:] >= 0).sum())
+        if gpu == own:
+            return own
+        i = min(own, gpu)  # the comparison where the two part
+        tol = self.tol * self.cfg.depth
+        if i < len(gains) and abs(np.log(max(gains[i], 1e-300)) - np.log(max(costs[i], 1e-300))) < tol:
+            self.rep.near_ties.append(("verify_count", b))
+            return gpu
+        self.rep.failures.append(("verify_count", b, own, gpu))
+        return own
 
     def select(self, b, scores, depths, m):
         own = [int(x) for x in super().select(b, scores, depths, m)]
         rank = {p: r for r, p in enumerate(own)}
         own_tree_order = sorted(own, key=lambda p: (depths[p], rank[p]))
-        gsel = [int(p) for p in self.g.tree["pool_index"][b, 1:]]
+        gsel = [int(p) for p in self.g.tree["pool_index"][b, 1:] if p >= 0]
         if gsel == own_tree_order:
             return own
         tol = self.tol * self.cfg.depth
@@ -175,7 +207,8 @@ class Follow(R.Decisions):
         return self._adopt(("bonus", b, node), [own], [g], scores, self.tol)[0]
 
 
-def compare(cfg, inp, gpu: GpuRound, temps, seed=0, round_id=0, prefix_kv=None, requests=None):
+def compare(cfg, inp, gpu: GpuRound, temps, seed=0, round_id=0, prefix_kv=None, requests=None,
+            ctl=None):
     """Conditioned oracle run and element-wise comparison.  Returns a Report."""
     tol = TOL[cfg.dtype]
     rep = Report()
@@ -189,18 +222,25 @@ def compare(cfg, inp, gpu: GpuRound, temps, seed=0, round_id=0, prefix_kv=None, 
         else:
             K, V = prefix_kv(b)
         dec = Follow(cfg, gpu, rep, tol["tie"])
-        dr = R.draft_request(w, cfg, K, V, feats[hi - 1], inp.tokens[hi - 1], P - 1, dec, b)
+        dr = R.draft_request(w, cfg, K, V, feats[hi - 1], inp.tokens[hi - 1], P - 1, dec, b, ctl,
+                             cfg.batch)
         pool = dr.pool
         n = len(pool.tok)
         # pool: tokens / parents / depth exact; log q and scores within tolerance
         for name, mine in (("tok", pool.tok), ("parent", pool.parent), ("depth", pool.depth)):
             if not np.array_equal(np.asarray(mine), gpu.pool[name][b, :n]):
                 rep.failures.append(("pool-" + name, b))
-        rep.err("logq", np.max(np.abs(np.asarray(pool.logq) - gpu.pool["logq"][b, :n])))
-        dsc = np.abs(np.asarray(pool.score) - gpu.pool["score"][b, :n]) / np.maximum(1, np.asarray(pool.depth))
-        rep.err("score/depth", np.max(dsc))
+        made = np.asarray(pool.tok) >= 0  # created nodes (the rest hold -inf)
+        if not (np.isneginf(gpu.pool["score"][b, :n][~made]).all()
+                and np.isneginf(gpu.pool["logq"][b, :n][~made]).all()):
+            rep.failures.append(("pool-uncreated", b))
+        if made.any():
+            rep.err("logq", np.max(np.abs(np.asarray(pool.logq)[made] - gpu.pool["logq"][b, :n][made])))
+            dsc = (np.abs(np.asarray(pool.score)[made] - gpu.pool["score"][b, :n][made])
+                   / np.maximum(1, np.asarray(pool.depth)[made]))
+            rep.err("score/depth", np.max(dsc))
         tree = R.build_tree(pool.tok, pool.parent, pool.score, pool.depth, inp.tokens[hi - 1], P - 1,
-                            cfg.n_verify, dec, b)
+                            cfg.n_verify, dec, b, ctl)
         for name, mine in (("tokens", tree.tok), ("parent", tree.parent), ("depth", tree.depth),
                            ("pos", tree.pos), ("pool_index", tree.pool_index)):
             if not np.array_equal(np.asarray(mine), gpu.tree[name][b]):
@@ -217,9 +257,10 @@ def compare(cfg, inp, gpu: GpuRound, temps, seed=0, round_id=0, prefix_kv=None, 
         z, _ = R.verify_logits(w, cfg, K, V, P - 1, tree, dr)
         for T in temps:
             st = gpu.verify[T]["stats"]
-            rep.err("z_max", np.max(np.abs(z.max(axis=1) - st["z_max"][b])))
+            nr = z.shape[0]  # the root and the kept nodes (padding slots are not verified)
+            rep.err("z_max", np.max(np.abs(z.max(axis=1) - st["z_max"][b][:nr])))
             zt = z / (T if T else 1.0)
-            rep.err("lse", np.max(np.abs(L.logsumexp(zt) - st["lse"][b])))
+            rep.err("lse", np.max(np.abs(L.logsumexp(zt) - st["lse"][b][:nr])))
             dec.T = T
             res = (R.verify_greedy(tree, z, dec, b) if T == 0 else
                    R.verify_sample(tree, z, T, seed, round_id, dec, b))

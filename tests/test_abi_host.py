@@ -91,3 +91,40 @@ def test_graph_calls_need_a_context(E):
     kv, tree = E.eagle3_kv(), E.eagle3_tree()
     assert E.eagle3_graph_launch(0, 0, 0) == E.ERR_INVALID_ARG
     assert E.eagle3_graph_capture(0, 1, 1, 1, 1, kv, tree, 1, 0, 1.0, 0, 1, 1, 1, 0) == E.ERR_INVALID_ARG
+
+
+def test_latency_costs_match_scipy_grid_interpolation(E):
+    """The warm-up table's lookup is trilinear interpolation clamped at the grid's
+    ends: checked against scipy's RegularGridInterpolator (an independent routine)."""
+    import numpy as np
+    from scipy.interpolate import RegularGridInterpolator
+    rng = np.random.default_rng(3)
+    batch, prefix, tokens = [1, 4, 16, 64], [256, 1024, 4096], [1, 2, 4, 8, 16, 32, 64]
+    shape = (len(batch), len(prefix), len(tokens))
+    draft = rng.uniform(50, 500, shape).astype(np.float32)
+    verify = rng.uniform(100, 900, shape).astype(np.float32)
+    fd = RegularGridInterpolator((batch, prefix, tokens), draft.astype(np.float64))
+    fv = RegularGridInterpolator((batch, prefix, tokens), verify.astype(np.float64))
+
+    def at(f, b, p, n):
+        pt = [min(max(b, batch[0]), batch[-1]), min(max(p, prefix[0]), prefix[-1]),
+              min(max(n, tokens[0]), tokens[-1])]
+        return float(f([pt])[0])
+    for B, P in ((1, 256), (3, 700), (64, 4096), (100, 9000), (7, 100), (16, 2048)):
+        depth, topk, M = 6, 10, 60
+        s, pu, vu = E.eagle3_latency_costs(batch, prefix, tokens, draft, verify, B, P, depth, topk, M)
+        assert s == E.OK
+        np.testing.assert_allclose(pu[0], at(fd, B, P, 1), rtol=1e-5)
+        np.testing.assert_allclose(pu[1:], [at(fd, B, P, topk)] * (depth - 1), rtol=1e-5)
+        assert vu[0] == 0.0
+        np.testing.assert_allclose(vu[1:], [at(fv, B, P, m) for m in range(1, M + 1)], rtol=1e-5)
+
+
+def test_latency_costs_and_control_reject_bad_arguments(E):
+    import numpy as np
+    g = np.ones((2, 1, 1), dtype=np.float32)
+    assert E.eagle3_latency_costs([4, 1], [8], [1], g, g, 1, 8, 2, 1, 1)[0] == E.ERR_INVALID_ARG
+    assert E.eagle3_latency_costs([1, 4], [8], [1], g, g, 1, 8, 0, 1, 1)[0] == E.ERR_INVALID_ARG
+    assert E.eagle3_latency_costs([1, 4], [8], [1], g, g, 1, 8, 2, 1, 1)[0] == E.OK
+    assert E.eagle3_set_control(0, None) == E.ERR_INVALID_ARG
+    assert E.eagle3_set_control(0, E.make_control(tau_depth=1.0)) == E.ERR_INVALID_ARG
