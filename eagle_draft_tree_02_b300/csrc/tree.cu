@@ -291,24 +291,49 @@ __global__ void build_tree_kernel(CtlDev ctl, int pool_n, int M, const int* __re
   int* tidx = sdep + pool_n;            // [pool_n] tree index of a kept node, else 0x7fffffff
   int* sel = tidx + pool_n;             // [M] pool index by rank
   int* tpar = sel + M;                  // [M+1] tree parent
+  // [P2] sort keys, P2 = the power of two >= pool_n (8-byte aligned after tpar)
+  unsigned long long* key =
+      reinterpret_cast<unsigned long long*>(smi + ((3 * pool_n + 2 * M + 1 + 1) & ~1));
+  int P2 = 1;
+  while (P2 < pool_n) P2 <<= 1;
   int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
   const size_t pb = (size_t)b * pool_n;
-  for (int i = tid; i < pool_n; i += nt) {
-    ssc[i] = score[pb + i];
-    sdep[i] = depth[pb + i];
-    tidx[i] = 0x7fffffff;
+  for (int i = tid; i < P2; i += nt) {
+    if (i < pool_n) {
+      const float sc = score[pb + i];
+      const int dp = depth[pb + i];
+      ssc[i] = sc;
+      sdep[i] = dp;
+      tidx[i] = 0x7fffffff;
+      // larger key = earlier in (score desc, depth asc, index asc)
+      const uint32_t u = __float_as_uint(sc == 0.f ? 0.f : sc);  // -0 ties with +0
+      const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+      key[i] = ((unsigned long long)o << 32) |
+               ((unsigned long long)(255 - min(max(dp, 0), 255)) << 24) |
+               (unsigned long long)(0xFFFFFFu - (uint32_t)i);
+    } else {
+      key[i] = 0ull;  // padding sorts last
+    }
   }
   __syncthreads();
-  for (int i = tid; i < pool_n; i += nt) {
-    float s = ssc[i];
-    int dd = sdep[i];
-    int rank = 0;
-    for (int j = 0; j < pool_n; ++j) {
-      float sj = ssc[j];
-      rank += (sj > s) || (sj == s && (sdep[j] < dd || (sdep[j] == dd && j < i)));
+  // bitonic sort, descending: rank r of the order is key[r]
+  for (int k = 2; k <= P2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < P2; i += nt) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = key[i], c = key[ixj];
+          if (((i & k) == 0) ? (a < c) : (a > c)) {
+            key[i] = c;
+            key[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
     }
-    if (rank < M) sel[rank] = i;
   }
+  for (int r = tid; r < M && r < pool_n; r += nt)
+    sel[r] = (int)(0xFFFFFFu - (uint32_t)(key[r] & 0xFFFFFFull));
   __shared__ int s_mb;
   if (tid == 0) s_mb = M;
   __syncthreads();
@@ -399,7 +424,9 @@ void launch_build_tree(const CtlDev& ctl, int B, int pool_n, int M, const int* t
                        const float* score, const int* depth, const int* root_tok,
                        const int* root_pos, int* t_tok, int* t_parent, int* t_depth, int* t_pos,
                        int* t_pidx, float* t_score, uint32_t* t_mask, int* flags, cudaStream_t st) {
-  size_t smem = (size_t)(3 * pool_n + M + M + 1) * sizeof(int);
+  int P2 = 1;
+  while (P2 < pool_n) P2 <<= 1;
+  size_t smem = (size_t)((3 * pool_n + 2 * M + 1 + 1) & ~1) * sizeof(int) + (size_t)P2 * 8;
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
@@ -488,6 +515,16 @@ __global__ void copy_rows_kernel(int row_bytes, const char* src, size_t src_step
   const int b = blockIdx.x;
   const char* sr = src + b * src_step;
   char* dr = dst + b * dst_step;
+  if (row_bytes % 16 == 0) {  // rows of d * element-size bytes: 16-byte pieces
+    const int n = row_bytes / 16;
+    const uint4* s4 = reinterpret_cast<const uint4*>(sr);
+    uint4* d4 = reinterpret_cast<uint4*>(dr);
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      d4[i] = s4[i];
+      if (dst_split) d4[n + i] = src_split ? s4[n + i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
   for (int i = threadIdx.x; i < row_bytes; i += blockDim.x) {
     dr[i] = sr[i];
     if (dst_split) dr[row_bytes + i] = src_split ? sr[row_bytes + i] : 0;

@@ -217,6 +217,49 @@ class Engine:
         st = stream if stream is not None else self.stream()
         E.check(self.ctx, E.eagle3_graph_launch(self.ctx, round_id, st))
 
+    def warmup_latency_table(self, reps=3):
+        """The EAGLE-Harness warm-up at this engine's batch size and prefix: draft
+        rounds under depth caps 1..D give the root pass and the later passes'
+        cost (by difference), verification under verify caps 1 and M the verify
+        cost.  Returns (batch, prefix, tokens, draft_us, verify_us) for
+        eagle3_latency_costs; tokens = [1, k, M] (k and M merged if equal)."""
+        cfg, dev = self.cfg, self.device
+        st = torch.cuda.current_stream(dev)
+
+        def timed(fn):
+            fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            for _ in range(reps):
+                fn()
+            b.record(st)
+            b.synchronize()
+            return a.elapsed_time(b) * 1e3 / reps  # microseconds
+
+        t_round = []
+        for d in range(1, cfg.depth + 1):
+            self.set_control(depth_cap=[d] * self.B)
+            t_round.append(timed(lambda: self.draft_round(with_pool=False)))
+        self.set_control()
+        root = t_round[0]
+        # on launch-bound shapes a pass costs nothing measurable: the difference is noise
+        later = max(0.0, (t_round[-1] - t_round[0]) / max(1, cfg.depth - 1))
+        t_ver = {}
+        for m in sorted({1, cfg.n_verify}):
+            self.set_control(verify_cap=[m] * self.B)
+            self.draft_round(with_pool=False)
+            t_ver[m] = timed(lambda: self.verify(0.0, with_stats=False))
+        self.set_control()
+        tokens = sorted({1, cfg.topk, cfg.n_verify})
+        draft = [root if n == 1 else later for n in tokens]
+        verify = [t_ver[1] if n == 1 else t_ver[cfg.n_verify] if n >= cfg.n_verify else
+                  t_ver[1] + (t_ver[cfg.n_verify] - t_ver[1]) * (n - 1) / max(1, cfg.n_verify - 1)
+                  for n in tokens]
+        shape = (1, 1, len(tokens))
+        return ([self.B], [int(self.max_prefix)], tokens,
+                np.asarray(draft, dtype=np.float32).reshape(shape),
+                np.asarray(verify, dtype=np.float32).reshape(shape))
+
     def check(self):
         E.check(self.ctx, E.eagle3_check(self.ctx))
 

@@ -93,3 +93,31 @@ def test_control_survives_graph_replay(cuda, lib_built):
         assert torch.equal(eng.out_tokens, want[2])
     eng.set_control()
     eng.close()
+
+
+@pytest.mark.gpu
+def test_warmup_table_feeds_the_depth_rule(cuda, lib_built):
+    """The warm-up measures the passes on the device; its table, looked up for the
+    engine's shape, gives the depth rule positive pass costs, and a threshold far
+    above any frontier mass stops every request after the root pass."""
+    from eagle_draft_tree_02_b300 import eagle3 as E
+    from eagle_draft_tree_02_b300.runner import Engine
+    cfg = SMALL_BF16
+    inp = make_inputs(cfg, seed=23)
+    eng = Engine(inp)
+    eng.prefill()
+    batch, prefix, tokens, draft_us, verify_us = eng.warmup_latency_table(reps=2)
+    # the root pass and verification cost time; a later pass may cost nothing
+    # measurable on a shape this small (every kernel is launch-bound)
+    assert draft_us[0, 0, 0] > 0 and (draft_us >= 0).all() and (verify_us > 0).all()
+    s, pu, vu = E.eagle3_latency_costs(batch, prefix, tokens, draft_us, verify_us, eng.B,
+                                       int(eng.max_prefix), cfg.depth, cfg.topk, cfg.n_verify)
+    assert s == E.OK and vu[0] == 0.0
+    assert pu[0] == pytest.approx(float(draft_us[0, 0, 0]))
+    assert vu[cfg.n_verify] == pytest.approx(float(verify_us[0, 0, tokens.index(cfg.n_verify)]))
+    eng.set_control(tau_depth=1e6, pass_us=[max(x, 1.0) for x in pu])
+    gpu = gpu_round(eng, (0.0,), seed=1, round_id=1)
+    made = gpu.pool["tok"] >= 0
+    assert (np.where(made, gpu.pool["depth"], 0).max(axis=1) == 1).all()
+    eng.set_control()
+    eng.close()
