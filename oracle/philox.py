@@ -15,9 +15,10 @@ design notes).  Use for the round:
     acceptance test i at node (b, node), stream 0:
         counter = (round_id, b * 2**32 + node, i, 0)
         U  = (w0 >> 40) * 2**-24                   (w0: the first output word)
-    Gumbel noise of token x at node (b, node), stream 1: one block serves
-    four tokens,
-        counter = (round_id, b * 2**32 + node, x // 4, 1)
+    Gumbel noise of token x at node (b, node), stream 1 (stream 2 for the
+    children of a sampled draft, node = the expanded node's slot): one block
+    serves four tokens,
+        counter = (round_id, b * 2**32 + node, x // 4, stream)
         U' = ((w >> 40) + 0.5) * 2**-24            (w: output word x % 4)
         gumbel = -log(-log U')
 
@@ -104,11 +105,12 @@ def uniform(seed, round_id, b, node, idx):
     return (w >> np.uint64(40)).astype(np.float64) * 2.0 ** -24
 
 
-def gumbel(seed, round_id, b, node, idx):
-    """Gumbel(0, 1) noise of token idx from stream 1: word idx % 4 of block idx // 4,
-    through the open-interval uniform U'."""
+def gumbel(seed, round_id, b, node, idx, stream=1):
+    """Gumbel(0, 1) noise of token idx: word idx % 4 of block idx // 4 of the
+    stream (1: the verify step's residual draw; 2: the sampled draft's children,
+    node = the expanded node's slot), through the open-interval uniform U'."""
     idx = np.asarray(idx, dtype=np.uint64)
-    ws = _words(seed, round_id, b, node, idx >> np.uint64(2), 1)
+    ws = _words(seed, round_id, b, node, idx >> np.uint64(2), stream)
     w = np.choose((idx & np.uint64(3)).astype(np.int64), ws)
     u = ((w >> np.uint64(40)).astype(np.float64) + 0.5) * 2.0 ** -24
     return -np.log(-np.log(u))

@@ -52,6 +52,16 @@ A node that a cap or rule leaves out is not created: its pool slot holds token
 -1, parent -1, score and log q -inf.  Tree slots past the kept count hold
 token -1, parent -1, depth 0, score -inf and only their own mask bit.
 
+Sampled drafting with q-ratio verification (R-17; §8(f) f3: "children sampled
+from q"; "EAGLE-3 精读" §5: sampling keeps the target distribution with the
+residual correction): a node's k children are drawn from q without
+replacement by Gumbel-top-k (Philox stream 2 at the node's slot), in draw
+order; a child's score is clipped to be non-increasing in draw order, so a
+kept sibling set is always the first draws.  Verification walks the draws:
+the i-th is accepted when U q_i(c) < p_i(c); on rejection p_{i+1} =
+norm(max(0, p_i - q_i)) and q_{i+1} = q_i without c; with no acceptance the
+bonus is the Gumbel-argmax of log p over its support (stream 1).
+
 Every decision goes through a ``Decisions`` object.  The plain class takes the
 oracle's own choice; tests may pass a subclass that, where the oracle's margin
 is inside a stated tolerance, adopts another valid choice (conditioned mode).
@@ -99,6 +109,10 @@ class Decisions:
     def bonus(self, b, node, scores):
         """Gumbel-argmax (scores already hold -inf at excluded tokens)."""
         return int(np.argmax(scores))
+
+    def accept_q(self, b, node, i, u, q_child, p_child):
+        """q-ratio test of the i-th draw: accept when U q_i(c) < p_i(c)."""
+        return u * q_child < p_child
 
     def keep_drafting(self, b, t, mass, threshold):
         """Cost-aware depth rule: run pass t (mass = the frontier's sum of exp(score))."""
@@ -221,11 +235,12 @@ def _tree_pass(w, cfg, K, V, root_pos, pool, nodes, states, s_root, tree_kv):
 
 
 def draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec: Decisions, b=0,
-                  ctl: Control | None = None, B=1):
+                  ctl: Control | None = None, B=1, samp=None):
     """Draft passes and pool of one request (steps 2-4 up to the kept set).
 
     With ``ctl`` the request's branch and depth caps and the depth rule apply
-    (R-16); the pool keeps its layout, with uncreated nodes as -inf slots."""
+    (R-16); the pool keeps its layout, with uncreated nodes as -inf slots.
+    With ``samp = (seed, round_id)`` the children are sampled (R-17)."""
     k_, D = cfg.topk, cfg.depth
     kb = ctl.k_for(b, B, k_) if ctl else k_
     db = ctl.d_for(b, D) if ctl else D
@@ -245,9 +260,18 @@ def draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec: Decisions, b
                 cand, logq = order, ell - L.logsumexp(ell)
             node_logq[(depth, rank)] = (np.asarray(cand), logq)
             base = 0.0 if parent < 0 else pool.score[parent]
-            for jr, j in enumerate(dec.children(b, depth, rank, cand, logq, k_)):
+            if samp is None:
+                order = dec.children(b, depth, rank, cand, logq, k_)
+            else:  # Gumbel-top-k: k draws without replacement, in draw order
+                slot = 0 if depth == 0 else 1 + (depth - 1) * k_ + rank
+                keys = logq + philox.gumbel(samp[0], samp[1], b, slot, np.asarray(cand), stream=2)
+                order = dec.children(b, depth, rank, cand, keys, k_)
+            run_min = 0.0
+            for jr, j in enumerate(order):
                 if jr < kb:
-                    pool.add(cand[j], parent, base + logq[j], depth + 1, logq[j])
+                    run_min = logq[j] if samp is None or jr == 0 else min(run_min, logq[j])
+                    pool.add(cand[j], parent, base + (logq[j] if samp is None else run_min),
+                             depth + 1, logq[j])
                 else:
                     pool.add(-1, -1, ninf, depth + 1, ninf)
 
@@ -418,6 +442,42 @@ def verify_sample(tree: Tree, z, temperature, seed, round_id, dec: Decisions | N
         path.append(u)
 
 
+def verify_qratio(tree: Tree, z, ell, temperature, seed, round_id, dec: Decisions | None = None,
+                  b=0) -> VerifyResult:
+    """Recursive rejection of sampled children against the draft q (R-17): the
+    draws of a node in draw order (pool index), p_i and q_i updated on each
+    rejection, the bonus drawn from the last residual."""
+    dec = dec or Decisions()
+    zt = np.asarray(z, dtype=np.float64) / temperature
+    ell = np.asarray(ell, dtype=np.float64)
+    u, path = 0, []
+    while True:
+        p = np.exp(zt[u] - L.logsumexp(zt[u]))
+        q = np.exp(ell[u] - L.logsumexp(ell[u]))
+        kids = sorted(tree.children(u), key=lambda c: int(tree.pool_index[c]))
+        taken = None
+        for i, c in enumerate(kids):
+            x = int(tree.tok[c])
+            U = float(philox.uniform(seed, round_id, b, u, i))
+            if dec.accept_q(b, u, i, U, q[x], p[x]):
+                taken = c
+                break
+            r = np.maximum(p - q, 0.0)
+            if r.sum() > 0:
+                p = r / r.sum()
+            q[x] = 0.0
+            if q.sum() > 0:
+                q = q / q.sum()
+        if taken is None:
+            g = philox.gumbel(seed, round_id, b, u, np.arange(zt.shape[1]))
+            with np.errstate(divide="ignore"):
+                sc = np.where(p > 0, np.log(p) + g, -np.inf)
+            x = dec.bonus(b, u, sc)
+            return VerifyResult(len(path), path, [int(tree.tok[q_]) for q_ in path] + [x])
+        u = taken
+        path.append(u)
+
+
 # --------------------------------------------------------------------------- whole round
 @dataclass
 class RequestRound:
@@ -429,18 +489,25 @@ class RequestRound:
 
 def round_request(w, cfg, K, V, feat_root, tok_root, root_pos, temperatures=(0.0,), seed=0,
                   round_id=0, dec: Decisions | None = None, b=0, with_verify=True,
-                  ctl: Control | None = None, B=1):
+                  ctl: Control | None = None, B=1, samp=None):
+    """One request's round.  With ``samp = (draft_seed, draft_round)`` the children
+    are sampled and T > 0 verification is the q-ratio scheme (R-17)."""
     dec = dec or Decisions()
-    dr = draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec, b, ctl, B)
+    dr = draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec, b, ctl, B, samp)
     p = dr.pool
     tree = build_tree(p.tok, p.parent, p.score, p.depth, tok_root, root_pos, cfg.n_verify, dec, b,
                       ctl)
     z, out = None, {}
     if with_verify:
-        z, _ = verify_logits(w, cfg, K, V, root_pos, tree, dr)
+        z, hv = verify_logits(w, cfg, K, V, root_pos, tree, dr)
+        ell = L.linear(hv, w["w_lm"]) if samp is not None else None
         for T in temperatures:
-            out[T] = (verify_greedy(tree, z, dec, b) if T == 0 else
-                      verify_sample(tree, z, T, seed, round_id, dec, b))
+            if T == 0:
+                out[T] = verify_greedy(tree, z, dec, b)
+            elif samp is None:
+                out[T] = verify_sample(tree, z, T, seed, round_id, dec, b)
+            else:
+                out[T] = verify_qratio(tree, z, ell, T, seed, round_id, dec, b)
     return RequestRound(dr, tree, z, out)
 
 

@@ -602,3 +602,84 @@ def test_greedy_on_a_capped_tree_is_the_longest_matching_path():
                 if all(tr.tok[c] == np.argmax(z[0 if i == 0 else q[i - 1]]) for i, c in enumerate(q))),
                key=len)
     assert res.path == best
+
+
+# ----------------------------------------------------------------------------- sampled drafting, q-ratio verify
+def _single_node_emissions(p, q, k, n, scheme, seed=5, sampled=True):
+    """Emitted token of a root with k children (drawn from q by Gumbel-top-k, or
+    the top-k of q), over n round ids, verified by the q-ratio or point-mass scheme."""
+    V = len(p)
+    out = np.empty(n, dtype=np.int64)
+    zrow, erow = np.log(p), np.log(q)
+    for rid in range(n):
+        keys = erow + philox.gumbel(seed, rid, 0, 0, np.arange(V), stream=2) if sampled else erow
+        kids = L.topk_order(keys, k)
+        tok = np.concatenate([[0], kids])
+        tr = R.Tree(tok, np.array([-1] + [0] * k), np.array([0] + [1] * k), np.zeros(k + 1),
+                    np.zeros(k + 1), np.array([-1] + list(range(k))), np.eye(k + 1, dtype=bool))
+        z = np.tile(zrow, (k + 1, 1))
+        if scheme == "qratio":
+            r = R.verify_qratio(tr, z, np.tile(erow, (k + 1, 1)), 1.0, seed, rid)
+        else:
+            r = R.verify_sample(tr, z, 1.0, seed, rid)
+        out[rid] = r.out_tokens[0]
+    return out
+
+
+def _chi2_p(samples, probs):
+    counts = np.bincount(samples, minlength=len(probs))
+    return stats.chisquare(counts, len(samples) * probs).pvalue
+
+
+def test_sampled_children_first_draw_follows_q():
+    """Gumbel-top-k over Philox stream 2: the first draw of a node is distributed as q."""
+    rng = np.random.default_rng(2)
+    q = rng.dirichlet(np.ones(8))
+    first = np.array([int(np.argmax(np.log(q) + philox.gumbel(7, rid, 0, 3, np.arange(8), stream=2)))
+                      for rid in range(20000)])
+    assert _chi2_p(first, q) > 1e-3
+
+
+def test_qratio_verification_emits_the_target_distribution():
+    """Exactness of recursive rejection over draws without replacement (R-17):
+    the emitted token is distributed as p for any draft q (chi-square, 7 dof)."""
+    rng = np.random.default_rng(4)
+    p = rng.dirichlet(np.ones(8))
+    q = rng.dirichlet(0.5 * np.ones(8))
+    assert _chi2_p(_single_node_emissions(p, q, 3, 20000, "qratio"), p) > 1e-3
+
+
+def test_qratio_on_top_k_children_is_biased_but_point_masses_are_not():
+    """Planted mistake: the q-ratio scheme on deterministic top-k children (not
+    draws from q) does not emit p, and the same chi-square sees it; the
+    point-mass scheme of the plain round is exact for any candidate set."""
+    p = np.array([0.30, 0.25, 0.15, 0.10, 0.08, 0.06, 0.04, 0.02])
+    q = np.array([0.02, 0.04, 0.06, 0.08, 0.10, 0.15, 0.25, 0.30])
+    assert _chi2_p(_single_node_emissions(p, q, 3, 20000, "qratio", sampled=False), p) < 1e-3
+    assert _chi2_p(_single_node_emissions(p, q, 3, 20000, "point", sampled=True), p) > 1e-3
+
+
+def test_sampled_round_keeps_sibling_prefixes_in_draw_order():
+    cfg = CONFIGS[0].scaled(name="samp_pin", prefix=24, depth=4, topk=3, n_verify=7)
+    inp = make_inputs(cfg, seed=33)
+    w = R.weights_f32(inp)
+    f = inp.feats_f32()
+    P = int(inp.prefix_lens[0])
+    K, V = R.prefix_kv(w, cfg, f[:P], inp.tokens[:P])
+    rr = R.round_request(w, cfg, K, V, f[P - 1], inp.tokens[P - 1], P - 1, temperatures=(0.0, 1.0),
+                         samp=(9, 2))
+    p = rr.draft.pool
+    kept = set(int(i) for i in rr.tree.pool_index[1:] if i >= 0)
+    by_parent = {}
+    for i, par in enumerate(p.parent):
+        if p.tok[i] >= 0:
+            by_parent.setdefault(par, []).append(i)
+    for par, sib in by_parent.items():
+        sc = [p.score[i] for i in sib]
+        assert all(a >= b for a, b in zip(sc, sc[1:]))          # non-increasing in draw order
+        mine = [i in kept for i in sib]
+        assert mine == sorted(mine, reverse=True)              # kept siblings: first draws
+    # the sampled children differ from the top-k ones somewhere, yet every token is a valid index
+    plain = R.round_request(w, cfg, K, V, f[P - 1], inp.tokens[P - 1], P - 1, with_verify=False)
+    assert p.tok != plain.draft.pool.tok
+    assert all(0 <= t < cfg.vocab for t in p.tok if t >= 0)
