@@ -39,6 +39,7 @@ class RoundConfig:
     fc_norm: bool = False   # drafter variant: RMSNorm (gain g_fc) on the fused feature
     post_norm: bool = False # drafter variant: norms after the residual adds
     gain_std: float = 0.0   # RMSNorm gains ~ 1 + N(0, gain_std^2) (0: all gains 1)
+    sampled_draft: bool = False  # children drawn from q; T > 0 verification by the q-ratio test
 
     @property
     def pool_size(self) -> int:

@@ -75,6 +75,11 @@ struct eagle3_ctx {
   float *d_pass_us = nullptr, *d_verify_us = nullptr;
   int *d_deff = nullptr, *d_active = nullptr;
   const int* skip = nullptr;  // set while a draft pass t >= 1 is launched: &d_active[t]
+  // sampled draft (EAGLE3_SAMPLED_DRAFT): logits [rows][V] and the walk's work rows
+  bool sampled = false;
+  unsigned long long draft_seed = 0;
+  unsigned long long* d_draft_round = nullptr;
+  float *lg = nullptr, *pqw = nullptr;
   // tcgen05 GEMM plans
   TcGemm* tc = nullptr;
   // CUDA graph of one step (draft round + verify), replayed by eagle3_graph_launch
@@ -98,6 +103,7 @@ bool use_split(const eagle3_ctx* c, int R) { return c->bf && R <= kSplitMaxRows;
 // The control of one call: the context's setting plus the branch cap of this batch size.
 CtlDev round_control(const eagle3_ctx* c, int B) {
   CtlDev d = c->ctl;
+  d.clip = c->sampled ? 1 : 0;
   if (!d.on) return d;
   const eagle3_control& h = c->ctl_host;
   int kc = c->k;
@@ -401,6 +407,26 @@ void draft_head(eagle3_ctx* c, const void* H, int R, bool split, int* tok, float
   c->launches++;
 }
 
+// Sampled draft: the pass's logits by the tensor-core GEMM, then each row's k
+// children drawn by Gumbel-top-k (rows b * rpr + j export to node slot slot0 + j).
+void sampled_head(eagle3_ctx* c, const void* H, int R, bool split, int slot0, int rpr,
+                  cudaStream_t st) {
+  const int V = c->cfg.vocab, d = c->cfg.d;
+  gemm1(c, TCW_LM, H, d, c->w.w_lm, V, d, c->lg, V, R, split, 1, 0, st);
+  SampleArgs sa{};
+  sa.V = V;
+  sa.k = c->k;
+  sa.rows_per_req = rpr;
+  sa.slot0 = slot0;
+  sa.seed = c->draft_seed;
+  sa.round_ptr = c->d_draft_round;
+  sa.logits = c->lg;
+  sa.tok = c->top_tok;
+  sa.logq = c->top_logq;
+  launch_sample_children(sa, R, st);
+  c->launches++;
+}
+
 bool kv_ok(const eagle3_ctx* c, const eagle3_kv* kv) {
   if (!kv || !kv->k || !kv->v || !kv->seq_lens) return false;
   if (c->cfg.page_size) {
@@ -442,8 +468,10 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
     return EAGLE3_ERR_INVALID_ARG;
   // bf16 streams U [V, r] in 64-column TMA boxes
   if (f.lr_rank > 0 && f.dtype == EAGLE3_BF16 && f.lr_rank % 64) return EAGLE3_ERR_UNSUPPORTED;
-  if ((f.variant & ~(EAGLE3_FC_NORM | EAGLE3_POST_NORM)) || ((f.variant & EAGLE3_FC_NORM) && !w->g_fc))
+  if ((f.variant & ~(EAGLE3_FC_NORM | EAGLE3_POST_NORM | EAGLE3_SAMPLED_DRAFT)) ||
+      ((f.variant & EAGLE3_FC_NORM) && !w->g_fc))
     return EAGLE3_ERR_INVALID_ARG;
+  if ((f.variant & EAGLE3_SAMPLED_DRAFT) && f.lr_rank > 0) return EAGLE3_ERR_UNSUPPORTED;
   if (!w->w_fc || !w->embed || !w->w_q || !w->w_k || !w->w_v || !w->w_o || !w->w_gate || !w->w_up ||
       !w->w_down || !w->g_emb || !w->g_hid || !w->g_post || !w->g_final || !w->w_lm)
     return EAGLE3_ERR_INVALID_ARG;
@@ -590,6 +618,13 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
   add((void**)&c->d_verify_us, (size_t)(f.n_verify + 1) * 4);
   add((void**)&c->d_deff, (size_t)B * 4);
   add((void**)&c->d_active, (size_t)(f.depth + 1) * 4);
+  c->sampled = (f.variant & EAGLE3_SAMPLED_DRAFT) != 0;
+  if (c->sampled) {
+    const size_t rows = std::max((size_t)B * k, (size_t)2 * B * (f.n_verify + 1));
+    add((void**)&c->lg, rows * f.vocab * 4);
+    add((void**)&c->pqw, (size_t)2 * B * f.vocab * 4);
+    add((void**)&c->d_draft_round, 8);
+  }
   size_t total = 0;
   for (auto& p : plan) total += align_up(p.second, 256);
   if (cudaMalloc(&c->arena, total) != cudaSuccess) {
@@ -702,7 +737,10 @@ eagle3_status draft_round_impl(eagle3_ctx* c, int B, int n_new, const int* cu_ne
   kv_rows(c, total_new, feats_new, true, nullptr, kv, KvTarget{nullptr, nullptr, 0},
           use_split(c, total_new), st);
   tail_rows(c, B, 1, c->g, kv, KvTarget{nullptr, nullptr, 0}, c->h_root, sp0, st);
-  draft_head(c, c->h_root, B, sp0, c->top_tok, c->top_logq, c->top_lse, st, 0, 1);
+  if (c->sampled)
+    sampled_head(c, c->h_root, B, sp0, 0, 1, st);
+  else
+    draft_head(c, c->h_root, B, sp0, c->top_tok, c->top_logq, c->top_lse, st, 0, 1);
   CtlDev ctl = round_control(c, B);
   if (ctl.on) cudaMemsetAsync(c->d_active, 0, (size_t)(D + 1) * 4, st);
   launch_expand(ctl, B, 0, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
@@ -715,7 +753,10 @@ eagle3_status draft_round_impl(eagle3_ctx* c, int B, int n_new, const int* cu_ne
     c->skip = ctl.on ? c->d_active + t : nullptr;
     kv_rows(c, B * k, nullptr, true, c->S, kv, tree, spk, st);
     tail_rows(c, B, k, c->S, kv, tree, c->h, spk, st);
-    draft_head(c, c->h, B * k, spk, c->top_tok, c->top_logq, c->top_lse, st, 1 + (t - 1) * k, k);
+    if (c->sampled)
+      sampled_head(c, c->h, B * k, spk, 1 + (t - 1) * k, k, st);
+    else
+      draft_head(c, c->h, B * k, spk, c->top_tok, c->top_logq, c->top_lse, st, 1 + (t - 1) * k, k);
     launch_expand(ctl, B, t, k, D, c->top_tok, c->top_logq, c->pool, c->frontier, c->slot_mask,
                   c->slot_words, c->root_pos, c->n_slots, c->rp, st);
     c->launches++;
@@ -822,8 +863,10 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   c->launches = 0;
   if (!c->have_round) return fail(c, EAGLE3_ERR_STATE, "verify needs a draft round on this context");
   if (B != c->last_B) return fail(c, EAGLE3_ERR_SHAPE, "B differs from the last draft round");
-  if (mode != 0 && mode != 1) return fail(c, EAGLE3_ERR_INVALID_ARG, "mode must be 0 or 1");
-  if (mode == 1 && !(temperature > 0.f)) return fail(c, EAGLE3_ERR_INVALID_ARG, "temperature must be > 0");
+  if (mode < 0 || mode > 2) return fail(c, EAGLE3_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
+  if (mode == 2 && !c->sampled)
+    return fail(c, EAGLE3_ERR_INVALID_ARG, "mode 2 needs the sampled-draft variant");
+  if (mode >= 1 && !(temperature > 0.f)) return fail(c, EAGLE3_ERR_INVALID_ARG, "temperature must be > 0");
   if (!c->w.w_target) return fail(c, EAGLE3_ERR_INVALID_ARG, "no target head in the weights");
   if (!tree_ok((eagle3_tree*)tree) || !accept_len || !path || !out_tokens)
     return fail(c, EAGLE3_ERR_INVALID_ARG, "null output");
@@ -850,7 +893,7 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   va.M1 = M1;
   va.kmax = k;
   va.sampling = mode == 1;
-  va.inv_t = mode == 1 ? 1.f / temperature : 1.f;
+  va.inv_t = mode >= 1 ? 1.f / temperature : 1.f;
   va.seed = seed;
   va.round_id = round_id;
   va.round_ptr = c->round_ptr;
@@ -867,6 +910,36 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   c->launches++;
   launch_verify_merge(va, c->z_max, c->z_arg, c->lse, c->g_arg, c->g_max, st);
   c->launches++;
+  if (mode == 2) {  // q-ratio walk over the draft and target logits of the kept nodes
+    const int V = f.vocab;
+    float* ell = c->lg;
+    float* zl = c->lg + (size_t)B * M1 * V;
+    gemm1(c, TCW_LM, c->h_ver, d, c->w.w_lm, V, d, ell, V, B * M1, spv, 1, 0, st);
+    gemm1(c, TCW_T, c->h_ver, d, c->w.w_target, V, d, zl, V, B * M1, spv, 1, 0, st);
+    QratioArgs qa{};
+    qa.B = B;
+    qa.M1 = M1;
+    qa.kmax = k;
+    qa.D = c->D;
+    qa.V = V;
+    qa.inv_t = 1.f / temperature;
+    qa.seed = seed;
+    qa.round_id = round_id;
+    qa.round_ptr = c->round_ptr;
+    qa.z = zl;
+    qa.ell = ell;
+    qa.pw = c->pqw;
+    qa.qw = c->pqw + (size_t)B * V;
+    qa.t_tok = tree->tokens;
+    qa.pidx = tree->pool_index;
+    qa.child_node = c->child_node;
+    qa.n_child = c->n_child;
+    qa.accept_len = accept_len;
+    qa.path = path;
+    qa.out_tokens = out_tokens;
+    launch_qratio_walk(qa, st);
+    c->launches++;
+  } else {
   WalkArgs wa{};
   wa.B = B;
   wa.M1 = M1;
@@ -889,6 +962,7 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   wa.out_tokens = out_tokens;
   launch_walk(wa, st);
   c->launches++;
+  }
   if (stats) {
     size_t n = (size_t)B * M1;
     if (stats->z_max) cudaMemcpyAsync(stats->z_max, c->z_max, n * 4, cudaMemcpyDeviceToDevice, st);
@@ -956,6 +1030,7 @@ eagle3_status eagle3_graph_launch(eagle3_ctx* c, unsigned long long round_id, ea
   cudaStream_t st = (cudaStream_t)stream;
   c->last = st;
   launch_set_u64(c->d_round, round_id, st);
+  if (c->sampled) launch_set_u64(c->d_draft_round, round_id, st);
   cudaError_t e = cudaGraphLaunch(c->gexec, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -1029,6 +1104,16 @@ const char* eagle3_last_error(const eagle3_ctx* c) { return c ? c->err.c_str() :
 size_t eagle3_workspace_bytes(const eagle3_ctx* c) { return c ? c->arena_bytes : 0; }
 
 int eagle3_last_launch_count(const eagle3_ctx* c) { return c ? c->launches : 0; }
+
+eagle3_status eagle3_draft_noise(eagle3_ctx* c, unsigned long long seed, unsigned long long round_id,
+                                 eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  if (!c->sampled) return fail(c, EAGLE3_ERR_STATE, "the context does not sample its draft");
+  c->draft_seed = seed;
+  launch_set_u64(c->d_draft_round, round_id, (cudaStream_t)stream);
+  return cuda_status(c, "draft_noise");
+}
 
 eagle3_status eagle3_set_control(eagle3_ctx* c, const eagle3_control* ctl) {
   if (!c) return EAGLE3_ERR_INVALID_ARG;

@@ -136,6 +136,7 @@ struct CtlDev {
   const float* verify_us;  // [M+1]
   int* d_eff;           // [B] depth the request runs to (set at pass 0, lowered by the rule)
   int* active;          // [D + 1] requests active at pass t
+  int clip;             // sampled draft: sibling scores non-increasing in draw order (any `on`)
 };
 // pass 0 rows: n_new rows per request, or the ragged rows given by cu_new [B+1]
 void launch_plan_root(int B, int n_new, const int* cu_new, int total, int max_new,
@@ -183,6 +184,28 @@ struct WalkArgs {
   int *accept_len, *path, *out_tokens;
 };
 void launch_walk(const WalkArgs& a, cudaStream_t st);
+
+// ----------------------------------------------------------------------------- sampled.cu
+struct SampleArgs {  // sampled children of a pass's rows (Gumbel-top-k over the logits)
+  int V, k, rows_per_req, slot0;
+  unsigned long long seed, round_id;
+  const unsigned long long* round_ptr;  // if set, the round id is read here
+  const float* logits;  // [R][V]
+  int* tok;             // [R][k] in draw order
+  float* logq;          // [R][k]
+};
+void launch_sample_children(const SampleArgs& a, int R, cudaStream_t st);
+struct QratioArgs {  // q-ratio verification walk
+  int B, M1, kmax, D, V;
+  float inv_t;
+  unsigned long long seed, round_id;
+  const unsigned long long* round_ptr;
+  const float *z, *ell;   // [B*M1][V] target and draft logits of the tree nodes
+  float *pw, *qw;         // [B][V] work rows
+  const int *t_tok, *pidx, *child_node, *n_child;
+  int *accept_len, *path, *out_tokens;
+};
+void launch_qratio_walk(const QratioArgs& a, cudaStream_t st);
 // *p = v, in stream order (sets the round id a captured graph reads)
 void launch_set_u64(unsigned long long* p, unsigned long long v, cudaStream_t st);
 

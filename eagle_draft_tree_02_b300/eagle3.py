@@ -34,7 +34,7 @@ class eagle3_config(C.Structure):
 
 WEIGHT_NAMES = ("w_fc", "embed", "w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down",
                 "g_emb", "g_hid", "g_post", "g_final", "w_lm", "w_target", "lr_u", "lr_v", "g_fc")
-FC_NORM, POST_NORM = 1, 2  # eagle3_config.variant bits
+FC_NORM, POST_NORM, SAMPLED_DRAFT = 1, 2, 4  # eagle3_config.variant bits
 
 
 class eagle3_weights(C.Structure):
@@ -101,6 +101,7 @@ _sig = {
     "eagle3_workspace_bytes": (C.c_size_t, [_P]),
     "eagle3_last_launch_count": (C.c_int, [_P]),
     "eagle3_set_control": (C.c_int, [_P, C.POINTER(eagle3_control)]),
+    "eagle3_draft_noise": (C.c_int, [_P, C.c_ulonglong, C.c_ulonglong, _P]),
     "eagle3_latency_costs": (C.c_int, [C.POINTER(eagle3_latency_table), C.c_int, C.c_int, C.c_int,
                                        C.c_int, C.c_int, C.POINTER(C.c_float),
                                        C.POINTER(C.c_float)]),
@@ -213,6 +214,10 @@ def eagle3_workspace_bytes(ctx) -> int:
 
 def eagle3_last_launch_count(ctx) -> int:
     return lib.eagle3_last_launch_count(ctx)
+
+
+def eagle3_draft_noise(ctx, seed, round_id, stream=0) -> int:
+    return lib.eagle3_draft_noise(_P(ctx), seed, round_id, _P(stream))
 
 
 def eagle3_set_control(ctx, ctl: eagle3_control | None) -> int:

@@ -30,7 +30,8 @@ def make_config(cfg: RoundConfig, max_prefix: int, max_new: int = 1, max_batch: 
     c.depth, c.topk, c.n_verify, c.page_size = cfg.depth, cfg.topk, cfg.n_verify, cfg.page_size
     c.max_batch = max_batch or cfg.batch
     c.max_prefix, c.max_new = max_prefix, max_new
-    c.variant = (E.FC_NORM if cfg.fc_norm else 0) | (E.POST_NORM if cfg.post_norm else 0)
+    c.variant = ((E.FC_NORM if cfg.fc_norm else 0) | (E.POST_NORM if cfg.post_norm else 0) |
+                 (E.SAMPLED_DRAFT if cfg.sampled_draft else 0))
     return c
 
 
@@ -189,8 +190,12 @@ class Engine:
         E.check(self.ctx, s)
         return self.tree
 
+    def draft_noise(self, seed, round_id):
+        """Seed and round id of the sampled draft's noise for the next rounds."""
+        E.check(self.ctx, E.eagle3_draft_noise(self.ctx, seed, round_id, self.stream()))
+
     def verify(self, temperature=0.0, seed=0, round_id=0, with_stats=True):
-        mode = 0 if temperature == 0 else 1
+        mode = 0 if temperature == 0 else (2 if self.cfg.sampled_draft else 1)
         s = E.eagle3_verify(self.ctx, self.B, self._tree_s, self.kv, mode, float(temperature or 1.0),
                             seed, round_id, self.accept_len.data_ptr(), self.path.data_ptr(),
                             self.out_tokens.data_ptr(), self.stats if with_stats else None,
@@ -204,7 +209,7 @@ class Engine:
         Needs an eager draft round first and a non-default stream; replays read
         the same input and output buffers (self.feats_new, self.tokens_new,
         self.tree, self.accept_len, ...)."""
-        mode = 0 if temperature == 0 else 1
+        mode = 0 if temperature == 0 else (2 if self.cfg.sampled_draft else 1)
         st = stream if stream is not None else self.stream()
         s = E.eagle3_graph_capture(self.ctx, self.B, 1, self.feats_new.data_ptr(),
                                    self.tokens_new.data_ptr(), self.kv, self._tree_s,

@@ -71,7 +71,15 @@ enum { EAGLE3_FP32 = 0, EAGLE3_BF16 = 1 };
  *                     and s is both the LM head's input and the state fed to
  *                     the node's children (no separate final norm).
  * 0 is the EAGLE-3 pre-norm drafter: z = rms(r) feeds the FFN, h = rms(s). */
-enum { EAGLE3_FC_NORM = 1, EAGLE3_POST_NORM = 2 };
+enum { EAGLE3_FC_NORM = 1, EAGLE3_POST_NORM = 2, EAGLE3_SAMPLED_DRAFT = 4 };
+/* EAGLE3_SAMPLED_DRAFT (single-stage head only): a node's k children are drawn
+ * from the draft distribution q without replacement -- the k largest
+ * log q(x) + G(x), G Gumbel noise from Philox stream 2 at (round id, b,
+ * node slot) keyed by the seed of eagle3_draft_noise -- in draw order, with
+ * their true log q; a child's score is clipped to be non-increasing in draw
+ * order, so a kept sibling set is always the first draws.  eagle3_verify mode
+ * 2 then verifies against q (recursive rejection over the draws; see there).
+ * The pass's logits are written to the workspace (rows x V fp32). */
 
 /* Shapes of the draft model and of the round.  All sizes in elements. */
 typedef struct {
@@ -214,6 +222,12 @@ typedef struct {
 eagle3_status eagle3_latency_costs(const eagle3_latency_table* table, int B, int P, int depth,
                                    int topk, int n_verify, float* pass_us, float* verify_us);
 
+/* Seed and round id of the sampled draft's noise (EAGLE3_SAMPLED_DRAFT), for
+ * the next draft rounds on `stream` (the round id is written in stream order;
+ * a graph replay uses its own round id). */
+eagle3_status eagle3_draft_noise(eagle3_ctx* ctx, unsigned long long seed,
+                                 unsigned long long round_id, eagle3_stream stream);
+
 /* Create a context: checks the config, borrows the weights, allocates the
  * workspace for max_batch requests once (nothing is allocated later) and
  * prepares the kernels' tensor maps.  It synchronizes the device first: the
@@ -288,7 +302,12 @@ eagle3_status eagle3_build_tree(eagle3_ctx* ctx, int B, int pool_n, const int* p
  * (walk while the target argmax is a child's token); mode 1: sampling at
  * `temperature` > 0 with sequential point-mass acceptance and a Gumbel draw
  * from the residual, using Philox4x64-10 with key (seed, 0) and counter
- * (round_id, b * 2^32 + node, idx, stream).  Outputs (device): accept_len [B],
+ * (round_id, b * 2^32 + node, idx, stream); mode 2 (EAGLE3_SAMPLED_DRAFT only):
+ * sampling at `temperature` with the q-ratio test -- the node's draws in draw
+ * order, the i-th accepted when U q_i(c) < p_i(c), on rejection p_{i+1} =
+ * norm(max(0, p_i - q_i)) and q_{i+1} = q_i without c, the bonus drawn from
+ * the last residual (q = softmax of the draft logits at the node, recomputed
+ * over the kept nodes).  Outputs (device): accept_len [B],
  * path [B, D] (tree indices, -1 padded), out_tokens [B, D+1] (accepted tokens
  * then the bonus token, -1 padded).  stats may be NULL. */
 eagle3_status eagle3_verify(eagle3_ctx* ctx, int B, const eagle3_tree* tree, const eagle3_kv* kv,

@@ -199,6 +199,34 @@ class Follow(R.Decisions):
         self.rep.failures.append(("accept", b, node, i, float(margin)))
         return own
 
+    def accept_q(self, b, node, i, u, q_child, p_child):
+        own = super().accept_q(b, node, i, u, q_child, p_child)
+        gpu_acc = self._gpu_acceptance(b, node, i)
+        if gpu_acc is None or gpu_acc == own:
+            return own
+        margin = abs(u * q_child - p_child)
+        if margin < max(p_child, 1e-30) * self.tol + 1e-7:
+            self.rep.near_ties.append(("accept_q", b, node, i))
+            return gpu_acc
+        self.rep.failures.append(("accept_q", b, node, i, float(margin)))
+        return own
+
+    def _gpu_acceptance(self, b, node, i):
+        """The GPU's choice at (node, i): accepted iff its path leaves `node` through
+        its i-th draw (children in pool order); None where the GPU never got there."""
+        v = self.g.verify[self.T]
+        path = [0] + [int(x) for x in v["path"][b] if x >= 0]
+        if node not in path:
+            return None
+        j = path.index(node)
+        if j + 1 >= len(path):
+            return False
+        nxt = path[j + 1]
+        par = self.g.tree["parent"][b]
+        kids = sorted((c for c in range(len(par)) if par[c] == node),
+                      key=lambda c: int(self.g.tree["pool_index"][b, c]))
+        return (kids.index(nxt) == i) if nxt in kids else None
+
     def bonus(self, b, node, scores):
         own = super().bonus(b, node, scores)
         v = self.g.verify[self.T]
@@ -208,7 +236,7 @@ class Follow(R.Decisions):
 
 
 def compare(cfg, inp, gpu: GpuRound, temps, seed=0, round_id=0, prefix_kv=None, requests=None,
-            ctl=None):
+            ctl=None, samp=None):
     """Conditioned oracle run and element-wise comparison.  Returns a Report."""
     tol = TOL[cfg.dtype]
     rep = Report()
@@ -223,7 +251,7 @@ def compare(cfg, inp, gpu: GpuRound, temps, seed=0, round_id=0, prefix_kv=None, 
             K, V = prefix_kv(b)
         dec = Follow(cfg, gpu, rep, tol["tie"])
         dr = R.draft_request(w, cfg, K, V, feats[hi - 1], inp.tokens[hi - 1], P - 1, dec, b, ctl,
-                             cfg.batch)
+                             cfg.batch, samp)
         pool = dr.pool
         n = len(pool.tok)
         # pool: tokens / parents / depth exact; log q and scores within tolerance
@@ -254,7 +282,7 @@ def compare(cfg, inp, gpu: GpuRound, temps, seed=0, round_id=0, prefix_kv=None, 
             rep.failures.append(("tree-mask", b))
         if not temps:
             continue
-        z, _ = R.verify_logits(w, cfg, K, V, P - 1, tree, dr)
+        z, hv = R.verify_logits(w, cfg, K, V, P - 1, tree, dr)
         for T in temps:
             st = gpu.verify[T]["stats"]
             nr = z.shape[0]  # the root and the kept nodes (padding slots are not verified)
@@ -262,8 +290,12 @@ def compare(cfg, inp, gpu: GpuRound, temps, seed=0, round_id=0, prefix_kv=None, 
             zt = z / (T if T else 1.0)
             rep.err("lse", np.max(np.abs(L.logsumexp(zt) - st["lse"][b][:nr])))
             dec.T = T
-            res = (R.verify_greedy(tree, z, dec, b) if T == 0 else
-                   R.verify_sample(tree, z, T, seed, round_id, dec, b))
+            if T == 0:
+                res = R.verify_greedy(tree, z, dec, b)
+            elif samp is None:
+                res = R.verify_sample(tree, z, T, seed, round_id, dec, b)
+            else:
+                res = R.verify_qratio(tree, z, L.linear(hv, w["w_lm"]), T, seed, round_id, dec, b)
             v = gpu.verify[T]
             if int(v["accept_len"][b]) != res.accept_len:
                 rep.failures.append(("accept_len", T, b))
