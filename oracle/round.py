@@ -148,16 +148,16 @@ class Control:
     verify_us: list | None = None
 
     def k_for(self, b, B, k):
-        kb = k if self.topk_cap is None else min(k, int(self.topk_cap[b]))
+        """Branch cap of request b (caps below 1 count as 1)."""
         if self.light_batch > 0:
-            kb = min(kb, self.k_light if B <= self.light_batch else self.k_heavy)
-        return kb
+            k = max(1, min(k, self.k_light if B <= self.light_batch else self.k_heavy))
+        return k if self.topk_cap is None else max(1, min(k, int(self.topk_cap[b])))
 
     def d_for(self, b, D):
-        return D if self.depth_cap is None else min(D, int(self.depth_cap[b]))
+        return D if self.depth_cap is None else max(1, min(D, int(self.depth_cap[b])))
 
     def m_for(self, b, M):
-        return M if self.verify_cap is None else min(M, int(self.verify_cap[b]))
+        return M if self.verify_cap is None else max(1, min(M, int(self.verify_cap[b])))
 
 
 # --------------------------------------------------------------------------- prefix
