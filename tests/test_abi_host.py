@@ -128,3 +128,7 @@ def test_latency_costs_and_control_reject_bad_arguments(E):
     assert E.eagle3_latency_costs([1, 4], [8], [1], g, g, 1, 8, 2, 1, 1)[0] == E.OK
     assert E.eagle3_set_control(0, None) == E.ERR_INVALID_ARG
     assert E.eagle3_set_control(0, E.make_control(tau_depth=1.0)) == E.ERR_INVALID_ARG
+
+
+def test_draft_noise_needs_a_context(E):
+    assert E.eagle3_draft_noise(0, 1, 2, 0) == E.ERR_INVALID_ARG
