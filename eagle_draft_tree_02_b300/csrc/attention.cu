@@ -13,15 +13,16 @@
 // partial (o, max, sum); a second kernel merges the splits.
 //
 // bf16 cache, prefix splits: one block of 4 warps per (request, KV head, group
-// of <= 64 queries, split); 64-key chunks of K and V move by 16-byte cp.async
-// into double-buffered shared memory, and the 16 queries of a warp take
-// Q K^T and P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
-// accumulate).  Q and P enter as hi + lo bf16 pairs (two MMAs each), so the
-// products keep about 16 significant bits, and K, V are the cache's exact
-// values.  (With P as one bf16, the 70B-shaped tree's log q error grew from
-// 2e-4 to 1e-3 at no measurable gain in time.)  A tree split stages its 64 fp32 slots as bf16 (hi, lo) pairs and
-// adds the lo products (three MMAs per fragment), with the ancestor mask
-// applied per query row.  The fp32 cache uses the CUDA-core kernel: 32
+// of <= 64 queries, split); 64-key chunks of K and V stream through a 3-stage
+// ring in shared memory, one 256-byte row per thread by a bulk copy that
+// completes on the stage's mbarrier, and the 16 queries of a warp take Q K^T
+// and P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+// Q and P enter as hi + lo bf16 pairs (two MMAs each), so the products keep
+// about 16 significant bits, and K, V are the cache's exact values.  (With P
+// as one bf16, the 70B-shaped tree's log q error grew from 2e-4 to 1e-3 at no
+// measurable gain in time.)  A tree split stages its 64 fp32 slots as bf16
+// (hi, lo) pairs and adds the lo products (three MMAs per fragment), with the
+// ancestor mask applied per query row.  The fp32 cache uses the CUDA-core kernel: 32
 // queries per block, K and V staged as fp32.
 #include <math.h>
 
