@@ -419,15 +419,16 @@ __global__ void __launch_bounds__(128, 1)
 
 // ----------------------------------------------------------------------------- persistent heads
 // The vocabulary heads (draft LM head, verify head) as a persistent kernel:
-// one CTA per SM walks the 128-token tiles mt = blockIdx.x, + gridDim.x, ...
-// Warp 0 issues the TMA loads into a ring of stages that runs on across tiles,
-// warp 1 issues the MMAs into one of two TMEM accumulators, and warps 2-5 run
-// the epilogue of tile i while tile i+1 is loaded and multiplied.  Each
-// epilogue warp keeps per-row running state in shared memory across its
-// CTA's tiles -- an online log-sum-exp and a sorted top-k list for the draft
-// head, or (best logit, log-sum-exp of z/T, Gumbel best) for the verify head
-// -- and writes one partial at the end, so the merge reads 4 partials per CTA
-// instead of 4 per tile.
+// each CTA (two per SM when their accumulators fit the SM's tensor memory)
+// walks the 128-token tiles mt = blockIdx.x, + gridDim.x, ...  Warp 0 issues
+// the TMA loads into a ring of stages that runs on across tiles, warp 1
+// issues the MMAs into one of two TMEM accumulators, and the epilogue warps
+// (kHeadEpiWarps, two per TMEM lane quarter) reduce tile i while tile i+1 is
+// loaded and multiplied.  Per-row running state lives in shared memory across
+// the CTA's tiles -- an online log-sum-exp and a sorted top-k list for the
+// draft head, or (best logit, log-sum-exp of z/T, Gumbel best) for the verify
+// head -- and the CTA writes one partial per row at the end, so the merge
+// reads one partial per CTA instead of four per tile.
 struct PhArgs {
   int R, ncols, split, n_kb, ntile, stages, n_mtiles, V, sw;
   int r_off, R_total;  // this launch's rows are rows r_off .. r_off + R - 1 of R_total
