@@ -40,6 +40,11 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", default="none", choices=["none", "fc_post", "sampled"],
+                    help="drafter variant: FC norm + post-norm, or sampled drafting with q-ratio "
+                         "verification (rows of the survey's next steps; the headline is 'none')")
+    ap.add_argument("--control", default="none", choices=["none", "caps"],
+                    help="per-request control: 'caps' halves every request's depth and verify count")
     ap.add_argument("--prefix-scale", type=float, default=1.0,
                     help="scale the prefix lengths (a small case of the same kernels for profiling; "
                          "the bench line is only valid at 1.0)")
@@ -189,6 +194,10 @@ def main():
         cfg = cfg.scaled(prefix=max(2, int(cfg.prefix * sc)),
                          prefix_range=None if rng is None else (max(2, int(rng[0] * sc)),
                                                                 max(2, int(rng[1] * sc))))
+    if args.variant == "fc_post":
+        cfg = cfg.scaled(fc_norm=True, post_norm=True)
+    elif args.variant == "sampled":
+        cfg = cfg.scaled(sampled_draft=True)
     if args.impl == "reference":
         run_reference(args, cfg)
         return
@@ -217,6 +226,11 @@ def main():
     inp = make_inputs(cfg, seed=None)
     eng = Engine(inp, device=dev)
     eng.prefill()
+    if cfg.sampled_draft:
+        eng.draft_noise(0, 0)
+    if args.control == "caps":
+        eng.set_control(depth_cap=[max(1, cfg.depth // 2)] * cfg.batch,
+                        verify_cap=[max(1, cfg.n_verify // 2)] * cfg.batch)
     torch.cuda.synchronize()
     eng.check()
     T = step_temperature(cfg)
@@ -340,6 +354,7 @@ def main():
         "dtype": cfg.dtype, "data": "synthetic (seeded weights, features, tokens; no trained model)",
         "config": {"workload": cfg.name, "batch": cfg.batch, "prefix": cfg.prefix, "d": cfg.d,
                    "prefix_scale": args.prefix_scale,
+                   "variant": args.variant, "control": args.control,
                    "vocab": cfg.vocab, "depth": cfg.depth, "topk": cfg.topk, "n_verify": cfg.n_verify,
                    "verify": f"T={T}" if T else "greedy",
                    "l2": f"inputs larger than L2: {rb['step'] / 1e9:.2f} GB of weights/KV streamed per step"},
