@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--variant", default="none", choices=["none", "fc_post", "sampled"],
                     help="drafter variant: FC norm + post-norm, or sampled drafting with q-ratio "
-                         "verification (rows of the survey's next steps; the headline is 'none')")
+                         "verification (the headline is 'none')")
     ap.add_argument("--control", default="none", choices=["none", "caps"],
                     help="per-request control: 'caps' halves every request's depth and verify count")
     ap.add_argument("--prefix-scale", type=float, default=1.0,

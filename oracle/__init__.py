@@ -20,5 +20,8 @@ Parity pins (the pages print no worked example):
   * greedy verification by brute force over all root-to-node paths;
   * sampling verification by a chi-square test of the output marginals against
     the target distribution at V = 8;
-  * Philox against numpy.random.Philox and published known-answer vectors.
+  * Philox against numpy.random.Philox and the published Random123
+    known-answer vectors;
+  * the layer's composition, the decoder input, the log-sum-exp and the
+    two-stage rescoring by closed-form special cases and scipy.
 """

@@ -52,12 +52,13 @@ A node that a cap or rule leaves out is not created: its pool slot holds token
 -1, parent -1, score and log q -inf.  Tree slots past the kept count hold
 token -1, parent -1, depth 0, score -inf and only their own mask bit.
 
-Sampled drafting with q-ratio verification (R-17; §8(f) f3: "children sampled
-from q"; "EAGLE-3 精读" §5: sampling keeps the target distribution with the
-residual correction): a node's k children are drawn from q without
-replacement by Gumbel-top-k (Philox stream 2 at the node's slot), in draw
-order; a child's score is clipped to be non-increasing in draw order, so a
-kept sibling set is always the first draws.  Verification walks the draws:
+Sampled drafting with q-ratio verification (R-17; "EAGLE-3 精读" §5: the
+draft's sampling verification keeps the target distribution with the residual
+correction, which with the min(1, p/q) rule needs children drawn from q): a
+node's k children are drawn from q without replacement by Gumbel-top-k
+(Philox stream 2 at the node's slot), in draw order; a child's score is
+clipped to be non-increasing in draw order, so a kept sibling set is always
+the first draws.  Verification walks the draws:
 the i-th is accepted when U q_i(c) < p_i(c); on rejection p_{i+1} =
 norm(max(0, p_i - q_i)) and q_{i+1} = q_i without c; with no acceptance the
 bonus is the Gumbel-argmax of log p over its support (stream 1).
