@@ -708,21 +708,12 @@ void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
   const bool mma = attention_uses_mma((int)sizeof(T), a.dh);
   size_t smem = (size_t)(QG * (a.dh + 1) + KC * (a.dh + 1) + KC * a.dh + QG * KC + 3 * QG) *
                 sizeof(float);
-  static bool attr_set[2] = {false, false};
-  int ti = sizeof(T) == 4 ? 0 : 1;
-  if (!attr_set[ti]) {
-    cudaFuncSetAttribute(tree_attention_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         160 * 1024);
-    cudaFuncSetAttribute(prefix_attention_mma_kernel<64, 1>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem(64));
-    cudaFuncSetAttribute(prefix_attention_mma_kernel<128, 1>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem(128));
-    cudaFuncSetAttribute(prefix_attention_mma_kernel<64, 4>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem(64));
-    cudaFuncSetAttribute(prefix_attention_mma_kernel<128, 4>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, mma_smem(128));
-    attr_set[ti] = true;
-  }
+  // a refused limit shows as the launch's own error, which the caller reports
+  smem_limit((const void*)tree_attention_kernel<T>, 160 * 1024);
+  smem_limit((const void*)prefix_attention_mma_kernel<64, 1>, mma_smem(64));
+  smem_limit((const void*)prefix_attention_mma_kernel<128, 1>, mma_smem(128));
+  smem_limit((const void*)prefix_attention_mma_kernel<64, 4>, mma_smem(64));
+  smem_limit((const void*)prefix_attention_mma_kernel<128, 4>, mma_smem(128));
   if (mma) {  // prefix and tree splits in one launch
     dim3 gp(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, true), n_splits);
     const size_t sm2 = mma_smem(a.dh);

@@ -103,6 +103,10 @@ __device__ __forceinline__ void pdl_begin() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device
+// (once per device and kernel; thread-safe).  False if the runtime refused.
+bool smem_limit(const void* kernel, int bytes);
+
 // Launch `kernel` with programmatic stream serialization allowed (see pdl_begin).
 template <typename... KArgs, typename... Args>
 inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

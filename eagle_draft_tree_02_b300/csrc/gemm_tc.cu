@@ -1152,12 +1152,7 @@ bool launch(TcGemm* t, const CUtensorMap* a0, const CUtensorMap* a1, const CUten
   args.stages = L.stages;
   args.tmem_cols = L.tmem_cols;
   args.idesc = make_idesc(L.ntile);
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kSmemBudgetWide + 4096);
-    attr = true;
-  }
+  if (!smem_limit((const void*)tc_gemm_kernel<MODE>, kSmemBudgetWide + 4096)) return false;
   dim3 grid(grid_x, L.n_tiles, S);
   launch_pdl(tc_gemm_kernel<MODE>, dim3(grid), dim3(128), L.smem, st, *a0, *a1, *a2, mb, args);
   return true;
@@ -1203,12 +1198,7 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
   args.tmem_cols = 2 * acc;
   args.idesc = make_idesc(ntile);
   const size_t smem = 1024 + stages * stage + (2 * stages + 4) * 8 + 32 + 16 + state;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(tc_head_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         232448);
-    attr = true;
-  }
+  if (!smem_limit((const void*)tc_head_kernel<MODE>, 232448)) return false;
   launch_pdl(tc_head_kernel<MODE>, dim3(grid), dim3(kHeadThreads), smem, st, *wmap, mb, args);
   n_parts = grid;  // one partial per CTA
   return true;
@@ -1325,8 +1315,9 @@ bool tc_lowrank(TcGemm* t, int mode, const LowRankArgs& la, int* flags, cudaStre
   return launch<4>(t, m, m, m, la.t, K, K, la.R, la.t_split != 0, 1, args, args.seg_end[0], st);
 }
 
-bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, HeadParts& hp,
-                    int* flags, cudaStream_t st) {
+int tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, HeadParts& hp,
+                   int* flags, cudaStream_t st) {
+  if (R <= 0 || R > 256 || V <= 0 || d <= 0) return 1;
   static const EncodeFn enc = []() -> EncodeFn {  // looked up once, thread-safe
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -1338,16 +1329,17 @@ bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, HeadParts
     }
     return reinterpret_cast<EncodeFn>(fn);
   }();
-  if (!enc) return false;
+  if (!enc) return 2;
   TcGemm t;
   t.encode = enc;
   t.V = V;
   t.n_sm = sm_count();
-  if (!encode_map(enc, &t.wmap[TCW_LM], W, V, d, (size_t)d * 2, BM)) return false;
+  if (!encode_map(enc, &t.wmap[TCW_LM], W, V, d, (size_t)d * 2, BM)) return 2;
   t.wptr[TCW_LM] = W;
   t.wN[TCW_LM] = V;
   t.wK[TCW_LM] = d;
-  return tc_lm_head(&t, H, R, false, hp, flags, st);
+  // the shapes were checked above: a refusal now is the driver's or the runtime's
+  return tc_lm_head(&t, H, R, false, hp, flags, st) ? 0 : 2;
 }
 
 }  // namespace e3

@@ -55,8 +55,11 @@ bool tc_verify_head(TcGemm* t, const void* H, bool split, VerifyHeadArgs& a, int
 bool tc_lowrank(TcGemm* t, int mode, const LowRankArgs& la, int* flags, cudaStream_t st);
 // The draft-head launch of tc_lm_head on a bare weight pointer W [V, d] (bf16),
 // with no TcGemm object: the tensor maps are encoded on the host stack and
-// nothing is allocated.  False (nothing launched) on an unusable argument.
-bool tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, HeadParts& hp,
-                    int* flags, cudaStream_t st);
+// nothing is allocated.  Returns 0 when launched, 1 for an unusable shape
+// (nothing launched), 2 when the driver or runtime refused (the tensor-map
+// entry point is missing, the driver rejected an encode, or a launch
+// attribute could not be set; nothing launched).
+int tc_lm_head_raw(const void* W, int V, int d, const void* H, int R, HeadParts& hp,
+                   int* flags, cudaStream_t st);
 
 }  // namespace e3

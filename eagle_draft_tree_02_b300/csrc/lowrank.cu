@@ -329,13 +329,7 @@ __global__ void __launch_bounds__(kSelThreads) lowrank_select_kernel(LowRankArgs
 template <typename T>
 void launch_lowrank_select(const LowRankArgs& a, cudaStream_t st) {
   const size_t smem = (size_t)kLrCap * 8 + (size_t)(a.d + a.r + 128) * 4 + 128 * 4;
-  static bool attr[2] = {false, false};
-  const int ti = sizeof(T) == 4 ? 0 : 1;
-  if (!attr[ti]) {
-    cudaFuncSetAttribute(lowrank_select_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         200 * 1024);
-    attr[ti] = true;
-  }
+  smem_limit((const void*)lowrank_select_kernel<T>, 200 * 1024);  // refusal: the launch fails
   launch_pdl(lowrank_select_kernel<T>, dim3(a.R), dim3(kSelThreads), smem, st, a);
 }
 

@@ -14,8 +14,15 @@
 // The array lives as long as the library is loaded, on every GPU that loads
 // it.  Its address is looked up once per device (first call with that device
 // current) and cached; later calls allocate nothing and call no allocating
-// routine.  All calls share the array, so calls whose work overlaps on the GPU
-// (two streams, or two host threads) race on it: the caller must order them.
+// routine.  The first call on a device is special: under CUDA's default lazy
+// module loading, the module holding this array is loaded onto the device
+// when its address is first looked up, and that load places the 16 MiB array
+// (and the module's code) in device memory, which may synchronise the device
+// and fails if the device has no 16 MiB left.  So make the first call on each
+// device early -- before the caller reserves its memory pools and before any
+// stream capture -- and treat later calls as the allocation-free ones.  All
+// calls share the array, so calls whose work overlaps on the GPU (two streams,
+// or two host threads) race on it: the caller must order them.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -103,7 +110,9 @@ extern "C" eagle3_status eagle3_lm_head_topk_noalloc(int dtype, int vocab, int d
     return EAGLE3_ERR_CUDA;
   }
   if (bf) {
-    if (!tc_lm_head_raw(w_lm, vocab, d, h, R, hp, flags, st)) return EAGLE3_ERR_INVALID_ARG;
+    const int rc = tc_lm_head_raw(w_lm, vocab, d, h, R, hp, flags, st);
+    if (rc == 1) return EAGLE3_ERR_INVALID_ARG;
+    if (rc != 0) return EAGLE3_ERR_CUDA;
   } else {
     launch_lm_head_simt<float>(h, w_lm, R, vocab, d, hp, st);
   }

@@ -430,11 +430,7 @@ void launch_build_tree(const CtlDev& ctl, int B, int pool_n, int M, const int* t
   int P2 = 1;
   while (P2 < pool_n) P2 <<= 1;
   size_t smem = (size_t)((3 * pool_n + 2 * M + 1 + 1) & ~1) * sizeof(int) + (size_t)P2 * 8;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(build_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-    attr = true;
-  }
+  smem_limit((const void*)build_tree_kernel, 100 * 1024);  // refusal: the launch fails
   launch_pdl(build_tree_kernel, dim3(B), dim3(512), smem, st, ctl, pool_n, M, tok, parent, score, depth, root_tok, root_pos,
                                           t_tok, t_parent, t_depth, t_pos, t_pidx, t_score, t_mask,
                                           flags);

@@ -251,7 +251,14 @@ eagle3_status eagle3_prefill(eagle3_ctx* ctx, int B, int total_rows, const int* 
                              const void* feats, const int* tokens, const eagle3_kv* kv,
                              eagle3_stream stream);
 
-/* One draft round: appends n_new rows per request at positions
+/* One draft round ("EAGLE-3 精读" §1, paragraph 2: the drafter fuses the
+ * target's low/mid/high features into g and runs one decoder layer over g, its
+ * own state and the token embedding; §2 Training-Time Test: deeper draft steps
+ * are fed the draft's own states; scholarfeed "EAGLE-3" page, the quote that
+ * each added tree depth costs one more sequential drafter pass; "EAGLE-3 精读"
+ * 核心变化 and the EAGLE-4 blog, 几条技术路线正在收敛, second trend: the
+ * EAGLE-2 confidence tree, confidence = product of draft probabilities).
+ * It appends n_new rows per request at positions
  * seq_lens[b] .. seq_lens[b] + n_new - 1 (the last is the tree's root), runs D
  * decoder passes (root, then one per tree depth), builds the pool of
  * k + (D-1) k^2 nodes and keeps the global top-M as `out`.
@@ -262,7 +269,9 @@ eagle3_status eagle3_draft_round(eagle3_ctx* ctx, int B, int n_new, const void* 
                                  eagle3_pool* pool_out, eagle3_stream stream);
 
 /* The same round with a different number of new rows per request, as in
- * steady-state decoding: request b's new rows are rows cu_new[b] ..
+ * steady-state decoding ("EAGLE-3 精读" §1 and §2 as for eagle3_draft_round;
+ * §2: after a verification the drafter continues from the target's accepted
+ * sequence, whose features arrive as several new rows): request b's new rows are rows cu_new[b] ..
  * cu_new[b+1] - 1 of feats_new [total_new, 3d] / tokens_new [total_new]
  * (device), at positions seq_lens[b] onward; the last is the request's root.
  * cu_new [B+1] (int32, device) with cu_new[0] = 0, cu_new[B] = total_new and
@@ -285,9 +294,12 @@ eagle3_status eagle3_draft_round_ragged(eagle3_ctx* ctx, int B, int total_new, c
 eagle3_status eagle3_next_rows(eagle3_ctx* ctx, int B, const int* accept_len, const int* out_tokens,
                                int* cu_new, int* tokens_new, eagle3_stream stream);
 
-/* Tree builder alone (for tests and outside drafters): keeps the top-M of a
- * pool by (score desc, depth asc, pool index asc) and writes the canonical
- * tree.  pool arrays [B, pool_n] (device; parent = pool index or -1), root_tok
+/* Tree builder alone (for tests and outside drafters).  "EAGLE-3 精读"
+ * 核心变化: EAGLE-3 keeps EAGLE-2's confidence-value dynamic draft tree; the
+ * EAGLE-4 blog, 几条技术路线正在收敛, second trend: a node's confidence is the
+ * product of its draft probabilities.  It keeps the top-M of a pool by (score
+ * desc, depth asc, pool index asc) -- score = cumulative log q -- and writes
+ * the canonical tree.  pool arrays [B, pool_n] (device; parent = pool index or -1), root_tok
  * and root_pos [B] (device).  pool_n <= 4096.  The kept set must be
  * ancestor-closed (child score <= parent score); otherwise the device flag
  * EAGLE3_ERR_DEVICE_ASSERT is raised and the tree is left partial. */
@@ -359,11 +371,17 @@ eagle3_status eagle3_lm_head_topk(eagle3_ctx* ctx, int R, const void* h, int* to
  * part, with P = 4*ceil(vocab/128) (bf16) or ceil(vocab/64) (fp32) -- return
  * EAGLE3_ERR_SHAPE and launch nothing.  bf16 also needs d % 8 == 0, 16-byte
  * aligned w_lm and h, and R <= 256 (EAGLE3_ERR_INVALID_ARG / _SHAPE).
- * Nothing is allocated and no allocating routine is called.  The first call
- * on a device looks up the array's device address (with that device current)
- * and caches it; make that first call before capturing any stream.  Every
- * call shares the array and it keeps the last call's contents: calls whose
- * work may overlap on the GPU race and must be ordered by the caller. */
+ * No call allocates or calls an allocating routine, but the first call on a
+ * device looks up the array's device address (with that device current) and
+ * caches it, and under CUDA's default lazy module loading that lookup is what
+ * loads the library module holding the array onto the device: the 16 MiB are
+ * placed then (the load may synchronise the device, and fails with
+ * EAGLE3_ERR_CUDA if 16 MiB are not free).  Make the first call on each device
+ * before reserving memory pools and before capturing any stream; later calls
+ * allocate nothing.  Every call shares the array and it keeps the last call's
+ * contents: calls whose work may overlap on the GPU race and must be ordered
+ * by the caller.  EAGLE3_ERR_CUDA also reports a driver that refuses the
+ * tensor-map encode or a failed launch. */
 eagle3_status eagle3_lm_head_topk_noalloc(int dtype, int vocab, int d, int topk, const void* w_lm,
                                           int R, const void* h, int* tok, float* logq, float* lse,
                                           int* dev_status, eagle3_stream stream);
