@@ -973,6 +973,92 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   return cuda_status(c, "verify");
 }
 
+eagle3_status eagle3_verify_logits(eagle3_ctx* c, int B, const eagle3_tree* tree, const void* logits,
+                                   int logits_dtype, long long ld, int mode, float temperature,
+                                   unsigned long long seed, unsigned long long round_id,
+                                   int* accept_len, int* path, int* out_tokens,
+                                   eagle3_verify_stats* stats, eagle3_stream stream) {
+  if (!c) return EAGLE3_ERR_INVALID_ARG;
+  c->err.clear();
+  c->launches = 0;
+  const eagle3_config& f = c->cfg;
+  if (B < 1 || B > f.max_batch) return fail(c, EAGLE3_ERR_SHAPE, "B out of range");
+  if (mode == 2) return fail(c, EAGLE3_ERR_UNSUPPORTED, "q-ratio verification needs the draft logits");
+  if (mode < 0 || mode > 1) return fail(c, EAGLE3_ERR_INVALID_ARG, "mode must be 0 or 1");
+  if (mode == 1 && !(temperature > 0.f)) return fail(c, EAGLE3_ERR_INVALID_ARG, "temperature must be > 0");
+  if (logits_dtype != EAGLE3_FP32 && logits_dtype != EAGLE3_BF16)
+    return fail(c, EAGLE3_ERR_INVALID_ARG, "logits_dtype must be EAGLE3_FP32 or EAGLE3_BF16");
+  if (!logits || !tree_ok((eagle3_tree*)tree) || !accept_len || !path || !out_tokens)
+    return fail(c, EAGLE3_ERR_INVALID_ARG, "null pointer");
+  const size_t esz = logits_dtype == EAGLE3_BF16 ? 2 : 4;
+  if (ld < f.vocab) return fail(c, EAGLE3_ERR_SHAPE, "ld must be at least the vocabulary size");
+  if (((uintptr_t)logits & 15) || ((size_t)ld * esz) % 16)
+    return fail(c, EAGLE3_ERR_INVALID_ARG, "logits rows must start on 16-byte boundaries");
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last = st;
+  const int M1 = c->M1;
+  LogitsVerifyArgs la{};
+  la.B = B;
+  la.M1 = M1;
+  la.kmax = c->k;
+  la.V = f.vocab;
+  la.R = B * M1;
+  la.ld = ld;
+  la.logits = logits;
+  la.t_tok = tree->tokens;
+  la.t_parent = tree->parent;
+  la.sampling = mode == 1;
+  la.inv_t = mode == 1 ? 1.f / temperature : 1.f;
+  la.seed = seed;
+  la.round_id = round_id;
+  la.round_ptr = c->round_ptr;
+  la.child_tok = c->child_tok;
+  la.child_node = c->child_node;
+  la.n_child = c->n_child;
+  la.child_z = c->child_z;
+  la.n_chunks = logits_verify_chunks(la.R, f.vocab, c->n_vparts);
+  la.part = c->vpart;
+  la.flags = c->flags;
+  launch_logits_verify(la, logits_dtype == EAGLE3_BF16, st);
+  c->launches += 2;
+  VerifyHeadArgs va{};
+  va.R = la.R;
+  va.n_parts = la.n_chunks;
+  va.part = c->vpart;
+  launch_verify_merge(va, c->z_max, c->z_arg, c->lse, c->g_arg, c->g_max, st);
+  c->launches++;
+  WalkArgs wa{};
+  wa.B = B;
+  wa.M1 = M1;
+  wa.kmax = c->k;
+  wa.D = c->D;
+  wa.sampling = mode == 1;
+  wa.inv_t = la.inv_t;
+  wa.seed = seed;
+  wa.round_id = round_id;
+  wa.round_ptr = c->round_ptr;
+  wa.t_tok = tree->tokens;
+  wa.child_node = c->child_node;
+  wa.n_child = c->n_child;
+  wa.child_z = c->child_z;
+  wa.lse = c->lse;
+  wa.z_arg = c->z_arg;
+  wa.g_arg = c->g_arg;
+  wa.accept_len = accept_len;
+  wa.path = path;
+  wa.out_tokens = out_tokens;
+  launch_walk(wa, st);
+  c->launches++;
+  if (stats) {
+    const size_t n = (size_t)B * M1;
+    if (stats->z_max) cudaMemcpyAsync(stats->z_max, c->z_max, n * 4, cudaMemcpyDeviceToDevice, st);
+    if (stats->lse) cudaMemcpyAsync(stats->lse, c->lse, n * 4, cudaMemcpyDeviceToDevice, st);
+    if (stats->z_argmax) cudaMemcpyAsync(stats->z_argmax, c->z_arg, n * 4, cudaMemcpyDeviceToDevice, st);
+    if (stats->g_argmax) cudaMemcpyAsync(stats->g_argmax, c->g_arg, n * 4, cudaMemcpyDeviceToDevice, st);
+  }
+  return cuda_status(c, "verify_logits");
+}
+
 eagle3_status eagle3_graph_capture(eagle3_ctx* c, int B, int n_new, const void* feats_new,
                                    const int* tokens_new, const eagle3_kv* kv, eagle3_tree* out,
                                    int with_verify, int mode, float temperature,

@@ -206,6 +206,27 @@ struct QratioArgs {  // q-ratio verification walk
   int *accept_len, *path, *out_tokens;
 };
 void launch_qratio_walk(const QratioArgs& a, cudaStream_t st);
+// ----------------------------------------------------------------------------- target_logits.cu
+struct LogitsVerifyArgs {  // verification against caller-supplied target logits
+  int B, M1, kmax, V, R;        // R = B * M1 rows
+  long long ld;                 // elements between consecutive logits rows
+  const void* logits;           // [R][ld], fp32 or bf16, 16-byte aligned rows
+  const int *t_tok, *t_parent;  // [B][M1] the kept tree
+  int sampling;
+  float inv_t;
+  unsigned long long seed, round_id;
+  const unsigned long long* round_ptr;  // if set, the round id is read here
+  int *child_tok, *child_node, *n_child;  // [R][kmax], [R][kmax], [R]
+  float* child_z;                         // [R][kmax]
+  int n_chunks, chunk;                    // vocabulary chunks per row, tokens per chunk
+  float* part;                            // [n_chunks][R][6], the verify_merge layout
+  int* flags;
+};
+// vocabulary chunks per row for R rows (at most max_parts)
+int logits_verify_chunks(int R, int V, int max_parts);
+// the children plan and the per-chunk scan (2 launches); verify_merge folds the chunks
+void launch_logits_verify(LogitsVerifyArgs a, bool bf, cudaStream_t st);
+
 // *p = v, in stream order (sets the round id a captured graph reads)
 void launch_set_u64(unsigned long long* p, unsigned long long v, cudaStream_t st);
 

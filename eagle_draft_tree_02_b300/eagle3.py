@@ -88,6 +88,10 @@ _sig = {
     "eagle3_verify": (C.c_int, [_P, C.c_int, C.POINTER(eagle3_tree), C.POINTER(eagle3_kv), C.c_int,
                                 C.c_float, C.c_ulonglong, C.c_ulonglong, _P, _P, _P,
                                 C.POINTER(eagle3_verify_stats), _P]),
+    "eagle3_verify_logits": (C.c_int, [_P, C.c_int, C.POINTER(eagle3_tree), _P, C.c_int,
+                                       C.c_longlong, C.c_int, C.c_float, C.c_ulonglong,
+                                       C.c_ulonglong, _P, _P, _P, C.POINTER(eagle3_verify_stats),
+                                       _P]),
     "eagle3_graph_capture": (C.c_int, [_P, C.c_int, C.c_int, _P, _P, C.POINTER(eagle3_kv),
                                        C.POINTER(eagle3_tree), C.c_int, C.c_int, C.c_float,
                                        C.c_ulonglong, _P, _P, _P, _P]),
@@ -171,6 +175,14 @@ def eagle3_verify(ctx, B, tree: eagle3_tree, kv: eagle3_kv, mode, temperature, s
                   stream=0) -> int:
     return lib.eagle3_verify(ctx, B, C.byref(tree), C.byref(kv), mode, temperature, seed, round_id,
                              accept_len, path, out_tokens, _ref(stats), stream)
+
+
+def eagle3_verify_logits(ctx, B, tree: eagle3_tree, logits, logits_dtype, ld, mode, temperature,
+                         seed, round_id, accept_len, path, out_tokens,
+                         stats: eagle3_verify_stats | None = None, stream=0) -> int:
+    return lib.eagle3_verify_logits(ctx, B, C.byref(tree), logits, logits_dtype, ld, mode,
+                                    temperature, seed, round_id, accept_len, path, out_tokens,
+                                    _ref(stats), stream)
 
 
 def eagle3_graph_capture(ctx, B, n_new, feats_new, tokens_new, kv: eagle3_kv, tree: eagle3_tree,

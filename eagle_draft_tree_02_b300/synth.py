@@ -190,3 +190,18 @@ def make_inputs(cfg: RoundConfig, seed: int | None = None, threads: int | None =
         page_table = perm.reshape(B, per)
     return RoundInputs(cfg=cfg, seed=seed, w=w, prefix_lens=plen, feats=feats, tokens=tokens,
                        cu_rows=cu, page_table=page_table, n_pages=n_pages)
+
+
+T_LOGITS = 40  # tensor id of caller-supplied target logits (test inputs)
+
+
+def draw_logits(seed: int, rows: int, V: int, ld: int, std: float, dtype: str) -> np.ndarray:
+    """Stand-in target logits [rows, ld]: N(0, std^2) in the first V columns,
+    zeros in the row padding, rounded once to the storage type (bf16 as raw
+    uint16 bits)."""
+    z = _rng(seed, T_LOGITS).standard_normal((rows, V)) * std
+    out = np.zeros((rows, ld), dtype=np.float64)
+    out[:, :V] = z
+    if dtype == "bf16":
+        return bf16_bits_from_f64(out.reshape(-1)).reshape(rows, ld)
+    return out.astype(np.float32)

@@ -327,6 +327,39 @@ eagle3_status eagle3_verify(eagle3_ctx* ctx, int B, const eagle3_tree* tree, con
                             unsigned long long round_id, int* accept_len, int* path,
                             int* out_tokens, eagle3_verify_stats* stats, eagle3_stream stream);
 
+/* Strict verification of a kept tree against target logits that the caller
+ * supplies ("EAGLE-3 精读" §5 正确性、复现与风险: greedy keeps the target's
+ * greedy sequence; sampling keeps the target's distribution when the residual
+ * correction is done).  This is the form a real target model drives: it
+ * scores every tree node in one forward pass and passes its logits here, in
+ * place of eagle3_verify's synthetic target.
+ *   tree: a kept tree in the layout of eagle3_draft_round's output (device;
+ *     node 0 the root, parents before children, padding slots token -1); at
+ *     most `topk` children per node and depth at most `depth` (the walk
+ *     accepts at most `depth` tokens).  The tree need not come from this
+ *     context's last round.
+ *   logits: [B, M+1, ld] device array (caller-owned) in logits_dtype
+ *     (EAGLE3_FP32 or EAGLE3_BF16): row (b, u) holds the target's logits of
+ *     the token after node u's root-to-node path; only the first `vocab`
+ *     entries of a row are read, and padding rows are not read.  ld >= vocab
+ *     elements; the base address and ld * element size must be multiples of
+ *     16 bytes (EAGLE3_ERR_INVALID_ARG otherwise).
+ *   mode 0: greedy -- walk from the root while the target's argmax (ties:
+ *     lowest token) is a child's token, then emit that argmax as the bonus;
+ *   mode 1: sampling at `temperature` > 0 -- point-mass acceptance of the
+ *     children in tree order and a Gumbel draw from the residual, with the
+ *     Philox4x64-10 counter layout of eagle3_verify mode 1 (identical logits
+ *     give identical draws); mode 2 returns EAGLE3_ERR_UNSUPPORTED.
+ * Outputs as eagle3_verify: accept_len [B], path [B, D], out_tokens [B, D+1],
+ * stats (may be NULL).  A node with more than topk children, a parent index
+ * out of range or a token outside [0, vocab) raises the device flag that
+ * eagle3_check reports.  The logits are read once, from HBM. */
+eagle3_status eagle3_verify_logits(eagle3_ctx* ctx, int B, const eagle3_tree* tree, const void* logits,
+                                   int logits_dtype, long long ld, int mode, float temperature,
+                                   unsigned long long seed, unsigned long long round_id,
+                                   int* accept_len, int* path, int* out_tokens,
+                                   eagle3_verify_stats* stats, eagle3_stream stream);
+
 /* Record one whole step -- eagle3_draft_round followed, if with_verify, by
  * eagle3_verify, with the same arguments as those two calls (no pool or stats
  * outputs; the verify arguments are ignored without with_verify) -- into a
