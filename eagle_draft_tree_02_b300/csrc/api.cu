@@ -104,6 +104,7 @@ bool use_split(const eagle3_ctx* c, int R) { return c->bf && R <= kSplitMaxRows;
 CtlDev round_control(const eagle3_ctx* c, int B) {
   CtlDev d = c->ctl;
   d.clip = c->sampled ? 1 : 0;
+  d.lmax = c->sampled ? c->top_lse : nullptr;  // written by the sampled head (largest log q)
   if (!d.on) return d;
   const eagle3_control& h = c->ctl_host;
   int kc = c->k;
@@ -423,6 +424,7 @@ void sampled_head(eagle3_ctx* c, const void* H, int R, bool split, int slot0, in
   sa.logits = c->lg;
   sa.tok = c->top_tok;
   sa.logq = c->top_logq;
+  sa.lmax = c->top_lse;
   launch_sample_children(sa, R, st);
   c->launches++;
 }

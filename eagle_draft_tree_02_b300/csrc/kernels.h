@@ -136,7 +136,8 @@ struct CtlDev {
   const float* verify_us;  // [M+1]
   int* d_eff;           // [B] depth the request runs to (set at pass 0, lowered by the rule)
   int* active;          // [D + 1] requests active at pass t
-  int clip;             // sampled draft: sibling scores non-increasing in draw order (any `on`)
+  int clip;             // sampled draft: a draw's score from the earlier draws only (any `on`)
+  const float* lmax;    // sampled draft: [rows] the row's largest log q (clip only)
 };
 // pass 0 rows: n_new rows per request, or the ragged rows given by cu_new [B+1]
 void launch_plan_root(int B, int n_new, const int* cu_new, int total, int max_new,
@@ -193,6 +194,7 @@ struct SampleArgs {  // sampled children of a pass's rows (Gumbel-top-k over the
   const float* logits;  // [R][V]
   int* tok;             // [R][k] in draw order
   float* logq;          // [R][k]
+  float* lmax;          // [R] largest log q of the row
 };
 void launch_sample_children(const SampleArgs& a, int R, cudaStream_t st);
 struct QratioArgs {  // q-ratio verification walk

@@ -5,7 +5,8 @@
 // Drafting: a node's k children are drawn from the draft distribution q
 // without replacement, as the k largest keys log q(x) + G(x) (Gumbel-top-k;
 // G from the Philox stream 2 counter of the node's slot), in draw order, with
-// their true log q.
+// their true log q and the row's largest log q, from which the expansion
+// scores the draws (each from the draws before it only).
 //
 // Verification at a node: the draws c_1 .. c_m in draw order are tested in
 // turn; c_i is accepted when U_i q_i(c_i) < p_i(c_i); on a rejection
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(kThreads) sample_children_kernel(SampleArgs a)
   for (int x = threadIdx.x; x < a.V; x += blockDim.x) s += __expf(ell[x] - m);
   s = block_sum(s, redf);
   const float lse = m + logf(s);
+  if (threadIdx.x == 0) a.lmax[row] = m - lse;  // log of the row's largest probability
   // Gumbel keys: thread t takes the 4-token groups t, t + blockDim, ...
   const int b = row / a.rows_per_req, slot = a.slot0 + row % a.rows_per_req;
   const unsigned long long rid = a.round_ptr ? *a.round_ptr : a.round_id;

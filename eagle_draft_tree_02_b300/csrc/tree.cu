@@ -181,9 +181,11 @@ __global__ void expand_kernel(CtlDev ctl, int B, int t, int k, int D, const int*
     pfwd[idx] = -1;
     if (real) {
       float lq = top_logq[(size_t)row * k + j];
-      float lc = lq;  // sampled draft: clipped to the smallest log q of the earlier draws
-      if (ctl.clip)
+      float lc = lq;
+      if (ctl.clip) {  // sampled draft: min(log max q, log q of the earlier draws), never its own
+        lc = ctl.lmax[row];
         for (int j2 = 0; j2 < j; ++j2) lc = fminf(lc, top_logq[(size_t)row * k + j2]);
+      }
       float s = (parent < 0 ? 0.f : psc[parent]) + lc;
       ptok[idx] = top_tok[(size_t)row * k + j];
       ppar[idx] = parent;

@@ -76,9 +76,12 @@ enum { EAGLE3_FC_NORM = 1, EAGLE3_POST_NORM = 2, EAGLE3_SAMPLED_DRAFT = 4 };
  * from the draft distribution q without replacement -- the k largest
  * log q(x) + G(x), G Gumbel noise from Philox stream 2 at (round id, b,
  * node slot) keyed by the seed of eagle3_draft_noise -- in draw order, with
- * their true log q; a child's score is clipped to be non-increasing in draw
- * order, so a kept sibling set is always the first draws.  eagle3_verify mode
- * 2 then verifies against q (recursive rejection over the draws; see there).
+ * their true log q.  The i-th draw's score is its parent's score plus
+ * min(log max q, log q of draws 1..i-1): it depends only on the draws before
+ * it, never on the draw itself, and is non-increasing in draw order, so a
+ * kept sibling set is always the first draws and is chosen by a stopping
+ * rule -- the condition under which eagle3_verify mode 2 (recursive
+ * rejection over the kept draws; see there) keeps the target distribution.
  * The pass's logits are written to the workspace (rows x V fp32). */
 
 /* Shapes of the draft model and of the round.  All sizes in elements. */

@@ -56,9 +56,15 @@ Sampled drafting with q-ratio verification (R-17; "EAGLE-3 精读" §5: the
 draft's sampling verification keeps the target distribution with the residual
 correction, which with the min(1, p/q) rule needs children drawn from q): a
 node's k children are drawn from q without replacement by Gumbel-top-k
-(Philox stream 2 at the node's slot), in draw order; a child's score is
-clipped to be non-increasing in draw order, so a kept sibling set is always
-the first draws.  Verification walks the draws:
+(Philox stream 2 at the node's slot), in draw order.  The i-th draw's score
+is its parent's plus min(log max q, log q of draws 1..i-1): it never depends
+on the draw itself, only on what was drawn before it, and it is
+non-increasing in draw order.  So a kept sibling set is always the first
+draws, and whether the i-th draw is kept is decided without looking at it --
+a stopping rule, under which recursive rejection over the kept draws keeps
+the target distribution (a score that used the draw's own log q made the
+number of verified siblings depend on the draws and biased the emitted
+tokens).  Verification walks the draws:
 the i-th is accepted when U q_i(c) < p_i(c); on rejection p_{i+1} =
 norm(max(0, p_i - q_i)) and q_{i+1} = q_i without c; with no acceptance the
 bonus is the Gumbel-argmax of log p over its support (stream 1).
@@ -114,6 +120,12 @@ class Decisions:
     def accept_q(self, b, node, i, u, q_child, p_child):
         """q-ratio test of the i-th draw: accept when U q_i(c) < p_i(c)."""
         return u * q_child < p_child
+
+    def draw_score(self, cap, logq_draw):
+        """Score increment of a sampled draw (R-17): `cap`, the node's largest
+        log q capped by the log q of its earlier draws; the draw's own log q
+        (logq_draw) is deliberately not used."""
+        return cap
 
     def keep_drafting(self, b, t, mass, threshold):
         """Cost-aware depth rule: run pass t (mass = the frontier's sum of exp(score))."""
@@ -267,12 +279,14 @@ def draft_request(w, cfg, K, V, feat_root, tok_root, root_pos, dec: Decisions, b
                 slot = 0 if depth == 0 else 1 + (depth - 1) * k_ + rank
                 keys = logq + philox.gumbel(samp[0], samp[1], b, slot, np.asarray(cand), stream=2)
                 order = dec.children(b, depth, rank, cand, keys, k_)
-            run_min = 0.0
+            # sampled draft: the i-th draw's score uses only what was drawn before it
+            # (the node's largest log q, capped by the earlier draws' log q)
+            cap = float(np.max(logq))
             for jr, j in enumerate(order):
                 if jr < kb:
-                    run_min = logq[j] if samp is None or jr == 0 else min(run_min, logq[j])
-                    pool.add(cand[j], parent, base + (logq[j] if samp is None else run_min),
-                             depth + 1, logq[j])
+                    inc = logq[j] if samp is None else dec.draw_score(cap, float(logq[j]))
+                    pool.add(cand[j], parent, base + inc, depth + 1, logq[j])
+                    cap = min(cap, float(logq[j]))
                 else:
                     pool.add(-1, -1, ninf, depth + 1, ninf)
 

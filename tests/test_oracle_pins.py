@@ -683,3 +683,64 @@ def test_sampled_round_keeps_sibling_prefixes_in_draw_order():
     plain = R.round_request(w, cfg, K, V, f[P - 1], inp.tokens[P - 1], P - 1, with_verify=False)
     assert p.tok != plain.draft.pool.tok
     assert all(0 <= t < cfg.vocab for t in p.tok if t >= 0)
+
+
+# whole sampled round at V = 8 (d = 32 so the draft and target heads differ)
+_V8_ROUND = CONFIGS[0].scaled(name="samp_round_v8", d=32, n_q_heads=2, n_kv_heads=2, head_dim=16,
+                              ffn=32, vocab=8, prefix=6, depth=3, topk=2, n_verify=6, lm_std=0.3,
+                              sampled_draft=True)
+
+
+class _OwnDrawScore(R.Decisions):
+    """Planted mistake: a draw's score uses its own log q (the running minimum
+    including the draw), so whether a draw is kept depends on the draw itself."""
+
+    def draw_score(self, cap, logq_draw):
+        return min(cap, logq_draw)
+
+
+def _sampled_round_marginals(n, dec=None):
+    """Emitted tokens of the whole sampled round (draft + q-ratio verification)
+    over n round ids, and the target distributions at the root and at the
+    depth-1 node of each token."""
+    cfg = _V8_ROUND
+    inp = make_inputs(cfg, seed=3)
+    w = R.weights_f32(inp)
+    f = inp.feats_f32()
+    P = int(inp.prefix_lens[0])
+    K, V = R.prefix_kv(w, cfg, f[:P], inp.tokens[:P])
+    acc, out = np.zeros(n, dtype=np.int64), np.full((n, cfg.depth + 1), -1)
+    for rid in range(n):
+        rr = R.round_request(w, cfg, K, V, f[P - 1], inp.tokens[P - 1], P - 1,
+                             temperatures=(1.0,), seed=17, round_id=rid, samp=(11, rid), dec=dec)
+        r = rr.verify[1.0]
+        acc[rid] = r.accept_len
+        out[rid, :len(r.out_tokens)] = r.out_tokens
+    s_root, h_root = R.root_forward(w, cfg, K, V, f[P - 1], inp.tokens[P - 1], P - 1)
+    z1 = {}
+    for c in range(cfg.vocab):   # a depth-1 node's target logits depend on its token only
+        pool = R.Pool()
+        pool.add(c, -1, 0.0, 1, 0.0)
+        tr = R.build_tree([c], [-1], np.array([0.0]), [1], int(inp.tokens[P - 1]), P - 1, 1)
+        z, _ = R.verify_logits(w, cfg, K, V, P - 1, tr, R.DraftResult(pool, s_root, h_root, {}, {},
+                                                                      {}, []))
+        z1[c] = z[1]
+    soft = lambda v: np.exp(v - L.logsumexp(v))
+    pv = [_chi2_p(out[:, 0], soft(z[0]))]
+    for c in range(cfg.vocab):
+        sel = (acc >= 1) & (out[:, 0] == c)
+        if sel.sum() > 1000:
+            pv.append(_chi2_p(out[sel, 1], soft(z1[c])))
+    return pv
+
+
+@pytest.mark.slow
+def test_sampled_round_second_token_follows_the_target():
+    """Whole sampled round (R-17): the first emitted token follows p at the root,
+    and given the accepted depth-1 child c the second follows p at c, because a
+    draw's score never looks at the draw itself; the planted own-draw score,
+    which lets the draws decide how many siblings are verified, is rejected."""
+    pv = _sampled_round_marginals(6000)
+    assert len(pv) >= 2 and min(pv) > 1e-3, pv
+    bad = _sampled_round_marginals(6000, _OwnDrawScore())
+    assert min(bad) < 1e-4, bad
