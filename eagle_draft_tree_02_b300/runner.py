@@ -74,7 +74,10 @@ class Engine:
     """One context plus the device copies of one round's inputs and its KV cache."""
 
     def __init__(self, inputs: RoundInputs, device="cuda", max_new: int = 1, with_target=True,
-                 max_prefix_extra: int = 0):
+                 max_prefix_extra: int = 0, page_capacity: tuple | None = None):
+        """page_capacity = (logical pages per request, physical pages) sizes a
+        paged cache for requests that join and leave the batch; the inputs'
+        page table fills the first columns of each request's row."""
         self.inp = inputs
         cfg = self.cfg = inputs.cfg
         self.device = torch.device(device)
@@ -85,7 +88,12 @@ class Engine:
         # contiguous cache: room for the prefix plus rows later rounds commit
         self.max_prefix = int(inputs.prefix_lens.max()) + max_prefix_extra
         if cfg.page_size:
-            self.max_prefix = inputs.page_table.shape[1] * cfg.page_size
+            pt = inputs.page_table.astype(np.int32)
+            pages_per_req, n_pages = (pt.shape[1], inputs.n_pages) if page_capacity is None \
+                else page_capacity
+            table = np.zeros((self.B, pages_per_req), dtype=np.int32)
+            table[:, :pt.shape[1]] = pt
+            self.max_prefix = pages_per_req * cfg.page_size
         ws = E.eagle3_weights()
         for n in E.WEIGHT_NAMES:
             setattr(ws, n, self.w[n].data_ptr() if n in self.w else None)
@@ -99,12 +107,11 @@ class Engine:
         kvd = (cfg.n_kv_heads, cfg.head_dim)
         self.kv = E.eagle3_kv()
         if cfg.page_size:
-            n_pages = inputs.n_pages
             self.k_cache = torch.zeros((n_pages, cfg.page_size) + kvd, dtype=dt, device=dev)
             self.v_cache = torch.zeros_like(self.k_cache)
-            self.page_table = to_device(inputs.page_table.astype(np.int32), dev)
+            self.page_table = to_device(table, dev)
             self.kv.page_table = self.page_table.data_ptr()
-            self.kv.max_pages = inputs.page_table.shape[1]
+            self.kv.max_pages = pages_per_req
             self.kv.n_pages = n_pages
         else:
             self.k_cache = torch.zeros((self.B, self.max_prefix) + kvd, dtype=dt, device=dev)

@@ -30,24 +30,8 @@ class GpuRound:
 
 
 def gpu_round(eng, temps=(0.0,), seed=0, round_id=0) -> GpuRound:
-    import torch
     eng.draft_round(with_pool=True)
-    torch.cuda.synchronize()
-    eng.check()
-    tree = {k: getattr(eng.tree, k).cpu().numpy() for k in
-            ("tokens", "parent", "depth", "pos", "pool_index", "score", "mask")}
-    pool = {k: getattr(eng.pool, k).cpu().numpy() for k in ("tok", "parent", "depth", "fwd", "score", "logq")}
-    if eng.pool.cand is not None:
-        pool["cand"] = eng.pool.cand.cpu().numpy()
-    out = GpuRound(tree, pool)
-    for T in temps:
-        a, p, o = eng.verify(T, seed, round_id)
-        torch.cuda.synchronize()
-        eng.check()
-        out.verify[T] = dict(accept_len=a.cpu().numpy().copy(), path=p.cpu().numpy().copy(),
-                             out_tokens=o.cpu().numpy().copy(),
-                             stats={k: v.cpu().numpy().copy() for k, v in eng.stats_t.items()})
-    return out
+    return gpu_outputs(eng, temps, lambda T: eng.verify(T, seed, round_id))
 
 
 class Report:
@@ -235,74 +219,105 @@ class Follow(R.Decisions):
         return self._adopt(("bonus", b, node), [own], [g], scores, self.tol)[0]
 
 
+def gpu_outputs(eng, temps, verify_fn) -> GpuRound:
+    """Host copies of the round just drafted on `eng` (its tree and pool buffers)
+    and of verify_fn(T) -> (accept_len, path, out_tokens) for each T."""
+    import torch
+    torch.cuda.synchronize()
+    eng.check()
+    tree = {k: getattr(eng.tree, k).cpu().numpy() for k in
+            ("tokens", "parent", "depth", "pos", "pool_index", "score", "mask")}
+    pool = {k: getattr(eng.pool, k).cpu().numpy() for k in ("tok", "parent", "depth", "fwd", "score", "logq")}
+    if eng.pool.cand is not None:
+        pool["cand"] = eng.pool.cand.cpu().numpy()
+    out = GpuRound(tree, pool)
+    for T in temps:
+        a, p, o = verify_fn(T)
+        torch.cuda.synchronize()
+        eng.check()
+        out.verify[T] = dict(accept_len=a.cpu().numpy().copy(), path=p.cpu().numpy().copy(),
+                             out_tokens=o.cpu().numpy().copy(),
+                             stats={k: v.cpu().numpy().copy() for k, v in eng.stats_t.items()})
+    return out
+
+
 def compare(cfg, inp, gpu: GpuRound, temps, seed=0, round_id=0, prefix_kv=None, requests=None,
             ctl=None, samp=None):
     """Conditioned oracle run and element-wise comparison.  Returns a Report."""
-    tol = TOL[cfg.dtype]
     rep = Report()
     w = R.weights_f32(inp)
     feats = inp.feats_f32()
     for b in (requests if requests is not None else range(cfg.batch)):
         lo, hi = int(inp.cu_rows[b]), int(inp.cu_rows[b + 1])
-        P = hi - lo
         if prefix_kv is None:
             K, V = R.prefix_kv(w, cfg, feats[lo:hi], inp.tokens[lo:hi])
         else:
             K, V = prefix_kv(b)
-        dec = Follow(cfg, gpu, rep, tol["tie"])
-        dr = R.draft_request(w, cfg, K, V, feats[hi - 1], inp.tokens[hi - 1], P - 1, dec, b, ctl,
-                             cfg.batch, samp)
-        pool = dr.pool
-        n = len(pool.tok)
-        # pool: tokens / parents / depth exact; log q and scores within tolerance
-        for name, mine in (("tok", pool.tok), ("parent", pool.parent), ("depth", pool.depth)):
-            if not np.array_equal(np.asarray(mine), gpu.pool[name][b, :n]):
-                rep.failures.append(("pool-" + name, b))
-        made = np.asarray(pool.tok) >= 0  # created nodes (the rest hold -inf)
-        if not (np.isneginf(gpu.pool["score"][b, :n][~made]).all()
-                and np.isneginf(gpu.pool["logq"][b, :n][~made]).all()):
-            rep.failures.append(("pool-uncreated", b))
-        if made.any():
-            rep.err("logq", np.max(np.abs(np.asarray(pool.logq)[made] - gpu.pool["logq"][b, :n][made])))
-            dsc = (np.abs(np.asarray(pool.score)[made] - gpu.pool["score"][b, :n][made])
-                   / np.maximum(1, np.asarray(pool.depth)[made]))
-            rep.err("score/depth", np.max(dsc))
-        tree = R.build_tree(pool.tok, pool.parent, pool.score, pool.depth, inp.tokens[hi - 1], P - 1,
-                            cfg.n_verify, dec, b, ctl)
-        for name, mine in (("tokens", tree.tok), ("parent", tree.parent), ("depth", tree.depth),
-                           ("pos", tree.pos), ("pool_index", tree.pool_index)):
-            if not np.array_equal(np.asarray(mine), gpu.tree[name][b]):
-                rep.failures.append(("tree-" + name, b))
-        mask_bits = np.zeros_like(tree.mask)
-        words = gpu.tree["mask"][b]
-        for i in range(tree.mask.shape[0]):
-            for j in range(tree.mask.shape[1]):
-                mask_bits[i, j] = (int(words[i, j >> 5]) >> (j & 31)) & 1
-        if not np.array_equal(mask_bits, tree.mask):
-            rep.failures.append(("tree-mask", b))
-        if not temps:
-            continue
-        z, hv = R.verify_logits(w, cfg, K, V, P - 1, tree, dr)
-        for T in temps:
-            st = gpu.verify[T]["stats"]
-            nr = z.shape[0]  # the root and the kept nodes (padding slots are not verified)
-            rep.err("z_max", np.max(np.abs(z.max(axis=1) - st["z_max"][b][:nr])))
-            zt = z / (T if T else 1.0)
-            rep.err("lse", np.max(np.abs(L.logsumexp(zt) - st["lse"][b][:nr])))
-            dec.T = T
-            if T == 0:
-                res = R.verify_greedy(tree, z, dec, b)
-            elif samp is None:
-                res = R.verify_sample(tree, z, T, seed, round_id, dec, b)
-            else:
-                res = R.verify_qratio(tree, z, L.linear(hv, w["w_lm"]), T, seed, round_id, dec, b)
-            v = gpu.verify[T]
-            if int(v["accept_len"][b]) != res.accept_len:
-                rep.failures.append(("accept_len", T, b))
-            gp = [int(x) for x in v["path"][b] if x >= 0]
-            if gp != res.path:
-                rep.failures.append(("path", T, b))
-            go = [int(x) for x in v["out_tokens"][b] if x >= 0]
-            if go != res.out_tokens:
-                rep.failures.append(("out_tokens", T, b))
+        compare_request(cfg, w, K, V, feats[hi - 1], inp.tokens[hi - 1], hi - lo, gpu, b, temps,
+                        rep, seed, round_id, ctl, samp)
+    return rep
+
+
+def compare_request(cfg, w, K, V, feat_root, tok_root, P, gpu: GpuRound, b, temps, rep: Report,
+                    seed=0, round_id=0, ctl=None, samp=None, B=None):
+    """Request b of a GPU round against the oracle's round from its committed
+    rows: K, V the prefix cache of rows 0..P-1 (the root, row P-1, included),
+    feat_root / tok_root the root row.  Adds failures, errors and near-ties to rep."""
+    tol = TOL[cfg.dtype]
+    B = cfg.batch if B is None else B
+    dec = Follow(cfg, gpu, rep, tol["tie"])
+    dr = R.draft_request(w, cfg, K, V, feat_root, tok_root, P - 1, dec, b, ctl, B, samp)
+    pool = dr.pool
+    n = len(pool.tok)
+    # pool: tokens / parents / depth exact; log q and scores within tolerance
+    for name, mine in (("tok", pool.tok), ("parent", pool.parent), ("depth", pool.depth)):
+        if not np.array_equal(np.asarray(mine), gpu.pool[name][b, :n]):
+            rep.failures.append(("pool-" + name, b))
+    made = np.asarray(pool.tok) >= 0  # created nodes (the rest hold -inf)
+    if not (np.isneginf(gpu.pool["score"][b, :n][~made]).all()
+            and np.isneginf(gpu.pool["logq"][b, :n][~made]).all()):
+        rep.failures.append(("pool-uncreated", b))
+    if made.any():
+        rep.err("logq", np.max(np.abs(np.asarray(pool.logq)[made] - gpu.pool["logq"][b, :n][made])))
+        dsc = (np.abs(np.asarray(pool.score)[made] - gpu.pool["score"][b, :n][made])
+               / np.maximum(1, np.asarray(pool.depth)[made]))
+        rep.err("score/depth", np.max(dsc))
+    tree = R.build_tree(pool.tok, pool.parent, pool.score, pool.depth, tok_root, P - 1,
+                        cfg.n_verify, dec, b, ctl)
+    for name, mine in (("tokens", tree.tok), ("parent", tree.parent), ("depth", tree.depth),
+                       ("pos", tree.pos), ("pool_index", tree.pool_index)):
+        if not np.array_equal(np.asarray(mine), gpu.tree[name][b]):
+            rep.failures.append(("tree-" + name, b))
+    mask_bits = np.zeros_like(tree.mask)
+    words = gpu.tree["mask"][b]
+    for i in range(tree.mask.shape[0]):
+        for j in range(tree.mask.shape[1]):
+            mask_bits[i, j] = (int(words[i, j >> 5]) >> (j & 31)) & 1
+    if not np.array_equal(mask_bits, tree.mask):
+        rep.failures.append(("tree-mask", b))
+    if not temps:
+        return rep
+    z, hv = R.verify_logits(w, cfg, K, V, P - 1, tree, dr)
+    for T in temps:
+        st = gpu.verify[T]["stats"]
+        nr = z.shape[0]  # the root and the kept nodes (padding slots are not verified)
+        rep.err("z_max", np.max(np.abs(z.max(axis=1) - st["z_max"][b][:nr])))
+        zt = z / (T if T else 1.0)
+        rep.err("lse", np.max(np.abs(L.logsumexp(zt) - st["lse"][b][:nr])))
+        dec.T = T
+        if T == 0:
+            res = R.verify_greedy(tree, z, dec, b)
+        elif samp is None:
+            res = R.verify_sample(tree, z, T, seed, round_id, dec, b)
+        else:
+            res = R.verify_qratio(tree, z, L.linear(hv, w["w_lm"]), T, seed, round_id, dec, b)
+        v = gpu.verify[T]
+        if int(v["accept_len"][b]) != res.accept_len:
+            rep.failures.append(("accept_len", T, b))
+        gp = [int(x) for x in v["path"][b] if x >= 0]
+        if gp != res.path:
+            rep.failures.append(("path", T, b))
+        go = [int(x) for x in v["out_tokens"][b] if x >= 0]
+        if go != res.out_tokens:
+            rep.failures.append(("out_tokens", T, b))
     return rep

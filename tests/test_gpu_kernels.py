@@ -15,6 +15,8 @@ C0 = CONFIGS[0]
 LIN_BF16 = C0.scaled(name="lin_bf16", dtype="bf16", d=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
                      ffn=512, vocab=1000, prefix=400, batch=2, depth=3, topk=4, n_verify=8,
                      lm_std=0.08)
+# the fp32 context needs a prefix long enough for 300 rows of row capacity
+LIN_FP32 = C0.scaled(name="lin_fp32", prefix=400)
 NAMES = ["w_fc", "w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down", "w_lm", "w_target"]
 
 
@@ -22,7 +24,7 @@ NAMES = ["w_fc", "w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down", "w_lm",
 def lin_engines(cuda, lib_built):
     from eagle_draft_tree_02_b300.runner import Engine
     out = {}
-    for cfg in (LIN_BF16, C0):
+    for cfg in (LIN_BF16, LIN_FP32):
         inp = make_inputs(cfg, seed=21)
         out[cfg.dtype] = (inp, Engine(inp))
     return out
