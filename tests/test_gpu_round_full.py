@@ -1,26 +1,48 @@
 """GPU parity at the workloads' full sizes (the launch configuration bench.py times).
 
-* 8B-shaped tree, batch 1, prefix 2048: the oracle recomputes everything
-  (prefix K/V included) and checks the whole round, greedy and T=1.
-* 8B-shaped serving batch 64, chain of 3, paged cache with 64-token pages:
-  sampled requests, each recomputed by the oracle from its own features.
-* 70B-shaped tree, batch 4, prefix 8192: sampled K/V rows of the cache are
-  checked against the oracle, then the oracle's round for a sampled request
-  runs on the GPU's cache (conditioned on the shared prefix K/V).
-* two-stage head tree, batch 16, prefix 4096, vocabulary 151936: as the 70B
-  case, for two sampled requests; the GPU's candidate sets must be valid
-  top-64 sets of the oracle's low-rank scores.
+Every request of every workload is checked.  The oracle runs each request's
+round on the GPU's own prefix K/V (read back from the cache, through the
+page table for the paged serving batch), after sampled rows of that cache
+have been checked against the oracle's own K/V at their true positions; this
+keeps the CPU work to the round itself.  Near-ties (decisions whose oracle
+margin is under the tie tolerance, which the parity rule counts instead of
+failing) are reported in every assertion message and bounded per workload.
+
+* 8B-shaped tree, batch 1, prefix 2048, greedy and T=1.
+* 8B-shaped serving batch 64, chain of 3, paged cache with 64-token pages.
+* 70B-shaped tree, batch 4, prefix 8192, T=1.
+* two-stage head tree, batch 16, prefix 4096, vocabulary 151936, greedy and
+  T=1; the GPU's candidate sets must be valid top-64 sets of the oracle's
+  low-rank scores.
 """
 import numpy as np
 import pytest
 
 from eagle_draft_tree_02_b300.configs import CONFIGS
 from eagle_draft_tree_02_b300.synth import make_inputs
+from oracle import layers as L
 from oracle import round as R
-from parity import TOL, compare, gpu_round
+from parity import TOL, Report, compare_request, gpu_round
+
+# largest near-tie count accepted per workload (all requests, all temperatures)
+NEAR_TIE_LIMIT = {"llama31_8b_b1_tree": 4, "llama31_8b_b64_chain3_paged": 8,
+                  "llama33_70b_b4_tree": 8, "two_stage_head_b16_tree": 16}
 
 
-def _run(cfg, requests=None, conditioned_kv=False, kv_rows_checked=0):
+def _cache_rows(eng, b, P):
+    """Request b's prefix K/V rows 0..P-1 from the GPU cache, as float64."""
+    cfg = eng.cfg
+    if cfg.page_size:
+        ps = cfg.page_size
+        pages = eng.page_table[b, :(P + ps - 1) // ps].long()
+        k = eng.k_cache[pages].reshape(-1, cfg.n_kv_heads, cfg.head_dim)[:P]
+        v = eng.v_cache[pages].reshape(-1, cfg.n_kv_heads, cfg.head_dim)[:P]
+    else:
+        k, v = eng.k_cache[b, :P], eng.v_cache[b, :P]
+    return (k.float().cpu().numpy().astype(np.float64), v.float().cpu().numpy().astype(np.float64))
+
+
+def _run(cfg, kv_rows_checked):
     import torch
     from eagle_draft_tree_02_b300.runner import Engine
     inp = make_inputs(cfg)
@@ -30,53 +52,53 @@ def _run(cfg, requests=None, conditioned_kv=False, kv_rows_checked=0):
     eng.check()
     temps = cfg.temperatures
     gpu = gpu_round(eng, temps, seed=0, round_id=7)
-    prefix_kv = None
-    if conditioned_kv:
-        w = R.weights_f32(inp)
-        f = inp.feats_f32()
-        rng = np.random.default_rng(0)
-        cache = {}
-        for b in requests:
-            lo, hi = int(inp.cu_rows[b]), int(inp.cu_rows[b + 1])
-            P = hi - lo
-            gk = eng.k_cache[b, :P].float().cpu().numpy().astype(np.float64)
-            gv = eng.v_cache[b, :P].float().cpu().numpy().astype(np.float64)
-            rows = np.sort(rng.choice(P, size=min(P, kv_rows_checked), replace=False))
-            # sampled rows at their true positions
-            from oracle import layers as L
-            g = L.fused_feature(w, cfg, f[lo:hi][rows])
-            x = L.decoder_input(w, cfg, inp.tokens[lo:hi][rows], g)
-            _, k, v = L.qkv(w, cfg, x, rows)
-            tol = TOL[cfg.dtype]["logit"]
-            assert np.abs(gk[rows] - k).max() < tol and np.abs(gv[rows] - v).max() < tol
-            cache[b] = (gk, gv)
-        prefix_kv = lambda b: cache[b]
-    rep = compare(cfg, inp, gpu, temps, seed=0, round_id=7, prefix_kv=prefix_kv, requests=requests)
+    # float64 copies of the weights, made once: the oracle's products then read them directly
+    w = {k: np.asarray(v, dtype=np.float64) if k != "embed" else v
+         for k, v in R.weights_f32(inp).items()}
+    f = inp.feats_f32()
+    rng = np.random.default_rng(0)
     tol = TOL[cfg.dtype]
-    print(cfg.name, rep)
-    assert not rep.failures, rep
-    assert rep.max_err["logq"] <= tol["logit"], rep
-    assert rep.max_err["score/depth"] <= tol["logit"], rep
-    assert rep.max_err["z_max"] <= tol["logit"] and rep.max_err["lse"] <= tol["logit"], rep
+    rep = Report()
+    kv_err = 0.0
+    for b in range(cfg.batch):
+        lo, hi = int(inp.cu_rows[b]), int(inp.cu_rows[b + 1])
+        P = hi - lo
+        K, V = _cache_rows(eng, b, P)
+        rows = np.sort(rng.choice(P, size=min(P, kv_rows_checked), replace=False))
+        g = L.fused_feature(w, cfg, f[lo:hi][rows])
+        x = L.decoder_input(w, cfg, inp.tokens[lo:hi][rows], g)
+        _, k, v = L.qkv(w, cfg, x, rows)
+        kv_err = max(kv_err, np.abs(K[rows] - k).max(), np.abs(V[rows] - v).max())
+        compare_request(cfg, w, K, V, f[hi - 1], inp.tokens[hi - 1], P, gpu, b, temps, rep,
+                        seed=0, round_id=7)
+    n_ties = len(rep.near_ties)
+    msg = f"{cfg.name}: near-ties {n_ties} (limit {NEAR_TIE_LIMIT[cfg.name]}), {rep}, kv_err {kv_err:.3g}"
+    print(msg)
+    assert kv_err < tol["logit"], msg
+    assert not rep.failures, msg
+    assert rep.max_err["logq"] <= tol["logit"], msg
+    assert rep.max_err["score/depth"] <= tol["logit"], msg
+    assert rep.max_err["z_max"] <= tol["logit"] and rep.max_err["lse"] <= tol["logit"], msg
+    assert n_ties <= NEAR_TIE_LIMIT[cfg.name], msg
     eng.close()
     return rep
 
 
 @pytest.mark.gpu
 def test_full_8b_batch1_tree(cuda, lib_built):
-    _run(CONFIGS[1])
+    _run(CONFIGS[1], kv_rows_checked=32)
 
 
 @pytest.mark.gpu
 def test_full_8b_batch64_chain_paged(cuda, lib_built):
-    _run(CONFIGS[2], requests=[0, 17, 63])
+    _run(CONFIGS[2], kv_rows_checked=4)
 
 
 @pytest.mark.gpu
 def test_full_70b_batch4_tree(cuda, lib_built):
-    _run(CONFIGS[3], requests=[2], conditioned_kv=True, kv_rows_checked=24)
+    _run(CONFIGS[3], kv_rows_checked=16)
 
 
 @pytest.mark.gpu
 def test_full_two_stage_b16_tree(cuda, lib_built):
-    _run(CONFIGS[4], requests=[0, 11], conditioned_kv=True, kv_rows_checked=24)
+    _run(CONFIGS[4], kv_rows_checked=8)
