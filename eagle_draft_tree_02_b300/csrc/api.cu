@@ -385,7 +385,7 @@ void draft_head_lowrank(eagle3_ctx* c, const void* H, int R, bool split, int* to
     }
   }
   DISPATCH(c, launch_lowrank_select, la, st);
-  c->launches++;
+  c->launches += 2;
 }
 
 void draft_head(eagle3_ctx* c, const void* H, int R, bool split, int* tok, float* logq, float* lse,
@@ -613,6 +613,9 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
     add((void**)&c->la.cval, (size_t)Rlm * kLrCap * 4);
     add((void**)&c->la.ctok, (size_t)Rlm * kLrCap * 4);
     add((void**)&c->cand_all, (size_t)B * c->n_exp * f.lr_cand * 4);
+    add((void**)&c->la.sel_tok, (size_t)Rlm * f.lr_cand * 4);
+    add((void**)&c->la.sel_z, (size_t)Rlm * f.lr_cand * 4);
+    add((void**)&c->la.sel_done, (size_t)Rlm * 4);
   }
   add((void**)&c->d_round, 8);
   add((void**)&c->flags, 64);

@@ -435,6 +435,7 @@ struct PhArgs {
   uint32_t tmem_cols, acc_cols, idesc;
   HeadParts hp;
   VerifyHeadArgs va;
+  LowRankArgs la;      // MODE 4: the two-stage head's threshold append
   int* flags;
 };
 
@@ -766,6 +767,30 @@ __device__ __forceinline__ void verify_chunk(float* mine, const VerifyHeadArgs& 
   __syncwarp();
 }
 
+// Two-stage head, threshold append over one chunk of 16 rows (nr of them
+// real) of this warp's 32 tokens: every token whose low-rank score reaches
+// its row's threshold joins the row's candidate buffer (one atomic per warp
+// and row that has any).  No running state: the buffer is the output.
+__device__ __forceinline__ void append_chunk(const LowRankArgs& la, int r0, int nr,
+                                             const float (&x)[16], int tok0, int lane) {
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    if (q >= nr) break;
+    const int r = r0 + q;
+    const bool ok = x[q] != -INFINITY && x[q] >= la.thr[r];
+    const unsigned bal = __ballot_sync(0xffffffffu, ok);
+    if (!bal) continue;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(la.cnt + r, __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+    if (ok && pos < kLrCap) {
+      la.cval[(size_t)r * kLrCap + pos] = x[q];
+      la.ctok[(size_t)r * kLrCap + pos] = tok0 + lane;
+    }
+  }
+}
+
 #ifndef E3_HEAD_CTAS_PER_SM
 #define E3_HEAD_CTAS_PER_SM 2
 #endif
@@ -949,8 +974,10 @@ __global__ void __launch_bounds__(kHeadThreads, 2)
         load_rows16(taddr, r0, a.split != 0, a.ncols, nr, valid, x);
         if (MODE == 1)
           draft_chunk(mine, a.sw, a.hp.k, r0, nr, x, tok0, lane);
-        else
+        else if (MODE == 2)
           verify_chunk(mine, a.va, a.R, a.r_off, r0, nr, x, tok0, lane, evs, n_ev);
+        else
+          append_chunk(a.la, r0, nr, x, tok0, lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -959,7 +986,7 @@ __global__ void __launch_bounds__(kHeadThreads, 2)
     // combine the four lane quarters' states; warp e takes rows r = e (mod
     // kHeadEpiWarps) and writes one partial per (CTA, row)
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kHeadEpiWarps) : "memory");
-    if (!*abort_f) {
+    if (MODE != 4 && !*abort_f) {
       const int part = blockIdx.x;
       for (int r = e; r < a.R; r += kHeadEpiWarps) {
         float* st = state + (size_t)r * a.sw;  // quarter 0's state of row r gathers the others
@@ -1169,7 +1196,7 @@ bool launch_head(TcGemm* t, const CUtensorMap* wmap, int V, int K, const void* X
   const int ntile = std::max(16, cdiv(ncols, 16) * 16);
   uint32_t acc = 32;
   while (acc < (uint32_t)ntile) acc <<= 1;
-  const int sw = MODE == 1 ? 2 + 2 * args.hp.k : 6;
+  const int sw = MODE == 1 ? 2 + 2 * args.hp.k : (MODE == 2 ? 6 : 0);
   const size_t state = (size_t)4 * R * sw * 4 + (MODE == 2 ? (size_t)R * args.va.kmax * 8 : 0);
   const size_t stage = (A_STAGE + (size_t)ntile * BK * 2) * kHeadKSub;
   // CTAs per SM: as configured, but their double-buffered accumulators must
@@ -1300,6 +1327,16 @@ int lowrank_tc_groups(int V) { return 4 * cdiv(std::min(V, kLrSampleTokens), BM)
 
 bool tc_lowrank(TcGemm* t, int mode, const LowRankArgs& la, int* flags, cudaStream_t st) {
   if (!t || !t->wptr[TCW_LRU] || la.R <= 0 || la.R > 256 || (mode != 0 && mode != 1)) return false;
+  if (mode == 1) {
+    // the append pass over the whole vocabulary: the persistent head when it fits
+    PhArgs pa{};
+    pa.la = la;
+    pa.flags = flags;
+    int n_parts = 0;
+    if (launch_head<4>(t, &t->wmap[TCW_LRU], t->wN[TCW_LRU], t->wK[TCW_LRU], la.t, la.R,
+                       la.t_split != 0, pa, n_parts, st))
+      return true;
+  }
   TcArgs args{};
   args.nseg = 1;
   args.seg_end[0] = cdiv(t->wN[TCW_LRU], BM);

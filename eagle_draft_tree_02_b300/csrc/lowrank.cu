@@ -219,21 +219,20 @@ __device__ void exact_topc(const LowRankArgs& a, int r, const float* t_s, unsign
   sort_keys_desc(key, 128);
 }
 
+// Per row: the C candidates in low-rank order (score desc, token asc) from the
+// appended buffer (or, after an overflow, the exact radix select), written to
+// sel_tok and, when asked, to the exported candidate lists.  Resets the row's
+// rescoring counter.
 template <typename T>
 __global__ void __launch_bounds__(kSelThreads) lowrank_select_kernel(LowRankArgs a) {
   pdl_begin();
   extern __shared__ unsigned long long sel_smem[];
-  unsigned long long* key = sel_smem;                 // [kLrCap]
-  float* h_s = reinterpret_cast<float*>(key + kLrCap);  // [d]
-  float* t_s = h_s + a.d;                             // [r]
-  float* ex = t_s + a.r;                              // [C] exact logits
-  int* ctk = reinterpret_cast<int*>(ex + 128);        // [C] candidate tokens
+  unsigned long long* key = sel_smem;                   // [kLrCap]
+  float* t_s = reinterpret_cast<float*>(key + kLrCap);  // [r]
   __shared__ unsigned hist[256];
   __shared__ int sh_n;
   __shared__ unsigned long long sh_prefix;
-  __shared__ float red[32];
-  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int nw = blockDim.x >> 5, C = a.C;
+  const int r = blockIdx.x, tid = threadIdx.x, C = a.C;
 
   const int n = a.cnt[r];
   if (n <= kLrCap - 128) {
@@ -259,63 +258,102 @@ __global__ void __launch_bounds__(kSelThreads) lowrank_select_kernel(LowRankArgs
     __syncthreads();
     exact_topc<T>(a, r, t_s, key, hist, &sh_n, &sh_prefix);
   }
-  for (int i = tid; i < C; i += blockDim.x)
-    ctk[i] = (int)(0xFFFFFFFFu - (uint32_t)(key[i] & 0xFFFFFFFFull));
-  for (int j = tid; j < a.d; j += blockDim.x) h_s[j] = act_at((const T*)a.H, r, a.d, j, a.h_split);
-  __syncthreads();
+  int* out = a.sel_tok + (size_t)r * C;
+  for (int i = tid; i < C; i += blockDim.x) out[i] = (int)(0xFFFFFFFFu - (uint32_t)(key[i] & 0xFFFFFFFFull));
   if (a.cand_out) {
     const int b = r / a.cand_rpr, j = r % a.cand_rpr;
     int* dst = a.cand_out + ((size_t)b * a.cand_n_exp + a.cand_slot0 + j) * C;
-    for (int i = tid; i < C; i += blockDim.x) dst[i] = ctk[i];
+    for (int i = tid; i < C; i += blockDim.x) dst[i] = (int)(0xFFFFFFFFu - (uint32_t)(key[i] & 0xFFFFFFFFull));
   }
-  // exact logits of the candidates: one warp per candidate, 16-byte loads of
-  // the head row (8 bf16 or 4 fp32 per lane and step)
-  constexpr int VEC = 16 / sizeof(T);
-  for (int c = wid; c < C; c += nw) {
-    if (ctk[c] < 0 || ctk[c] >= a.V) {  // only after an aborted low-rank pass
-      if (lane == 0) {
-        ex[c] = -INFINITY;
-        raise_flag(a.flags, FLAG_TOKEN_RANGE);
-      }
-      continue;
-    }
-    const T* w = (const T*)a.W + (size_t)ctk[c] * a.d;
-    float acc = 0.f;
-    if (a.d % VEC == 0 && ((uintptr_t)w & 15) == 0) {
-      for (int j = lane * VEC; j < a.d; j += 32 * VEC) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(w + j);
-        const T* e = reinterpret_cast<const T*>(&raw);
-#pragma unroll
-        for (int u = 0; u < VEC; ++u) acc = fmaf(ldf(e + u), h_s[j + u], acc);
-      }
-    } else {
-      for (int j = lane; j < a.d; j += 32) acc = fmaf(ldf(w + j), h_s[j], acc);
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) ex[c] = acc;
-  }
+  if (tid == 0) a.sel_done[r] = 0;
+}
+
+// Exact logits of the candidates: block (row, group of kRescoreWarps
+// candidates), one warp per candidate, every load of the head row in flight
+// before the products.  The last block of a row to finish takes log q over
+// the C candidates and the k best of them.
+constexpr int kRescoreWarps = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kRescoreWarps) lowrank_rescore_kernel(LowRankArgs a) {
+  pdl_begin();
+  extern __shared__ float h_s[];  // [d]
+  __shared__ int s_last;
+  __shared__ float red[32];
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int C = a.C;
+  for (int j = tid; j < a.d; j += blockDim.x) h_s[j] = act_at((const T*)a.H, r, a.d, j, a.h_split);
   __syncthreads();
-  // log-sum-exp over C
+  const int c = blockIdx.y * kRescoreWarps + wid;
+  if (c < C) {
+    const int x = a.sel_tok[(size_t)r * C + c];
+    float z = -INFINITY;
+    if (x < 0 || x >= a.V) {  // only after an aborted low-rank pass
+      if (lane == 0) raise_flag(a.flags, FLAG_TOKEN_RANGE);
+    } else {
+      const T* w = (const T*)a.W + (size_t)x * a.d;
+      constexpr int VEC = 16 / sizeof(T);
+      constexpr int U = 8;  // 16-byte loads in flight per lane
+      float acc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = 0.f;
+      if (a.d % VEC == 0 && ((uintptr_t)w & 15) == 0) {
+        for (int j0 = lane * VEC; j0 < a.d; j0 += 32 * VEC * U) {
+          uint4 raw[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * 32 * VEC;
+            raw[u] = j < a.d ? __ldg(reinterpret_cast<const uint4*>(w + j)) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * 32 * VEC;
+            if (j < a.d) {
+              const T* e = reinterpret_cast<const T*>(&raw[u]);
+#pragma unroll
+              for (int v = 0; v < VEC; ++v) acc[u] = fmaf(ldf(e + v), h_s[j + v], acc[u]);
+            }
+          }
+        }
+      } else {
+        for (int j = lane; j < a.d; j += 32) acc[0] = fmaf(ldf(w + j), h_s[j], acc[0]);
+      }
+      float t = 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u) t += acc[u];
+      z = warp_sum(t);
+    }
+    if (lane == 0) a.sel_z[(size_t)r * C + c] = z;
+  }
+  // the last block of this row to finish: log q over the C candidates, top k
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.sel_done + r, 1) == (int)gridDim.y - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* ex = a.sel_z + (size_t)r * C;
+  const int* ctk = a.sel_tok + (size_t)r * C;
   float m = -INFINITY;
-  for (int c = tid; c < C; c += blockDim.x) m = fmaxf(m, ex[c]);
+  for (int i = tid; i < C; i += blockDim.x) m = fmaxf(m, ex[i]);
   m = warp_max(m);
   if (lane == 0) red[wid] = m;
   __syncthreads();
   if (tid < 32) {
-    float v = tid < nw ? red[tid] : -INFINITY;
+    float v = tid < kRescoreWarps ? red[tid] : -INFINITY;
     v = warp_max(v);
     if (tid == 0) red[0] = v;
   }
   __syncthreads();
   m = red[0];
   float s = 0.f;
-  for (int c = tid; c < C; c += blockDim.x) s += expf(ex[c] - m);
+  for (int i = tid; i < C; i += blockDim.x) s += expf(ex[i] - m);
   s = block_sum(s, red);
   const float lse = m + logf(s);
   // the k best of C by (exact logit desc, token asc)
-  for (int c = tid; c < C; c += blockDim.x) {
-    const float v = ex[c];
-    const int x = ctk[c];
+  for (int i = tid; i < C; i += blockDim.x) {
+    const float v = ex[i];
+    const int x = ctk[i];
     int rank = 0;
     for (int o = 0; o < C; ++o) rank += better(ex[o], ctk[o], v, x);
     if (rank < a.k) {
@@ -328,9 +366,12 @@ __global__ void __launch_bounds__(kSelThreads) lowrank_select_kernel(LowRankArgs
 
 template <typename T>
 void launch_lowrank_select(const LowRankArgs& a, cudaStream_t st) {
-  const size_t smem = (size_t)kLrCap * 8 + (size_t)(a.d + a.r + 128) * 4 + 128 * 4;
+  const size_t smem = (size_t)kLrCap * 8 + (size_t)a.r * 4;
   smem_limit((const void*)lowrank_select_kernel<T>, 200 * 1024);  // refusal: the launch fails
   launch_pdl(lowrank_select_kernel<T>, dim3(a.R), dim3(kSelThreads), smem, st, a);
+  smem_limit((const void*)lowrank_rescore_kernel<T>, 200 * 1024);
+  launch_pdl(lowrank_rescore_kernel<T>, dim3(a.R, (a.C + kRescoreWarps - 1) / kRescoreWarps),
+             dim3(32 * kRescoreWarps), (size_t)a.d * 4, st, a);
 }
 
 template void launch_reduce_store<float>(int, int, int, const float*, void*, bool, cudaStream_t);

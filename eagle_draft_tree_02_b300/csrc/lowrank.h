@@ -37,6 +37,9 @@ struct LowRankArgs {
   float* lse;              // [R] log-sum-exp over the C candidates (may be NULL)
   int* cand_out;           // optional [B][n_exp][C] candidates in low-rank order
   int cand_n_exp, cand_slot0, cand_rpr;
+  int* sel_tok;            // [R][C] candidates of each row, low-rank order (workspace)
+  float* sel_z;            // [R][C] their exact logits (workspace)
+  int* sel_done;           // [R] rescoring blocks finished per row (workspace)
   int* flags;
 };
 // fp32 storage: low-rank scores of a 64x64 tile on CUDA cores; mode 0 writes
@@ -47,6 +50,7 @@ int lowrank_tc_groups(int V);
 // per row: thr = C-th largest group maximum (-inf when there are fewer than C
 // groups), and the append counter reset to 0
 void launch_lowrank_threshold(const LowRankArgs& a, cudaStream_t st);
+// per row: the C candidates, then their exact logits, log q over C and top k (2 launches)
 template <typename T> void launch_lowrank_select(const LowRankArgs& a, cudaStream_t st);
 // Y rows from split-K partials: out row r (split or plain) = sum_s part[s][r]
 template <typename T>
