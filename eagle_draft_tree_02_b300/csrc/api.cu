@@ -325,6 +325,8 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   a.split = split;
   a.flags = c->flags;
   a.skip = c->skip;
+  // only the root pass writes prefix rows (its new rows) in the same pass
+  a.prefix_stable = tree.slots > 0;
   DISPATCH(c, launch_tree_attention, a, st);
   c->launches += 2;
   // r = hid + W_o o ; z = rms(r)

@@ -308,8 +308,6 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 // and merge their softmax states at the end; KW = 1: one warp per 16 queries.
 template <int DH, int KW>
 __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
-  pdl_begin();
-  if (a.skip && *a.skip == 0) return;
   constexpr int LD = DH + 8;       // shared row stride (bf16): conflict-free fragment loads
   constexpr int NKT = KC / 8 / KW; // key tiles of 8 per chunk and warp
   constexpr int NDT = DH / 8;      // output tiles of 8 dims
@@ -344,38 +342,6 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
     key_hi = min(a.tree_slots, key_lo + KC);
   }
   const int n_chunks = key_hi > key_lo ? (tree ? 1 : (key_hi - key_lo + KC - 1) / KC) : 0;
-
-  // this thread's two query rows (g and g + 8 of the warp's 16), scaled by 1/sqrt(dh)
-  const int qr[2] = {qw + g, qw + g + 8};
-  const float* qp[2];
-  const uint32_t* mrow_bits[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    qp[h] = nullptr;
-    mrow_bits[h] = nullptr;
-    if (qr[h] < nq) {
-      const int row = b * a.rows_per_req + qr[h] / G, head = kvh * G + qr[h] % G;
-      qp[h] = a.q + (size_t)a.q_row[row] * a.Hq * DH + (size_t)head * DH;
-      mrow_bits[h] = a.mask + (size_t)row * a.mask_words;
-    }
-  }
-  const float scale = rsqrtf((float)DH);
-  uint32_t qh[NKS][4], ql[NKS][4];
-#pragma unroll
-  for (int ks = 0; ks < NKS; ++ks) {
-#pragma unroll
-    for (int f = 0; f < 4; ++f) {  // fragment f: row g (+8 if f odd), cols +8 if f >= 2
-      const float* p = qp[f & 1];
-      const int c = ks * 16 + t4 * 2 + (f >> 1) * 8;
-      const float x0 = p ? p[c] * scale : 0.f, x1 = p ? p[c + 1] * scale : 0.f;
-      split_pair(x0, x1, qh[ks][f], ql[ks][f]);
-    }
-  }
-  float o[NDT][4];
-#pragma unroll
-  for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  const bool active = qw < nq;
 
   // Prefix chunks stream through a ring of KST stages.  Thread t copies one
   // row of every chunk -- key t % KC of K (t < KC) or of V -- with a bulk copy
@@ -412,6 +378,59 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
       att_arrive(bar);
     }
   };
+  auto start_ring = [&]() -> int {  // the first KST - 1 chunks; returns the next chunk's page
+    if (tid == 0) {
+      for (int st = 0; st < KST; ++st) att_mbar_init(bar0 + 8u * st, blockDim.x);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    for (int ci = 0; ci < KST - 1 && ci < n_chunks; ++ci) issue(ci, page_of(ci));
+    return page_of(KST - 1);
+  };
+  // When no kernel of this pass writes the prefix cache (every pass after the
+  // root's), the first chunks are requested before the wait for the previous
+  // kernel, so their latency overlaps its tail; the queries and tree rows follow.
+  const bool early = a.prefix_stable && !tree && n_chunks > 0;
+  int pg_next = early ? start_ring() : 0;
+  pdl_begin();
+  if (a.skip && *a.skip == 0) {
+    if (early)  // let the requested chunks land before the shared memory is released
+      for (int ci = 0; ci < KST - 1 && ci < n_chunks; ++ci) att_wait(bar0 + 8u * ci, 0u, a.flags);
+    return;
+  }
+
+  // this thread's two query rows (g and g + 8 of the warp's 16), scaled by 1/sqrt(dh)
+  const int qr[2] = {qw + g, qw + g + 8};
+  const float* qp[2];
+  const uint32_t* mrow_bits[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    qp[h] = nullptr;
+    mrow_bits[h] = nullptr;
+    if (qr[h] < nq) {
+      const int row = b * a.rows_per_req + qr[h] / G, head = kvh * G + qr[h] % G;
+      qp[h] = a.q + (size_t)a.q_row[row] * a.Hq * DH + (size_t)head * DH;
+      mrow_bits[h] = a.mask + (size_t)row * a.mask_words;
+    }
+  }
+  const float scale = rsqrtf((float)DH);
+  uint32_t qh[NKS][4], ql[NKS][4];
+#pragma unroll
+  for (int ks = 0; ks < NKS; ++ks) {
+#pragma unroll
+    for (int f = 0; f < 4; ++f) {  // fragment f: row g (+8 if f odd), cols +8 if f >= 2
+      const float* p = qp[f & 1];
+      const int c = ks * 16 + t4 * 2 + (f >> 1) * 8;
+      const float x0 = p ? p[c] * scale : 0.f, x1 = p ? p[c + 1] * scale : 0.f;
+      split_pair(x0, x1, qh[ks][f], ql[ks][f]);
+    }
+  }
+  float o[NDT][4];
+#pragma unroll
+  for (int i = 0; i < NDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  const bool active = qw < nq;
+
   // tree chunk: buffer 0 holds hi, buffer 1 lo, of K and of V
   auto load_tree = [&]() {
     for (int i = tid; i < KC * PIECES; i += blockDim.x) {
@@ -444,17 +463,10 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
     }
   };
 
-  int pg_next = 0;
   if (tree) {
     if (n_chunks > 0) load_tree();
-  } else {
-    if (tid == 0) {
-      for (int st = 0; st < KST; ++st) att_mbar_init(bar0 + 8u * st, blockDim.x);
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    for (int ci = 0; ci < KST - 1 && ci < n_chunks; ++ci) issue(ci, page_of(ci));
-    pg_next = page_of(KST - 1);
+  } else if (!early) {
+    pg_next = start_ring();
   }
   for (int ci = 0; ci < n_chunks; ++ci) {
     const int c0 = key_lo + ci * KC, buf = tree ? 0 : ci % KST;
@@ -685,13 +697,23 @@ __global__ void attention_combine_kernel(AttnArgs a) {
   }
   l = block_sum(l, red);
   const float inv = l > 0.f ? 1.f / l : 0.f;
+  const size_t sstride = (size_t)R * a.Hq * a.dh;  // one split's partials
   for (int dd = tid; dd < a.dh; dd += blockDim.x) {
-    float o = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < n_splits; ++s) {
-      const float w = wts[s];
-      if (w != 0.f) o += a.o_part[(((size_t)s * R + row) * a.Hq + head) * a.dh + dd] * w;
+    // eight splits' loads in flight at a time, each into its own accumulator
+    const float* op = a.o_part + ((size_t)row * a.Hq + head) * a.dh + dd;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int s = 0;
+    for (; s + 8 <= n_splits; s += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = op[(size_t)(s + u) * sstride];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] += v[u] * wts[s + u];
     }
+    for (; s < n_splits; ++s) acc[0] += op[(size_t)s * sstride] * wts[s];
+    float o = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) o += acc[u];
     st_act((T*)a.out + act_row(row, a.Hq * a.dh, a.split), a.Hq * a.dh, head * a.dh + dd, o * inv,
            a.split);
   }

@@ -49,10 +49,18 @@ __global__ void build_input_kernel(int R, int d, int V, float eps, const int* __
 
 // ----------------------------------------------------------------------------- split-K sum
 __device__ __forceinline__ float sum_parts(const float* p, size_t stride, int S) {
-  float v = p[0];
-#pragma unroll 4
-  for (int s = 1; s < S; ++s) v += p[(size_t)s * stride];
-  return v;
+  // eight partials' loads in flight at a time
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int s = 0;
+  for (; s + 8 <= S; s += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = p[(size_t)(s + u) * stride];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc[u] += v[u];
+  }
+  for (; s < S; ++s) acc[0] += p[(size_t)s * stride];
+  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
 // g = sum of fusion partials (fp32 [R, d])

@@ -72,6 +72,7 @@ struct AttnArgs {
   bool split;
   int* flags;
   const int* skip;  // if set and *skip == 0 (no request active in the pass), the kernels return
+  bool prefix_stable;  // no kernel since the last completed one writes the prefix cache
 };
 // Launches the key splits (prefix and tree) and their merge: 2 launches.
 template <typename T> void launch_tree_attention(const AttnArgs& a, cudaStream_t st);
@@ -151,6 +152,7 @@ void launch_plan_prefill(int rows, int r0, int B, const int* cu_rows, const int*
 void launch_expand(const CtlDev& ctl, int B, int t, int k, int D, const int* top_tok, const float* top_logq,
                    const PoolDev& pool, int* frontier, uint32_t* slot_mask, int slot_words,
                    const int* root_pos, int n_slots, const RowPlan& rp, cudaStream_t st);
+
 void launch_build_tree(const CtlDev& ctl, int B, int pool_n, int M, const int* tok, const int* parent,
                        const float* score, const int* depth, const int* root_tok,
                        const int* root_pos, int* t_tok, int* t_parent, int* t_depth, int* t_pos,
