@@ -148,9 +148,6 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(HeadParts hp,
   pdl_begin();
   if (hp.skip && *hp.skip == 0) return;
   __shared__ float red_m[32], red_s[32];
-  __shared__ int red_i[32];
-  __shared__ float win_v;
-  __shared__ int win_i;
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nw = blockDim.x >> 5, k = K;
   float m = -INFINITY, s = 0.f;
@@ -195,42 +192,15 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(HeadParts hp,
     red_m[wid] = m;
     red_s[wid] = s;
   }
-  __syncthreads();
-  if (wid == 0) {
-    float m2 = lane < nw ? red_m[lane] : -INFINITY;
-    float s2 = lane < nw ? red_s[lane] : 0.f;
-    warp_lse(m2, s2);
-    if (lane == 0) {
-      red_m[0] = m2;
-      red_s[0] = s2;
-    }
-  }
-  __syncthreads();
-  const float lse = red_m[0] + logf(red_s[0]);
-  if (tid == 0 && lse_out) lse_out[r] = lse;
-  // k rounds of block argmax over the list heads
-  for (int j = 0; j < k; ++j) {
-    __syncthreads();  // red_* and win_* free again
+  // each warp's k best: k rounds of a warp argmax over its lanes' list heads
+  __shared__ float wv[kMergeThreads / 32][K];
+  __shared__ int wi_s[kMergeThreads / 32][K];
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
     float bv = lv[0];
     int bi = li[0];
     warp_best(bv, bi);
-    if (lane == 0) {
-      red_m[wid] = bv;
-      red_i[wid] = bi;
-    }
-    __syncthreads();
-    if (wid == 0) {
-      float v2 = lane < nw ? red_m[lane] : -INFINITY;
-      int i2 = lane < nw ? red_i[lane] : 0x7fffffff;
-      warp_best(v2, i2);
-      if (lane == 0) {
-        win_v = v2;
-        win_i = i2;
-      }
-    }
-    __syncthreads();
-    const int wi = win_i;
-    if (wi != 0x7fffffff && li[0] == wi) {  // the owner pops its head
+    if (bi != 0x7fffffff && li[0] == bi) {  // the owner pops its head
 #pragma unroll
       for (int q = 0; q < K - 1; ++q) {
         lv[q] = lv[q + 1];
@@ -239,9 +209,30 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(HeadParts hp,
       lv[K - 1] = -INFINITY;
       li[K - 1] = 0x7fffffff;
     }
-    if (tid == 0) {
-      tok[(size_t)r * k + j] = wi == 0x7fffffff ? -1 : wi;
-      logq[(size_t)r * k + j] = win_v - lse;
+    if (lane == 0) {
+      wv[wid][j] = bv;
+      wi_s[wid][j] = bi;
+    }
+  }
+  __syncthreads();
+  if (wid != 0) return;
+  float m2 = lane < nw ? red_m[lane] : -INFINITY;
+  float s2 = lane < nw ? red_s[lane] : 0.f;
+  warp_lse(m2, s2);
+  const float lse = m2 + logf(s2);
+  if (lane == 0 && lse_out) lse_out[r] = lse;
+  // the block's k best: k rounds of a warp argmax over the warps' sorted lists
+  int head = 0;  // lane j walks warp j's list
+#pragma unroll
+  for (int j = 0; j < K; ++j) {
+    float bv = (lane < nw && head < K) ? wv[lane][head] : -INFINITY;
+    int bi = (lane < nw && head < K) ? wi_s[lane][head] : 0x7fffffff;
+    const int mine = bi;
+    warp_best(bv, bi);
+    if (bi != 0x7fffffff && mine == bi) ++head;
+    if (lane == 0) {
+      tok[(size_t)r * k + j] = bi == 0x7fffffff ? -1 : bi;
+      logq[(size_t)r * k + j] = bv - lse;
     }
   }
 }
