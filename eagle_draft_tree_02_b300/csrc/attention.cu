@@ -20,7 +20,12 @@
 // Q and P enter as hi + lo bf16 pairs (two MMAs each), so the products keep
 // about 16 significant bits, and K, V are the cache's exact values.  (With P
 // as one bf16, the 70B-shaped tree's log q error grew from 2e-4 to 1e-3 at no
-// measurable gain in time.)  A tree split stages its 64 fp32 slots as bf16
+// measurable gain in time.  With fp16 operands -- K and V converted exactly
+// after each chunk lands, Q and P one fp16 each, one MMA per product -- the
+// 8B-shaped launch fell from 19 to 15 us, but the 70B-shaped log q error grew
+// from 2.5e-4 to 8.5e-3; splitting Q as fp16 hi + lo brought the error back and
+// the time with it, and the conversion pass slowed the paged batch of chains.)
+// A tree split stages its 64 fp32 slots as bf16
 // (hi, lo) pairs and adds the lo products (three MMAs per fragment), with the
 // ancestor mask applied per query row.  The fp32 cache uses the CUDA-core kernel: 32
 // queries per block, K and V staged as fp32.
