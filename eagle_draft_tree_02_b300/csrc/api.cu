@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -82,6 +83,11 @@ struct eagle3_ctx {
   float *lg = nullptr, *pqw = nullptr;
   // tcgen05 GEMM plans
   TcGemm* tc = nullptr;
+  // tensor maps of the caller's K/V cache (tensor-core attention), re-encoded
+  // when the cache pointers or sizes change
+  const void *km_k = nullptr, *km_v = nullptr;
+  int km_T = 0, km_rows = 0;
+  CUtensorMap km_mk, km_mv;
   // CUDA graph of one step (draft round + verify), replayed by eagle3_graph_launch
   unsigned long long* d_round = nullptr;        // round id read by the captured verify kernels
   const unsigned long long* round_ptr = nullptr; // set while capturing
@@ -280,7 +286,7 @@ void kv_rows(eagle3_ctx* c, int R, const void* feats, bool has_q, const float* h
 // queries per KV head make it compute-bound, e.g. 240 verify queries.)
 void attn_splits(const eagle3_ctx* c, int B, int rows_per_req, int& kps, int& nps) {
   const eagle3_config& f = c->cfg;
-  const bool mma = attention_uses_mma(c->esz, f.head_dim);
+  const bool mma = attention_uses_mma(c->esz, f.head_dim, f.page_size);
   int blocks = B * f.n_kv_heads * attention_qgroups(rows_per_req, f.n_q_heads, f.n_kv_heads, mma);
   int maxp = f.max_prefix;
   const int target = mma ? 4 * 148 : kTargetBlocks;
@@ -312,6 +318,31 @@ void tail_rows(eagle3_ctx* c, int B, int rows_per_req, const float* hid_base, co
   a.max_pages = kv->max_pages;
   a.n_pages = kv->n_pages;
   a.max_prefix = f.max_prefix;
+  if (attention_uses_mma(c->esz, f.head_dim, f.page_size)) {
+    const int rows = attention_box_rows(f.page_size);
+    const long long T =
+        f.page_size ? (long long)kv->n_pages * f.page_size : (long long)f.max_batch * f.max_prefix;
+    if (T <= 0 || T > (long long)INT_MAX - 2 * 64) {
+      tc_error(c, "K/V cache rows out of the attention's tensor-map range");
+      return;
+    }
+    if (c->km_k != kv->k || c->km_v != kv->v || c->km_T != (int)T || c->km_rows != rows) {
+      c->km_k = c->km_v = nullptr;
+      if (!encode_kv_map(&c->km_mk, kv->k, (int)T, f.n_kv_heads, f.head_dim, rows) ||
+          !encode_kv_map(&c->km_mv, kv->v, (int)T, f.n_kv_heads, f.head_dim, rows)) {
+        tc_error(c, "cuTensorMapEncodeTiled refused the K/V cache");
+        return;
+      }
+      c->km_k = kv->k;
+      c->km_v = kv->v;
+      c->km_T = (int)T;
+      c->km_rows = rows;
+    }
+    a.tm_rows = rows;
+    a.tm_T = (int)T;
+    a.tm_k = c->km_mk;
+    a.tm_v = c->km_mv;
+  }
   a.tree_k = tree.k;
   a.tree_v = tree.v;
   a.tree_slots = tree.slots;

@@ -14,8 +14,11 @@
 //
 // bf16 cache, prefix splits: one block of 4 warps per (request, KV head, group
 // of <= 64 queries, split); 64-key chunks of K and V stream through a 3-stage
-// ring in shared memory, one 256-byte row per thread by a bulk copy that
-// completes on the stage's mbarrier, and the 16 queries of a warp take Q K^T
+// ring in shared memory as tensor-map boxes (64 dims x 1 KV head x 64 tokens,
+// or a page's share of them; 128-byte swizzle), a few per chunk from lanes of
+// warp 0, completing on the stage's mbarrier.  (One 256-byte bulk copy per
+// row and thread, 128 per chunk, held the batch-64 paged pass to 2.2 TB/s:
+// the copies, not the bytes, set the pace.)  The 16 queries of a warp take Q K^T
 // and P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
 // Q and P enter as hi + lo bf16 pairs (two MMAs each), so the products keep
 // about 16 significant bits, and K, V are the cache's exact values.  (With P
@@ -55,7 +58,23 @@ int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma) {
   return (per + q - 1) / q;
 }
 
-bool attention_uses_mma(int elem_bytes, int dh) { return elem_bytes == 2 && (dh == 64 || dh == 128); }
+// The tensor-core kernel loads whole boxes of at least 8 tokens, so a paged
+// cache needs pages of a multiple of 8 tokens; other page sizes (and fp32)
+// take the CUDA-core kernel.
+bool attention_uses_mma(int elem_bytes, int dh, int page_size) {
+  return elem_bytes == 2 && (dh == 64 || dh == 128) && page_size >= 0 && page_size % 8 == 0;
+}
+
+int attention_box_rows(int page_size) {
+  if (page_size <= 0) return KC;
+  int a = KC, b = page_size;
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
 
 template <typename T>
 __device__ __forceinline__ const T* kv_row_ptr(const AttnArgs& a, const void* cache, int b, int pos,
@@ -257,12 +276,13 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-// One-dimensional bulk copy global -> shared, completing on an mbarrier.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+// One box of a three-dimensional tensor map global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                            int y, int z) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 __device__ __forceinline__ void att_mbar_init(uint32_t bar, uint32_t count) {
@@ -271,9 +291,6 @@ __device__ __forceinline__ void att_mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void att_arrive_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
-}
-__device__ __forceinline__ void att_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 // Bounded wait for the phase with the given parity: false (and the timeout
 // flag) after about two seconds.
@@ -312,16 +329,22 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
 // chunk (KW = 4 when a KV head has at most 16 queries, as in a batch of chains),
 // and merge their softmax states at the end; KW = 1: one warp per 16 queries.
 template <int DH, int KW>
-__global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
-  constexpr int LD = DH + 8;       // shared row stride (bf16): conflict-free fragment loads
+__global__ void __launch_bounds__(128) prefix_attention_mma_kernel(const __grid_constant__ AttnArgs a) {
   constexpr int NKT = KC / 8 / KW; // key tiles of 8 per chunk and warp
   constexpr int NDT = DH / 8;      // output tiles of 8 dims
   constexpr int NKS = DH / 16;     // k16 steps over dh
   constexpr int PIECES = DH / 8;   // 16-byte pieces per K or V row
+  constexpr int NH = DH / 64;      // 128-byte halves of a row
+  constexpr int HB = KC * 128;     // bytes of one half of a chunk: 64 rows of 128 B
+  constexpr int STB = 2 * NH * HB; // bytes of a stage: the K halves, then the V halves
+  // Stage layout: half h of key row n sits at h * HB + n * 128, its 16-byte
+  // piece j at ((j ^ (n & 7)) << 4) within the row (the tensor map's 128-byte
+  // swizzle), so the fragment loads of 8 consecutive rows hit 8 bank groups.
   extern __shared__ __align__(16) unsigned char att_smem[];
-  bf16* Ks = reinterpret_cast<bf16*>(att_smem);  // [KST][KC][LD]
-  bf16* Vs = Ks + KST * KC * LD;                 // [KST][KC][LD]
-  const uint32_t bar0 = smem_u32(Vs + KST * KC * LD);  // [KST] mbarriers
+  const uint32_t raw = smem_u32(att_smem);
+  unsigned char* sb = att_smem + (((raw + 1023u) & ~1023u) - raw);  // [KST][STB], 1024-aligned
+  const uint32_t sb32 = smem_u32(sb);
+  const uint32_t bar0 = sb32 + KST * STB;  // [KST] mbarriers
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv, split = blockIdx.z;
@@ -348,47 +371,47 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
   }
   const int n_chunks = key_hi > key_lo ? (tree ? 1 : (key_hi - key_lo + KC - 1) / KC) : 0;
 
-  // Prefix chunks stream through a ring of KST stages.  Thread t copies one
-  // row of every chunk -- key t % KC of K (t < KC) or of V -- with a bulk copy
-  // that completes on the stage's mbarrier; a key past the split's end, or on
-  // a bad page, gets a zero row instead.  Its page-table entry is fetched one
-  // chunk ahead of the copy.
-  const int ck = tid % KC;
-  const bf16* ccache = reinterpret_cast<const bf16*>(tid < KC ? a.cache_k : a.cache_v);
-  bf16* crow = (tid < KC ? Ks : Vs) + (size_t)ck * LD;
+  // Prefix chunks stream through a ring of KST stages, as tensor-map boxes
+  // of tm_rows tokens x 64 dims (one KV head): a chunk is KC / tm_rows token
+  // groups, each in 2 * NH boxes (K and V, each half of the row), and lane l
+  // of warp 0 (l < n_ops) copies box l of every chunk.  A group past the
+  // split's end, or on a bad page, is read at token row tm_T, past the tensor,
+  // which fills zeros.  The lane's page-table entry is fetched one chunk ahead.
+  const int per_group = 2 * NH, n_ops = (KC / a.tm_rows) * per_group;  // n_ops <= 32
+  const int my_grp = lane / per_group, my_box = lane % per_group;
+  const bool op_lane = warp == 0 && lane < n_ops;
   auto page_of = [&](int ci) -> int {
-    const int pos = key_lo + ci * KC + ck;
-    if (!a.page_table || ci >= n_chunks || pos >= key_hi) return 0;
+    const int pos = key_lo + ci * KC + my_grp * a.tm_rows;
+    if (!op_lane || !a.page_table || ci >= n_chunks || pos >= key_hi) return 0;
     return a.page_table[(size_t)b * a.max_pages + pos / a.page_size];
   };
-  auto issue = [&](int ci, int pg) {
-    const int st = ci % KST, pos = key_lo + ci * KC + ck;
-    const uint32_t dst = smem_u32(crow + (size_t)st * KC * LD), bar = bar0 + 8u * st;
-    long long row = -1;
-    if (pos < key_hi) {
-      if (!a.page_table)
-        row = (long long)b * a.max_prefix + pos;
-      else if (pg >= 0 && pg < a.n_pages)
-        row = (long long)pg * a.page_size + pos % a.page_size;
-      else
-        raise_flag(a.flags, FLAG_PAGE_RANGE);
-    }
-    if (row >= 0) {
-      att_arrive_tx(bar, DH * 2);
-      bulk_g2s(dst, ccache + ((size_t)row * a.Hkv + kvh) * DH, DH * 2, bar);
-    } else {
-#pragma unroll
-      for (int p = 0; p < PIECES; ++p)
-        *reinterpret_cast<uint4*>(crow + (size_t)st * KC * LD + p * 8) = make_uint4(0u, 0u, 0u, 0u);
-      att_arrive(bar);
+  auto issue = [&](int ci, int pg) {  // warp 0 only
+    const int st = ci % KST, pos = key_lo + ci * KC + my_grp * a.tm_rows;
+    const uint32_t bar = bar0 + 8u * st;
+    if (lane == 0) att_arrive_tx(bar, (uint32_t)STB);  // every box lands in full
+    __syncwarp();
+    if (lane < n_ops) {
+      int row = a.tm_T;
+      if (pos < key_hi) {
+        if (!a.page_table)
+          row = b * a.max_prefix + pos;
+        else if (pg >= 0 && pg < a.n_pages)
+          row = pg * a.page_size + pos % a.page_size;
+        else
+          raise_flag(a.flags, FLAG_PAGE_RANGE);
+      }
+      const int v = my_box / NH, h = my_box % NH;
+      const uint32_t dst = sb32 + st * STB + (v * NH + h) * HB + my_grp * a.tm_rows * 128;
+      tma_load_3d(dst, v ? &a.tm_v : &a.tm_k, bar, h * 64, kvh, row);
     }
   };
   auto start_ring = [&]() -> int {  // the first KST - 1 chunks; returns the next chunk's page
     if (tid == 0) {
-      for (int st = 0; st < KST; ++st) att_mbar_init(bar0 + 8u * st, blockDim.x);
+      for (int st = 0; st < KST; ++st) att_mbar_init(bar0 + 8u * st, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    if (warp != 0) return 0;
     for (int ci = 0; ci < KST - 1 && ci < n_chunks; ++ci) issue(ci, page_of(ci));
     return page_of(KST - 1);
   };
@@ -436,7 +459,7 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   const bool active = qw < nq;
 
-  // tree chunk: buffer 0 holds hi, buffer 1 lo, of K and of V
+  // tree chunk: stage 0 holds hi, stage 1 lo, of K and of V (same swizzled rows)
   auto load_tree = [&]() {
     for (int i = tid; i < KC * PIECES; i += blockDim.x) {
       const int kk = i / PIECES, piece = i % PIECES, slot = key_lo + kk;
@@ -460,11 +483,11 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
         split_pair(kx[2 * e], kx[2 * e + 1], khi[e], klo[e]);
         split_pair(vx[2 * e], vx[2 * e + 1], vhi[e], vlo[e]);
       }
-      const size_t o0 = (size_t)kk * LD + piece * 8, o1 = (size_t)(KC + kk) * LD + piece * 8;
-      *reinterpret_cast<uint4*>(Ks + o0) = make_uint4(khi[0], khi[1], khi[2], khi[3]);
-      *reinterpret_cast<uint4*>(Ks + o1) = make_uint4(klo[0], klo[1], klo[2], klo[3]);
-      *reinterpret_cast<uint4*>(Vs + o0) = make_uint4(vhi[0], vhi[1], vhi[2], vhi[3]);
-      *reinterpret_cast<uint4*>(Vs + o1) = make_uint4(vlo[0], vlo[1], vlo[2], vlo[3]);
+      const int o0 = (piece >> 3) * HB + kk * 128 + (((piece & 7) ^ (kk & 7)) << 4);
+      *reinterpret_cast<uint4*>(sb + o0) = make_uint4(khi[0], khi[1], khi[2], khi[3]);
+      *reinterpret_cast<uint4*>(sb + STB + o0) = make_uint4(klo[0], klo[1], klo[2], klo[3]);
+      *reinterpret_cast<uint4*>(sb + NH * HB + o0) = make_uint4(vhi[0], vhi[1], vhi[2], vhi[3]);
+      *reinterpret_cast<uint4*>(sb + STB + NH * HB + o0) = make_uint4(vlo[0], vlo[1], vlo[2], vlo[3]);
     }
   };
 
@@ -478,11 +501,21 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
     if (!tree) {
       // refill the stage that the previous chunk used, then wait for this one
       const int cn = ci + KST - 1;
-      if (cn < n_chunks) {
+      if (warp == 0 && cn < n_chunks) {
         issue(cn, pg_next);
         pg_next = page_of(cn + 1);
       }
       const bool ok = att_wait(bar0 + 8u * buf, (uint32_t)(ci / KST) & 1u, a.flags);
+      if (ok && c0 + KC > key_hi) {
+        // the split's last chunk is ragged: its rows past key_hi hold whatever
+        // follows in the cache, so V gets zero rows there (P is 0 on them, and
+        // 0 times a stale non-finite value would not be)
+        unsigned char* vz = sb + buf * STB + NH * HB;
+        for (int i = tid; i < (c0 + KC - key_hi) * NH * 8; i += blockDim.x) {
+          const int n = key_hi - c0 + i / (NH * 8), h = (i / 8) % NH, piece = i % 8;
+          *reinterpret_cast<uint4*>(vz + h * HB + n * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
       if (!__syncthreads_and(ok)) {
         // a copy never landed: let the ones still in flight land before leaving
         for (int c = ci + 1; c < n_chunks && c < ci + KST; ++c)
@@ -493,25 +526,25 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
       __syncthreads();
     }
     if (active) {
-      const bf16* kb = Ks + (size_t)buf * KC * LD;
-      const bf16* vb = Vs + (size_t)buf * KC * LD;
-      const bf16* kbl = Ks + (size_t)KC * LD;  // tree chunk: lo halves
-      const bf16* vbl = Vs + (size_t)KC * LD;
+      const unsigned char* kb = sb + buf * STB;  // K halves; V halves at + NH * HB
+      const uint32_t vb32 = sb32 + buf * STB + NH * HB;
       float s[NKT][4];
 #pragma unroll
       for (int nt = 0; nt < NKT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < NKS; ++ks) {
+        const int j = (ks & 3) * 2;  // 16-byte piece of dims ks*16 .. +7 within the half
 #pragma unroll
         for (int nt = 0; nt < NKT; ++nt) {
-          const size_t ko = (size_t)((kslice * NKT + nt) * 8 + g) * LD + ks * 16 + t4 * 2;
-          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kb + ko);
-          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kb + ko + 8);
+          // key row n = (kslice * NKT + nt) * 8 + g, so n & 7 = g
+          const unsigned char* kr = kb + (ks >> 2) * HB + ((kslice * NKT + nt) * 8 + g) * 128 + t4 * 4;
+          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + ((j ^ g) << 4));
+          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + (((j + 1) ^ g) << 4));
           mma_16816(s[nt], qh[ks], b0, b1);
           mma_16816(s[nt], ql[ks], b0, b1);
-          if (tree) {
-            const uint32_t c0l = *reinterpret_cast<const uint32_t*>(kbl + ko);
-            const uint32_t c1l = *reinterpret_cast<const uint32_t*>(kbl + ko + 8);
+          if (tree) {  // stage 1: the lo halves of the tree chunk's fp32 K
+            const uint32_t c0l = *reinterpret_cast<const uint32_t*>(kr + STB + ((j ^ g) << 4));
+            const uint32_t c1l = *reinterpret_cast<const uint32_t*>(kr + STB + (((j + 1) ^ g) << 4));
             mma_16816(s[nt], qh[ks], c0l, c1l);
           }
         }
@@ -575,17 +608,19 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(AttnArgs a) {
         split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
         const int mat = lane >> 3, r8 = lane & 7;
         const int kg = kslice * (KC / 16 / KW) + kk;  // this 16-key group within the chunk
-        const size_t vo = (size_t)(kg * 16 + r8 + (mat & 1) * 8) * LD + (mat >> 1) * 8;
+        // lane's row of matrix mat: key kg*16 + r8 (+8), dims d2*16 (+8); key & 7 = r8
+        const uint32_t vrow = vb32 + (kg * 16 + r8 + (mat & 1) * 8) * 128;
 #pragma unroll
         for (int d2 = 0; d2 < DH / 16; ++d2) {
+          const uint32_t va = vrow + (d2 >> 2) * HB + ((((d2 & 3) * 2 + (mat >> 1)) ^ r8) << 4);
           uint32_t v0, v1, v2, v3;
-          ldsm_x4_trans(v0, v1, v2, v3, smem_u32(vb + vo + d2 * 16));
+          ldsm_x4_trans(v0, v1, v2, v3, va);
           mma_16816(o[2 * d2], ph, v0, v1);
           mma_16816(o[2 * d2], pl, v0, v1);
           mma_16816(o[2 * d2 + 1], ph, v2, v3);
           mma_16816(o[2 * d2 + 1], pl, v2, v3);
-          if (tree) {  // the lo halves of the tree chunk's fp32 V
-            ldsm_x4_trans(v0, v1, v2, v3, smem_u32(vbl + vo + d2 * 16));
+          if (tree) {  // stage 1: the lo halves of the tree chunk's fp32 V
+            ldsm_x4_trans(v0, v1, v2, v3, va + STB);
             mma_16816(o[2 * d2], ph, v0, v1);
             mma_16816(o[2 * d2 + 1], ph, v2, v3);
           }
@@ -724,15 +759,16 @@ __global__ void attention_combine_kernel(AttnArgs a) {
   }
 }
 
-// K and V rings of the tensor-core kernel, then one mbarrier per stage
-static int mma_smem(int dh) { return 2 * KST * KC * (dh + 8) * 2 + 8 * KST; }
+// 1024 bytes of alignment slack, the K and V rings of the tensor-core kernel,
+// then one mbarrier per stage
+static int mma_smem(int dh) { return 1024 + KST * 2 * (dh / 64) * KC * 128 + 8 * KST; }
 
 template <typename T>
 void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
   int R = a.B * a.rows_per_req;
   if (R <= 0) return;
   int n_splits = a.n_prefix_splits + a.n_tree_splits;
-  const bool mma = attention_uses_mma((int)sizeof(T), a.dh);
+  const bool mma = attention_uses_mma((int)sizeof(T), a.dh, a.page_size);
   size_t smem = (size_t)(QG * (a.dh + 1) + KC * (a.dh + 1) + KC * a.dh + QG * KC + 3 * QG) *
                 sizeof(float);
   // a refused limit shows as the launch's own error, which the caller reports

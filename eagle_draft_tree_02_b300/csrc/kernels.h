@@ -1,6 +1,7 @@
 // Internal launch interface of the CUDA path (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -73,13 +74,23 @@ struct AttnArgs {
   int* flags;
   const int* skip;  // if set and *skip == 0 (no request active in the pass), the kernels return
   bool prefix_stable;  // no kernel since the last completed one writes the prefix cache
+  // tensor-core kernel: the caches as tensor maps (encode_kv_map), box_rows
+  // tokens per box, tm_T tokens in the tensor (a box at row tm_T reads zeros)
+  int tm_rows, tm_T;
+  CUtensorMap tm_k, tm_v;
 };
 // Launches the key splits (prefix and tree) and their merge: 2 launches.
 template <typename T> void launch_tree_attention(const AttnArgs& a, cudaStream_t st);
 // query groups per (request, KV head) of the prefix-split kernel
 int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma);
 int attention_kw(int rows_per_req, int Hq, int Hkv);
-bool attention_uses_mma(int elem_bytes, int dh);
+bool attention_uses_mma(int elem_bytes, int dh, int page_size);
+// tokens per tensor-map box of the tensor-core kernel: 64, or the largest
+// divisor of 64 that divides the page size (at least 8 when the kernel is used)
+int attention_box_rows(int page_size);
+// runtime.cu: the cache [T][Hkv][dh] (bf16) as a tensor map with boxes of
+// 64 dims x 1 head x box_rows tokens, 128-byte swizzle; false if refused
+bool encode_kv_map(CUtensorMap* m, const void* base, int T, int Hkv, int dh, int box_rows);
 
 // ----------------------------------------------------------------------------- lmhead.cu
 struct HeadParts {
