@@ -41,20 +41,17 @@ namespace e3 {
 
 namespace {
 constexpr int QG = 32;   // query heads per block (CUDA-core kernel)
-constexpr int QGM = 64;  // queries per block (tensor-core kernel: 4 warps x 16)
+constexpr int QGM = 64;  // queries per block (queries-as-M kernel: 4 warps x 16)
+constexpr int QKT = 16;  // at most this many queries per KV head: the keys-as-M kernel
 constexpr int KC = 64;   // keys per chunk
 constexpr int KST = 3;   // prefix stages in flight (tensor-core kernel)
 constexpr int NT = 256;  // threads (CUDA-core kernel)
 }
 
-// key-sharing warps per query group of the tensor-core kernel
-int attention_kw(int rows_per_req, int Hq, int Hkv) {
-  return rows_per_req * (Hq / Hkv) <= 16 ? 4 : 1;
-}
-
 int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma) {
   int per = rows_per_req * (Hq / Hkv);
-  const int q = mma ? QGM / attention_kw(rows_per_req, Hq, Hkv) : QG;
+  if (mma && per <= QKT) return 1;
+  const int q = mma ? QGM : QG;
   return (per + q - 1) / q;
 }
 
@@ -270,11 +267,23 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4],
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
                                               uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
+}
+// Transpose of an 8 x 8 matrix of 16-bit pairs held one pair per lane in the
+// fragment layout (row lane / 4, columns 2 (lane % 4) and + 1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 // One box of a three-dimensional tensor map global -> shared, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
@@ -323,76 +332,89 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
   hi = bf2_bits(h);
   lo = bf2_bits(__floats2bfloat162_rn(x0 - hf.x, x1 - hf.y));
 }
-}  // namespace
 
-// KW warps share each group of 16 queries, each taking KC / KW keys of every
-// chunk (KW = 4 when a KV head has at most 16 queries, as in a batch of chains),
-// and merge their softmax states at the end; KW = 1: one warp per 16 queries.
-template <int DH, int KW>
-__global__ void __launch_bounds__(128) prefix_attention_mma_kernel(const __grid_constant__ AttnArgs a) {
-  constexpr int NKT = KC / 8 / KW; // key tiles of 8 per chunk and warp
-  constexpr int NDT = DH / 8;      // output tiles of 8 dims
-  constexpr int NKS = DH / 16;     // k16 steps over dh
-  constexpr int PIECES = DH / 8;   // 16-byte pieces per K or V row
-  constexpr int NH = DH / 64;      // 128-byte halves of a row
-  constexpr int HB = KC * 128;     // bytes of one half of a chunk: 64 rows of 128 B
-  constexpr int STB = 2 * NH * HB; // bytes of a stage: the K halves, then the V halves
-  // Stage layout: half h of key row n sits at h * HB + n * 128, its 16-byte
-  // piece j at ((j ^ (n & 7)) << 4) within the row (the tensor map's 128-byte
-  // swizzle), so the fragment loads of 8 consecutive rows hit 8 bank groups.
-  extern __shared__ __align__(16) unsigned char att_smem[];
-  const uint32_t raw = smem_u32(att_smem);
-  unsigned char* sb = att_smem + (((raw + 1023u) & ~1023u) - raw);  // [KST][STB], 1024-aligned
-  const uint32_t sb32 = smem_u32(sb);
-  const uint32_t bar0 = sb32 + KST * STB;  // [KST] mbarriers
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t4 = lane & 3;
-  const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv, split = blockIdx.z;
-  const int G = a.Hq / a.Hkv, nq = a.rows_per_req * G;
-  const int R = a.B * a.rows_per_req;
-  const int kslice = warp % KW;                  // this warp's share of each chunk's keys
-  const int qw = blockIdx.y * (QGM / KW) + (warp / KW) * 16;  // first query of this warp
-  // prefix splits: keys [key_lo, key_hi) of the cache; tree splits: 64 tree
-  // slots, fp32 scratch staged as bf16 (hi, lo) pairs in the two buffers
-  const bool tree = split >= a.n_prefix_splits;
-  int key_lo, key_hi;
-  if (!tree) {
+// The key range of split blockIdx.z: prefix splits take keys
+// [split * keys_per_split, +keys_per_split) of the cache, tree splits 64 tree
+// slots each.
+struct SplitKeys {
+  bool tree;
+  int lo, hi, n_chunks;
+};
+__device__ __forceinline__ SplitKeys split_keys(const AttnArgs& a, int b, int split, bool report) {
+  SplitKeys k;
+  k.tree = split >= a.n_prefix_splits;
+  if (!k.tree) {
     int np = a.n_prefix[b];
     const int cap = a.page_table ? a.max_pages * a.page_size : a.max_prefix;
     if (np > cap || np < 0) {
-      if (tid == 0 && split == 0 && kvh == 0 && blockIdx.y == 0) raise_flag(a.flags, FLAG_POS_RANGE);
+      if (report) raise_flag(a.flags, FLAG_POS_RANGE);
       np = np < 0 ? 0 : cap;
     }
-    key_lo = split * a.keys_per_split;
-    key_hi = min(np, key_lo + a.keys_per_split);
+    k.lo = split * a.keys_per_split;
+    k.hi = min(np, k.lo + a.keys_per_split);
   } else {
-    key_lo = (split - a.n_prefix_splits) * KC;
-    key_hi = min(a.tree_slots, key_lo + KC);
+    k.lo = (split - a.n_prefix_splits) * KC;
+    k.hi = min(a.tree_slots, k.lo + KC);
   }
-  const int n_chunks = key_hi > key_lo ? (tree ? 1 : (key_hi - key_lo + KC - 1) / KC) : 0;
+  k.n_chunks = k.hi > k.lo ? (k.tree ? 1 : (k.hi - k.lo + KC - 1) / KC) : 0;
+  return k;
+}
+}  // namespace
 
-  // Prefix chunks stream through a ring of KST stages, as tensor-map boxes
-  // of tm_rows tokens x 64 dims (one KV head): a chunk is KC / tm_rows token
-  // groups, each in 2 * NH boxes (K and V, each half of the row), and lane l
-  // of warp 0 (l < n_ops) copies box l of every chunk.  A group past the
-  // split's end, or on a bad page, is read at token row tm_T, past the tensor,
-  // which fills zeros.  The lane's page-table entry is fetched one chunk ahead.
-  const int per_group = 2 * NH, n_ops = (KC / a.tm_rows) * per_group;  // n_ops <= 32
-  const int my_grp = lane / per_group, my_box = lane % per_group;
-  const bool op_lane = warp == 0 && lane < n_ops;
-  auto page_of = [&](int ci) -> int {
-    const int pos = key_lo + ci * KC + my_grp * a.tm_rows;
-    if (!op_lane || !a.page_table || ci >= n_chunks || pos >= key_hi) return 0;
+// The K/V ring of the tensor-core kernels.  KST stages each hold one 64-key
+// chunk: the K halves, then the V halves (NH halves of 128 bytes per row).
+// Half h of key row n sits at h * HB + n * 128 and its 16-byte piece j at
+// ((j ^ (n & 7)) << 4) within the row -- the tensor map's 128-byte swizzle --
+// so fragment loads of 8 consecutive rows touch 8 distinct bank groups.
+//
+// A chunk arrives as tensor-map boxes of tm_rows tokens x 64 dims of one KV
+// head: KC / tm_rows token groups, 2 * NH boxes each (K and V, per half).
+// Lane l < n_ops of warp 0 copies box l of every chunk; lane 0 arms the
+// stage's mbarrier with the chunk's bytes.  A group past the split's end, or
+// on a bad page, is read at token row tm_T, past the tensor, which fills
+// zeros.  Each lane fetches its page-table entry one chunk ahead.
+template <int DH>
+struct KvRing {
+  static constexpr int NH = DH / 64;
+  static constexpr int HB = KC * 128;
+  static constexpr int STB = 2 * NH * HB;
+  static constexpr int SMEM = 1024 + KST * STB + 8 * KST;  // with alignment slack
+
+  unsigned char* sb;  // stage 0, 1024-aligned
+  uint32_t sb32, bar0;
+  int b, kvh, lane, warp;
+  SplitKeys k;
+  int my_grp, my_box, n_ops, pg_next;
+
+  __device__ __forceinline__ void init(unsigned char* smem, int b_, int kvh_, const SplitKeys& k_) {
+    const uint32_t raw = smem_u32(smem);
+    sb = smem + (((raw + 1023u) & ~1023u) - raw);
+    sb32 = smem_u32(sb);
+    bar0 = sb32 + KST * STB;
+    b = b_;
+    kvh = kvh_;
+    k = k_;
+    lane = threadIdx.x & 31;
+    warp = threadIdx.x >> 5;
+    pg_next = 0;
+  }
+  __device__ __forceinline__ unsigned char* kstage(int st) const { return sb + st * STB; }
+  __device__ __forceinline__ uint32_t kstage32(int st) const { return sb32 + st * STB; }
+  __device__ __forceinline__ uint32_t vstage32(int st) const { return sb32 + st * STB + NH * HB; }
+
+  __device__ __forceinline__ int page_of(const AttnArgs& a, int ci) const {
+    const int pos = k.lo + ci * KC + my_grp * a.tm_rows;
+    if (warp != 0 || lane >= n_ops || !a.page_table || ci >= k.n_chunks || pos >= k.hi) return 0;
     return a.page_table[(size_t)b * a.max_pages + pos / a.page_size];
-  };
-  auto issue = [&](int ci, int pg) {  // warp 0 only
-    const int st = ci % KST, pos = key_lo + ci * KC + my_grp * a.tm_rows;
+  }
+  __device__ __forceinline__ void issue(const AttnArgs& a, int ci, int pg) const {  // warp 0 only
+    const int st = ci % KST, pos = k.lo + ci * KC + my_grp * a.tm_rows;
     const uint32_t bar = bar0 + 8u * st;
     if (lane == 0) att_arrive_tx(bar, (uint32_t)STB);  // every box lands in full
     __syncwarp();
     if (lane < n_ops) {
       int row = a.tm_T;
-      if (pos < key_hi) {
+      if (pos < k.hi) {
         if (!a.page_table)
           row = b * a.max_prefix + pos;
         else if (pg >= 0 && pg < a.n_pages)
@@ -401,29 +423,115 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(const __grid_
           raise_flag(a.flags, FLAG_PAGE_RANGE);
       }
       const int v = my_box / NH, h = my_box % NH;
-      const uint32_t dst = sb32 + st * STB + (v * NH + h) * HB + my_grp * a.tm_rows * 128;
-      tma_load_3d(dst, v ? &a.tm_v : &a.tm_k, bar, h * 64, kvh, row);
+      tma_load_3d(kstage32(st) + (v * NH + h) * HB + my_grp * a.tm_rows * 128, v ? &a.tm_v : &a.tm_k,
+                  bar, h * 64, kvh, row);
     }
-  };
-  auto start_ring = [&]() -> int {  // the first KST - 1 chunks; returns the next chunk's page
-    if (tid == 0) {
+  }
+  // Barriers, then the first KST - 1 chunks (all threads of the block call it).
+  __device__ __forceinline__ void start(const AttnArgs& a) {
+    const int per_group = 2 * NH;
+    n_ops = (KC / a.tm_rows) * per_group;  // <= 32 for tm_rows >= 8
+    my_grp = lane / per_group;
+    my_box = lane % per_group;
+    if (threadIdx.x == 0) {
       for (int st = 0; st < KST; ++st) att_mbar_init(bar0 + 8u * st, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    if (warp != 0) return 0;
-    for (int ci = 0; ci < KST - 1 && ci < n_chunks; ++ci) issue(ci, page_of(ci));
-    return page_of(KST - 1);
-  };
+    if (warp != 0) return;
+    for (int ci = 0; ci < KST - 1 && ci < k.n_chunks; ++ci) issue(a, ci, page_of(a, ci));
+    pg_next = page_of(a, KST - 1);
+  }
+  // Let the chunks that start() requested land (a block that leaves early).
+  __device__ __forceinline__ void drain_start(const AttnArgs& a) const {
+    for (int ci = 0; ci < KST - 1 && ci < k.n_chunks; ++ci) att_wait(bar0 + 8u * ci, 0u, a.flags);
+  }
+  // Refill the stage that chunk ci - 1 used, wait for chunk ci, and give V
+  // zero rows past the split's end (stale cache rows there meet P = 0, and 0
+  // times a non-finite value would not be 0).  Ends with a block barrier;
+  // false, once the copies still in flight have landed, if a copy never did.
+  __device__ __forceinline__ bool next(const AttnArgs& a, int ci) {
+    const int cn = ci + KST - 1;
+    if (warp == 0 && cn < k.n_chunks) {
+      issue(a, cn, pg_next);
+      pg_next = page_of(a, cn + 1);
+    }
+    const int st = ci % KST, c0 = k.lo + ci * KC;
+    const bool ok = att_wait(bar0 + 8u * st, (uint32_t)(ci / KST) & 1u, a.flags);
+    if (ok && c0 + KC > k.hi) {
+      unsigned char* vz = kstage(st) + NH * HB;
+      for (int i = threadIdx.x; i < (c0 + KC - k.hi) * NH * 8; i += blockDim.x) {
+        const int n = k.hi - c0 + i / (NH * 8), h = (i / 8) % NH, piece = i % 8;
+        *reinterpret_cast<uint4*>(vz + h * HB + n * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if (__syncthreads_and(ok)) return true;
+    for (int c = ci + 1; c < k.n_chunks && c < ci + KST; ++c)
+      att_wait(bar0 + 8u * (c % KST), (uint32_t)(c / KST) & 1u, a.flags);
+    return false;
+  }
+  // A tree split's 64 fp32 slots as bf16 hi (stage 0) + lo (stage 1), in the
+  // ring's row layout; slots past the end are zero rows.
+  __device__ __forceinline__ void load_tree(const AttnArgs& a) {
+    constexpr int PIECES = DH / 8;
+    for (int i = threadIdx.x; i < KC * PIECES; i += blockDim.x) {
+      const int kk = i / PIECES, piece = i % PIECES, slot = k.lo + kk;
+      float kx[8], vx[8];
+      if (slot < k.hi) {
+        const size_t off = (((size_t)b * a.tree_slots + slot) * a.Hkv + kvh) * DH + piece * 8;
+        const float4* kq = reinterpret_cast<const float4*>((const float*)a.tree_k + off);
+        const float4* vq = reinterpret_cast<const float4*>((const float*)a.tree_v + off);
+        const float4 k0 = kq[0], k1 = kq[1], v0 = vq[0], v1 = vq[1];
+        kx[0] = k0.x; kx[1] = k0.y; kx[2] = k0.z; kx[3] = k0.w;
+        kx[4] = k1.x; kx[5] = k1.y; kx[6] = k1.z; kx[7] = k1.w;
+        vx[0] = v0.x; vx[1] = v0.y; vx[2] = v0.z; vx[3] = v0.w;
+        vx[4] = v1.x; vx[5] = v1.y; vx[6] = v1.z; vx[7] = v1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kx[e] = vx[e] = 0.f;
+      }
+      uint32_t khi[4], klo[4], vhi[4], vlo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        split_pair(kx[2 * e], kx[2 * e + 1], khi[e], klo[e]);
+        split_pair(vx[2 * e], vx[2 * e + 1], vhi[e], vlo[e]);
+      }
+      const int o0 = (piece >> 3) * HB + kk * 128 + (((piece & 7) ^ (kk & 7)) << 4);
+      *reinterpret_cast<uint4*>(sb + o0) = make_uint4(khi[0], khi[1], khi[2], khi[3]);
+      *reinterpret_cast<uint4*>(sb + STB + o0) = make_uint4(klo[0], klo[1], klo[2], klo[3]);
+      *reinterpret_cast<uint4*>(sb + NH * HB + o0) = make_uint4(vhi[0], vhi[1], vhi[2], vhi[3]);
+      *reinterpret_cast<uint4*>(sb + STB + NH * HB + o0) = make_uint4(vlo[0], vlo[1], vlo[2], vlo[3]);
+    }
+  }
+};
+
+// Queries as the MMA's M dimension: one warp per 16 queries of a KV head
+// (groups of more than 16 queries: the tree frontiers, the verify passes of
+// wide trees).  S = Q K^T and O += P V, m16n8k16, Q and P as bf16 hi + lo.
+template <int DH>
+__global__ void __launch_bounds__(128) prefix_attention_mma_kernel(const __grid_constant__ AttnArgs a) {
+  constexpr int NKT = KC / 8;      // key tiles of 8 per chunk
+  constexpr int NDT = DH / 8;      // output tiles of 8 dims
+  constexpr int NKS = DH / 16;     // k16 steps over dh
+  using Ring = KvRing<DH>;
+  extern __shared__ __align__(16) unsigned char att_smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv, split = blockIdx.z;
+  const int G = a.Hq / a.Hkv, nq = a.rows_per_req * G;
+  const int R = a.B * a.rows_per_req;
+  const int qw = blockIdx.y * QGM + warp * 16;  // first query of this warp
+  const SplitKeys sk = split_keys(a, b, split, tid == 0 && split == 0 && kvh == 0 && blockIdx.y == 0);
+  Ring ring;
+  ring.init(att_smem, b, kvh, sk);
   // When no kernel of this pass writes the prefix cache (every pass after the
   // root's), the first chunks are requested before the wait for the previous
   // kernel, so their latency overlaps its tail; the queries and tree rows follow.
-  const bool early = a.prefix_stable && !tree && n_chunks > 0;
-  int pg_next = early ? start_ring() : 0;
+  const bool early = a.prefix_stable && !sk.tree && sk.n_chunks > 0;
+  if (early) ring.start(a);
   pdl_begin();
   if (a.skip && *a.skip == 0) {
-    if (early)  // let the requested chunks land before the shared memory is released
-      for (int ci = 0; ci < KST - 1 && ci < n_chunks; ++ci) att_wait(bar0 + 8u * ci, 0u, a.flags);
+    if (early) ring.drain_start(a);  // the requested chunks land before the shared memory is released
     return;
   }
 
@@ -459,75 +567,21 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(const __grid_
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   const bool active = qw < nq;
 
-  // tree chunk: stage 0 holds hi, stage 1 lo, of K and of V (same swizzled rows)
-  auto load_tree = [&]() {
-    for (int i = tid; i < KC * PIECES; i += blockDim.x) {
-      const int kk = i / PIECES, piece = i % PIECES, slot = key_lo + kk;
-      float kx[8], vx[8];
-      if (slot < key_hi) {
-        const size_t off = (((size_t)b * a.tree_slots + slot) * a.Hkv + kvh) * DH + piece * 8;
-        const float4* kq = reinterpret_cast<const float4*>((const float*)a.tree_k + off);
-        const float4* vq = reinterpret_cast<const float4*>((const float*)a.tree_v + off);
-        const float4 k0 = kq[0], k1 = kq[1], v0 = vq[0], v1 = vq[1];
-        kx[0] = k0.x; kx[1] = k0.y; kx[2] = k0.z; kx[3] = k0.w;
-        kx[4] = k1.x; kx[5] = k1.y; kx[6] = k1.z; kx[7] = k1.w;
-        vx[0] = v0.x; vx[1] = v0.y; vx[2] = v0.z; vx[3] = v0.w;
-        vx[4] = v1.x; vx[5] = v1.y; vx[6] = v1.z; vx[7] = v1.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) kx[e] = vx[e] = 0.f;
-      }
-      uint32_t khi[4], klo[4], vhi[4], vlo[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        split_pair(kx[2 * e], kx[2 * e + 1], khi[e], klo[e]);
-        split_pair(vx[2 * e], vx[2 * e + 1], vhi[e], vlo[e]);
-      }
-      const int o0 = (piece >> 3) * HB + kk * 128 + (((piece & 7) ^ (kk & 7)) << 4);
-      *reinterpret_cast<uint4*>(sb + o0) = make_uint4(khi[0], khi[1], khi[2], khi[3]);
-      *reinterpret_cast<uint4*>(sb + STB + o0) = make_uint4(klo[0], klo[1], klo[2], klo[3]);
-      *reinterpret_cast<uint4*>(sb + NH * HB + o0) = make_uint4(vhi[0], vhi[1], vhi[2], vhi[3]);
-      *reinterpret_cast<uint4*>(sb + STB + NH * HB + o0) = make_uint4(vlo[0], vlo[1], vlo[2], vlo[3]);
-    }
-  };
-
-  if (tree) {
-    if (n_chunks > 0) load_tree();
+  if (sk.tree) {
+    if (sk.n_chunks > 0) ring.load_tree(a);
   } else if (!early) {
-    pg_next = start_ring();
+    ring.start(a);
   }
-  for (int ci = 0; ci < n_chunks; ++ci) {
-    const int c0 = key_lo + ci * KC, buf = tree ? 0 : ci % KST;
-    if (!tree) {
-      // refill the stage that the previous chunk used, then wait for this one
-      const int cn = ci + KST - 1;
-      if (warp == 0 && cn < n_chunks) {
-        issue(cn, pg_next);
-        pg_next = page_of(cn + 1);
-      }
-      const bool ok = att_wait(bar0 + 8u * buf, (uint32_t)(ci / KST) & 1u, a.flags);
-      if (ok && c0 + KC > key_hi) {
-        // the split's last chunk is ragged: its rows past key_hi hold whatever
-        // follows in the cache, so V gets zero rows there (P is 0 on them, and
-        // 0 times a stale non-finite value would not be)
-        unsigned char* vz = sb + buf * STB + NH * HB;
-        for (int i = tid; i < (c0 + KC - key_hi) * NH * 8; i += blockDim.x) {
-          const int n = key_hi - c0 + i / (NH * 8), h = (i / 8) % NH, piece = i % 8;
-          *reinterpret_cast<uint4*>(vz + h * HB + n * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      if (!__syncthreads_and(ok)) {
-        // a copy never landed: let the ones still in flight land before leaving
-        for (int c = ci + 1; c < n_chunks && c < ci + KST; ++c)
-          att_wait(bar0 + 8u * (c % KST), (uint32_t)(c / KST) & 1u, a.flags);
-        break;
-      }
+  for (int ci = 0; ci < sk.n_chunks; ++ci) {
+    const int c0 = sk.lo + ci * KC, st = sk.tree ? 0 : ci % KST;
+    if (!sk.tree) {
+      if (!ring.next(a, ci)) break;
     } else {
       __syncthreads();
     }
     if (active) {
-      const unsigned char* kb = sb + buf * STB;  // K halves; V halves at + NH * HB
-      const uint32_t vb32 = sb32 + buf * STB + NH * HB;
+      const unsigned char* kb = ring.kstage(st);  // tree chunk: lo halves one stage on
+      const uint32_t vb32 = ring.vstage32(st);
       float s[NKT][4];
 #pragma unroll
       for (int nt = 0; nt < NKT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -536,15 +590,16 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(const __grid_
         const int j = (ks & 3) * 2;  // 16-byte piece of dims ks*16 .. +7 within the half
 #pragma unroll
         for (int nt = 0; nt < NKT; ++nt) {
-          // key row n = (kslice * NKT + nt) * 8 + g, so n & 7 = g
-          const unsigned char* kr = kb + (ks >> 2) * HB + ((kslice * NKT + nt) * 8 + g) * 128 + t4 * 4;
+          // key row n = nt * 8 + g, so n & 7 = g
+          const unsigned char* kr = kb + (ks >> 2) * Ring::HB + (nt * 8 + g) * 128 + t4 * 4;
           const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + ((j ^ g) << 4));
           const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + (((j + 1) ^ g) << 4));
           mma_16816(s[nt], qh[ks], b0, b1);
           mma_16816(s[nt], ql[ks], b0, b1);
-          if (tree) {  // stage 1: the lo halves of the tree chunk's fp32 K
-            const uint32_t c0l = *reinterpret_cast<const uint32_t*>(kr + STB + ((j ^ g) << 4));
-            const uint32_t c1l = *reinterpret_cast<const uint32_t*>(kr + STB + (((j + 1) ^ g) << 4));
+          if (sk.tree) {  // + q hi . k lo
+            const uint32_t c0l = *reinterpret_cast<const uint32_t*>(kr + Ring::STB + ((j ^ g) << 4));
+            const uint32_t c1l =
+                *reinterpret_cast<const uint32_t*>(kr + Ring::STB + (((j + 1) ^ g) << 4));
             mma_16816(s[nt], qh[ks], c0l, c1l);
           }
         }
@@ -554,9 +609,9 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(const __grid_
       for (int nt = 0; nt < NKT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int key = c0 + (kslice * NKT + nt) * 8 + t4 * 2 + (e & 1);
-          bool ok = key < key_hi;
-          if (ok && tree) {
+          const int key = c0 + nt * 8 + t4 * 2 + (e & 1);
+          bool ok = key < sk.hi;
+          if (ok && sk.tree) {
             const uint32_t* mb = mrow_bits[e >> 1];
             ok = mb && ((mb[key >> 5] >> (key & 31)) & 1u);
           }
@@ -600,27 +655,26 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(const __grid_
       }
       // O += P V over the chunk's keys, 16 at a time
 #pragma unroll
-      for (int kk = 0; kk < KC / 16 / KW; ++kk) {
+      for (int kk = 0; kk < KC / 16; ++kk) {
         uint32_t ph[4], pl[4];
         split_pair(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
         split_pair(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
         split_pair(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
         split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
         const int mat = lane >> 3, r8 = lane & 7;
-        const int kg = kslice * (KC / 16 / KW) + kk;  // this 16-key group within the chunk
-        // lane's row of matrix mat: key kg*16 + r8 (+8), dims d2*16 (+8); key & 7 = r8
-        const uint32_t vrow = vb32 + (kg * 16 + r8 + (mat & 1) * 8) * 128;
+        // lane's row of matrix mat: key kk*16 + r8 (+8), dims d2*16 (+8); key & 7 = r8
+        const uint32_t vrow = vb32 + (kk * 16 + r8 + (mat & 1) * 8) * 128;
 #pragma unroll
         for (int d2 = 0; d2 < DH / 16; ++d2) {
-          const uint32_t va = vrow + (d2 >> 2) * HB + ((((d2 & 3) * 2 + (mat >> 1)) ^ r8) << 4);
+          const uint32_t va = vrow + (d2 >> 2) * Ring::HB + ((((d2 & 3) * 2 + (mat >> 1)) ^ r8) << 4);
           uint32_t v0, v1, v2, v3;
           ldsm_x4_trans(v0, v1, v2, v3, va);
           mma_16816(o[2 * d2], ph, v0, v1);
           mma_16816(o[2 * d2], pl, v0, v1);
           mma_16816(o[2 * d2 + 1], ph, v2, v3);
           mma_16816(o[2 * d2 + 1], pl, v2, v3);
-          if (tree) {  // stage 1: the lo halves of the tree chunk's fp32 V
-            ldsm_x4_trans(v0, v1, v2, v3, va + STB);
+          if (sk.tree) {  // stage 1: the lo halves of the tree chunk's fp32 V
+            ldsm_x4_trans(v0, v1, v2, v3, va + Ring::STB);
             mma_16816(o[2 * d2], ph, v0, v1);
             mma_16816(o[2 * d2 + 1], ph, v2, v3);
           }
@@ -635,60 +689,249 @@ __global__ void __launch_bounds__(128) prefix_attention_mma_kernel(const __grid_
     lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
     lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
   }
-  if (KW == 1) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (qr[h] >= nq) continue;
-      const int row = b * a.rows_per_req + qr[h] / G, head = kvh * G + qr[h] % G;
-      const size_t base = ((size_t)split * R + row) * a.Hq + head;
-      float* op = a.o_part + base * DH;
-#pragma unroll
-      for (int dt = 0; dt < NDT; ++dt) {
-        op[dt * 8 + t4 * 2] = o[dt][2 * h];
-        op[dt * 8 + t4 * 2 + 1] = o[dt][2 * h + 1];
-      }
-      if (t4 == 0) {
-        a.ml_part[base * 2] = mrow[h];
-        a.ml_part[base * 2 + 1] = lrow[h];
-      }
-    }
-    return;
-  }
-  // KW > 1: the warps of a query group merge their states through shared
-  // memory (the K/V buffers are free after the last chunk)
-  float* cm = reinterpret_cast<float*>(att_smem);  // [4 warps][16] max
-  float* cl = cm + 4 * 16;                          // [4][16] sum
-  float* co = cl + 4 * 16;                          // [4][16][DH] unnormalised o
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int r16 = g + 8 * h;
-    if (t4 == 0) {
-      cm[warp * 16 + r16] = mrow[h];
-      cl[warp * 16 + r16] = lrow[h];
-    }
+    if (qr[h] >= nq) continue;
+    const int row = b * a.rows_per_req + qr[h] / G, head = kvh * G + qr[h] % G;
+    const size_t base = ((size_t)split * R + row) * a.Hq + head;
+    float* op = a.o_part + base * DH;
 #pragma unroll
     for (int dt = 0; dt < NDT; ++dt) {
-      co[((size_t)warp * 16 + r16) * DH + dt * 8 + t4 * 2] = o[dt][2 * h];
-      co[((size_t)warp * 16 + r16) * DH + dt * 8 + t4 * 2 + 1] = o[dt][2 * h + 1];
+      op[dt * 8 + t4 * 2] = o[dt][2 * h];
+      op[dt * 8 + t4 * 2 + 1] = o[dt][2 * h + 1];
+    }
+    if (t4 == 0) {
+      a.ml_part[base * 2] = mrow[h];
+      a.ml_part[base * 2 + 1] = lrow[h];
     }
   }
+}
+
+// Keys as the MMA's M dimension, for at most 16 queries per KV head (a batch
+// of chains or of small trees): S^T = K Q^T and O^T += V^T P^T, with the
+// queries as the 8-wide N dimension (NQT tiles of 8), so no MMA row is spent
+// on an absent query.  Each warp takes 16 keys of every chunk and keeps its
+// own softmax state per query; the four warps merge at the end.  P^T goes
+// from the accumulator layout to the B operand by movmatrix (an in-register
+// 8 x 8 transpose).  Q and P enter as bf16 hi + lo, as in the kernel above.
+template <int DH, int NQT>
+__global__ void __launch_bounds__(128) prefix_attention_kt_kernel(const __grid_constant__ AttnArgs a) {
+  constexpr int NKS = DH / 16;  // k16 steps over dh; also the 16-dim tiles of O^T
+  using Ring = KvRing<DH>;
+  extern __shared__ __align__(16) unsigned char att_smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3, mat = lane >> 3, r8 = lane & 7;
+  const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv, split = blockIdx.z;
+  const int G = a.Hq / a.Hkv, nq = min(a.rows_per_req * G, 8 * NQT);
+  const int R = a.B * a.rows_per_req;
+  const SplitKeys sk = split_keys(a, b, split, tid == 0 && split == 0 && kvh == 0);
+  Ring ring;
+  ring.init(att_smem, b, kvh, sk);
+  const bool early = a.prefix_stable && !sk.tree && sk.n_chunks > 0;  // as in the kernel above
+  if (early) ring.start(a);
+  pdl_begin();
+  if (a.skip && *a.skip == 0) {
+    if (early) ring.drain_start(a);
+    return;
+  }
+
+  // B operand of S^T: query qt*8 + g, dims ks*16 + 2 t4 (+1) and + 8, scaled by 1/sqrt(dh)
+  const float scale = rsqrtf((float)DH);
+  uint32_t qb[NQT][NKS][2], qbl[NQT][NKS][2];
+#pragma unroll
+  for (int qt = 0; qt < NQT; ++qt) {
+    const int q = qt * 8 + g;
+    const float* qp = nullptr;
+    if (q < nq) {
+      const int row = b * a.rows_per_req + q / G, head = kvh * G + q % G;
+      qp = a.q + (size_t)a.q_row[row] * a.Hq * DH + (size_t)head * DH;
+    }
+#pragma unroll
+    for (int ks = 0; ks < NKS; ++ks) {
+#pragma unroll
+      for (int f = 0; f < 2; ++f) {
+        const int c = ks * 16 + t4 * 2 + f * 8;
+        const float x0 = qp ? qp[c] * scale : 0.f, x1 = qp ? qp[c + 1] * scale : 0.f;
+        split_pair(x0, x1, qb[qt][ks][f], qbl[qt][ks][f]);
+      }
+    }
+  }
+  // this thread's accumulator columns: queries qt*8 + 2 t4 + e, and their mask rows
+  const uint32_t* mrow_bits[NQT][2];
+#pragma unroll
+  for (int qt = 0; qt < NQT; ++qt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int q = qt * 8 + t4 * 2 + e;
+      mrow_bits[qt][e] = q < nq ? a.mask + (size_t)(b * a.rows_per_req + q / G) * a.mask_words : nullptr;
+    }
+  float ot[NKS][NQT][4];  // O^T: dims dt*16 + g (+8) x queries qt*8 + 2 t4 (+1)
+#pragma unroll
+  for (int dt = 0; dt < NKS; ++dt)
+#pragma unroll
+    for (int qt = 0; qt < NQT; ++qt) ot[dt][qt][0] = ot[dt][qt][1] = ot[dt][qt][2] = ot[dt][qt][3] = 0.f;
+  float mq[NQT][2], lq[NQT][2];
+#pragma unroll
+  for (int qt = 0; qt < NQT; ++qt) mq[qt][0] = mq[qt][1] = -INFINITY, lq[qt][0] = lq[qt][1] = 0.f;
+
+  if (sk.tree) {
+    if (sk.n_chunks > 0) ring.load_tree(a);
+  } else if (!early) {
+    ring.start(a);
+  }
+  const int kw = warp * 16;  // this warp's 16 keys of each chunk
+  for (int ci = 0; ci < sk.n_chunks; ++ci) {
+    const int c0 = sk.lo + ci * KC, st = sk.tree ? 0 : ci % KST;
+    if (!sk.tree) {
+      if (!ring.next(a, ci)) break;
+    } else {
+      __syncthreads();
+    }
+    // S^T over keys kw + g (+8): the A operand is a 16 x 16 tile of K, lane l
+    // addressing row r8 of matrix mat (keys +8 if mat & 1, dims +8 if mat >> 1);
+    // even and odd k steps accumulate apart, to shorten the dependent chains
+    float sa[NQT][4], sz[NQT][4];
+#pragma unroll
+    for (int qt = 0; qt < NQT; ++qt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sa[qt][e] = sz[qt][e] = 0.f;
+    const uint32_t krow = ring.kstage32(st) + (kw + r8 + (mat & 1) * 8) * 128;
+#pragma unroll
+    for (int ks = 0; ks < NKS; ++ks) {
+      const uint32_t ka = krow + (ks >> 2) * Ring::HB + ((((ks & 3) * 2 + (mat >> 1)) ^ r8) << 4);
+      uint32_t af[4];
+      ldsm_x4(af, ka);
+#pragma unroll
+      for (int qt = 0; qt < NQT; ++qt) {
+        float(&acc)[4] = (ks & 1) ? sz[qt] : sa[qt];
+        mma_16816(acc, af, qb[qt][ks][0], qb[qt][ks][1]);
+        mma_16816(acc, af, qbl[qt][ks][0], qbl[qt][ks][1]);
+      }
+      if (sk.tree) {  // + k lo . q hi (stage 1 holds the tree chunk's lo halves)
+        ldsm_x4(af, ka + Ring::STB);
+#pragma unroll
+        for (int qt = 0; qt < NQT; ++qt) {
+          float(&acc)[4] = (ks & 1) ? sz[qt] : sa[qt];
+          mma_16816(acc, af, qb[qt][ks][0], qb[qt][ks][1]);
+        }
+      }
+    }
+    // element e: key kw + g + 8 (e >> 1), query qt*8 + 2 t4 + (e & 1)
+    float s[NQT][4];
+#pragma unroll
+    for (int qt = 0; qt < NQT; ++qt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = c0 + kw + g + (e >> 1) * 8;
+        const uint32_t* mb = mrow_bits[qt][e & 1];
+        bool ok = key < sk.hi && mb;
+        if (ok && sk.tree) ok = (mb[key >> 5] >> (key & 31)) & 1u;
+        s[qt][e] = ok ? sa[qt][e] + sz[qt][e] : -INFINITY;
+      }
+    // online softmax per query column: max over the warp's 16 keys (lanes that
+    // differ in g), rescale, exponentials; sums stay per lane until the end
+    float alpha[NQT][2];
+#pragma unroll
+    for (int qt = 0; qt < NQT; ++qt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float mx = fmaxf(s[qt][e], s[qt][e + 2]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(mq[qt][e], mx);
+        alpha[qt][e] = (mq[qt][e] == -INFINITY) ? 0.f : expf(mq[qt][e] - mn);
+        mq[qt][e] = mn;
+        float ps = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float v = s[qt][e + 2 * h];
+          const float p = (mn == -INFINITY || v == -INFINITY) ? 0.f : expf(v - mn);
+          s[qt][e + 2 * h] = p;
+          ps += p;
+        }
+        lq[qt][e] = lq[qt][e] * alpha[qt][e] + ps;
+      }
+    // P^T as the B operand: (keys g, queries 2 t4 .. +1) pairs, transposed to
+    // (keys 2 t4 .. +1, query g); keys 0-7 give b0, keys 8-15 b1
+    uint32_t pb[NQT][2], pbl[NQT][2];
+#pragma unroll
+    for (int qt = 0; qt < NQT; ++qt) {
+      uint32_t h0, l0, h1, l1;
+      split_pair(s[qt][0], s[qt][1], h0, l0);
+      split_pair(s[qt][2], s[qt][3], h1, l1);
+      pb[qt][0] = movmatrix_t(h0);
+      pb[qt][1] = movmatrix_t(h1);
+      pbl[qt][0] = movmatrix_t(l0);
+      pbl[qt][1] = movmatrix_t(l1);
+    }
+    // O^T += V^T P^T: the A operand is V^T's 16 x 16 tile (dims x keys), read
+    // transposed from V's rows -- matrix mat: keys +8 if mat >> 1, dims +8 if mat & 1
+    const uint32_t vrow = ring.vstage32(st) + (kw + r8 + (mat >> 1) * 8) * 128;
+#pragma unroll
+    for (int dt = 0; dt < NKS; ++dt) {
+      const uint32_t va = vrow + (dt >> 2) * Ring::HB + ((((dt & 3) * 2 + (mat & 1)) ^ r8) << 4);
+      uint32_t av[4];
+      ldsm_x4_trans(av[0], av[1], av[2], av[3], va);
+#pragma unroll
+      for (int qt = 0; qt < NQT; ++qt) {
+        ot[dt][qt][0] *= alpha[qt][0];
+        ot[dt][qt][1] *= alpha[qt][1];
+        ot[dt][qt][2] *= alpha[qt][0];
+        ot[dt][qt][3] *= alpha[qt][1];
+        mma_16816(ot[dt][qt], av, pb[qt][0], pb[qt][1]);
+        mma_16816(ot[dt][qt], av, pbl[qt][0], pbl[qt][1]);
+      }
+      if (sk.tree) {  // + v lo . p hi
+        ldsm_x4_trans(av[0], av[1], av[2], av[3], va + Ring::STB);
+#pragma unroll
+        for (int qt = 0; qt < NQT; ++qt) mma_16816(ot[dt][qt], av, pb[qt][0], pb[qt][1]);
+      }
+    }
+    __syncthreads();  // this stage is refilled at the next chunk
+  }
+  // sums over the warp's keys (lanes that differ in g)
+#pragma unroll
+  for (int qt = 0; qt < NQT; ++qt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      lq[qt][e] += __shfl_xor_sync(0xffffffffu, lq[qt][e], 4);
+      lq[qt][e] += __shfl_xor_sync(0xffffffffu, lq[qt][e], 8);
+      lq[qt][e] += __shfl_xor_sync(0xffffffffu, lq[qt][e], 16);
+    }
+  // the four warps' states meet in shared memory (the ring is free by now)
+  constexpr int NQ = 8 * NQT;
+  float* cm = reinterpret_cast<float*>(att_smem);  // [4 warps][NQ] max
+  float* cl = cm + 4 * NQ;                          // [4][NQ] sum
+  float* co = cl + 4 * NQ;                          // [4][NQ][DH] unnormalised o
+#pragma unroll
+  for (int qt = 0; qt < NQT; ++qt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int q = qt * 8 + t4 * 2 + e;
+      if (g == 0) {
+        cm[warp * NQ + q] = mq[qt][e];
+        cl[warp * NQ + q] = lq[qt][e];
+      }
+#pragma unroll
+      for (int dt = 0; dt < NKS; ++dt) {
+        co[((size_t)warp * NQ + q) * DH + dt * 16 + g] = ot[dt][qt][e];
+        co[((size_t)warp * NQ + q) * DH + dt * 16 + g + 8] = ot[dt][qt][e + 2];
+      }
+    }
   __syncthreads();
-  constexpr int QWB = 4 / KW;  // query groups in the block
-  for (int idx = tid; idx < QWB * 16 * DH; idx += blockDim.x) {
-    const int grp = idx / (16 * DH), r16 = (idx / DH) % 16, dim = idx % DH;
-    const int q = blockIdx.y * (QGM / KW) + grp * 16 + r16;
-    if (q >= nq) continue;
+  for (int idx = tid; idx < nq * DH; idx += blockDim.x) {
+    const int q = idx / DH, dim = idx % DH;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < KW; ++w) M = fmaxf(M, cm[(grp * KW + w) * 16 + r16]);
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, cm[w * NQ + q]);
     float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < KW; ++w) {
-      const int wi = grp * KW + w;
-      const float mw = cm[wi * 16 + r16];
+    for (int w = 0; w < 4; ++w) {
+      const float mw = cm[w * NQ + q];
       const float e = mw == -INFINITY ? 0.f : expf(mw - M);
-      L += cl[wi * 16 + r16] * e;
-      O += co[((size_t)wi * 16 + r16) * DH + dim] * e;
+      L += cl[w * NQ + q] * e;
+      O += co[((size_t)w * NQ + q) * DH + dim] * e;
     }
     const int row = b * a.rows_per_req + q / G, head = kvh * G + q % G;
     const size_t base = ((size_t)split * R + row) * a.Hq + head;
@@ -759,10 +1002,6 @@ __global__ void attention_combine_kernel(AttnArgs a) {
   }
 }
 
-// 1024 bytes of alignment slack, the K and V rings of the tensor-core kernel,
-// then one mbarrier per stage
-static int mma_smem(int dh) { return 1024 + KST * 2 * (dh / 64) * KC * 128 + 8 * KST; }
-
 template <typename T>
 void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
   int R = a.B * a.rows_per_req;
@@ -773,24 +1012,32 @@ void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
                 sizeof(float);
   // a refused limit shows as the launch's own error, which the caller reports
   smem_limit((const void*)tree_attention_kernel<T>, 160 * 1024);
-  smem_limit((const void*)prefix_attention_mma_kernel<64, 1>, mma_smem(64));
-  smem_limit((const void*)prefix_attention_mma_kernel<128, 1>, mma_smem(128));
-  smem_limit((const void*)prefix_attention_mma_kernel<64, 4>, mma_smem(64));
-  smem_limit((const void*)prefix_attention_mma_kernel<128, 4>, mma_smem(128));
+  smem_limit((const void*)prefix_attention_mma_kernel<64>, KvRing<64>::SMEM);
+  smem_limit((const void*)prefix_attention_mma_kernel<128>, KvRing<128>::SMEM);
+  smem_limit((const void*)prefix_attention_kt_kernel<64, 1>, KvRing<64>::SMEM);
+  smem_limit((const void*)prefix_attention_kt_kernel<64, 2>, KvRing<64>::SMEM);
+  smem_limit((const void*)prefix_attention_kt_kernel<128, 1>, KvRing<128>::SMEM);
+  smem_limit((const void*)prefix_attention_kt_kernel<128, 2>, KvRing<128>::SMEM);
   if (mma) {  // prefix and tree splits in one launch
     dim3 gp(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, true), n_splits);
-    const size_t sm2 = mma_smem(a.dh);
-    const bool kw4 = attention_kw(a.rows_per_req, a.Hq, a.Hkv) == 4;
+    const int nq = a.rows_per_req * (a.Hq / a.Hkv);
+    const dim3 blk(128);
     if (a.dh == 128) {
-      if (kw4)
-        launch_pdl(prefix_attention_mma_kernel<128, 4>, dim3(gp), dim3(128), sm2, st, a);
+      const size_t sm2 = KvRing<128>::SMEM;
+      if (nq <= 8)
+        launch_pdl(prefix_attention_kt_kernel<128, 1>, dim3(gp), blk, sm2, st, a);
+      else if (nq <= QKT)
+        launch_pdl(prefix_attention_kt_kernel<128, 2>, dim3(gp), blk, sm2, st, a);
       else
-        launch_pdl(prefix_attention_mma_kernel<128, 1>, dim3(gp), dim3(128), sm2, st, a);
+        launch_pdl(prefix_attention_mma_kernel<128>, dim3(gp), blk, sm2, st, a);
     } else {
-      if (kw4)
-        launch_pdl(prefix_attention_mma_kernel<64, 4>, dim3(gp), dim3(128), sm2, st, a);
+      const size_t sm2 = KvRing<64>::SMEM;
+      if (nq <= 8)
+        launch_pdl(prefix_attention_kt_kernel<64, 1>, dim3(gp), blk, sm2, st, a);
+      else if (nq <= QKT)
+        launch_pdl(prefix_attention_kt_kernel<64, 2>, dim3(gp), blk, sm2, st, a);
       else
-        launch_pdl(prefix_attention_mma_kernel<64, 1>, dim3(gp), dim3(128), sm2, st, a);
+        launch_pdl(prefix_attention_mma_kernel<64>, dim3(gp), blk, sm2, st, a);
     }
   } else {
     dim3 grid(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, false), n_splits);

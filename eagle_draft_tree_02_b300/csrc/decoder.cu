@@ -9,10 +9,56 @@
 //   s = r + W_down(silu(W_gate z) * W_up z);  h = rms(s)
 // Every GEMM writes fp32 split-K partials [S][R][N]; the kernels here sum the
 // partials and apply the element-wise parts.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace e3 {
+
+namespace cg = cooperative_groups;
+
+// Row kernels (the ones with a norm over a whole row) give each row a cluster
+// of kRowCluster CTAs, each taking one slice of the row's columns; the slices'
+// sums of squares meet in distributed shared memory.  (With one block per
+// row, the few rows of a draft pass ran on as many SMs, each pulling its
+// row's split-K partials alone.)
+constexpr int kRowCluster = 8;
+constexpr int kRowThreads = 256;
+
+struct RowSlice {
+  int r, c0, c1;  // row, columns [c0, c1)
+};
+__device__ __forceinline__ RowSlice row_slice(int n) {
+  const int cw = (n + kRowCluster - 1) / kRowCluster;
+  RowSlice sl;
+  sl.r = blockIdx.x / kRowCluster;
+  sl.c0 = min(n, (int)(blockIdx.x % kRowCluster) * cw);
+  sl.c1 = min(n, sl.c0 + cw);
+  return sl;
+}
+// v[i] := the sum of v[i] over every thread of the cluster, the same value
+// (same summation order) in every CTA.  The second barrier keeps each CTA
+// alive until its peers have read its sums.
+template <int N>
+__device__ __forceinline__ void cluster_sum(float (&v)[N], float* red) {
+  __shared__ float mine[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = block_sum(v[i], red);
+  if (threadIdx.x == 0)
+#pragma unroll
+    for (int i = 0; i < N; ++i) mine[i] = v[i];
+  cg::cluster_group cl = cg::this_cluster();
+  cl.sync();
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRowCluster; ++k) t += cl.map_shared_rank(mine, k)[i];
+    v[i] = t;
+  }
+  cl.sync();
+}
 
 // ----------------------------------------------------------------------------- x = [rms(E[y]); rms(hid)]
 template <typename T>
@@ -23,25 +69,25 @@ __global__ void build_input_kernel(int R, int d, int V, float eps, const int* __
                                    int* flags) {
   pdl_begin();
   __shared__ float red[32];
-  int r = blockIdx.x;
+  const RowSlice sl = row_slice(d);
+  const int r = sl.r;
   int t = tok[r];
   if (t < 0 || t >= V) {
-    if (threadIdx.x == 0) raise_flag(flags, FLAG_TOKEN_RANGE);
+    if (threadIdx.x == 0 && sl.c0 == 0) raise_flag(flags, FLAG_TOKEN_RANGE);
     t = t < 0 ? 0 : V - 1;
   }
   const T* e = E + (size_t)t * d;
   const float* h = hid_base + (size_t)hid_row[r] * d;
-  float se = 0.f, sh = 0.f;
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+  float ss[2] = {0.f, 0.f};  // embedding row, hidden row
+  for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x) {
     float a = ldf(e + j), b = h[j];
-    se += a * a;
-    sh += b * b;
+    ss[0] += a * a;
+    ss[1] += b * b;
   }
-  se = block_sum(se, red);
-  sh = block_sum(sh, red);
-  float ie = rsqrtf(se / d + eps), ih = rsqrtf(sh / d + eps);
+  cluster_sum<2>(ss, red);
+  float ie = rsqrtf(ss[0] / d + eps), ih = rsqrtf(ss[1] / d + eps);
   T* xr = x + act_row(r, 2 * d, split);
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+  for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x) {
     st_act(xr, 2 * d, j, ldf(e + j) * ie * ldf(g_emb + j), split);
     st_act(xr, 2 * d, d + j, h[j] * ih * ldf(g_hid + j), split);
   }
@@ -72,23 +118,24 @@ __global__ void reduce_parts_kernel(int R, int N, int S, const float* __restrict
     out[i] = sum_parts(part + i, n, S);
 }
 
-// g = rms(sum of fusion partials) * g_fc: the FC-norm variant, one block per row
+// g = rms(sum of fusion partials) * g_fc: the FC-norm variant, one cluster per row
 template <typename T>
 __global__ void reduce_norm_kernel(int R, int N, int S, float eps, const float* __restrict__ part,
                                    const T* __restrict__ g_fc, float* __restrict__ out) {
   pdl_begin();
   __shared__ float red[32];
-  const int r = blockIdx.x;
+  const RowSlice sl = row_slice(N);
+  const int r = sl.r;
   const size_t n = (size_t)R * N;
-  float ss = 0.f;
-  for (int j = threadIdx.x; j < N; j += blockDim.x) {
+  float ss[1] = {0.f};
+  for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x) {
     const float v = sum_parts(part + (size_t)r * N + j, n, S);
     out[(size_t)r * N + j] = v;
-    ss += v * v;
+    ss[0] += v * v;
   }
-  ss = block_sum(ss, red);
-  const float inv = rsqrtf(ss / N + eps);
-  for (int j = threadIdx.x; j < N; j += blockDim.x)
+  cluster_sum<1>(ss, red);
+  const float inv = rsqrtf(ss[0] / N + eps);
+  for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x)
     out[(size_t)r * N + j] *= inv * ldf(g_fc + j);
 }
 
@@ -175,19 +222,20 @@ __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* _
                                   T* __restrict__ z_out, bool split, bool post) {
   pdl_begin();
   __shared__ float red[32];
-  int r = blockIdx.x;
+  const RowSlice sl = row_slice(d);
+  const int r = sl.r;
   const float* h = hid_base + (size_t)hid_row[r] * d;
   size_t stride = (size_t)R * d;
-  float ss = 0.f;
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+  float ss[1] = {0.f};
+  for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x) {
     float v = h[j] + sum_parts(part + (size_t)r * d + j, stride, S);
     r_out[(size_t)r * d + j] = v;
-    ss += v * v;
+    ss[0] += v * v;
   }
-  ss = block_sum(ss, red);
-  float inv = rsqrtf(ss / d + eps);
+  cluster_sum<1>(ss, red);
+  float inv = rsqrtf(ss[0] / d + eps);
   T* zr = z_out + act_row(r, d, split);
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+  for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x) {
     const float z = r_out[(size_t)r * d + j] * inv * ldf(g_post + j);
     if (post) r_out[(size_t)r * d + j] = z;  // post-norm: the residual stream is normalised too
     st_act(zr, d, j, z, split);
@@ -220,39 +268,38 @@ __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float
                                      bool split, bool post) {
   pdl_begin();
   __shared__ float red[32];
-  extern __shared__ float srow[];
-  int r = blockIdx.x;
+  extern __shared__ float srow[];  // this CTA's slice of s
+  const RowSlice sl = row_slice(d);
+  const int r = sl.r;
   size_t stride = (size_t)R * d;
-  float ss = 0.f;
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+  float ss[1] = {0.f};
+  for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x) {
     float v = r_in[(size_t)r * d + j] + sum_parts(part + (size_t)r * d + j, stride, S);
-    srow[j] = v;
-    ss += v * v;
+    srow[j - sl.c0] = v;
+    ss[0] += v * v;
   }
-  ss = block_sum(ss, red);
-  float inv = rsqrtf(ss / d + eps);
+  cluster_sum<1>(ss, red);
+  float inv = rsqrtf(ss[0] / d + eps);
   int sd = s_dst ? s_dst[r] : -1;
   int hd = h_dst ? h_dst[r] : r;
   T* hr = h_base + act_row(hd, d, split);
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
-    const float h = srow[j] * inv * ldf(g_final + j);
-    if (sd >= 0) s_base[(size_t)sd * d + j] = post ? h : srow[j];  // post-norm: the state is h
+  for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x) {
+    const float h = srow[j - sl.c0] * inv * ldf(g_final + j);
+    if (sd >= 0) s_base[(size_t)sd * d + j] = post ? h : srow[j - sl.c0];  // post-norm: the state is h
     st_act(hr, d, j, h, split);
   }
 }
 
 // ----------------------------------------------------------------------------- host launchers
-// Row kernels run one block per row; a full block keeps enough loads of the
-// split-K partials in flight for the few rows of a draft pass.
-constexpr int kRowThreads = 1024;
 
 template <typename T>
 void launch_build_input(int R, int d, int V, float eps, const int* tok, const float* hid_base,
                         const int* hid_row, const void* E, const void* g_emb, const void* g_hid,
                         void* x, bool split, int* flags, cudaStream_t st) {
   if (R <= 0) return;
-  launch_pdl(build_input_kernel<T>, dim3(R), dim3(kRowThreads), 0, st, R, d, V, eps, tok, hid_base, hid_row, (const T*)E,
-                                           (const T*)g_emb, (const T*)g_hid, (T*)x, split, flags);
+  launch_pdl_cluster(build_input_kernel<T>, dim3(R * kRowCluster), dim3(kRowThreads), 0, st, kRowCluster,
+                     R, d, V, eps, tok, hid_base, hid_row, (const T*)E, (const T*)g_emb, (const T*)g_hid,
+                     (T*)x, split, flags);
 }
 
 void launch_reduce_parts(int R, int N, int S, const float* part, float* out, cudaStream_t st) {
@@ -267,8 +314,8 @@ template <typename T>
 void launch_reduce_norm(int R, int N, int S, float eps, const float* part, const void* g_fc,
                         float* out, cudaStream_t st) {
   if (R <= 0) return;
-  launch_pdl(reduce_norm_kernel<T>, dim3(R), dim3(kRowThreads), 0, st, R, N, S, eps, part,
-             (const T*)g_fc, out);
+  launch_pdl_cluster(reduce_norm_kernel<T>, dim3(R * kRowCluster), dim3(kRowThreads), 0, st, kRowCluster,
+                     R, N, S, eps, part, (const T*)g_fc, out);
 }
 
 template <typename T>
@@ -285,8 +332,8 @@ void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const 
                        const int* hid_row, const void* g_post, float* r_out, void* z_out,
                        bool split, bool post, cudaStream_t st) {
   if (R <= 0) return;
-  launch_pdl(o_epilogue_kernel<T>, dim3(R), dim3(kRowThreads), 0, st, R, d, S, eps, part, hid_base,
-             hid_row, (const T*)g_post, r_out, (T*)z_out, split, post);
+  launch_pdl_cluster(o_epilogue_kernel<T>, dim3(R * kRowCluster), dim3(kRowThreads), 0, st, kRowCluster,
+                     R, d, S, eps, part, hid_base, hid_row, (const T*)g_post, r_out, (T*)z_out, split, post);
 }
 
 template <typename T>
@@ -303,8 +350,10 @@ void launch_down_epilogue(int R, int d, int S, float eps, const float* part, con
                           const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
                           void* h_base, bool split, bool post, cudaStream_t st) {
   if (R <= 0) return;
-  launch_pdl(down_epilogue_kernel<T>, dim3(R), dim3(kRowThreads), d * sizeof(float), st, R, d, S,
-             eps, part, r_in, (const T*)g_final, s_dst, s_base, h_dst, (T*)h_base, split, post);
+  const size_t slice = (size_t)((d + kRowCluster - 1) / kRowCluster) * sizeof(float);
+  launch_pdl_cluster(down_epilogue_kernel<T>, dim3(R * kRowCluster), dim3(kRowThreads), slice, st,
+                     kRowCluster, R, d, S, eps, part, r_in, (const T*)g_final, s_dst, s_base, h_dst,
+                     (T*)h_base, split, post);
 }
 
 #define E3_INST(T)                                                                                   \
