@@ -27,6 +27,8 @@ constexpr int kTargetBlocks = 2 * 148;
 // bf16 GEMM inputs of at most this many rows are stored split (hi, lo): the
 // MMA then runs 2R columns, which is free while the weights bound the time.
 constexpr int kSplitMaxRows = 128;
+// largest logits buffer of the deferred bonus draw (see the workspace plan)
+constexpr size_t kDeferMaxBytes = (size_t)4 << 30;
 
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -68,6 +70,8 @@ struct eagle3_ctx {
   // verify
   int *child_tok, *child_node, *n_child, *z_arg, *g_arg;
   float *child_z, *vpart, *z_max, *lse, *g_max;
+  float* vlogits = nullptr;  // [B*M1][V] target logits of a sampling pass (deferred bonus draw)
+  unsigned long long* bonus_best = nullptr;  // [B] packed best (score, token) of the bonus draw
   int n_vparts;
   int* flags;
   // per-request caps and cost-aware rules (eagle3_set_control)
@@ -635,6 +639,13 @@ eagle3_status eagle3_create(const eagle3_config* cfg, const eagle3_weights* w, e
   add((void**)&c->lse, (size_t)Rv * 4);
   add((void**)&c->g_arg, (size_t)Rv * 4);
   add((void**)&c->g_max, (size_t)Rv * 4);
+  // The tensor-core verify head stores the target logits of a sampling pass
+  // and leaves the Gumbel draw to the one node where each walk stops; past
+  // kDeferMaxBytes of logits it draws in its epilogue instead.
+  if (c->bf && (size_t)Rv * f.vocab * 4 <= kDeferMaxBytes) {
+    add((void**)&c->vlogits, (size_t)Rv * f.vocab * 4);
+    add((void**)&c->bonus_best, (size_t)B * 8);
+  }
   c->lr = f.lr_rank > 0;
   c->n_exp = 1 + (f.depth - 1) * k;
   const int lr_groups = c->lr ? (c->bf ? lowrank_tc_groups(f.vocab) : lowrank_simt_groups(f.vocab)) : 0;
@@ -939,6 +950,8 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   va.child_z = c->child_z;
   va.n_parts = c->n_vparts;
   va.part = c->vpart;
+  // per-node Gumbel-argmax asked for: draw it at every node, in the head
+  va.logits = (mode == 1 && c->vlogits && !(stats && stats->g_argmax)) ? c->vlogits : nullptr;
   if (c->bf) {
     if (!tc_verify_head(c->tc, c->h_ver, spv, va, c->flags, st))
       tc_error(c, "tcgen05 verify head rejected its arguments");
@@ -998,8 +1011,30 @@ eagle3_status eagle3_verify(eagle3_ctx* c, int B, const eagle3_tree* tree, const
   wa.accept_len = accept_len;
   wa.path = path;
   wa.out_tokens = out_tokens;
+  wa.bonus_best = va.logits ? c->bonus_best : nullptr;
   launch_walk(wa, st);
   c->launches++;
+  if (va.logits) {
+    BonusArgs ba{};
+    ba.B = B;
+    ba.M1 = M1;
+    ba.kmax = k;
+    ba.D = c->D;
+    ba.V = f.vocab;
+    ba.inv_t = va.inv_t;
+    ba.seed = seed;
+    ba.round_id = round_id;
+    ba.round_ptr = c->round_ptr;
+    ba.logits = va.logits;
+    ba.child_tok = c->child_tok;
+    ba.accept_len = accept_len;
+    ba.path = path;
+    ba.out_tokens = out_tokens;
+    ba.g_arg = c->g_arg;
+    ba.best = c->bonus_best;
+    launch_bonus_gumbel(ba, st);
+    c->launches += 2;
+  }
   }
   if (stats) {
     size_t n = (size_t)B * M1;

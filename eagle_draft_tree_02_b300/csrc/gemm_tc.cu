@@ -230,7 +230,9 @@ __device__ __forceinline__ void verify_row(const VerifyHeadArgs& va, int part, i
         va.child_z[(size_t)r * va.kmax + c] = z;
       }
     }
-    if (va.sampling && !child) {
+    if (va.logits) {
+      va.logits[(size_t)r * va.V + x] = z;
+    } else if (va.sampling && !child) {
       const unsigned long long rid = va.round_ptr ? *va.round_ptr : va.round_id;
       gb = t + verify_gumbel(va.seed, rid, b, u, x);
       gi = x;
@@ -634,10 +636,16 @@ __device__ __forceinline__ void verify_chunk(float* mine, const VerifyHeadArgs& 
       if (lane == lh) excl |= 1u << qh;
     }
   }
+  const bool draw = va.sampling && !va.logits;  // Gumbel noise here, or deferred
+  if (va.logits && tok0 + lane < va.V) {
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      if (q < nr) va.logits[(size_t)(r_off + r0 + q) * va.V + tok0 + lane] = x[q];
+  }
   float g[16];
 #pragma unroll
   for (int q = 0; q < 16; ++q) g[q] = 0.f;
-  if (va.sampling) {
+  if (draw) {
     const unsigned long long rid = va.round_ptr ? *va.round_ptr : va.round_id;
 #pragma unroll
     for (int g4 = 0; g4 < 16; g4 += 4) {
@@ -677,8 +685,9 @@ __device__ __forceinline__ void verify_chunk(float* mine, const VerifyHeadArgs& 
         Mo = M;
         bz = b;
       }
-      if (va.sampling) {
-        const float s = (x[q] == -INFINITY || ((excl >> q) & 1u)) ? -INFINITY : x[q] * va.inv_t + g[q];
+      if (draw) {
+        const float s =
+            (x[q] == -INFINITY || ((excl >> q) & 1u)) ? -INFINITY : __fmaf_rn(x[q], va.inv_t, g[q]);
         const float G = warp_max_f32(s);
         const unsigned bs = __ballot_sync(0xffffffffu, s == G && s != -INFINITY);
         if (q == qo) {

@@ -116,6 +116,10 @@ struct VerifyHeadArgs {
   float* child_z;            // [R][kmax]  target logit at each child token
   int n_parts;
   float* part;               // [n_parts][R][6]
+  // Deferred draw (sampling, tensor-core head): if set, the head stores z
+  // here ([R][V], fp32) and draws no Gumbel noise; bonus_gumbel then draws
+  // it over the one row where each request's walk stops.
+  float* logits;
 };
 template <typename T>
 void launch_verify_head_simt(const void* H, const void* W, const VerifyHeadArgs& a, cudaStream_t st);
@@ -195,8 +199,27 @@ struct WalkArgs {
   const int* z_arg;       // [B*M1]
   const int* g_arg;       // [B*M1]
   int *accept_len, *path, *out_tokens;
+  unsigned long long* bonus_best;  // if set: [B], zeroed here for the deferred bonus draw
 };
 void launch_walk(const WalkArgs& a, cudaStream_t st);
+// The bonus token of a sampling walk whose head deferred the Gumbel draw: at
+// the node where request b's walk stopped, the Gumbel-argmax of z / T over the
+// node's non-children, from the stored logits row.  Blocks (n_blk per
+// request) fold their best into best[b] by atomicMax of a packed key; a
+// second launch writes the token.  2 launches.
+struct BonusArgs {
+  int B, M1, kmax, D, V;
+  float inv_t;
+  unsigned long long seed, round_id;
+  const unsigned long long* round_ptr;  // if set, the round id is read here
+  const float* logits;    // [B*M1][V]
+  const int* child_tok;   // [B*M1][kmax] (-1 padded)
+  const int *accept_len, *path;
+  int* out_tokens;        // [B][D+1]: the slot at accept_len is written
+  int* g_arg;             // [B*M1]: written at the stop node
+  unsigned long long* best;  // [B] (score, token) keys, zeroed by the walk
+};
+void launch_bonus_gumbel(const BonusArgs& a, cudaStream_t st);
 
 // ----------------------------------------------------------------------------- sampled.cu
 struct SampleArgs {  // sampled children of a pass's rows (Gumbel-top-k over the logits)

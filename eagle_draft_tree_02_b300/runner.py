@@ -147,8 +147,12 @@ class Engine:
         self.stats_t = dict(z_max=torch.empty((self.B, M1), **f32), lse=torch.empty((self.B, M1), **f32),
                             z_argmax=torch.empty((self.B, M1), **i32),
                             g_argmax=torch.empty((self.B, M1), **i32))
+        # the per-node Gumbel-argmax makes the head draw noise at every node;
+        # without it a sampling pass draws only where each walk stops
         self.stats = E.eagle3_verify_stats(*(self.stats_t[n].data_ptr()
-                                             for n in ("z_max", "lse", "z_argmax", "g_argmax")))
+                                             for n in ("z_max", "lse", "z_argmax")), None)
+        self.stats_g = E.eagle3_verify_stats(*(self.stats_t[n].data_ptr()
+                                               for n in ("z_max", "lse", "z_argmax", "g_argmax")))
         self._tree_s = self.tree.struct()
         self._pool_s = self.pool.struct()
 
@@ -201,12 +205,14 @@ class Engine:
         """Seed and round id of the sampled draft's noise for the next rounds."""
         E.check(self.ctx, E.eagle3_draft_noise(self.ctx, seed, round_id, self.stream()))
 
-    def verify(self, temperature=0.0, seed=0, round_id=0, with_stats=True):
+    def verify(self, temperature=0.0, seed=0, round_id=0, with_stats=True, g_argmax=False):
+        """g_argmax: also fill stats_t["g_argmax"] at every node (the head then
+        draws the Gumbel noise of every node instead of deferring it)."""
         mode = 0 if temperature == 0 else (2 if self.cfg.sampled_draft else 1)
+        stats = (self.stats_g if g_argmax else self.stats) if with_stats else None
         s = E.eagle3_verify(self.ctx, self.B, self._tree_s, self.kv, mode, float(temperature or 1.0),
                             seed, round_id, self.accept_len.data_ptr(), self.path.data_ptr(),
-                            self.out_tokens.data_ptr(), self.stats if with_stats else None,
-                            self.stream())
+                            self.out_tokens.data_ptr(), stats, self.stream())
         E.check(self.ctx, s)
         return self.accept_len, self.path, self.out_tokens
 

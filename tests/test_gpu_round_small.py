@@ -248,3 +248,25 @@ def test_two_stage_head_all_tied_lowrank_scores(cuda, lib_built, cfg):
         order = np.lexsort((cand[r], -logq[r]))[:k]
         assert tok[r].cpu().numpy().tolist() == [int(cand[r][j]) for j in order]
         np.testing.assert_allclose(lq[r].cpu().numpy(), logq[r][order], atol=tol)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg", [SMALL_BF16, TWO_STAGE_BF16], ids=["bf16", "two_stage_bf16"])
+def test_deferred_bonus_matches_the_head_draw(cuda, lib_built, cfg):
+    """Sampling without the per-node Gumbel-argmax: the tensor-core head stores
+    the target logits and the bonus is drawn only at each request's stop node.
+    The walk's outputs equal those of the draw made inside the head (stats with
+    g_argmax) over many round ids, and the bonus is that draw's Gumbel-argmax
+    at the stop node."""
+    import torch
+    inp, eng = _engine(cfg, 6)
+    eng.draft_round()
+    for rid in range(48):
+        a1, p1, o1 = [t.clone() for t in eng.verify(1.0, 5, rid, g_argmax=True)]
+        g = eng.stats_t["g_argmax"].clone()
+        a2, p2, o2 = [t.clone() for t in eng.verify(1.0, 5, rid)]
+        assert torch.equal(a1, a2) and torch.equal(p1, p2) and torch.equal(o1, o2), rid
+        for b in range(cfg.batch):
+            n = int(a1[b])
+            u = 0 if n == 0 else int(p1[b, n - 1])
+            assert int(o1[b, n]) == int(g[b, u]) >= 0, (rid, b)

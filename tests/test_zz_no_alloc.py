@@ -69,8 +69,7 @@ def _run_pair(cuda, cfg, seed, rows=None):
     w_lm = eng.w["w_lm"]
     w_host = inp.f32("w_lm")
     st = eng.stream()
-    torch.cuda.synchronize()
-    free = [torch.cuda.mem_get_info()[0]]
+    free = []  # (before, after) the allocation-free call, per call
     for call in range(2):
         h = torch.from_numpy(np.random.default_rng(100 + call).standard_normal((R, cfg.d))
                              .astype(np.float32)).to(cuda).to(dt)
@@ -81,14 +80,17 @@ def _run_pair(cuda, cfg, seed, rows=None):
         tok_b = torch.full((R, k), -7, **i32)
         lq_b, lse_b = torch.full((R, k), 9.0, **f32), torch.full((R,), 9.0, **f32)
         status = torch.full((1,), -1, **i32)
+        # every tensor of the call exists before the first reading, so the two
+        # readings bracket the entry point alone (not the test's own tensors)
         torch.cuda.synchronize()
+        before = torch.cuda.mem_get_info()[0]
         s = E.eagle3_lm_head_topk_noalloc(code, cfg.vocab, cfg.d, k, w_lm.data_ptr(), R, h.data_ptr(),
                                           tok_b.data_ptr(), lq_b.data_ptr(), lse_b.data_ptr(),
                                           status.data_ptr(), st)
         assert s == E.OK
         torch.cuda.synchronize()
+        free.append((before, torch.cuda.mem_get_info()[0]))
         eng.check()
-        free.append(torch.cuda.mem_get_info()[0])
         assert int(status.item()) == 0
         assert torch.equal(tok_a, tok_b), (call, tok_a, tok_b)
         assert (lq_a - lq_b).abs().max().item() <= tol
@@ -96,8 +98,8 @@ def _run_pair(cuda, cfg, seed, rows=None):
         _against_oracle(cfg, w_host, h, tok_b, lq_b, lse_b)
     # the first call on a device may load the module that holds the fixed
     # array (lazy loading); the second call allocated nothing
-    print(f"{cfg.name}: free memory before/after call 1/after call 2: {free}")
-    assert free[2] == free[1]
+    print(f"{cfg.name}: free memory (before, after) call 1, call 2: {free}")
+    assert free[1][1] == free[1][0]
     eng.close()
 
 
