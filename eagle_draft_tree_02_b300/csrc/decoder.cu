@@ -18,33 +18,39 @@ namespace e3 {
 
 namespace cg = cooperative_groups;
 
-// Row kernels (the ones with a norm over a whole row) give each row a cluster
-// of kRowCluster CTAs, each taking one slice of the row's columns; the slices'
-// sums of squares meet in distributed shared memory.  (With one block per
-// row, the few rows of a draft pass ran on as many SMs, each pulling its
-// row's split-K partials alone.)
+// Row kernels (the ones with a norm over a whole row) give each of a few rows
+// a cluster of CL = 8 CTAs, each taking one slice of the row's columns; the
+// slices' sums of squares meet in distributed shared memory.  (With one block
+// per row, the few rows of a draft pass ran on as many SMs, each pulling its
+// row's split-K partials alone.)  From kRowClusterMaxRows rows on -- prefill
+// chunks, wide verify passes -- one 1024-thread block per row (CL = 1)
+// already fills the GPU and costs less.
 constexpr int kRowCluster = 8;
-constexpr int kRowThreads = 256;
+constexpr int kRowClusterMaxRows = 148;
+constexpr int kRowThreads = 256;      // with clusters
+constexpr int kRowThreadsWide = 1024;  // one block per row
 
 struct RowSlice {
   int r, c0, c1;  // row, columns [c0, c1)
 };
+template <int CL>
 __device__ __forceinline__ RowSlice row_slice(int n) {
-  const int cw = (n + kRowCluster - 1) / kRowCluster;
+  const int cw = (n + CL - 1) / CL;
   RowSlice sl;
-  sl.r = blockIdx.x / kRowCluster;
-  sl.c0 = min(n, (int)(blockIdx.x % kRowCluster) * cw);
+  sl.r = blockIdx.x / CL;
+  sl.c0 = min(n, (int)(blockIdx.x % CL) * cw);
   sl.c1 = min(n, sl.c0 + cw);
   return sl;
 }
-// v[i] := the sum of v[i] over every thread of the cluster, the same value
-// (same summation order) in every CTA.  The second barrier keeps each CTA
-// alive until its peers have read its sums.
-template <int N>
+// v[i] := the sum of v[i] over every thread of the row's CL CTAs, the same
+// value (same summation order) in every CTA.  The second cluster barrier keeps
+// each CTA alive until its peers have read its sums.
+template <int CL, int N>
 __device__ __forceinline__ void cluster_sum(float (&v)[N], float* red) {
   __shared__ float mine[N];
 #pragma unroll
   for (int i = 0; i < N; ++i) v[i] = block_sum(v[i], red);
+  if (CL == 1) return;
   if (threadIdx.x == 0)
 #pragma unroll
     for (int i = 0; i < N; ++i) mine[i] = v[i];
@@ -54,14 +60,14 @@ __device__ __forceinline__ void cluster_sum(float (&v)[N], float* red) {
   for (int i = 0; i < N; ++i) {
     float t = 0.f;
 #pragma unroll
-    for (int k = 0; k < kRowCluster; ++k) t += cl.map_shared_rank(mine, k)[i];
+    for (int k = 0; k < CL; ++k) t += cl.map_shared_rank(mine, k)[i];
     v[i] = t;
   }
   cl.sync();
 }
 
 // ----------------------------------------------------------------------------- x = [rms(E[y]); rms(hid)]
-template <typename T>
+template <typename T, int CL>
 __global__ void build_input_kernel(int R, int d, int V, float eps, const int* __restrict__ tok,
                                    const float* __restrict__ hid_base, const int* __restrict__ hid_row,
                                    const T* __restrict__ E, const T* __restrict__ g_emb,
@@ -69,7 +75,7 @@ __global__ void build_input_kernel(int R, int d, int V, float eps, const int* __
                                    int* flags) {
   pdl_begin();
   __shared__ float red[32];
-  const RowSlice sl = row_slice(d);
+  const RowSlice sl = row_slice<CL>(d);
   const int r = sl.r;
   int t = tok[r];
   if (t < 0 || t >= V) {
@@ -84,7 +90,7 @@ __global__ void build_input_kernel(int R, int d, int V, float eps, const int* __
     ss[0] += a * a;
     ss[1] += b * b;
   }
-  cluster_sum<2>(ss, red);
+  cluster_sum<CL, 2>(ss, red);
   float ie = rsqrtf(ss[0] / d + eps), ih = rsqrtf(ss[1] / d + eps);
   T* xr = x + act_row(r, 2 * d, split);
   for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x) {
@@ -119,12 +125,12 @@ __global__ void reduce_parts_kernel(int R, int N, int S, const float* __restrict
 }
 
 // g = rms(sum of fusion partials) * g_fc: the FC-norm variant, one cluster per row
-template <typename T>
+template <typename T, int CL>
 __global__ void reduce_norm_kernel(int R, int N, int S, float eps, const float* __restrict__ part,
                                    const T* __restrict__ g_fc, float* __restrict__ out) {
   pdl_begin();
   __shared__ float red[32];
-  const RowSlice sl = row_slice(N);
+  const RowSlice sl = row_slice<CL>(N);
   const int r = sl.r;
   const size_t n = (size_t)R * N;
   float ss[1] = {0.f};
@@ -133,7 +139,7 @@ __global__ void reduce_norm_kernel(int R, int N, int S, float eps, const float* 
     out[(size_t)r * N + j] = v;
     ss[0] += v * v;
   }
-  cluster_sum<1>(ss, red);
+  cluster_sum<CL, 1>(ss, red);
   const float inv = rsqrtf(ss[0] / N + eps);
   for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x)
     out[(size_t)r * N + j] *= inv * ldf(g_fc + j);
@@ -215,14 +221,14 @@ __global__ void qkv_epilogue_kernel(QkvEpi p) {
 }
 
 // ----------------------------------------------------------------------------- r = hid + W_o o;  z = rms(r)
-template <typename T>
+template <typename T, int CL>
 __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* __restrict__ part,
                                   const float* __restrict__ hid_base, const int* __restrict__ hid_row,
                                   const T* __restrict__ g_post, float* __restrict__ r_out,
                                   T* __restrict__ z_out, bool split, bool post) {
   pdl_begin();
   __shared__ float red[32];
-  const RowSlice sl = row_slice(d);
+  const RowSlice sl = row_slice<CL>(d);
   const int r = sl.r;
   const float* h = hid_base + (size_t)hid_row[r] * d;
   size_t stride = (size_t)R * d;
@@ -232,7 +238,7 @@ __global__ void o_epilogue_kernel(int R, int d, int S, float eps, const float* _
     r_out[(size_t)r * d + j] = v;
     ss[0] += v * v;
   }
-  cluster_sum<1>(ss, red);
+  cluster_sum<CL, 1>(ss, red);
   float inv = rsqrtf(ss[0] / d + eps);
   T* zr = z_out + act_row(r, d, split);
   for (int j = sl.c0 + threadIdx.x; j < sl.c1; j += blockDim.x) {
@@ -260,7 +266,7 @@ __global__ void swiglu_kernel(int R, int F, int S, const float* __restrict__ par
 }
 
 // ----------------------------------------------------------------------------- s = r + W_down a;  h = rms(s)
-template <typename T>
+template <typename T, int CL>
 __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float* __restrict__ part,
                                      const float* __restrict__ r_in, const T* __restrict__ g_final,
                                      const int* __restrict__ s_dst, float* __restrict__ s_base,
@@ -269,7 +275,7 @@ __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float
   pdl_begin();
   __shared__ float red[32];
   extern __shared__ float srow[];  // this CTA's slice of s
-  const RowSlice sl = row_slice(d);
+  const RowSlice sl = row_slice<CL>(d);
   const int r = sl.r;
   size_t stride = (size_t)R * d;
   float ss[1] = {0.f};
@@ -278,7 +284,7 @@ __global__ void down_epilogue_kernel(int R, int d, int S, float eps, const float
     srow[j - sl.c0] = v;
     ss[0] += v * v;
   }
-  cluster_sum<1>(ss, red);
+  cluster_sum<CL, 1>(ss, red);
   float inv = rsqrtf(ss[0] / d + eps);
   int sd = s_dst ? s_dst[r] : -1;
   int hd = h_dst ? h_dst[r] : r;
@@ -297,9 +303,13 @@ void launch_build_input(int R, int d, int V, float eps, const int* tok, const fl
                         const int* hid_row, const void* E, const void* g_emb, const void* g_hid,
                         void* x, bool split, int* flags, cudaStream_t st) {
   if (R <= 0) return;
-  launch_pdl_cluster(build_input_kernel<T>, dim3(R * kRowCluster), dim3(kRowThreads), 0, st, kRowCluster,
-                     R, d, V, eps, tok, hid_base, hid_row, (const T*)E, (const T*)g_emb, (const T*)g_hid,
-                     (T*)x, split, flags);
+  if (R < kRowClusterMaxRows)
+    launch_pdl_cluster(build_input_kernel<T, kRowCluster>, dim3(R * kRowCluster), dim3(kRowThreads), 0, st,
+                       kRowCluster, R, d, V, eps, tok, hid_base, hid_row, (const T*)E, (const T*)g_emb,
+                       (const T*)g_hid, (T*)x, split, flags);
+  else
+    launch_pdl(build_input_kernel<T, 1>, dim3(R), dim3(kRowThreadsWide), 0, st, R, d, V, eps, tok, hid_base,
+               hid_row, (const T*)E, (const T*)g_emb, (const T*)g_hid, (T*)x, split, flags);
 }
 
 void launch_reduce_parts(int R, int N, int S, const float* part, float* out, cudaStream_t st) {
@@ -314,8 +324,12 @@ template <typename T>
 void launch_reduce_norm(int R, int N, int S, float eps, const float* part, const void* g_fc,
                         float* out, cudaStream_t st) {
   if (R <= 0) return;
-  launch_pdl_cluster(reduce_norm_kernel<T>, dim3(R * kRowCluster), dim3(kRowThreads), 0, st, kRowCluster,
-                     R, N, S, eps, part, (const T*)g_fc, out);
+  if (R < kRowClusterMaxRows)
+    launch_pdl_cluster(reduce_norm_kernel<T, kRowCluster>, dim3(R * kRowCluster), dim3(kRowThreads), 0, st,
+                       kRowCluster, R, N, S, eps, part, (const T*)g_fc, out);
+  else
+    launch_pdl(reduce_norm_kernel<T, 1>, dim3(R), dim3(kRowThreadsWide), 0, st, R, N, S, eps, part,
+               (const T*)g_fc, out);
 }
 
 template <typename T>
@@ -332,8 +346,13 @@ void launch_o_epilogue(int R, int d, int S, float eps, const float* part, const 
                        const int* hid_row, const void* g_post, float* r_out, void* z_out,
                        bool split, bool post, cudaStream_t st) {
   if (R <= 0) return;
-  launch_pdl_cluster(o_epilogue_kernel<T>, dim3(R * kRowCluster), dim3(kRowThreads), 0, st, kRowCluster,
-                     R, d, S, eps, part, hid_base, hid_row, (const T*)g_post, r_out, (T*)z_out, split, post);
+  if (R < kRowClusterMaxRows)
+    launch_pdl_cluster(o_epilogue_kernel<T, kRowCluster>, dim3(R * kRowCluster), dim3(kRowThreads), 0, st,
+                       kRowCluster, R, d, S, eps, part, hid_base, hid_row, (const T*)g_post, r_out,
+                       (T*)z_out, split, post);
+  else
+    launch_pdl(o_epilogue_kernel<T, 1>, dim3(R), dim3(kRowThreadsWide), 0, st, R, d, S, eps, part, hid_base,
+               hid_row, (const T*)g_post, r_out, (T*)z_out, split, post);
 }
 
 template <typename T>
@@ -350,10 +369,15 @@ void launch_down_epilogue(int R, int d, int S, float eps, const float* part, con
                           const void* g_final, const int* s_dst, float* s_base, const int* h_dst,
                           void* h_base, bool split, bool post, cudaStream_t st) {
   if (R <= 0) return;
-  const size_t slice = (size_t)((d + kRowCluster - 1) / kRowCluster) * sizeof(float);
-  launch_pdl_cluster(down_epilogue_kernel<T>, dim3(R * kRowCluster), dim3(kRowThreads), slice, st,
-                     kRowCluster, R, d, S, eps, part, r_in, (const T*)g_final, s_dst, s_base, h_dst,
-                     (T*)h_base, split, post);
+  if (R < kRowClusterMaxRows) {
+    const size_t slice = (size_t)((d + kRowCluster - 1) / kRowCluster) * sizeof(float);
+    launch_pdl_cluster(down_epilogue_kernel<T, kRowCluster>, dim3(R * kRowCluster), dim3(kRowThreads), slice,
+                       st, kRowCluster, R, d, S, eps, part, r_in, (const T*)g_final, s_dst, s_base, h_dst,
+                       (T*)h_base, split, post);
+  } else {
+    launch_pdl(down_epilogue_kernel<T, 1>, dim3(R), dim3(kRowThreadsWide), d * sizeof(float), st, R, d, S,
+               eps, part, r_in, (const T*)g_final, s_dst, s_base, h_dst, (T*)h_base, split, post);
+  }
 }
 
 #define E3_INST(T)                                                                                   \

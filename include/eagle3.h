@@ -164,7 +164,12 @@ typedef struct {
 /* Optional per-node verification details, device arrays [B, M+1]:
  * z_max / z_argmax: largest target logit and its token (ties: lowest token);
  * lse: log-sum-exp of z / T (of z when greedy); g_argmax: Gumbel-argmax of
- * z / T over the tokens that are not children of the node (sampling only). */
+ * z / T over the tokens that are not children of the node (sampling only).
+ * Any of the four may be NULL.  Cost: without g_argmax a sampling pass draws
+ * the Gumbel noise only at the node where each request's walk stops (the bf16
+ * head stores the target logits in the context's workspace meanwhile); with
+ * g_argmax it draws it at every node, as the walk's own draw at the stop node
+ * would be, which for wide passes costs most of the verify head's time. */
 typedef struct {
   float *z_max, *lse;
   int *z_argmax, *g_argmax;
