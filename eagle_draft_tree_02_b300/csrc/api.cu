@@ -293,8 +293,11 @@ void attn_splits(const eagle3_ctx* c, int B, int rows_per_req, int& kps, int& np
   const bool mma = attention_uses_mma(c->esz, f.head_dim, f.page_size);
   int blocks = B * f.n_kv_heads * attention_qgroups(rows_per_req, f.n_q_heads, f.n_kv_heads, mma);
   int maxp = f.max_prefix;
-  const int target = mma ? 4 * 148 : kTargetBlocks;
-  nps = std::max(1, std::min(cdiv(target, blocks), cdiv(maxp, 64)));
+  // the tcgen05 kernel (groups of more than 128 queries) runs one CTA per SM
+  // and stages its queries once per block: about two waves, 256+ keys a block
+  const bool tc = mma && attention_uses_tc(rows_per_req, f.n_q_heads, f.n_kv_heads);
+  const int target = tc ? 2 * 148 : mma ? 4 * 148 : kTargetBlocks;
+  nps = std::max(1, std::min(cdiv(target, blocks), cdiv(maxp, tc ? 256 : 64)));
   nps = std::min(nps, 240);  // the merge keeps one weight per split (with the tree splits) in 256
   kps = cdiv(cdiv(maxp, nps), 64) * 64;
   nps = cdiv(maxp, kps);

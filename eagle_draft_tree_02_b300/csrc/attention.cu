@@ -43,15 +43,18 @@ namespace {
 constexpr int QG = 32;   // query heads per block (CUDA-core kernel)
 constexpr int QGM = 64;  // queries per block (queries-as-M kernel: 4 warps x 16)
 constexpr int QKT = 16;  // at most this many queries per KV head: the keys-as-M kernel
+constexpr int QTC = 128; // more than this many: the tcgen05 kernel, 128 queries per block
 constexpr int KC = 64;   // keys per chunk
 constexpr int KST = 3;   // prefix stages in flight (tensor-core kernel)
 constexpr int NT = 256;  // threads (CUDA-core kernel)
 }
 
+bool attention_uses_tc(int rows_per_req, int Hq, int Hkv) { return rows_per_req * (Hq / Hkv) > QTC; }
+
 int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma) {
   int per = rows_per_req * (Hq / Hkv);
   if (mma && per <= QKT) return 1;
-  const int q = mma ? QGM : QG;
+  const int q = !mma ? QG : per <= QTC ? QGM : QTC;
   return (per + q - 1) / q;
 }
 
@@ -333,6 +336,131 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
   lo = bf2_bits(__floats2bfloat162_rn(x0 - hf.x, x1 - hf.y));
 }
 
+// ---- tcgen05 pieces of the wide-group kernel (one CTA issues, TMEM holds S and O)
+__device__ __forceinline__ void utc_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void utc_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void utc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void utc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void utc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void utc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// generic-proxy writes to shared memory, made visible to the tensor core's reads
+__device__ __forceinline__ void async_proxy_fence() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 32 consecutive TMEM columns of this thread's lane (load, and its wait)
+__device__ __forceinline__ void utc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void utc_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+// Shared-memory operand descriptor, 128-byte swizzle, 8-row groups 1024 bytes
+// apart.  K-major: rows of 64 K-elements (128 B).  MN-major: rows of 64
+// MN-elements, one row per K index; with N = 64 per MMA the operand is one
+// swizzle atom wide, so the leading offset (between atoms along MN) is unused.
+__device__ __forceinline__ uint64_t att_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+// MN-major operand one swizzle atom wide (64 elements along MN): both offset
+// fields carry the 8-row group stride, so the descriptor holds whichever of
+// the two the hardware takes as the stride along K.
+__device__ __forceinline__ uint64_t att_desc_mn(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(1024 >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, M = 128;
+// b_mn: B is MN-major.
+__host__ __device__ constexpr uint32_t att_idesc(int n, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(128 >> 4) << 24);
+}
+// bounded mbarrier wait of the wide-group kernel: false (flag raised) after ~2 s
+__device__ __forceinline__ bool att_wait_abort(uint32_t bar, uint32_t parity, int* flags,
+                                               volatile int* abort_f) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 63) == 63) {
+      if (*abort_f) return false;
+      if (clock64() - t0 > 4000000000LL) {
+        *abort_f = 1;
+        raise_flag(flags, FLAG_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // The key range of split blockIdx.z: prefix splits take keys
 // [split * keys_per_split, +keys_per_split) of the cache, tree splits 64 tree
 // slots each.
@@ -464,6 +592,7 @@ struct KvRing {
         const int n = k.hi - c0 + i / (NH * 8), h = (i / 8) % NH, piece = i % 8;
         *reinterpret_cast<uint4*>(vz + h * HB + n * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for tensor-core reads of V
     }
     if (__syncthreads_and(ok)) return true;
     for (int c = ci + 1; c < k.n_chunks && c < ci + KST; ++c)
@@ -943,6 +1072,280 @@ __global__ void __launch_bounds__(128) prefix_attention_kt_kernel(const __grid_c
   }
 }
 
+// Wide query groups (more than 16 queries per KV head: tree frontiers, verify
+// passes) on the tcgen05 tensor cores.  The 128 query rows of a group are the
+// MMA's M dimension and TMEM's lanes; warps w and w + 4 share lane quarter
+// w % 4 (rows 32 (w % 4) .. + 31), each taking half of a chunk's 64 keys and
+// half of O's columns, so the softmax of a row is split over two threads that
+// meet once per chunk (their row maxima, through shared memory).  Per chunk:
+//   S = Q K^T: Q staged once as bf16 hi + lo, scaled by log2(e)/sqrt(dh) so S
+//     is in base-2 units; K the ring's rows as a K-major B operand.
+//   P = 2^(S - m) (one ex2.approx per element) with a lazy reference max m: O
+//     and l are rescaled only when the row max has grown by more than kRescale
+//     (P stays below 2^kRescale; O and l share m, so the result is exact).
+//   O += P V: P written as bf16 hi + lo rows (K-major A operand), V read in
+//     place as an MN-major B operand, one 64-dim half (N = 64) per MMA.
+// One thread issues the MMAs; tcgen05.commit arrives on s_bar / o_bar.
+template <int DH>
+struct TcAttLayout {
+  using Ring = KvRing<DH>;
+  static constexpr int NH = DH / 64;
+  static constexpr int QB = 128 * 128;  // bytes of a 64-dim half of the 128-row Q tile
+  static constexpr int PB = 128 * 128;  // bytes of a P tile: 128 rows x 64 keys
+  static constexpr int GAP = 2048;      // barriers, TMEM slot, abort word, the row maxima exchange
+  static constexpr int SMEM = 1024 + KST * Ring::STB + GAP + 2 * NH * QB + 2 * PB;
+  static constexpr uint32_t S_COL = 0, O_COL = 64, TM_COLS = DH == 128 ? 256 : 128;
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {  // 2^x; 2^-inf = 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(256, 1) prefix_attention_tc_kernel(const __grid_constant__ AttnArgs a) {
+  using L = TcAttLayout<DH>;
+  using Ring = KvRing<DH>;
+  constexpr int NH = L::NH;
+  constexpr int OC = DH / 2;            // O columns of each of a row's two threads
+  constexpr float kRescale = 12.f;      // base-2 units
+  constexpr float kLn2 = 0.6931471805599453f, kLog2e = 1.4426950408889634f;
+  constexpr uint32_t IDESC_S = att_idesc(64, false), IDESC_O = att_idesc(64, true);
+  extern __shared__ __align__(16) unsigned char att_smem[];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int rt = tid & 127, hv = tid >> 7;  // row of the group; which half of keys and of O
+  const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv, split = blockIdx.z;
+  const int G = a.Hq / a.Hkv, nq = a.rows_per_req * G;
+  const int R = a.B * a.rows_per_req;
+  const SplitKeys sk = split_keys(a, b, split, tid == 0 && split == 0 && kvh == 0 && blockIdx.y == 0);
+  Ring ring;
+  ring.init(att_smem, b, kvh, sk);
+  unsigned char* gap = ring.sb + KST * Ring::STB;  // the ring's barriers take its first 8 KST bytes
+  const uint32_t gap32 = ring.sb32 + KST * Ring::STB;
+  const uint32_t s_bar = gap32 + 64, o_bar = gap32 + 72;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(gap + 80);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(gap + 84);
+  float* xmax = reinterpret_cast<float*>(gap + 1024);  // [2 halves][128 rows]
+  unsigned char* qs = gap + L::GAP;         // [hi, lo][NH][128 rows][128 B]
+  unsigned char* ps = qs + 2 * NH * L::QB;  // [hi, lo][128 rows][128 B]
+  const uint32_t qs32 = smem_u32(qs), ps32 = smem_u32(ps);
+
+  if (warp == 0) utc_alloc(smem_u32(tslot), L::TM_COLS);
+  if (tid == 0) {
+    att_mbar_init(s_bar, 1);
+    att_mbar_init(o_bar, 1);
+    *abort_f = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  utc_fence_before();
+  // as in the kernels above: with a stable prefix the first chunks are
+  // requested before the wait for the previous kernel
+  const bool early = a.prefix_stable && !sk.tree && sk.n_chunks > 0;
+  if (early)
+    ring.start(a);  // ends in a block barrier
+  else
+    __syncthreads();
+  utc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's TMEM lanes
+  pdl_begin();
+  const bool live = !(a.skip && *a.skip == 0);
+
+  // this thread's query row
+  const int q = blockIdx.y * 128 + rt;
+  const bool qv = live && q < nq;
+  const float* qp = nullptr;
+  const uint32_t* mrow = nullptr;
+  int row = 0, head = 0;
+  if (qv) {
+    row = b * a.rows_per_req + q / G;
+    head = kvh * G + q % G;
+    qp = a.q + (size_t)a.q_row[row] * a.Hq * DH + (size_t)head * DH;
+    mrow = a.mask + (size_t)row * a.mask_words;
+  }
+  if (live) {
+    // the row of Q (this thread: half hv of its 16-byte pieces), scaled to base-2 units
+    const float scale = rsqrtf((float)DH) * kLog2e;
+#pragma unroll 1
+    for (int p = hv * (DH / 16); p < (hv + 1) * (DH / 16); ++p) {
+      float x[8];
+      if (qp) {
+        const float4 u0 = reinterpret_cast<const float4*>(qp)[2 * p];
+        const float4 u1 = reinterpret_cast<const float4*>(qp)[2 * p + 1];
+        x[0] = u0.x; x[1] = u0.y; x[2] = u0.z; x[3] = u0.w;
+        x[4] = u1.x; x[5] = u1.y; x[6] = u1.z; x[7] = u1.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      }
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split_pair(x[2 * e] * scale, x[2 * e + 1] * scale, hi[e], lo[e]);
+      const int off = (p >> 3) * L::QB + rt * 128 + (((p & 7) ^ (rt & 7)) << 4);
+      *reinterpret_cast<uint4*>(qs + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(qs + NH * L::QB + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    // O = 0 (this warp's half of the columns)
+    float z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < OC; c += 32) utc_st32(trow + L::O_COL + hv * OC + c, z);
+    if (sk.tree) {
+      if (sk.n_chunks > 0) ring.load_tree(a);
+    } else if (!early) {
+      ring.start(a);
+    }
+  } else if (early) {
+    ring.drain_start(a);  // the requested chunks land before the shared memory is released
+  }
+  async_proxy_fence();  // Q, O's zeros and a tree chunk, before the tensor core reads them
+  utc_fence_before();
+  __syncthreads();
+
+  float m = -INFINITY, l = 0.f;  // base-2 reference max of the row; this thread's share of the sum
+  int done = 0;    // chunks whose P V was issued
+  int landed = 0;  // prefix chunks awaited (those up to landed + KST - 2 were requested)
+  bool drain = false;
+  for (int ci = 0; live && ci < sk.n_chunks; ++ci) {
+    const int c0 = sk.lo + ci * KC, st = sk.tree ? 0 : ci % KST;
+    // the previous chunk's P V must be complete: its stage is refilled next and P rewritten
+    bool ok = ci == 0 || att_wait_abort(o_bar, (uint32_t)(ci - 1) & 1u, a.flags, abort_f);
+    if (!__syncthreads_and(ok)) {
+      drain = !sk.tree;
+      break;
+    }
+    if (!sk.tree) {
+      if (!ring.next(a, ci)) break;  // it lets its own requests land
+      landed = ci + 1;
+    }
+    if (tid == 0) {  // S = Q K^T
+      utc_fence_after();
+      const uint32_t kb = ring.kstage32(st);
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bk = att_desc(kb + h * Ring::HB + kk * 32);
+          const uint32_t qa = qs32 + h * L::QB + kk * 32;
+          utc_mma(tmem + L::S_COL, att_desc(qa), bk, IDESC_S, (h | kk) ? 1u : 0u);
+          utc_mma(tmem + L::S_COL, att_desc(qa + NH * L::QB), bk, IDESC_S, 1u);
+          if (sk.tree)  // + q hi . k lo (stage 1 holds the tree chunk's lo halves)
+            utc_mma(tmem + L::S_COL, att_desc(qa), att_desc(kb + Ring::STB + h * Ring::HB + kk * 32),
+                    IDESC_S, 1u);
+        }
+      utc_commit(s_bar);
+    }
+    ok = att_wait_abort(s_bar, (uint32_t)ci & 1u, a.flags, abort_f);
+    if (!__syncthreads_and(ok)) {
+      drain = !sk.tree;
+      break;
+    }
+    utc_fence_after();
+    float sv[32];  // keys c0 + 32 hv + j
+    utc_ld32(trow + L::S_COL + 32 * hv, sv);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int key = c0 + 32 * hv + j;
+      bool keep = qv && key < sk.hi;
+      if (keep && sk.tree) keep = (mrow[key >> 5] >> (key & 31)) & 1u;
+      if (!keep) sv[j] = -INFINITY;
+      mx = fmaxf(mx, sv[j]);
+    }
+    // the two threads of the row meet: row max over the chunk's 64 keys
+    xmax[hv * 128 + rt] = mx;
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+    mx = fmaxf(mx, xmax[(hv ^ 1) * 128 + rt]);
+    // lazy reference max (the same decision in both threads of the row)
+    float alpha = 1.f;
+    if (mx > m + kRescale) {
+      alpha = m == -INFINITY ? 0.f : ex2_approx(m - mx);
+      m = mx;
+    }
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {  // the TMEM row access is warp-wide
+#pragma unroll
+      for (int c = 0; c < OC; c += 32) {
+        float o[32];
+        utc_ld32(trow + L::O_COL + hv * OC + c, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        utc_st32(trow + L::O_COL + hv * OC + c, o);
+      }
+    }
+    l *= alpha;
+    // P: this thread's 4 pieces of 8 keys, hi and lo, swizzled like the other operands
+#pragma unroll
+    for (int pc = 0; pc < 4; ++pc) {
+      float pv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float v = sv[pc * 8 + e];
+        pv[e] = (v == -INFINITY) ? 0.f : ex2_approx(v - m);
+        l += pv[e];
+      }
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split_pair(pv[2 * e], pv[2 * e + 1], hi[e], lo[e]);
+      const int piece = 4 * hv + pc;
+      const int off = rt * 128 + ((piece ^ (rt & 7)) << 4);
+      *reinterpret_cast<uint4*>(ps + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(ps + L::PB + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    async_proxy_fence();
+    utc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // O += P V
+      utc_fence_after();
+      const uint32_t vb = ring.vstage32(st);
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // keys 16 kk .. + 15: rows 16 kk of V's half h
+          const uint64_t bv = att_desc_mn(vb + h * Ring::HB + kk * 2048);
+          const uint32_t od = tmem + L::O_COL + 64 * h;
+          utc_mma(od, att_desc(ps32 + kk * 32), bv, IDESC_O, 1u);
+          utc_mma(od, att_desc(ps32 + L::PB + kk * 32), bv, IDESC_O, 1u);
+          if (sk.tree)  // + p hi . v lo
+            utc_mma(od, att_desc(ps32 + kk * 32), att_desc_mn(vb + Ring::STB + h * Ring::HB + kk * 2048),
+                    IDESC_O, 1u);
+        }
+      utc_commit(o_bar);
+    }
+    done = ci + 1;
+  }
+  if (drain)  // requested chunks land before the shared memory is released
+    for (int c = landed; c < sk.n_chunks && c < landed + KST - 1; ++c)
+      att_wait(ring.bar0 + 8u * (c % KST), (uint32_t)(c / KST) & 1u, a.flags);
+  // the last P V, then the row's O, max (natural units) and sum
+  bool ok = done == 0 || att_wait_abort(o_bar, (uint32_t)(done - 1) & 1u, a.flags, abort_f);
+  ok = __syncthreads_and(ok) && live && !*abort_f;
+  utc_fence_after();
+  if (ok) {
+    xmax[hv * 128 + rt] = l;
+    const size_t base = ((size_t)split * R + row) * a.Hq + head;
+#pragma unroll
+    for (int c = 0; c < OC; c += 32) {
+      float o[32];
+      utc_ld32(trow + L::O_COL + hv * OC + c, o);  // warp-wide: every lane loads
+      if (qv) {
+        float4* op = reinterpret_cast<float4*>(a.o_part + base * DH + hv * OC + c);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) op[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      }
+    }
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+    if (qv && hv == 0) {
+      a.ml_part[base * 2] = m * kLn2;
+      a.ml_part[base * 2 + 1] = l + xmax[128 + rt];
+    }
+  }
+  utc_fence_before();
+  __syncthreads();
+  if (warp == 0) utc_dealloc(tmem, L::TM_COLS);
+}
+
 // merge the key splits of one (row, head): o = sum_s o_s e^{m_s - m} / sum_s l_s e^{m_s - m}
 template <typename T>
 __global__ void attention_combine_kernel(AttnArgs a) {
@@ -1014,6 +1417,8 @@ void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
   smem_limit((const void*)tree_attention_kernel<T>, 160 * 1024);
   smem_limit((const void*)prefix_attention_mma_kernel<64>, KvRing<64>::SMEM);
   smem_limit((const void*)prefix_attention_mma_kernel<128>, KvRing<128>::SMEM);
+  smem_limit((const void*)prefix_attention_tc_kernel<64>, TcAttLayout<64>::SMEM);
+  smem_limit((const void*)prefix_attention_tc_kernel<128>, TcAttLayout<128>::SMEM);
   smem_limit((const void*)prefix_attention_kt_kernel<64, 1>, KvRing<64>::SMEM);
   smem_limit((const void*)prefix_attention_kt_kernel<64, 2>, KvRing<64>::SMEM);
   smem_limit((const void*)prefix_attention_kt_kernel<128, 1>, KvRing<128>::SMEM);
@@ -1028,16 +1433,20 @@ void launch_tree_attention(const AttnArgs& a, cudaStream_t st) {
         launch_pdl(prefix_attention_kt_kernel<128, 1>, dim3(gp), blk, sm2, st, a);
       else if (nq <= QKT)
         launch_pdl(prefix_attention_kt_kernel<128, 2>, dim3(gp), blk, sm2, st, a);
-      else
+      else if (nq <= QTC)
         launch_pdl(prefix_attention_mma_kernel<128>, dim3(gp), blk, sm2, st, a);
+      else
+        launch_pdl(prefix_attention_tc_kernel<128>, dim3(gp), dim3(256), (size_t)TcAttLayout<128>::SMEM, st, a);
     } else {
       const size_t sm2 = KvRing<64>::SMEM;
       if (nq <= 8)
         launch_pdl(prefix_attention_kt_kernel<64, 1>, dim3(gp), blk, sm2, st, a);
       else if (nq <= QKT)
         launch_pdl(prefix_attention_kt_kernel<64, 2>, dim3(gp), blk, sm2, st, a);
-      else
+      else if (nq <= QTC)
         launch_pdl(prefix_attention_mma_kernel<64>, dim3(gp), blk, sm2, st, a);
+      else
+        launch_pdl(prefix_attention_tc_kernel<64>, dim3(gp), dim3(256), (size_t)TcAttLayout<64>::SMEM, st, a);
     }
   } else {
     dim3 grid(a.B * a.Hkv, attention_qgroups(a.rows_per_req, a.Hq, a.Hkv, false), n_splits);

@@ -83,6 +83,8 @@ struct AttnArgs {
 template <typename T> void launch_tree_attention(const AttnArgs& a, cudaStream_t st);
 // query groups per (request, KV head) of the prefix-split kernel
 int attention_qgroups(int rows_per_req, int Hq, int Hkv, bool mma);
+// the tensor-core path takes the tcgen05 kernel (more than 128 queries per KV head)
+bool attention_uses_tc(int rows_per_req, int Hq, int Hkv);
 bool attention_uses_mma(int elem_bytes, int dh, int page_size);
 // tokens per tensor-map box of the tensor-core kernel: 64, or the largest
 // divisor of 64 that divides the page size (at least 8 when the kernel is used)

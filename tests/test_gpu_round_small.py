@@ -39,6 +39,11 @@ CASES = {
     "variant_post_norm_fp32": (C0.scaled(name="post_norm_fp32", post_norm=True, gain_std=0.1), 11),
     "variant_fc_post_bf16": (SMALL_BF16.scaled(name="fc_post_bf16", fc_norm=True, post_norm=True,
                                                gain_std=0.1), 12),
+    # 16 query heads on one KV head: the verify pass's 208 queries per KV head
+    # take the tcgen05 attention (two groups of up to 128), the draft passes'
+    # 64 the queries-as-M kernel, the root's 16 the keys-as-M kernel
+    "wide_groups_bf16": (SMALL_BF16.scaled(name="wide_groups_bf16", d=1024, n_q_heads=16, n_kv_heads=1,
+                                           head_dim=64, ffn=1024), 13),
 }
 
 
