@@ -162,12 +162,21 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(HeadParts hp,
   int ti = 0x7fffffff;
   for (int p = tid; p < hp.n_parts; p += blockDim.x) {
     const size_t pr = (size_t)p * hp.R + r;
-    lse_fold(m, s, hp.ms[pr * 2], hp.ms[pr * 2 + 1]);
     const float* pv = hp.val + pr * k;
     const int* pi = hp.idx + pr * k;
-    for (int q = 0; q < k; ++q) {
-      const int i = pi[q];
-      const float v = pv[q];
+    // the partial's whole list first: independent loads, one round trip
+    float pvs[K];
+    int pis[K];
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+      pvs[q] = pv[q];
+      pis[q] = pi[q];
+    }
+    lse_fold(m, s, hp.ms[pr * 2], hp.ms[pr * 2 + 1]);
+#pragma unroll
+    for (int q = 0; q < K; ++q) {
+      const int i = pis[q];
+      const float v = pvs[q];
       if (i < 0 || !better(v, i, tv, ti)) break;
       float cv = v;
       int ci = i;
