@@ -20,9 +20,9 @@ def test_library_exports_every_declared_symbol(E):
 
 
 def _cfg(E, **kw):
-    from eagle_draft_tree_02_b300.configs import CONFIGS
+    from eagle_draft_tree_02_b300.configs import by_name
     from eagle_draft_tree_02_b300.runner import make_config
-    c = make_config(CONFIGS[0], max_prefix=64)
+    c = make_config(by_name("tiny_fp32_b1"), max_prefix=64)
     for k, v in kw.items():
         setattr(c, k, v)
     return c

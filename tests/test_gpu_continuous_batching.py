@@ -21,12 +21,12 @@ memory, so it stays valid without a new capture.
 import numpy as np
 import pytest
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import bf16_bits_from_f64, bf16_bits_to_f32, make_inputs
 from oracle import round as R
 from parity import TOL, compare_request, gpu_outputs, Report
 
-C0 = CONFIGS[0]
+C0 = by_name("tiny_fp32_b1")
 CASES = {
     "fp32": C0.scaled(name="cb_fp32", batch=4, prefix=48, prefix_range=(20, 48), depth=4, topk=3,
                       n_verify=10, page_size=16, lm_std=0.3),

@@ -8,10 +8,10 @@ for bit, for every round id (the sampling draws depend on it).
 import numpy as np
 import pytest
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import make_inputs
 
-C0 = CONFIGS[0]
+C0 = by_name("tiny_fp32_b1")
 SMALL_BF16 = C0.scaled(name="graph_bf16", dtype="bf16", d=256, n_q_heads=4, n_kv_heads=2,
                        head_dim=64, ffn=512, vocab=2048, prefix=100, batch=2, depth=4, topk=4,
                        n_verify=12, lm_std=0.08, temperatures=(0.0, 1.0))

@@ -8,10 +8,10 @@
 import numpy as np
 import pytest
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import make_inputs
 
-C0 = CONFIGS[0]
+C0 = by_name("tiny_fp32_b1")
 LIN_BF16 = C0.scaled(name="lin_bf16", dtype="bf16", d=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
                      ffn=512, vocab=1000, prefix=400, batch=2, depth=3, topk=4, n_verify=8,
                      lm_std=0.08)

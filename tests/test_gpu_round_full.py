@@ -18,7 +18,7 @@ failing) are reported in every assertion message and bounded per workload.
 import numpy as np
 import pytest
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import make_inputs
 from oracle import layers as L
 from oracle import round as R
@@ -94,19 +94,19 @@ def _run(cfg, kv_rows_checked):
 
 @pytest.mark.gpu
 def test_full_8b_batch1_tree(cuda, lib_built):
-    _run(CONFIGS[1], kv_rows_checked=32)
+    _run(by_name("llama31_8b_b1_tree"), kv_rows_checked=32)
 
 
 @pytest.mark.gpu
 def test_full_8b_batch64_chain_paged(cuda, lib_built):
-    _run(CONFIGS[2], kv_rows_checked=4)
+    _run(by_name("llama31_8b_b64_chain3_paged"), kv_rows_checked=4)
 
 
 @pytest.mark.gpu
 def test_full_70b_batch4_tree(cuda, lib_built):
-    _run(CONFIGS[3], kv_rows_checked=16)
+    _run(by_name("llama33_70b_b4_tree"), kv_rows_checked=16)
 
 
 @pytest.mark.gpu
 def test_full_two_stage_b16_tree(cuda, lib_built):
-    _run(CONFIGS[4], kv_rows_checked=8)
+    _run(by_name("two_stage_head_b16_tree"), kv_rows_checked=8)

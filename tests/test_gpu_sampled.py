@@ -12,11 +12,11 @@ calls made with that round id.
 import numpy as np
 import pytest
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import make_inputs
 from parity import TOL, compare, gpu_round
 
-C0 = CONFIGS[0]
+C0 = by_name("tiny_fp32_b1")
 CASES = {
     "sampled_fp32": (C0.scaled(name="samp_fp32", sampled_draft=True, temperatures=(0.0, 1.0)), 3),
     "sampled_fp32_b3": (C0.scaled(name="samp_fp32_b3", sampled_draft=True, batch=3, prefix=64,

@@ -17,12 +17,12 @@ import numpy as np
 import pytest
 from scipy import stats
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import make_inputs
 from oracle import layers as L
 from oracle import round as R
 
-V8 = CONFIGS[0].scaled(name="chi2_v8_gpu", d=32, n_q_heads=2, n_kv_heads=2, head_dim=16, ffn=32,
+V8 = by_name("tiny_fp32_b1").scaled(name="chi2_v8_gpu", d=32, n_q_heads=2, n_kv_heads=2, head_dim=16, ffn=32,
                        vocab=8, prefix=6, depth=3, topk=2, n_verify=6, lm_std=0.3,
                        temperatures=(1.0,))
 N = 24000

@@ -11,12 +11,12 @@ of all of a request's rows and runs the round from the last one.
 import numpy as np
 import pytest
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import make_inputs
 from oracle import round as R
 from parity import TOL
 
-C0 = CONFIGS[0]
+C0 = by_name("tiny_fp32_b1")
 CASES = {
     "fp32_b3": C0.scaled(batch=3, prefix=40, prefix_range=(20, 40), depth=4, topk=3, n_verify=10,
                          lm_std=0.3),

@@ -18,13 +18,13 @@ vocabulary that is not a multiple of the vector width.
 import numpy as np
 import pytest
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import bf16_bits_to_f32, draw_logits, make_inputs
 from oracle import layers as L
 from oracle import round as R
 from parity import TOL, Follow, GpuRound, Report
 
-C0 = CONFIGS[0]
+C0 = by_name("tiny_fp32_b1")
 CASES = {
     # fp32 context, ragged vocabulary (1003 is not a multiple of 4), B = 2
     "fp32_b2_v1003": (C0.scaled(name="vl_fp32", batch=2, vocab=1003, prefix=40), "fp32", 1004, {}),

@@ -25,7 +25,7 @@ import torch
 import torch.nn.functional as F
 from scipy.special import logsumexp as sp_logsumexp
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import make_inputs
 from oracle import layers as L
 from oracle import philox
@@ -44,7 +44,7 @@ def _rms(v, g, eps):
 
 
 def _layer_setup(seed, d=16, ffn=12, heads=2, dh=8, eps=1e-5):
-    cfg = CONFIGS[0].scaled(d=d, ffn=ffn, n_q_heads=heads, n_kv_heads=heads, head_dim=dh,
+    cfg = by_name("tiny_fp32_b1").scaled(d=d, ffn=ffn, n_q_heads=heads, n_kv_heads=heads, head_dim=dh,
                             rms_eps=eps)
     rng = np.random.default_rng(seed)
     od = heads * dh
@@ -113,7 +113,7 @@ def test_decoder_input_halves_and_gains_in_closed_form():
     has RMS |kappa|, so rms(hid; g_hid) = sign(kappa) g_hid.  The first half is the
     embedding's, the second the hidden state's."""
     d, V = 8, 8
-    cfg = CONFIGS[0].scaled(d=d, vocab=V, rms_eps=0.0)
+    cfg = by_name("tiny_fp32_b1").scaled(d=d, vocab=V, rms_eps=0.0)
     rng = np.random.default_rng(4)
     c = np.array([2.0, -0.5, 3.0, 1.0, -4.0, 0.25, 7.0, -1.5])
     w = {"embed": np.diag(c), "g_emb": 1.0 + rng.standard_normal(d), "g_hid": 1.0 + rng.standard_normal(d)}
@@ -143,7 +143,7 @@ def test_logsumexp_matches_scipy():
 
 
 def test_draft_logq_single_stage_is_a_log_softmax():
-    cfg = CONFIGS[0].scaled(d=24, vocab=50)
+    cfg = by_name("tiny_fp32_b1").scaled(d=24, vocab=50)
     rng = np.random.default_rng(6)
     w = {"w_lm": rng.standard_normal((50, 24)).astype(np.float32)}
     h = rng.standard_normal((3, 24))
@@ -159,7 +159,7 @@ def test_two_stage_round_with_every_token_a_candidate_is_the_single_stage_round(
     over the candidates, children from them) must give the single-stage pool
     when the candidate set is the whole vocabulary."""
     V = 96
-    cfg2 = CONFIGS[0].scaled(name="two_stage_pin", d=32, n_q_heads=2, n_kv_heads=2, head_dim=16,
+    cfg2 = by_name("tiny_fp32_b1").scaled(name="two_stage_pin", d=32, n_q_heads=2, n_kv_heads=2, head_dim=16,
                              ffn=48, vocab=V, prefix=20, depth=4, topk=3, n_verify=10,
                              lr_rank=8, lr_cand=V, lm_std=0.3)
     cfg1 = cfg2.scaled(lr_rank=0, lr_cand=0)

@@ -32,7 +32,7 @@ import torch
 import torch.nn.functional as F
 from scipy import stats
 
-from eagle_draft_tree_02_b300.configs import CONFIGS, TINY_V8
+from eagle_draft_tree_02_b300.configs import by_name, TINY_V8
 from eagle_draft_tree_02_b300.synth import bf16_bits_from_f64, bf16_bits_to_f32, make_inputs
 from oracle import layers as L
 from oracle import philox
@@ -61,7 +61,7 @@ def test_linear_rmsnorm_silu_match_torch():
 def test_attend_matches_torch_sdpa_gqa(hq, hkv):
     rng = np.random.default_rng(hq * 10 + hkv)
     dh, n = 16, 23
-    cfg = CONFIGS[0].scaled(n_q_heads=hq, n_kv_heads=hkv, head_dim=dh)
+    cfg = by_name("tiny_fp32_b1").scaled(n_q_heads=hq, n_kv_heads=hkv, head_dim=dh)
     q = rng.standard_normal((hq, dh))
     K = rng.standard_normal((n, hkv, dh))
     V = rng.standard_normal((n, hkv, dh))
@@ -164,7 +164,7 @@ def _brute_path_states(w, cfg, f, tok, P, pool, node):
 
 @pytest.fixture(scope="module")
 def tiny_round():
-    cfg = CONFIGS[0].scaled(prefix=24, depth=4, topk=3, n_verify=10)
+    cfg = by_name("tiny_fp32_b1").scaled(prefix=24, depth=4, topk=3, n_verify=10)
     inp = make_inputs(cfg, seed=11)
     w = R.weights_f32(inp)
     f = inp.feats_f32()
@@ -273,7 +273,7 @@ def test_build_tree_random_pools(seed):
 
 
 def test_chain_k1_is_a_chain():
-    cfg = CONFIGS[0].scaled(prefix=8, depth=3, topk=1, n_verify=3)
+    cfg = by_name("tiny_fp32_b1").scaled(prefix=8, depth=3, topk=1, n_verify=3)
     inp = make_inputs(cfg, seed=5)
     w = R.weights_f32(inp); f = inp.feats_f32(); P = 8
     K, V = R.prefix_kv(w, cfg, f[:P], inp.tokens[:P])
@@ -382,7 +382,7 @@ def test_sampling_deterministic_in_seed_and_round():
 def test_two_stage_head_reduces_to_single_stage():
     rng = np.random.default_rng(9)
     V, d, r = 300, 24, 8
-    cfg1 = CONFIGS[0].scaled(d=d, vocab=V)
+    cfg1 = by_name("tiny_fp32_b1").scaled(d=d, vocab=V)
     w = {"w_lm": rng.standard_normal((V, d)).astype(np.float32),
          "lr_u": rng.standard_normal((V, r)).astype(np.float32),
          "lr_v": rng.standard_normal((r, d)).astype(np.float32)}
@@ -416,7 +416,7 @@ def test_bf16_rounding_is_nearest_even():
 
 
 def test_inputs_are_deterministic():
-    cfg = CONFIGS[0]
+    cfg = by_name("tiny_fp32_b1")
     a, b = make_inputs(cfg, threads=1), make_inputs(cfg, threads=4)
     for k in a.w:
         assert np.array_equal(a.w[k], b.w[k]), k
@@ -425,7 +425,7 @@ def test_inputs_are_deterministic():
 
 # ----------------------------------------------------------------------------- drafter variants
 def _variant_cfg(**kw):
-    return CONFIGS[0].scaled(name="variant_pin", prefix=24, depth=3, topk=3, n_verify=8,
+    return by_name("tiny_fp32_b1").scaled(name="variant_pin", prefix=24, depth=3, topk=3, n_verify=8,
                              gain_std=0.1, **kw)
 
 
@@ -500,7 +500,7 @@ def test_variant_tree_states_equal_sequential_path_forward(variant_round):
 
 # ----------------------------------------------------------------------------- per-request control
 def _ctl_setup(seed=31, **kw):
-    cfg = CONFIGS[0].scaled(name="ctl_pin", prefix=24, depth=4, topk=3, n_verify=10, **kw)
+    cfg = by_name("tiny_fp32_b1").scaled(name="ctl_pin", prefix=24, depth=4, topk=3, n_verify=10, **kw)
     inp = make_inputs(cfg, seed=seed)
     w = R.weights_f32(inp)
     f = inp.feats_f32()
@@ -660,7 +660,7 @@ def test_qratio_on_top_k_children_is_biased_but_point_masses_are_not():
 
 
 def test_sampled_round_keeps_sibling_prefixes_in_draw_order():
-    cfg = CONFIGS[0].scaled(name="samp_pin", prefix=24, depth=4, topk=3, n_verify=7)
+    cfg = by_name("tiny_fp32_b1").scaled(name="samp_pin", prefix=24, depth=4, topk=3, n_verify=7)
     inp = make_inputs(cfg, seed=33)
     w = R.weights_f32(inp)
     f = inp.feats_f32()
@@ -686,7 +686,7 @@ def test_sampled_round_keeps_sibling_prefixes_in_draw_order():
 
 
 # whole sampled round at V = 8 (d = 32 so the draft and target heads differ)
-_V8_ROUND = CONFIGS[0].scaled(name="samp_round_v8", d=32, n_q_heads=2, n_kv_heads=2, head_dim=16,
+_V8_ROUND = by_name("tiny_fp32_b1").scaled(name="samp_round_v8", d=32, n_q_heads=2, n_kv_heads=2, head_dim=16,
                               ffn=32, vocab=8, prefix=6, depth=3, topk=2, n_verify=6, lm_std=0.3,
                               sampled_draft=True)
 

@@ -18,12 +18,12 @@ failure has already run every other test.
 import numpy as np
 import pytest
 
-from eagle_draft_tree_02_b300.configs import CONFIGS
+from eagle_draft_tree_02_b300.configs import by_name
 from eagle_draft_tree_02_b300.synth import bf16_bits_to_f32, make_inputs
 from oracle import layers as L
 from parity import TOL, _valid_choice
 
-C0 = CONFIGS[0]
+C0 = by_name("tiny_fp32_b1")
 SMALL_BF16 = C0.scaled(name="noalloc_bf16", dtype="bf16", d=256, n_q_heads=4, n_kv_heads=2,
                        head_dim=64, ffn=512, vocab=5000, prefix=40, batch=3, depth=3, topk=5,
                        n_verify=8, lm_std=0.08)
