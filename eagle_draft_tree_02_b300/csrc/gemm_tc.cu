@@ -35,6 +35,7 @@ constexpr uint32_t A_STAGE = BM * BK * 2;  // 16 KB
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr int kSmemBudget = 110 * 1024;   // per CTA when two CTAs share an SM
 constexpr int kSmemBudgetWide = 220 * 1024;  // one CTA per SM: tiles of more than 64 columns
+constexpr int kNumSmsNominal = 148;
 
 struct TcArgs {
   int R;       // activation rows
@@ -1087,7 +1088,8 @@ struct Launch {
   size_t smem;
 };
 
-Launch plan_launch(int R, int n_kb) {
+// kb_cta: k-blocks each CTA runs (after split-K); ctas: CTAs in the grid.
+Launch plan_launch(int R, int kb_cta, int ctas) {
   Launch L;
   L.n_tiles = cdiv(std::max(R, 1), 256);
   L.ntile = std::max(16, cdiv(cdiv(std::max(R, 1), L.n_tiles), 16) * 16);
@@ -1098,9 +1100,14 @@ Launch plan_launch(int R, int n_kb) {
   const size_t fixed = 1024 + 64;
   // A wide activation tile (a stage of more than 24 KB) would leave two CTAs
   // with 2-3 stages each; one CTA with the whole shared memory keeps 4+ --
-  // worth it only for a long K loop (a short one, like the low-rank head's
-  // 4 k-blocks, is better served by two CTAs per SM).
-  const size_t budget = (stage > 24 * 1024 && n_kb >= 16) ? kSmemBudgetWide : kSmemBudget;
+  // worth it only for a long K loop per CTA (a short one, like a split-K
+  // slice of 8 k-blocks or the low-rank head's 4, is better served by two
+  // CTAs per SM), and only while the grid fits one CTA per SM or two CTAs
+  // would get fewer than 3 stages: a 64-row layer GEMM's 224-288 CTAs ran in
+  // 1.5-2 waves of one per SM.
+  const bool two_fit = (kSmemBudget - 1088) / stage >= 3;
+  const bool wide = stage > 24 * 1024 && kb_cta >= 16 && !(ctas > kNumSmsNominal && two_fit);
+  const size_t budget = wide ? kSmemBudgetWide : kSmemBudget;
   L.stages = (int)std::max<size_t>(2, std::min<size_t>(8, (budget - fixed) / stage));
   L.smem = fixed + L.stages * stage + 16 * L.stages + 16;
   return L;
@@ -1119,7 +1126,8 @@ bool launch(TcGemm* t, const CUtensorMap* a0, const CUtensorMap* a1, const CUten
             const void* X, int ldx, int K, int R, bool split, int S, TcArgs& args, int grid_x,
             cudaStream_t st) {
   const int ncols = split ? 2 * R : R;
-  Launch L = plan_launch(ncols, cdiv(K, BK));
+  const int n_tiles = cdiv(std::max(ncols, 1), 256);
+  Launch L = plan_launch(ncols, cdiv(cdiv(K, BK), S), grid_x * n_tiles * S);
   CUtensorMap mb;
   if (!encode_map(t->encode, &mb, X, ncols, K, (size_t)ldx * 2, L.ntile)) return false;
   args.R = R;
