@@ -44,6 +44,8 @@ CASES = {
     # 64 the queries-as-M kernel, the root's 16 the keys-as-M kernel
     "wide_groups_bf16": (SMALL_BF16.scaled(name="wide_groups_bf16", d=1024, n_q_heads=16, n_kv_heads=1,
                                            head_dim=64, ffn=1024), 13),
+    # sampling at T != 1: 1/T scales the target logits in the head, the walk and the bonus draw
+    "small_bf16_t07": (SMALL_BF16.scaled(name="small_bf16_t07", temperatures=(0.7,)), 14),
 }
 
 
@@ -256,8 +258,9 @@ def test_two_stage_head_all_tied_lowrank_scores(cuda, lib_built, cfg):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("cfg", [SMALL_BF16, TWO_STAGE_BF16], ids=["bf16", "two_stage_bf16"])
-def test_deferred_bonus_matches_the_head_draw(cuda, lib_built, cfg):
+@pytest.mark.parametrize("cfg,T", [(SMALL_BF16, 1.0), (TWO_STAGE_BF16, 1.0), (SMALL_BF16, 0.7)],
+                         ids=["bf16", "two_stage_bf16", "bf16_t07"])
+def test_deferred_bonus_matches_the_head_draw(cuda, lib_built, cfg, T):
     """Sampling without the per-node Gumbel-argmax: the tensor-core head stores
     the target logits and the bonus is drawn only at each request's stop node.
     The walk's outputs equal those of the draw made inside the head (stats with
@@ -267,9 +270,9 @@ def test_deferred_bonus_matches_the_head_draw(cuda, lib_built, cfg):
     inp, eng = _engine(cfg, 6)
     eng.draft_round()
     for rid in range(48):
-        a1, p1, o1 = [t.clone() for t in eng.verify(1.0, 5, rid, g_argmax=True)]
+        a1, p1, o1 = [t.clone() for t in eng.verify(T, 5, rid, g_argmax=True)]
         g = eng.stats_t["g_argmax"].clone()
-        a2, p2, o2 = [t.clone() for t in eng.verify(1.0, 5, rid)]
+        a2, p2, o2 = [t.clone() for t in eng.verify(T, 5, rid)]
         assert torch.equal(a1, a2) and torch.equal(p1, p2) and torch.equal(o1, o2), rid
         for b in range(cfg.batch):
             n = int(a1[b])
